@@ -1,0 +1,108 @@
+"""Named workloads and the seeded synthetic input generator.
+
+This module holds no arithmetic of the CfC method: it only names the
+workload shapes and draws random inputs.  Both the CUDA path (through the
+Python binding) and the CPU oracle under ``oracle/`` are fed from here, so
+the two sides always see the same fp32 (or bf16-valued) inputs.
+
+Input recipe (fixed draw order, one ``numpy.random.default_rng(seed)``):
+
+1. ``x``     [B, K, n_in]  ~ N(0, 1)
+2. ``h0``    [B, n_hid]    ~ N(0, h0_std^2)   (std 1, or 0.5 for the large case)
+3. ``W_in``  [3, n_hid, n_in]  ~ U(-1/sqrt(n_in), +1/sqrt(n_in))   heads f, g, h~
+4. ``W_rec`` [3, n_hid, n_hid] ~ U(-1/sqrt(n_hid), +1/sqrt(n_hid))
+5. ``y``     [B, n_hid]    ~ N(0, 1)          target of the loss 0.5*||h_K - y||^2
+6. ``dt``    [B]           ~ U(0.5, 1.5) when ``dt_per_sample``; else the scalar 1.0
+
+``b`` is all zeros.  When the workload stores activations and weights in
+bf16, x, h0, W_in and W_rec are quantised to bf16 (round to nearest even)
+after drawing; the arrays stay float32 but every value is bf16-exact.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+MATH_FP32 = 0
+MATH_TF32 = 1
+MATH_BF16 = 2
+MATH_NAMES = {MATH_FP32: "fp32", MATH_TF32: "tf32", MATH_BF16: "bf16"}
+
+GRAD_SCRATCH = 0
+GRAD_GEMM = 1
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    K: int
+    n_in: int
+    n_hid: int
+    math: int = MATH_FP32
+    grad_path: int = GRAD_SCRATCH
+    h0_std: float = 1.0
+    dt_per_sample: bool = False
+    seed: int = 0
+
+    @property
+    def N(self) -> int:
+        """Packed per-sample parameter-gradient length 3*(n_in+n_hid+1)*n_hid."""
+        return 3 * (self.n_in + self.n_hid + 1) * self.n_hid
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five configurations of the method's benchmark suite.
+TINY = Workload("tiny_B4_K8_16x32_fp32", B=4, K=8, n_in=16, n_hid=32)
+SMOKE = Workload("smoke_B32_K64_64x128_fp32", B=32, K=64, n_in=64, n_hid=128)
+MID = Workload("mid_B1024_K64_64x128_tf32", B=1024, K=64, n_in=64, n_hid=128,
+               math=MATH_TF32, grad_path=GRAD_GEMM)
+LARGE = Workload("large_B8192_K8_128x256_bf16", B=8192, K=8, n_in=128, n_hid=256,
+                 math=MATH_BF16, grad_path=GRAD_GEMM, h0_std=0.5, dt_per_sample=True)
+WORKLOADS = {w.name: w for w in (TINY, SMOKE, MID, LARGE)}
+SHORT_NAMES = {"tiny": TINY, "smoke": SMOKE, "mid": MID, "large": LARGE}
+
+# Standalone reduce_axis0 cases: [B, N] fp32 ~ N(0, 1).
+REDUCE_BATCHES = (32, 256, 1024)
+REDUCE_TAILS = (40960, 40961)
+
+
+def bf16_quantise(a: np.ndarray) -> np.ndarray:
+    """Quantise float32 values to the nearest bf16 (ties to even), kept as float32.
+
+    Used only to synthesise bf16-valued inputs.
+    """
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def make_inputs(w: Workload, seed: int | None = None) -> dict:
+    """Draw the inputs of workload ``w`` (all float32 numpy arrays)."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+    x = rng.standard_normal((B, K, n_in), dtype=np.float64).astype(np.float32)
+    h0 = (rng.standard_normal((B, H), dtype=np.float64) * w.h0_std).astype(np.float32)
+    a_in = 1.0 / np.sqrt(n_in)
+    a_rec = 1.0 / np.sqrt(H)
+    W_in = rng.uniform(-a_in, a_in, size=(3, H, n_in)).astype(np.float32)
+    W_rec = rng.uniform(-a_rec, a_rec, size=(3, H, H)).astype(np.float32)
+    y = rng.standard_normal((B, H), dtype=np.float64).astype(np.float32)
+    if w.dt_per_sample:
+        dt = rng.uniform(0.5, 1.5, size=(B,)).astype(np.float32)
+    else:
+        dt = np.full((1,), 1.0, dtype=np.float32)
+    b = np.zeros((3, H), dtype=np.float32)
+    if w.math == MATH_BF16:
+        x, h0, W_in, W_rec = (bf16_quantise(a) for a in (x, h0, W_in, W_rec))
+    return dict(x=x, h0=h0, W_in=W_in, W_rec=W_rec, b=b, dt=dt, y=y)
+
+
+def make_reduce_input(B: int, N: int, seed: int = 0) -> np.ndarray:
+    """[B, N] float32 ~ N(0, 1) for the standalone reduce_axis0 cases."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((B, N), dtype=np.float32)
