@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the batched CfC K-loop (forward + backward through time +
+deterministic gradient reduction) on one GB300, printing ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload smoke|tiny|mid|large]
+                  [--impl ours|reference] [--no-secondary]
+
+A step is one pass of the whole path over one batch of synthetic input:
+cfc_kloop_forward followed by cfc_kloop_backward with the loss seed
+0.5*||h_K - y||^2 (which ends in reduce_axis0 of the gradient partials).
+Inputs are resident in device memory; L2 is flushed between timed steps by
+writing a 512 MiB buffer (outside the per-step events).  Throughput is
+samples*steps per second (B*K / step time).  For N > 1 (torchrun) every rank
+runs an independent replica of the workload on its own GPU (there is no
+exchange step on this path in a single-GPU deployment), timing is the max
+over ranks and the value is the total over ranks.
+
+--impl reference times the CPU oracle (numpy, single BLAS thread) on a
+bounded sample of the same workload.
+"""
+
+import os
+
+# The CPU oracle leg is timed single-threaded: pin BLAS threads before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from recurrent_cell_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "CfC K-loop fwd+bwd samples·steps/sec; reduce_axis0 GB/s; % roofline"
+UNIT = "samples·steps/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            p = json.load(fh)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sust=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    sm_max_mhz=float(p.get("sm_max_mhz", 2070.0)), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sust=1700.0,
+                    sm_max_mhz=2070.0, source="fallback")
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    """FFMA peak: SMs x 128 fp32 lanes x 2 flop x SM clock."""
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------
+# per-kernel algorithmic work (per launch) for the roofline
+# ----------------------------------------------------------------------------
+
+def kernel_work(name, w, n_split):
+    """(bound, amount per launch, unit) for a kernel of workload w."""
+    B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+    Zc, H3 = n_in + H, 3 * H
+    s = 2 if w.math == wl.MATH_BF16 else 4
+    if name.startswith("cfc_fwd") or name.startswith("cfc_bwd"):
+        return ("flop", 2.0 * B * K * H3 * Zc)
+    if name.startswith("wgrad"):
+        return ("flop", 2.0 * B * K * H3 * (Zc + 1))
+    if name == "reduce_axis0":
+        N = w.N
+        return ("byte", 4.0 * (n_split * N + N))
+    if name == "prep_wt":
+        return ("byte", 2.0 * H3 * Zc * s)
+    return ("byte", 0.0)
+
+
+def roofline_for(name, w, n_split, avg_ms, peaks, sustained):
+    kind, amount = kernel_work(name, w, n_split)
+    if kind == "byte":
+        achieved = amount / (avg_ms * 1e-3) / 1e9
+        peak = peaks["hbm"]
+        return dict(kernel=name, bound="hbm", achieved=achieved, peak=peak, unit="GB/s",
+                    frac=achieved / peak, traffic=None, algorithmic_per_launch=amount,
+                    peak_source=f"{peaks['source']} hbm_gbs")
+    achieved = amount / (avg_ms * 1e-3) / 1e12
+    # SIMT kernels run fp32 FFMA on the CUDA cores: ALU bound against the FFMA peak.
+    peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+    return dict(kernel=name, bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s",
+                frac=achieved / peak, traffic=None, algorithmic_per_launch=amount,
+                peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz")
+
+
+# ----------------------------------------------------------------------------
+# clocks sampler
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.lines = []
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        cmd = [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[2:6]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+class Path:
+    """Device-resident buffers for one workload and the step = fwd + bwd."""
+
+    def __init__(self, w, device):
+        import torch
+        import recurrent_cell_gb300 as cfc
+        self.torch, self.cfc, self.w = torch, cfc, w
+        inp = wl.make_inputs(w)
+        st = torch.bfloat16 if w.math == wl.MATH_BF16 else torch.float32
+        self.st = st
+        B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+        f32 = torch.float32
+        self.host = {k: torch.from_numpy(v).to(dtype=(st if k in ("x", "h0", "W_in", "W_rec") else f32))
+                     .pin_memory() for k, v in inp.items()}
+        self.t = {k: v.to(device) for k, v in self.host.items()}
+        self.ws = torch.empty(cfc.cfc_kloop_workspace_bytes(B, K, n_in, H, w.math, w.grad_path),
+                              dtype=torch.uint8, device=device)
+        self.h_seq = torch.empty(B, K, H, dtype=st, device=device)
+        self.gWi = torch.empty(3, H, n_in, device=device)
+        self.gWr = torch.empty(3, H, H, device=device)
+        self.gb = torch.empty(3, H, device=device)
+        self.scratch = (torch.empty(B, w.N, device=device) if w.grad_path == wl.GRAD_SCRATCH else None)
+        self.out_host = [torch.empty(t.shape, dtype=f32).pin_memory() for t in (self.gWi, self.gWr, self.gb)]
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.d2h_bytes = sum(v.numel() * v.element_size() for v in self.out_host)
+        # split count of the GEMM gradient path (as the library computes it)
+        if w.grad_path == wl.GRAD_SCRATCH:
+            self.n_split = B
+        else:
+            tiles = ((3 * H + 63) // 64) * ((n_in + H + 1 + 63) // 64)
+            split = max(1, min(-(-4 * SM_COUNT // tiles), min(B * K, 256)))
+            rps = -(-(B * K) // split)
+            self.n_split = -(-(B * K) // rps)
+
+    def step(self):
+        t, cfc, w = self.t, self.cfc, self.w
+        cfc.cfc_kloop_forward(t["x"], t["h0"], t["W_in"], t["W_rec"], t["b"], t["dt"], self.h_seq,
+                              self.ws, math=w.math)
+        cfc.cfc_kloop_backward(t["x"], t["h0"], t["W_in"], t["W_rec"], t["b"], t["dt"], self.h_seq,
+                               self.gWi, self.gWr, self.gb, self.ws, y=t["y"],
+                               per_sample_scratch=self.scratch, grad_path=w.grad_path, math=w.math)
+
+    def step_e2e(self):
+        for k, v in self.host.items():
+            self.t[k].copy_(v, non_blocking=True)
+        self.step()
+        for dst, src in zip(self.out_host, (self.gWi, self.gWr, self.gb)):
+            dst.copy_(src, non_blocking=True)
+
+
+def timed(torch, fn, steps, flush=None):
+    """Per-step CUDA-event times (ms) on the current stream; flush between steps."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        if flush is not None:
+            flush()
+        s.record()
+        fn()
+        e.record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def summarize_trace(records, steps):
+    per = {}
+    for name, ms in records:
+        d = per.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += ms
+    total = sum(v[1] for v in per.values()) or 1.0
+    return {n: dict(launches=v[0], launches_per_step=v[0] / steps, ms_total=v[1],
+                    avg_ms=v[1] / v[0], share=v[1] / total) for n, v in per.items()}
+
+
+def measure_workload(w, steps, warmup, device, peaks, flush, dist_ctx=None, with_e2e=True):
+    import torch
+    import recurrent_cell_gb300 as cfc
+    p = Path(w, device)
+    for _ in range(warmup):
+        p.step()
+    torch.cuda.synchronize()
+    if dist_ctx:
+        dist_ctx.barrier()
+    torch.cuda.synchronize()
+    cfc.cfc_trace_enable(True)
+    ms = timed(torch, p.step, steps, flush)
+    records = cfc.cfc_trace_records()
+    cfc.cfc_trace_enable(False)
+    torch.cuda.synchronize()
+    if dist_ctx:
+        dist_ctx.barrier()
+    ms_step = sum(ms) / len(ms)
+    kernels = summarize_trace(records, steps)
+    top = max(kernels, key=lambda n: kernels[n]["ms_total"])
+    roof = roofline_for(top, w, p.n_split, kernels[top]["avg_ms"], peaks, sustained=False)
+    out = dict(ms_per_step=ms_step, ms_per_step_median=statistics.median(ms), kernels=kernels,
+               roofline=roof, gpu_launches=len(records), n_split=p.n_split)
+    if with_e2e:
+        e2e_steps = max(3, min(steps, 50))
+        for _ in range(2):
+            p.step_e2e()
+        torch.cuda.synchronize()
+        ems = timed(torch, p.step_e2e, e2e_steps, flush)
+        out["e2e_ms"] = sum(ems) / len(ems)
+        out["h2d"] = p.h2d_bytes
+        out["d2h"] = p.d2h_bytes
+    del p
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_reduce(B, N, steps, device, peaks, flush):
+    import torch
+    import recurrent_cell_gb300 as cfc
+    a = torch.from_numpy(wl.make_reduce_input(B, N, seed=B + N)).to(device)
+    out = torch.empty(N, device=device)
+    for _ in range(3):
+        cfc.reduce_axis0(a, out)
+    torch.cuda.synchronize()
+    ms = timed(torch, lambda: cfc.reduce_axis0(a, out), steps, flush)
+    avg = sum(ms) / len(ms)
+    gbs = 4.0 * (B * N + N) / (avg * 1e-3) / 1e9
+    return dict(B=B, N=N, ms=avg, GBps=gbs, frac_of_hbm=gbs / peaks["hbm"])
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+
+def oracle_sample_batch(w):
+    """Samples per oracle call: the whole batch when small, else a slice
+    (samples are independent, so throughput scales with the slice)."""
+    return min(w.B, {wl.MATH_FP32: 64}.get(w.math, 128))
+
+
+def time_oracle(w, seconds=10.0, max_reps=None):
+    import oracle
+    b = oracle_sample_batch(w)
+    inp = wl.make_inputs(w)
+    sl = {k: (v[:b] if k in ("x", "h0", "y") or (k == "dt" and v.size > 1) else v) for k, v in inp.items()}
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.backward(sl["x"], sl["h0"], sl["W_in"], sl["W_rec"], sl["b"], sl["dt"], mode=w.math,
+                        y=sl["y"], per_sample=(w.grad_path == wl.GRAD_SCRATCH))
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_reps and reps >= max_reps):
+            break
+    value = reps * b * w.K / el
+    return dict(value=value, unit=UNIT, cores=1, kind="oracle",
+                sample=f"{reps} x oracle fwd+bwd on {b} of {w.B} samples, K={w.K} "
+                       f"({el:.1f} s, numpy float64, 1 BLAS thread)"), el / reps
+
+
+# ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="smoke", choices=sorted(wl.SHORT_NAMES))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    w = wl.SHORT_NAMES[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        per_step = []
+        for _ in range(args.warmup):
+            time_oracle(w, seconds=0.0, max_reps=1)
+        for _ in range(args.steps):
+            _, t = time_oracle(w, seconds=0.0, max_reps=1)
+            per_step.append(t)
+        b = oracle_sample_batch(w)
+        value = b * w.K / (sum(per_step) / len(per_step))
+        line = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus,
+                    steps=args.steps, warmup=args.warmup,
+                    ms_per_step=1e3 * sum(per_step) / len(per_step), higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype="f64",
+                    data="synthetic",
+                    config=dict(workload=w.name, B=w.B, K=w.K, n_in=w.n_in, n_hid=w.n_hid,
+                                math=wl.MATH_NAMES[w.math], sample_batch=b),
+                    cpu_baseline=dict(kind="oracle", cores=1, value=value, unit=UNIT,
+                                      sample=f"each step: oracle fwd+bwd on {b} of {w.B} samples"),
+                    e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dist_ctx = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist_ctx = dist
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = lambda: flush_buf.fill_(1.0)  # noqa: E731
+
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else uuid
+    sampler = ClockSampler(str(uuid) if uuid else None)
+    main_res = measure_workload(w, args.steps, args.warmup, device, peaks, flush, dist_ctx)
+    clocks = sampler.stop()
+
+    ms = main_res["ms_per_step"]
+    if dist_ctx:
+        t = torch.tensor([ms], device=device)
+        dist_ctx.all_reduce(t, op=dist_ctx.ReduceOp.MAX)
+        ms = float(t.item())
+        e = torch.tensor([main_res["e2e_ms"]], device=device)
+        dist_ctx.all_reduce(e, op=dist_ctx.ReduceOp.MAX)
+        main_res["e2e_ms"] = float(e.item())
+    units = w.B * w.K * world
+    value = units / (ms * 1e-3)
+
+    secondary = {}
+    cpu = None
+    if rank == 0 and not args.no_secondary and world == 1:
+        for name in ("mid", "large"):
+            if name == args.workload:
+                continue
+            ow = wl.SHORT_NAMES[name]
+            r = measure_workload(ow, max(5, min(args.steps, 30)), 3, device, peaks, flush, None,
+                                 with_e2e=False)
+            secondary[ow.name] = dict(value=ow.B * ow.K / (r["ms_per_step"] * 1e-3), unit=UNIT,
+                                      ms_per_step=r["ms_per_step"], roofline=r["roofline"],
+                                      kernels=r["kernels"])
+        red = [measure_reduce(B, N, 20, device, peaks, flush)
+               for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
+        secondary["reduce_axis0"] = red
+    if rank == 0 and world == 1:
+        cpu, _ = time_oracle(w, seconds=args.cpu_seconds)
+    if rank != 0:
+        return 0
+    line = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype={wl.MATH_FP32: "f32", wl.MATH_TF32: "tf32", wl.MATH_BF16: "bf16"}[w.math],
+        data="synthetic",
+        config=dict(workload=w.name, B=w.B, K=w.K, n_in=w.n_in, n_hid=w.n_hid,
+                    math=wl.MATH_NAMES[w.math],
+                    grad_path="scratch+reduce_axis0" if w.grad_path == wl.GRAD_SCRATCH else "gemm+reduce_axis0",
+                    l2="flushed between timed steps (512 MiB write, outside the step events)",
+                    parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        roofline=main_res["roofline"],
+        e2e=dict(value=units / (main_res["e2e_ms"] * 1e-3), unit=UNIT,
+                 h2d_bytes_per_step=main_res["h2d"], d2h_bytes_per_step=main_res["d2h"]),
+        gpu_launches=main_res["gpu_launches"],
+        clocks=clocks,
+        kernels=main_res["kernels"],
+    )
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if secondary:
+        line["secondary"] = secondary
+    print(json.dumps(line))
+    if dist_ctx:
+        dist_ctx.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

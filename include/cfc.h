@@ -1,0 +1,168 @@
+/*
+ * cfc.h -- C ABI of the batched CfC K-loop library for one NVIDIA GB300 (sm_103a).
+ *
+ * Three operations:
+ *
+ *   cfc_kloop_forward   the three-head closed-form continuous-time (CfC) cell
+ *                       run over K steps for B independent samples;
+ *   cfc_kloop_backward  backward through time: parameter gradients summed over
+ *                       the batch, grad_h0 and (optionally) grad_x;
+ *   reduce_axis0        deterministic, atomic-free column sum [B, N] -> [N].
+ *
+ * Cell (per sample, step k = 0..K-1, heads c = f, g, h~ in that order):
+ *   A_c    = b[c] + W_in[c] x_k + W_rec[c] h_k
+ *   g      = tanh(A_g),  hh = tanh(A_h~),  gate = sigmoid(-A_f * dt) = 1/(1+exp(A_f dt))
+ *   h_{k+1} = gate * g + (1 - gate) * hh,   h_seq[:, k] = h_{k+1}
+ * The per-sample pre-activation over row-major [n_hid, n_in] / [n_hid, n_hid]
+ * weights, tanh as the squashing function, the argument order of the backward,
+ * overwrite-vs-accumulate rules and the optional grad_x follow "K-loop
+ * Parallelization Implementation Plan", Tasks 2 and 3 (cfc_step_batched and
+ * cfc_step_backward_batched).  The reducer follows Task 1 of that page
+ * (reduce_axis0: argument order, overwrite, summation order).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer.  Nothing is allocated, freed or synchronised inside a call.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and runs asynchronously in stream order.
+ *   - A non-zero return value means the arguments were rejected (nothing was
+ *     launched) or a launch failed; cfc_status_string() names the reason.
+ *   - Results are bit-identical from run to run for the same inputs,
+ *     configuration and GPU model: no atomics, fixed summation orders.
+ *   - Layouts are dense row-major with the last index fastest.
+ *
+ * Precision modes (`math`):
+ *   CFC_MATH_FP32  x, h0, W_in, W_rec, h_seq are float; all arithmetic fp32.
+ *   CFC_MATH_TF32  same storage as FP32; every operand of the projections and
+ *                  gradient contractions (x, h, W, dA) is rounded to TF32 (10
+ *                  mantissa bits, nearest, ties away from zero), products are
+ *                  accumulated in fp32.  Activations and state stay fp32.
+ *   CFC_MATH_BF16  x, h0, W_in, W_rec and h_seq are bfloat16 (raw 16-bit);
+ *                  b, dt, y, grad inputs and all gradient outputs are float.
+ *                  h_{k+1} is rounded to bf16 (nearest even) and that value is
+ *                  stored and carried; dA is rounded to bf16 before the
+ *                  gradient contractions; accumulation is fp32.
+ */
+#ifndef CFC_H_
+#define CFC_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CFC_OK = 0,
+  CFC_ERR_NULL = -1,      /* a required pointer is NULL                        */
+  CFC_ERR_SHAPE = -2,     /* a size is negative, zero where not allowed, or too large */
+  CFC_ERR_ALIGN = -3,     /* a pointer is not aligned to its element size      */
+  CFC_ERR_WORKSPACE = -4, /* workspace NULL or smaller than cfc_kloop_workspace_bytes() */
+  CFC_ERR_MODE = -5,      /* unknown math mode or gradient path                */
+  CFC_ERR_LAUNCH = -6,    /* a kernel launch failed (cudaGetLastError != 0)    */
+  CFC_ERR_DEVICE = -7     /* no usable CUDA device / unsupported architecture  */
+} cfc_status;
+
+typedef enum { CFC_MATH_FP32 = 0, CFC_MATH_TF32 = 1, CFC_MATH_BF16 = 2 } cfc_math;
+
+/* How the per-sample parameter gradients are summed over the batch.
+ *   CFC_GRAD_SCRATCH: each sample's packed gradient row (length N, below) is
+ *     written once to a caller-provided per_sample_scratch[B, N] (overwrite;
+ *     the K steps are summed on chip), then reduce_axis0 sums the B rows.
+ *     This is the pages' per-batch scratch + reducer scheme ("K-loop
+ *     Parallelization Implementation Plan", Tasks 3-5).
+ *   CFC_GRAD_GEMM: the gradients are contracted directly over all B*K rows
+ *     (dW = dA^T [x; h; 1]) as one batch-dimension GEMM with a fixed split
+ *     over row blocks; the split partials live in the workspace and are summed
+ *     by reduce_axis0 ("kernel-optimization" plan, Task 2 Step 3: weight
+ *     gradient as a batch-dimension GEMM).
+ * Packed per-sample layout, N = 3*(n_in + n_hid + 1)*n_hid floats:
+ *   [ gW_in (c, i, j) : 3*n_hid*n_in | gW_rec (c, i, j) : 3*n_hid*n_hid | gb (c, i) : 3*n_hid ] */
+typedef enum { CFC_GRAD_SCRATCH = 0, CFC_GRAD_GEMM = 1 } cfc_grad_path;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* cfc_status_string(int status);
+
+/* N = 3*(n_in + n_hid + 1)*n_hid, or 0 for invalid sizes. Host-only. */
+long long cfc_per_sample_length(int n_in, int n_hid);
+
+/* Bytes of device workspace that cfc_kloop_forward and cfc_kloop_backward
+ * need for these sizes (the same value for both calls).  Host-only; returns 0
+ * for invalid arguments.  The forward stores the activations of every step
+ * there and the backward reads them, so the same workspace, untouched, must be
+ * passed to the backward of the same inputs. */
+size_t cfc_kloop_workspace_bytes(int B, int K, int n_in, int n_hid, int math, int grad_path);
+
+/* Forward K-loop.
+ *   x      [B, K, n_in]      (float or bf16 by `math`)
+ *   h0     [B, n_hid]        (float or bf16)
+ *   W_in   [3, n_hid, n_in]  heads f, g, h~ (float or bf16)
+ *   W_rec  [3, n_hid, n_hid] (float or bf16)
+ *   b      [3, n_hid]        float
+ *   dt     [B] float if dt_stride == 1, or one float broadcast if dt_stride == 0
+ *   h_seq  [B, K, n_hid]     OUTPUT, overwrite: h_seq[:, k] = h_{k+1}
+ *   workspace / workspace_bytes: see cfc_kloop_workspace_bytes.
+ * Requirements: B >= 1, K >= 1, 1 <= n_in, 1 <= n_hid <= 1024, n_in + n_hid <= 1024;
+ * every pointer aligned to 16 bytes. */
+int cfc_kloop_forward(const void* x, const void* h0, const void* W_in, const void* W_rec,
+                      const float* b, const float* dt, int dt_stride,
+                      int B, int K, int n_in, int n_hid, int math,
+                      void* h_seq, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward through the K loop of the forward that wrote `workspace`.
+ * Inputs as in the forward, plus
+ *   h_seq        [B, K, n_hid] as written by that forward
+ *   grad_h_seq   [B, K, n_hid] float or NULL: upstream gradient of every h_seq[:, k]
+ *   grad_h_last  [B, n_hid] float or NULL: extra upstream gradient of h_K
+ *   y            [B, n_hid] float or NULL: target of the loss 0.5*||h_K - y||^2;
+ *                adds h_K - y to the gradient of h_K
+ * Outputs (all overwrite; the three parameter gradients are summed over B):
+ *   grad_W_in [3, n_hid, n_in], grad_W_rec [3, n_hid, n_hid], grad_b [3, n_hid]
+ *   grad_h0   [B, n_hid] or NULL
+ *   grad_x    [B, K, n_in] or NULL (as in the pages' backward, grad_x is optional)
+ *   per_sample_scratch [B, N] float: required for CFC_GRAD_SCRATCH (it then
+ *                holds each sample's packed gradient), ignored (may be NULL)
+ *                for CFC_GRAD_GEMM.
+ * At least one upstream gradient (grad_h_seq, grad_h_last or y) must be given. */
+int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const void* W_rec,
+                       const float* b, const float* dt, int dt_stride,
+                       int B, int K, int n_in, int n_hid, int math,
+                       const void* h_seq, const float* grad_h_seq, const float* grad_h_last,
+                       const float* y,
+                       float* grad_W_in, float* grad_W_rec, float* grad_b,
+                       float* grad_h0, float* grad_x,
+                       float* per_sample_scratch, int grad_path,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Column sum of a row-major [n_batch, n_tail] float matrix into out[n_tail]
+ * (overwrite), atomic-free, in a fixed association order that is bit-identical
+ * to the pages' reference reducer ("K-loop Parallelization Implementation
+ * Plan", Task 1): with 256 partial sums,
+ *   p[t] = ((0.0f + in[t]) + in[t+256]) + in[t+512] + ...,  t = 0..255,
+ * then p[t] += p[t+s] for s = 128, 64, ..., 1 and t < s;  out[j] = p[0].
+ * n_batch == 0 writes +0.0f.  n_batch >= 0, 0 <= n_tail <= 2^35; per_batch and
+ * out must be 4-byte aligned and must not overlap (16-byte alignment and
+ * n_tail % 4 == 0 select the float4 path; otherwise scalar, same order). */
+int reduce_axis0(const float* per_batch, int n_batch, long long n_tail, float* out, void* stream);
+
+/* Kernel tracing (diagnostics, off by default).  While enabled, every kernel
+ * that this library launches is bracketed by two CUDA events recorded on its
+ * launch stream, so per-kernel device time can be read back afterwards.
+ * Host-side state, not thread-safe; the events are created by the library
+ * (the only resources it creates), so do not enable tracing inside CUDA-graph
+ * capture.
+ *   cfc_trace_enable(on): clears all records; on != 0 starts recording.
+ *   cfc_trace_count():    number of recorded launches.
+ *   cfc_trace_get(i, &name, &ms): kernel name (static string) and device time
+ *                         in milliseconds of record i; waits for that record's
+ *                         stop event.  Returns CFC_OK or CFC_ERR_SHAPE for a
+ *                         bad index. */
+int cfc_trace_enable(int on);
+int cfc_trace_count(void);
+int cfc_trace_get(int i, const char** name, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CFC_H_ */

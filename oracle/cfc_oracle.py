@@ -109,8 +109,11 @@ def cell_forward(x_k, h_k, W_in, W_rec, b, dt, mode: int = FP32):
     ho = _operand(h_k, mode)
     Wi = _operand(W_in, mode)
     Wr = _operand(W_rec, mode)
-    bb = np.asarray(b, dtype=np.float64)
-    A = bb[None] + np.einsum("cij,nj->nci", Wi, xo) + np.einsum("cij,nj->nci", Wr, ho)
+    n = xo.shape[0]
+    H = Wr.shape[1]
+    # A[n, c, i] = b[c, i] + sum_j W_in[c, i, j] x[n, j] + sum_j W_rec[c, i, j] h[n, j]
+    A = (np.asarray(b, dtype=np.float64).reshape(1, 3 * H)
+         + xo @ Wi.reshape(3 * H, -1).T + ho @ Wr.reshape(3 * H, H).T).reshape(n, 3, H)
     f = A[:, 0]
     g = np.tanh(A[:, 1])
     hh = np.tanh(A[:, 2])
@@ -148,7 +151,7 @@ def per_sample_length(n_in: int, H: int) -> int:
 
 
 def backward(x, h0, W_in, W_rec, b, dt, mode: int = FP32,
-             grad_h_seq=None, grad_h_last=None, y=None) -> dict:
+             grad_h_seq=None, grad_h_last=None, y=None, per_sample: bool = True) -> dict:
     """Backward through the K loop.
 
     Upstream gradient of h_seq[:, k] is grad_h_seq[:, k] (optional); the last
@@ -161,13 +164,18 @@ def backward(x, h0, W_in, W_rec, b, dt, mode: int = FP32,
       dA_f = -dt * delta * (g - hh) * gate * (1 - gate)
       carry      = sum_c W_rec[c]^T dA_c
       grad_x[k]  = sum_c W_in[c]^T  dA_c
-      gW_in[c]  += dA_c (x) x_k,  gW_rec[c] += dA_c (x) h_k,  gb[c] += dA_c
-    grad_h0 = carry after step 0.
+    grad_h0 = carry after step 0.  The parameter gradients are the sums over
+    all rows r = (b, k) of the outer products dA_r (x) [x_r; h_r; 1]:
+      gW_in[c] = sum dA_c (x) x_k,  gW_rec[c] = sum dA_c (x) h_k,  gb[c] = sum dA_c
+    taken as one matrix product over the B*K rows (the batch-dimension GEMM of
+    the "kernel-optimization" plan, Task 2 Step 3) and, per sample, over that
+    sample's K rows.
 
-    Returns per-sample packed gradients ``per_sample`` [B, N] laid out as
-    [gW_in (c, i, j) | gW_rec (c, i, j) | gb (c, i)], their float64 batch sums
-    ``grad_W_in`` [3, H, n_in], ``grad_W_rec`` [3, H, H], ``grad_b`` [3, H],
-    ``grad_h0`` [B, H], ``grad_x`` [B, K, n_in], ``h_seq`` and ``dA`` [B, K, 3, H].
+    Returns ``grad_W_in`` [3, H, n_in], ``grad_W_rec`` [3, H, H], ``grad_b``
+    [3, H] (float64 sums over the batch), ``grad_h0`` [B, H], ``grad_x``
+    [B, K, n_in], ``h_seq``, ``dA`` [B, K, 3, H] and, if ``per_sample``, the
+    packed per-sample gradients ``per_sample`` [B, N] laid out as
+    [gW_in (c, i, j) | gW_rec (c, i, j) | gb (c, i)].
     """
     x = np.asarray(x)
     B, K, n_in = x.shape
@@ -178,11 +186,8 @@ def backward(x, h0, W_in, W_rec, b, dt, mode: int = FP32,
     h_prev = np.concatenate(
         [_stored_state(np.asarray(h0, dtype=np.float64), mode)[:, None], h_seq[:, :-1]], axis=1)
 
-    Wi = _operand(W_in, mode)
-    Wr = _operand(W_rec, mode)
-    gW_in = np.zeros((B, 3, H, n_in))
-    gW_rec = np.zeros((B, 3, H, H))
-    gb = np.zeros((B, 3, H))
+    Wi = _operand(W_in, mode).reshape(3 * H, n_in)
+    Wr = _operand(W_rec, mode).reshape(3 * H, H)
     grad_x = np.zeros((B, K, n_in))
     dA_all = np.zeros((B, K, 3, H))
     carry = np.zeros((B, H))
@@ -202,17 +207,23 @@ def backward(x, h0, W_in, W_rec, b, dt, mode: int = FP32,
         dA[:, 0] = -dtv[:, None] * delta * (g - hh) * gate * (1.0 - gate)
         dAo = _operand(dA, mode)
         dA_all[:, k] = dAo
-        xo = _operand(x[:, k], mode)
-        ho = _operand(h_prev[:, k], mode)
-        gW_in += np.einsum("nci,nj->ncij", dAo, xo)
-        gW_rec += np.einsum("nci,nj->ncij", dAo, ho)
-        gb += dAo
-        grad_x[:, k] = np.einsum("cij,nci->nj", Wi, dAo)
-        carry = np.einsum("cij,nci->nj", Wr, dAo)
-    per_sample = np.concatenate(
-        [gW_in.reshape(B, -1), gW_rec.reshape(B, -1), gb.reshape(B, -1)], axis=1)
-    return dict(per_sample=per_sample, grad_W_in=gW_in.sum(0), grad_W_rec=gW_rec.sum(0),
-                grad_b=gb.sum(0), grad_h0=carry, grad_x=grad_x, h_seq=h_seq, dA=dA_all)
+        grad_x[:, k] = dAo.reshape(B, 3 * H) @ Wi
+        carry = dAo.reshape(B, 3 * H) @ Wr
+
+    # rows r = (b, k): z_r = [x_r; h_r; 1] as contraction operands
+    Z = np.concatenate([_operand(x, mode), _operand(h_prev, mode), np.ones((B, K, 1))], axis=2)
+    D = dA_all.reshape(B, K, 3 * H)
+    G = D.reshape(B * K, 3 * H).T @ Z.reshape(B * K, n_in + H + 1)       # [3H, n_in + H + 1]
+    out = dict(grad_W_in=G[:, :n_in].reshape(3, H, n_in),
+               grad_W_rec=G[:, n_in:n_in + H].reshape(3, H, H),
+               grad_b=G[:, n_in + H].reshape(3, H),
+               grad_h0=carry, grad_x=grad_x, h_seq=h_seq, dA=dA_all)
+    if per_sample:
+        Gs = np.matmul(D.transpose(0, 2, 1), Z)                           # [B, 3H, n_in + H + 1]
+        out["per_sample"] = np.concatenate(
+            [Gs[:, :, :n_in].reshape(B, -1), Gs[:, :, n_in:n_in + H].reshape(B, -1),
+             Gs[:, :, n_in + H].reshape(B, -1)], axis=1)
+    return out
 
 
 def unpack_per_sample(vec, n_in: int, H: int):

@@ -1,0 +1,112 @@
+// cfc_internal.cuh -- internal declarations shared by the CUDA translation
+// units of libcfc (not part of the public C ABI in include/cfc.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/cfc.h"
+
+namespace cfc {
+
+constexpr int kNumSMs = 152;  // GB300: 2 dies x 76 SMs
+
+// ---------------------------------------------------------------------------
+// Precision helpers.  The rounding points of each mode are part of the
+// method's definition (see include/cfc.h); both the SIMT and the tensor-core
+// kernels apply them at the same places.
+// ---------------------------------------------------------------------------
+
+// TF32 = binary32 with the low 13 significand bits cleared, rounded to nearest
+// with ties away from zero (add half of the dropped range to the magnitude).
+__device__ __forceinline__ float round_tf32(float v) {
+  uint32_t u = __float_as_uint(v);
+  u = (u + 0x1000u) & 0xFFFFE000u;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ float round_bf16(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Value of a float as it enters a contraction in mode MODE.
+template <int MODE>
+__device__ __forceinline__ float to_operand(float v) {
+  if constexpr (MODE == CFC_MATH_TF32) return round_tf32(v);
+  else if constexpr (MODE == CFC_MATH_BF16) return round_bf16(v);
+  else return v;
+}
+
+// Load an element of storage type T as float.
+__device__ __forceinline__ float ldf(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// Load of a stored operand (x, h, W) already in the mode's operand form when
+// stored as bf16; fp32 storage is rounded for TF32.
+template <int MODE, typename T>
+__device__ __forceinline__ float ld_operand(const T* p) {
+  if constexpr (sizeof(T) == 2) return ldf(p);
+  else return to_operand<MODE>(ldf(p));
+}
+
+__device__ __forceinline__ void stf(float* p, float v) { *p = v; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// Workspace layout (byte offsets, every region 256-byte aligned).
+// ---------------------------------------------------------------------------
+struct Layout {
+  int B, K, n_in, H, Zc, H3, math, grad_path;
+  size_t elem;          // bytes of a stored x/h/W element (4 or 2)
+  size_t dA_elem;       // bytes of a stored dA element (4 or 2)
+  long long N;          // packed per-sample gradient length
+  long long R;          // B*K rows of the gradient contraction
+  int n_split;          // row blocks of the GEMM-path contraction
+  long long rows_per_split;
+  size_t off_wt, off_act, off_dA, off_part, total;
+};
+
+bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Layout* L);
+
+// ---------------------------------------------------------------------------
+// Optional kernel tracing (see cfc_trace_enable in include/cfc.h).
+// ---------------------------------------------------------------------------
+void trace_begin(const char* name, cudaStream_t s);
+void trace_end(cudaStream_t s);
+
+struct TraceScope {
+  cudaStream_t s;
+  TraceScope(const char* name, cudaStream_t st) : s(st) { trace_begin(name, s); }
+  ~TraceScope() { trace_end(s); }
+};
+
+// ---------------------------------------------------------------------------
+// Launchers (return cudaError_t of the launch).
+// ---------------------------------------------------------------------------
+struct ReduceOut {
+  float* ptr[3];
+  long long begin[3];
+  int nseg;
+};
+
+cudaError_t launch_reduce(const float* in, int n_batch, long long n_tail, long long ld,
+                          const ReduceOut& out, cudaStream_t stream);
+
+struct CfcArgs {
+  const void* x; const void* h0; const void* W_in; const void* W_rec;
+  const float* b; const float* dt; int dt_stride;
+  void* h_seq;
+  const float* grad_h_seq; const float* grad_h_last; const float* y;
+  float* grad_W_in; float* grad_W_rec; float* grad_b; float* grad_h0; float* grad_x;
+  float* per_sample_scratch;
+  char* ws;
+};
+
+cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
+cudaError_t launch_backward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
+cudaError_t launch_wgrad_simt(const Layout& L, const CfcArgs& a, float* out, int n_split,
+                              long long rows_per_split, cudaStream_t s);
+
+}  // namespace cfc

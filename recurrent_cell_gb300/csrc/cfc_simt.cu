@@ -1,0 +1,418 @@
+// cfc_simt.cu -- CUDA-core (FFMA) kernels of the batched CfC K-loop.
+//
+//   k_prep_wt      W_cat^T [Zc, 3H] (Zc = n_in + H): transposed, mode-rounded
+//                  copy of [W_in | W_rec] so that a thread per hidden unit reads
+//                  weights with coalesced loads in the forward.
+//   k_cfc_fwd      persistent forward: one block per tile of BT samples, one
+//                  thread per hidden unit, the K loop inside the kernel.  The
+//                  operand vector z = [x_k; h_k] of the tile lives in shared
+//                  memory; h_{k+1} never leaves the block between steps.
+//   k_cfc_bwd      persistent reverse-K loop: one thread per hidden unit for
+//                  the elementwise dA, one thread per column of z for
+//                  dz = W_cat^T dA (grad_x | carry); writes dA of every step.
+//   k_wgrad        gradient contraction out[s] = sum_{rows r in block s}
+//                  dA[r]^T (x) [x_r; h_r; 1] written in the packed per-sample
+//                  layout (one row block per sample for the scratch path, or
+//                  a fixed split of all B*K rows for the GEMM path).
+//
+// Samples are independent through the whole K loop, so blocks never wait on
+// one another.  The pages' kernels ("K-loop Parallelization Implementation
+// Plan", Tasks 2-3) launch one block per sample per step and accumulate the
+// per-sample gradients with += in global scratch at every step; here the K
+// loop runs inside one launch and every gradient element is written once.
+#include <algorithm>
+
+#include "cfc_internal.cuh"
+
+namespace cfc {
+namespace {
+
+template <typename T, int MODE>
+__global__ void k_prep_wt(const T* __restrict__ W_in, const T* __restrict__ W_rec,
+                          int n_in, int H, T* __restrict__ WT) {
+  const int H3 = 3 * H, Zc = n_in + H;
+  const long long total = (long long)H3 * Zc;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int j = (int)(e / H3);
+    const int r = (int)(e - (long long)j * H3);
+    const float v = (j < n_in) ? ld_operand<MODE>(W_in + (long long)r * n_in + j)
+                               : ld_operand<MODE>(W_rec + (long long)r * H + (j - n_in));
+    stf(WT + e, v);
+  }
+}
+
+constexpr int kMaxThreads = 512;
+
+// Forward.  blockDim.x = min(512, round_up(H, 32)); dynamic smem = 2 * BT * Zc
+// floats: two copies of the operand tile z = [x_k; h_k] used alternately, so
+// step k reads one copy while h_{k+1} and x_{k+1} are written to the other and
+// a single barrier per step orders them.
+template <typename T, int MODE, int BT>
+__global__ void __launch_bounds__(kMaxThreads)
+k_cfc_fwd(const T* __restrict__ x, const T* __restrict__ h0, const T* __restrict__ WT,
+          const float* __restrict__ bias, const float* __restrict__ dt, int dt_stride,
+          int B, int K, int n_in, int H, T* __restrict__ h_seq, float* __restrict__ act) {
+  extern __shared__ float zbuf[];  // [2][BT][Zc]
+  const int Zc = n_in + H, H3 = 3 * H;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int b0 = blockIdx.x * BT;
+
+  for (int e = tid; e < BT * H; e += nthr) {
+    const int n = e / H, u = e - n * H, bb = b0 + n;
+    zbuf[n * Zc + n_in + u] = (bb < B) ? ld_operand<MODE>(h0 + (long long)bb * H + u) : 0.f;
+  }
+  for (int e = tid; e < BT * n_in; e += nthr) {
+    const int n = e / n_in, j = e - n * n_in, bb = b0 + n;
+    zbuf[n * Zc + j] = (bb < B) ? ld_operand<MODE>(x + (long long)bb * K * n_in + j) : 0.f;
+  }
+  float dtn[BT];
+#pragma unroll
+  for (int n = 0; n < BT; ++n) dtn[n] = (b0 + n < B) ? dt[dt_stride ? b0 + n : 0] : 0.f;
+  __syncthreads();
+
+  for (int k = 0; k < K; ++k) {
+    const float* zs = zbuf + (k & 1) * BT * Zc;
+    float* zn = zbuf + ((k + 1) & 1) * BT * Zc;
+    for (int i = tid; i < H; i += nthr) {
+      float af[BT], ag[BT], ah[BT];
+      const float bf = bias[i], bg = bias[H + i], bh = bias[2 * H + i];
+#pragma unroll
+      for (int n = 0; n < BT; ++n) { af[n] = bf; ag[n] = bg; ah[n] = bh; }
+      const T* w = WT + i;
+#pragma unroll 4
+      for (int j = 0; j < Zc; ++j) {
+        const float wf = ldf(w + (long long)j * H3);
+        const float wg = ldf(w + (long long)j * H3 + H);
+        const float wh = ldf(w + (long long)j * H3 + 2 * H);
+#pragma unroll
+        for (int n = 0; n < BT; ++n) {
+          const float z = zs[n * Zc + j];
+          af[n] = fmaf(wf, z, af[n]);
+          ag[n] = fmaf(wg, z, ag[n]);
+          ah[n] = fmaf(wh, z, ah[n]);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < BT; ++n) {
+        const int bb = b0 + n;
+        const float g = tanhf(ag[n]);
+        const float hh = tanhf(ah[n]);
+        const float gate = 1.f / (1.f + expf(af[n] * dtn[n]));
+        const float h = gate * g + (1.f - gate) * hh;
+        if (bb < B) {
+          const long long row = (long long)bb * K + k;
+          act[row * H3 + i] = gate;
+          act[row * H3 + H + i] = g;
+          act[row * H3 + 2 * H + i] = hh;
+          stf(h_seq + row * H + i, h);
+        }
+        float hop;
+        if constexpr (sizeof(T) == 2) hop = round_bf16(h);   // the stored bf16 state
+        else hop = to_operand<MODE>(h);
+        zn[n * Zc + n_in + i] = (bb < B) ? hop : 0.f;
+      }
+    }
+    if (k + 1 < K) {
+      for (int e = tid; e < BT * n_in; e += nthr) {
+        const int n = e / n_in, j = e - n * n_in, bb = b0 + n;
+        zn[n * Zc + j] = (bb < B) ? ld_operand<MODE>(x + ((long long)bb * K + k + 1) * n_in + j) : 0.f;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Backward.  blockDim.x = min(512, round_up(Zc, 32)); dynamic smem = BT * 4H floats.
+template <typename T, typename DT, int MODE, int BT>
+__global__ void __launch_bounds__(kMaxThreads)
+k_cfc_bwd(const T* __restrict__ W_in, const T* __restrict__ W_rec,
+          const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H,
+          const T* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
+          const float* __restrict__ grad_h_last, const float* __restrict__ y,
+          const float* __restrict__ act, DT* __restrict__ dA_out,
+          float* __restrict__ grad_h0, float* __restrict__ grad_x) {
+  extern __shared__ float sm[];
+  const int Zc = n_in + H, H3 = 3 * H;
+  float* dAs = sm;               // [BT][3H] operand values of dA
+  float* carry = sm + BT * H3;   // [BT][H]   gradient reaching h_{k+1} through step k+1
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int b0 = blockIdx.x * BT;
+
+  for (int e = tid; e < BT * H; e += nthr) carry[e] = 0.f;
+  float dtn[BT];
+#pragma unroll
+  for (int n = 0; n < BT; ++n) dtn[n] = (b0 + n < B) ? dt[dt_stride ? b0 + n : 0] : 0.f;
+  __syncthreads();
+
+  for (int k = K - 1; k >= 0; --k) {
+    for (int i = tid; i < H; i += nthr) {
+#pragma unroll
+      for (int n = 0; n < BT; ++n) {
+        const int bb = b0 + n;
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+        if (bb < B) {
+          const long long row = (long long)bb * K + k;
+          float delta = carry[n * H + i];
+          if (grad_h_seq) delta += grad_h_seq[row * H + i];
+          if (k == K - 1) {
+            if (grad_h_last) delta += grad_h_last[(long long)bb * H + i];
+            if (y) delta += ldf(h_seq + row * H + i) - y[(long long)bb * H + i];
+          }
+          const float gate = act[row * H3 + i];
+          const float g = act[row * H3 + H + i];
+          const float hh = act[row * H3 + 2 * H + i];
+          d1 = delta * gate * (1.f - g * g);
+          d2 = delta * (1.f - gate) * (1.f - hh * hh);
+          d0 = -dtn[n] * delta * (g - hh) * gate * (1.f - gate);
+          d0 = to_operand<MODE>(d0);
+          d1 = to_operand<MODE>(d1);
+          d2 = to_operand<MODE>(d2);
+          stf(dA_out + row * H3 + i, d0);
+          stf(dA_out + row * H3 + H + i, d1);
+          stf(dA_out + row * H3 + 2 * H + i, d2);
+        }
+        dAs[n * H3 + i] = d0;
+        dAs[n * H3 + H + i] = d1;
+        dAs[n * H3 + 2 * H + i] = d2;
+      }
+    }
+    __syncthreads();
+    // dz[j] = sum_r W_cat[r, j] dA[r]: column j of W_cat = [W_in | W_rec]
+    // (coalesced over j).  carry is not read in this phase, so it is
+    // overwritten in place.
+    for (int j = tid; j < Zc; j += nthr) {
+      const T* wcol = (j < n_in) ? (W_in + j) : (W_rec + (j - n_in));
+      const int ldw = (j < n_in) ? n_in : H;
+      float acc[BT];
+#pragma unroll
+      for (int n = 0; n < BT; ++n) acc[n] = 0.f;
+#pragma unroll 4
+      for (int r = 0; r < H3; ++r) {
+        const float w = ld_operand<MODE>(wcol + (long long)r * ldw);
+#pragma unroll
+        for (int n = 0; n < BT; ++n) acc[n] = fmaf(w, dAs[n * H3 + r], acc[n]);
+      }
+#pragma unroll
+      for (int n = 0; n < BT; ++n) {
+        const int bb = b0 + n;
+        if (j < n_in) {
+          if (grad_x && bb < B) grad_x[((long long)bb * K + k) * n_in + j] = acc[n];
+        } else {
+          carry[n * H + (j - n_in)] = acc[n];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (grad_h0) {
+    for (int e = tid; e < BT * H; e += nthr) {
+      const int n = e / H, u = e - n * H;
+      if (b0 + n < B) grad_h0[(long long)(b0 + n) * H + u] = carry[e];
+    }
+  }
+}
+
+// Gradient contraction, 64 x 64 output tile per block, 4 x 4 per thread.
+constexpr int kTM = 64, kTN = 64, kTR = 16;
+
+template <typename T, typename DT, int MODE>
+__global__ void __launch_bounds__(256)
+k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict__ h0,
+        const T* __restrict__ h_seq, int K, int n_in, int H, long long R,
+        long long rows_per_split, float* __restrict__ out) {
+  __shared__ float sA[kTR][kTM + 4];
+  __shared__ float sZ[kTR][kTN + 4];
+  const int H3 = 3 * H, Zc = n_in + H, Zb = Zc + 1;
+  const long long N = (long long)H3 * Zb;
+  const int m0 = blockIdx.x * kTM, j0 = blockIdx.y * kTN;
+  const long long s = blockIdx.z;
+  const long long r_begin = s * rows_per_split;
+  const long long r_end = min(R, r_begin + rows_per_split);
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+
+  float acc[4][4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
+
+  for (long long r = r_begin; r < r_end; r += kTR) {
+#pragma unroll
+    for (int q = 0; q < (kTR * kTM) / 256; ++q) {
+      const int e = tid + q * 256;
+      const int rr = e / kTM, cc = e - rr * kTM;
+      const long long row = r + rr;
+      const int m = m0 + cc, j = j0 + cc;
+      float a = 0.f, z = 0.f;
+      if (row < r_end) {
+        if (m < H3) a = ldf(dA + row * H3 + m);
+        if (j < n_in) {
+          z = ld_operand<MODE>(x + row * n_in + j);
+        } else if (j < Zc) {
+          const long long bidx = row / K;
+          const int kk = (int)(row - bidx * K);
+          const int u = j - n_in;
+          z = (kk == 0) ? ld_operand<MODE>(h0 + bidx * H + u)
+                        : ld_operand<MODE>(h_seq + (row - 1) * H + u);
+        } else if (j == Zc) {
+          z = 1.f;
+        }
+      }
+      sA[rr][cc] = a;
+      sZ[rr][cc] = z;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < kTR; ++rr) {
+      float av[4], zv[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) av[p] = sA[rr][ty + 16 * p];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) zv[q] = sZ[rr][tx + 16 * q];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(av[p], zv[q], acc[p][q]);
+    }
+    __syncthreads();
+  }
+  float* o = out + s * N;
+  const long long off_rec = (long long)H3 * n_in;
+  const long long off_b = (long long)H3 * Zc;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int m = m0 + ty + 16 * p;
+    if (m >= H3) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + tx + 16 * q;
+      if (j < n_in) o[(long long)m * n_in + j] = acc[p][q];
+      else if (j < Zc) o[off_rec + (long long)m * H + (j - n_in)] = acc[p][q];
+      else if (j == Zc) o[off_b + m] = acc[p][q];
+    }
+  }
+}
+
+// Samples per block: the smallest tile that keeps the grid within about two
+// blocks per SM, limited so that the tile's shared memory (smem_per_sample
+// bytes per sample) stays within 200 KB.
+int pick_bt(int B, size_t smem_per_sample) {
+  const int bts[5] = {1, 2, 4, 8, 16};
+  int pick = 16;
+  for (int t : bts)
+    if ((B + t - 1) / t <= 2 * kNumSMs) { pick = t; break; }
+  while (pick > 1 && (size_t)pick * smem_per_sample > 200 * 1024) pick /= 2;
+  return pick;
+}
+
+template <typename T, int MODE, int BT>
+cudaError_t fwd_bt(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  const int threads = std::min(kMaxThreads, (L.H + 31) / 32 * 32);
+  const size_t smem = 2 * (size_t)BT * L.Zc * sizeof(float);
+  auto kern = k_cfc_fwd<T, MODE, BT>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = (L.B + BT - 1) / BT;
+  TraceScope trace("cfc_fwd_simt", s);
+  kern<<<grid, threads, smem, s>>>(
+      static_cast<const T*>(a.x), static_cast<const T*>(a.h0),
+      reinterpret_cast<const T*>(a.ws + L.off_wt), a.b, a.dt, a.dt_stride,
+      L.B, L.K, L.n_in, L.H, static_cast<T*>(a.h_seq), reinterpret_cast<float*>(a.ws + L.off_act));
+  return cudaGetLastError();
+}
+
+template <typename T, typename DT, int MODE, int BT>
+cudaError_t bwd_bt(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  const int threads = std::min(kMaxThreads, (L.Zc + 31) / 32 * 32);
+  const size_t smem = (size_t)BT * 4 * L.H * sizeof(float);
+  auto kern = k_cfc_bwd<T, DT, MODE, BT>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = (L.B + BT - 1) / BT;
+  TraceScope trace("cfc_bwd_simt", s);
+  kern<<<grid, threads, smem, s>>>(
+      static_cast<const T*>(a.W_in), static_cast<const T*>(a.W_rec), a.dt, a.dt_stride,
+      L.B, L.K, L.n_in, L.H, static_cast<const T*>(a.h_seq), a.grad_h_seq, a.grad_h_last, a.y,
+      reinterpret_cast<const float*>(a.ws + L.off_act), reinterpret_cast<DT*>(a.ws + L.off_dA),
+      a.grad_h0, a.grad_x);
+  return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+cudaError_t forward_mode(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  {
+    const long long total = (long long)L.H3 * L.Zc;
+    const int threads = 256;
+    const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 4 * kNumSMs);
+    TraceScope trace("prep_wt", s);
+    k_prep_wt<T, MODE><<<blocks, threads, 0, s>>>(static_cast<const T*>(a.W_in),
+                                                  static_cast<const T*>(a.W_rec), L.n_in, L.H,
+                                                  reinterpret_cast<T*>(a.ws + L.off_wt));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  switch (pick_bt(L.B, 2 * (size_t)L.Zc * sizeof(float))) {
+    case 1: return fwd_bt<T, MODE, 1>(L, a, s);
+    case 2: return fwd_bt<T, MODE, 2>(L, a, s);
+    case 4: return fwd_bt<T, MODE, 4>(L, a, s);
+    case 8: return fwd_bt<T, MODE, 8>(L, a, s);
+    default: return fwd_bt<T, MODE, 16>(L, a, s);
+  }
+}
+
+template <typename T, typename DT, int MODE>
+cudaError_t backward_mode(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  switch (pick_bt(L.B, 4 * (size_t)L.H * sizeof(float))) {
+    case 1: return bwd_bt<T, DT, MODE, 1>(L, a, s);
+    case 2: return bwd_bt<T, DT, MODE, 2>(L, a, s);
+    case 4: return bwd_bt<T, DT, MODE, 4>(L, a, s);
+    case 8: return bwd_bt<T, DT, MODE, 8>(L, a, s);
+    default: return bwd_bt<T, DT, MODE, 16>(L, a, s);
+  }
+}
+
+template <typename T, typename DT, int MODE>
+cudaError_t wgrad_mode(const Layout& L, const CfcArgs& a, float* out, int n_split,
+                       long long rows_per_split, cudaStream_t s) {
+  dim3 grid((L.H3 + kTM - 1) / kTM, (L.Zc + 1 + kTN - 1) / kTN, n_split);
+  TraceScope trace("wgrad_simt", s);
+  k_wgrad<T, DT, MODE><<<grid, 256, 0, s>>>(
+      reinterpret_cast<const DT*>(a.ws + L.off_dA), static_cast<const T*>(a.x),
+      static_cast<const T*>(a.h0), static_cast<const T*>(a.h_seq), L.K, L.n_in, L.H, L.R,
+      rows_per_split, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  switch (L.math) {
+    case CFC_MATH_FP32: return forward_mode<float, CFC_MATH_FP32>(L, a, s);
+    case CFC_MATH_TF32: return forward_mode<float, CFC_MATH_TF32>(L, a, s);
+    default: return forward_mode<__nv_bfloat16, CFC_MATH_BF16>(L, a, s);
+  }
+}
+
+cudaError_t launch_backward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  switch (L.math) {
+    case CFC_MATH_FP32: return backward_mode<float, float, CFC_MATH_FP32>(L, a, s);
+    case CFC_MATH_TF32: return backward_mode<float, float, CFC_MATH_TF32>(L, a, s);
+    default: return backward_mode<__nv_bfloat16, __nv_bfloat16, CFC_MATH_BF16>(L, a, s);
+  }
+}
+
+cudaError_t launch_wgrad_simt(const Layout& L, const CfcArgs& a, float* out, int n_split,
+                              long long rows_per_split, cudaStream_t s) {
+  switch (L.math) {
+    case CFC_MATH_FP32: return wgrad_mode<float, float, CFC_MATH_FP32>(L, a, out, n_split, rows_per_split, s);
+    case CFC_MATH_TF32: return wgrad_mode<float, float, CFC_MATH_TF32>(L, a, out, n_split, rows_per_split, s);
+    default: return wgrad_mode<__nv_bfloat16, __nv_bfloat16, CFC_MATH_BF16>(L, a, out, n_split, rows_per_split, s);
+  }
+}
+
+}  // namespace cfc

@@ -1,0 +1,121 @@
+"""Helpers of the GPU parity tests: run the C-ABI path through the Python
+binding on seeded inputs and compare with the oracle."""
+
+import numpy as np
+import pytest
+
+import recurrent_cell_gb300 as cfc
+from recurrent_cell_gb300 import workloads as wl
+
+# Tolerances.  fp32 path: |gpu - ref| <= 1e-5 + 1e-4 |ref| elementwise.
+# TF32 / bf16 tensor paths: |gpu - ref| <= 2e-3 |ref| + 2e-3 max|ref| per tensor;
+# a bf16-stored state may additionally differ by one bf16 ulp (2^-7 |ref|).
+FP32_REL, FP32_ABS = 1e-4, 1e-5
+LP_REL, LP_ABS_FRAC = 2e-3, 2e-3
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def require_gpu():
+    torch = torch_mod()
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without a CUDA device")
+    from recurrent_cell_gb300 import build as b
+    b.build()
+    cfc.load_library()
+
+
+def dev(a, dtype=None):
+    torch = torch_mod()
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device="cuda", dtype=dtype if dtype is not None else t.dtype)
+
+
+def host(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(got, ref, math, name, state_bf16=False):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    if math == wl.MATH_FP32:
+        tol = FP32_ABS + FP32_REL * np.abs(ref)
+    else:
+        tol = LP_REL * np.abs(ref) + LP_ABS_FRAC * (np.abs(ref).max() if ref.size else 0.0)
+        if state_bf16:
+            tol = tol + 2.0 ** -7 * np.abs(ref)
+    excess = np.abs(got - ref) - tol
+    if np.any(excess > 0):
+        idx = np.unravel_index(np.argmax(excess), excess.shape)
+        raise AssertionError(f"{name}: {np.sum(excess > 0)} of {excess.size} elements out of "
+                             f"tolerance; worst at {idx}: gpu={got[idx]!r} ref={ref[idx]!r}")
+
+
+class CfcRun:
+    """Device buffers for one workload; forward() + backward() via the C ABI."""
+
+    def __init__(self, w: wl.Workload, inp: dict, grad_path=None, pad=0):
+        torch = torch_mod()
+        self.w = w
+        self.grad_path = w.grad_path if grad_path is None else grad_path
+        st = torch.bfloat16 if w.math == wl.MATH_BF16 else torch.float32
+        self.st = st
+        B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+        self.t = dict(x=dev(inp["x"], st), h0=dev(inp["h0"], st), W_in=dev(inp["W_in"], st),
+                      W_rec=dev(inp["W_rec"], st), b=dev(inp["b"], torch.float32),
+                      dt=dev(inp["dt"], torch.float32), y=dev(inp["y"], torch.float32))
+        nbytes = cfc.cfc_kloop_workspace_bytes(B, K, n_in, H, w.math, self.grad_path)
+        assert nbytes > 0
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.h_seq = torch.empty(B, K, H, dtype=st, device="cuda")
+        self.gWi = torch.empty(3, H, n_in, device="cuda")
+        self.gWr = torch.empty(3, H, H, device="cuda")
+        self.gb = torch.empty(3, H, device="cuda")
+        self.gh0 = torch.empty(B, H, device="cuda")
+        self.gx = torch.empty(B, K, n_in, device="cuda")
+        self.scratch = (torch.empty(B, w.N, device="cuda")
+                        if self.grad_path == wl.GRAD_SCRATCH else None)
+
+    def set_inputs(self, inp):
+        for k in ("x", "h0", "W_in", "W_rec", "b", "dt", "y"):
+            self.t[k].copy_(dev(inp[k], self.t[k].dtype))
+
+    def forward(self):
+        t = self.t
+        cfc.cfc_kloop_forward(t["x"], t["h0"], t["W_in"], t["W_rec"], t["b"], t["dt"], self.h_seq,
+                              self.ws, math=self.w.math)
+
+    def backward(self, y=True, grad_h_seq=None, grad_h_last=None, grad_x=True, grad_h0=True):
+        t = self.t
+        cfc.cfc_kloop_backward(t["x"], t["h0"], t["W_in"], t["W_rec"], t["b"], t["dt"], self.h_seq,
+                               self.gWi, self.gWr, self.gb, self.ws,
+                               grad_h_seq=grad_h_seq, grad_h_last=grad_h_last,
+                               y=t["y"] if y else None,
+                               grad_h0=self.gh0 if grad_h0 else None,
+                               grad_x=self.gx if grad_x else None,
+                               per_sample_scratch=self.scratch, grad_path=self.grad_path,
+                               math=self.w.math)
+
+    def results(self):
+        torch = torch_mod()
+        torch.cuda.synchronize()
+        out = dict(h_seq=host(self.h_seq), grad_W_in=host(self.gWi), grad_W_rec=host(self.gWr),
+                   grad_b=host(self.gb), grad_h0=host(self.gh0), grad_x=host(self.gx))
+        if self.scratch is not None:
+            out["per_sample"] = host(self.scratch)
+        return out
+
+    def raw(self):
+        """Bit patterns of every output (for exact run-to-run comparisons)."""
+        torch = torch_mod()
+        torch.cuda.synchronize()
+        ts = [self.h_seq, self.gWi, self.gWr, self.gb, self.gh0, self.gx]
+        if self.scratch is not None:
+            ts.append(self.scratch)
+        return [t.detach().cpu().view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
+                .numpy().copy() for t in ts]
