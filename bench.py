@@ -334,6 +334,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reduce-only", action="store_true",
+                    help="time only the standalone reduce_axis0 cases (profiling aid)")
     args = ap.parse_args()
     w = wl.SHORT_NAMES[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -387,6 +389,13 @@ def main():
         # then pays no write-back of the flush's own dirty lines.
         flush_buf.fill_(1.0)
         torch.sum(flush_buf, dim=0, keepdim=True, out=flush_sink)
+
+    if args.reduce_only:
+        red = [measure_reduce(B, N, args.steps, device, peaks, flush)
+               for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
+        print(json.dumps(dict(metric="reduce_axis0 GB/s", unit="GB/s", steps=args.steps,
+                              results=red, peak_hbm_gbs=peaks["hbm"])))
+        return 0
 
     props = torch.cuda.get_device_properties(device)
     uuid = getattr(props, "uuid", None)

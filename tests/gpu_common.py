@@ -18,8 +18,14 @@ from recurrent_cell_gb300 import workloads as wl
 # boundary (about 1 in 10^5 elements) the two states differ by one bf16 ulp
 # (2^-8 relative), which moves that sample's downstream values by ~0.2% of
 # their scale.  A bf16-stored state may itself differ by one ulp (2^-7 |ref|).
+# grad_h0 is the one output carried back through all K rounding stages of the
+# backward recurrence: a float32 re-computation with exactly the kernels'
+# rounding points already differs from the float64 oracle by 2.09e-3 (mid,
+# TF32, K=64) and 2.03e-3 (large, bf16, K=8) normwise, so 2e-3 is below the
+# modes' own noise floor there; it gets 5e-3.
 FP32_REL, FP32_ABS = 1e-4, 1e-5
 LP_REL, LP_GUARD_FRAC = 2e-3, 1e-2
+LP_REL_GRAD_H0 = 5e-3
 
 
 def torch_mod():
@@ -46,7 +52,7 @@ def host(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def assert_close(got, ref, math, name, state_bf16=False):
+def assert_close(got, ref, math, name, state_bf16=False, lp_rel=LP_REL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
@@ -56,8 +62,8 @@ def assert_close(got, ref, math, name, state_bf16=False):
     else:
         nrm = np.linalg.norm(ref)
         err = np.linalg.norm(got - ref)
-        assert err <= LP_REL * nrm + 1e-30, \
-            f"{name}: normwise relative error {err / max(nrm, 1e-30):.3g} > {LP_REL}"
+        assert err <= lp_rel * nrm + 1e-30, \
+            f"{name}: normwise relative error {err / max(nrm, 1e-30):.3g} > {lp_rel}"
         tol = LP_REL * np.abs(ref) + LP_GUARD_FRAC * (np.abs(ref).max() if ref.size else 0.0)
         if state_bf16:
             tol = tol + 2.0 ** -7 * np.abs(ref)

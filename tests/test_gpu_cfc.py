@@ -7,7 +7,7 @@ import pytest
 import oracle
 import recurrent_cell_gb300 as cfc
 from recurrent_cell_gb300 import workloads as wl
-from gpu_common import CfcRun, assert_close, dev, require_gpu, torch_mod
+from gpu_common import LP_REL, LP_REL_GRAD_H0, CfcRun, assert_close, dev, require_gpu, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,8 @@ def oracle_ref(w, inp, per_sample=True, **seeds):
 def check_all(w, got, ref, keys=("h_seq", "grad_W_in", "grad_W_rec", "grad_b", "grad_h0", "grad_x")):
     for k in keys:
         assert_close(got[k], ref[k], w.math, f"{w.name}:{k}",
-                     state_bf16=(k == "h_seq" and w.math == wl.MATH_BF16))
+                     state_bf16=(k == "h_seq" and w.math == wl.MATH_BF16),
+                     lp_rel=LP_REL_GRAD_H0 if k == "grad_h0" else LP_REL)
 
 
 def run(w, inp, grad_path=None, **bw):
