@@ -60,7 +60,8 @@ typedef enum {
   CFC_ERR_WORKSPACE = -4, /* workspace NULL or smaller than cfc_kloop_workspace_bytes() */
   CFC_ERR_MODE = -5,      /* unknown math mode or gradient path                */
   CFC_ERR_LAUNCH = -6,    /* a kernel launch failed (cudaGetLastError != 0)    */
-  CFC_ERR_DEVICE = -7     /* no usable CUDA device / unsupported architecture  */
+  CFC_ERR_DEVICE = -7,    /* no usable CUDA device / unsupported architecture  */
+  CFC_ERR_TOO_LARGE = -8  /* sizes need more than CFC_STATIC_WORKSPACE_BYTES   */
 } cfc_status;
 
 typedef enum { CFC_MATH_FP32 = 0, CFC_MATH_TF32 = 1, CFC_MATH_BF16 = 2 } cfc_math;
@@ -144,6 +145,36 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
  * out must be 4-byte aligned and must not overlap (16-byte alignment and
  * n_tail % 4 == 0 select the float4 path; otherwise scalar, same order). */
 int reduce_axis0(const float* per_batch, int n_batch, long long n_tail, float* out, void* stream);
+
+/* Forward + backward without allocation.  This entry point has no counterpart
+ * in the pages; it exists for callers that cannot allocate device memory
+ * when they run the K loop (code running under an allocator it does not own,
+ * plugins barred from cudaMalloc, real-time loops where an allocation would
+ * stall).  It computes exactly what cfc_kloop_forward followed by
+ * cfc_kloop_backward with CFC_GRAD_GEMM computes, with the same kernels, but
+ * keeps the whole workspace in a fixed device array inside the library.
+ *   - The array holds CFC_STATIC_WORKSPACE_BYTES bytes on every device that
+ *     loads the library, until the process exits.  Sizes whose workspace
+ *     (cfc_kloop_workspace_bytes(..., CFC_GRAD_GEMM)) is larger are rejected
+ *     with CFC_ERR_TOO_LARGE before anything is launched.
+ *   - The caller passes all inputs and outputs (same meaning, layout and
+ *     overwrite rules as the two calls it replaces); nothing is allocated or
+ *     freed by the call.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Nothing in it has to start at zero (every part that is read is written
+ *     earlier in the same call), but calls whose work overlaps on the GPU
+ *     (for example on two streams) race on it and must be serialised. */
+#define CFC_STATIC_WORKSPACE_BYTES (16u << 20)
+int cfc_kloop_forward_backward_static(const void* x, const void* h0, const void* W_in,
+                                      const void* W_rec, const float* b, const float* dt,
+                                      int dt_stride, int B, int K, int n_in, int n_hid, int math,
+                                      const float* grad_h_seq, const float* grad_h_last,
+                                      const float* y,
+                                      void* h_seq, float* grad_W_in, float* grad_W_rec,
+                                      float* grad_b, float* grad_h0, float* grad_x, void* stream);
 
 /* Kernel tracing (diagnostics, off by default).  While enabled, every kernel
  * that this library launches is bracketed by two CUDA events recorded on its

@@ -54,6 +54,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cfc_kloop_backward.restype = i32
     lib.reduce_axis0.argtypes = [vp, i32, i64, vp, vp]
     lib.reduce_axis0.restype = i32
+    lib.cfc_kloop_forward_backward_static.argtypes = [vp] * 6 + [i32] * 6 + [vp] * 3 + [vp] * 6 + [vp]
+    lib.cfc_kloop_forward_backward_static.restype = i32
     lib.cfc_trace_enable.argtypes = [i32]
     lib.cfc_trace_enable.restype = i32
     lib.cfc_trace_count.argtypes = []
@@ -174,6 +176,36 @@ def reduce_axis0(per_batch, out, stream=None):
         _ptr(per_batch, "per_batch", torch.float32), B, N,
         _ptr(out, "out", torch.float32, (N,)), _stream(stream))
     _check("reduce_axis0", status)
+
+
+def cfc_kloop_forward_backward_static(x, h0, W_in, W_rec, b, dt, h_seq, grad_W_in, grad_W_rec,
+                                      grad_b, grad_h_seq=None, grad_h_last=None, y=None,
+                                      grad_h0=None, grad_x=None, math=MATH_FP32, stream=None):
+    """Forward + backward with the library's fixed internal workspace: for
+    callers that cannot allocate device memory.  Same results as
+    cfc_kloop_forward + cfc_kloop_backward(grad_path=GRAD_GEMM)."""
+    torch = _torch()
+    B, K, n_in = x.shape
+    H = h0.shape[1]
+    st = _storage_dtype(math)
+    f32 = torch.float32
+    dt_stride = 0 if dt.numel() == 1 else 1
+    status = load_library().cfc_kloop_forward_backward_static(
+        _ptr(x, "x", st, (B, K, n_in)), _ptr(h0, "h0", st, (B, H)),
+        _ptr(W_in, "W_in", st, (3, H, n_in)), _ptr(W_rec, "W_rec", st, (3, H, H)),
+        _ptr(b, "b", f32, (3, H)), _ptr(dt, "dt", f32, (B,) if dt_stride else None),
+        dt_stride, B, K, n_in, H, math,
+        _ptr(grad_h_seq, "grad_h_seq", f32, (B, K, H), optional=True),
+        _ptr(grad_h_last, "grad_h_last", f32, (B, H), optional=True),
+        _ptr(y, "y", f32, (B, H), optional=True),
+        _ptr(h_seq, "h_seq", st, (B, K, H)),
+        _ptr(grad_W_in, "grad_W_in", f32, (3, H, n_in)),
+        _ptr(grad_W_rec, "grad_W_rec", f32, (3, H, H)),
+        _ptr(grad_b, "grad_b", f32, (3, H)),
+        _ptr(grad_h0, "grad_h0", f32, (B, H), optional=True),
+        _ptr(grad_x, "grad_x", f32, (B, K, n_in), optional=True),
+        _stream(stream))
+    _check("cfc_kloop_forward_backward_static", status)
 
 
 def cfc_trace_enable(on: bool) -> None:

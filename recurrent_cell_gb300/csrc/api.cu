@@ -99,6 +99,7 @@ const char* cfc_status_string(int status) {
     case CFC_ERR_MODE: return "unknown math mode or gradient path";
     case CFC_ERR_LAUNCH: return "kernel launch failed";
     case CFC_ERR_DEVICE: return "no usable CUDA device";
+    case CFC_ERR_TOO_LARGE: return "sizes need more workspace than CFC_STATIC_WORKSPACE_BYTES";
     default: return "unknown status";
   }
 }
