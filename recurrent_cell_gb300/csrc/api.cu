@@ -138,7 +138,9 @@ int cfc_kloop_forward(const void* x, const void* h0, const void* W_in, const voi
   CfcArgs a{};
   a.x = x; a.h0 = h0; a.W_in = W_in; a.W_rec = W_rec; a.b = b; a.dt = dt; a.dt_stride = dt_stride;
   a.h_seq = h_seq; a.ws = static_cast<char*>(workspace);
-  cudaError_t e = launch_forward_simt(L, a, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_forward_cluster(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_forward_simt(L, a, s);
   return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
 }
 
@@ -174,7 +176,8 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
   a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  cudaError_t e = launch_backward_simt(L, a, s);
+  cudaError_t e = launch_backward_cluster(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_backward_simt(L, a, s);
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;
   float* part = (grad_path == CFC_GRAD_SCRATCH) ? per_sample_scratch
                                                 : reinterpret_cast<float*>(a.ws + L.off_part);

@@ -1,0 +1,427 @@
+// cfc_cluster.cu -- K-loop forward/backward with the weights resident in the
+// shared memory of a thread-block cluster.
+//
+// A cluster of C blocks owns a tile of BT samples for the whole K loop.
+//
+// Forward: block r of the cluster owns hidden units [r*Hc, (r+1)*Hc)
+// (Hc = H / C) and keeps the rows of W_cat = [W_in | W_rec] of those units
+// (all three heads) in shared memory, transposed to [Zc][3][Hc] so that the
+// threads of a warp read consecutive units.  Each step it computes the three
+// pre-activations of its units (the Zc-long dot products split over S thread
+// groups, summed in a fixed order), applies the cell, and writes its slice of
+// h_{k+1} into the next operand buffer of EVERY block of the cluster
+// (distributed shared memory).  One cluster barrier per step publishes the
+// slices; the operand buffer is double-buffered so that no second barrier is
+// needed.
+//
+// Backward: block r owns the same units for the elementwise dA and a set of
+// output columns of dz = W_cat^T dA: a slice of the x columns (grad_x) and the
+// h columns of its own units (the carry of its own units, which it needs next
+// step).  It keeps the columns of W_cat for that set in shared memory,
+// [3H][nJ].  Each step it computes dA of its units, broadcasts it to every
+// block of the cluster (distributed shared memory, double-buffered), and after
+// the cluster barrier contracts the full dA vector with its columns.
+//
+// Every kernel here reads the weights from HBM once per block per launch; the
+// K loop runs on chip.  No spin waits: the only synchronisation is the
+// hardware cluster barrier (barrier.cluster via cooperative groups).
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <cooperative_groups.h>
+
+#include "cfc_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace cfc {
+namespace {
+
+constexpr int kClusterThreads = 256;
+
+struct ClusterPlan {
+  int C = 0, BT = 0, S = 0, threads = 0;
+  size_t smem = 0;
+};
+
+// ---------------------------------------------------------------------------
+// Forward
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int BT>
+__global__ void __launch_bounds__(kClusterThreads)
+k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __restrict__ W_in,
+                  const T* __restrict__ W_rec, const float* __restrict__ bias,
+                  const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H, int S,
+                  T* __restrict__ h_seq, float* __restrict__ act) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int r = (int)cluster.block_rank();
+  const int Hc = H / C, Zc = n_in + H, H3 = 3 * H;
+  const int b0 = (int)(blockIdx.x / C) * BT;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+
+  extern __shared__ float sm[];
+  float* Ws = sm;                              // [Zc][3][Hc] operand values
+  float* zb = Ws + (size_t)Zc * 3 * Hc;        // [2][BT][Zc]
+  float* part = zb + 2 * BT * Zc;              // [S][BT][3][Hc]
+
+  for (int e = tid; e < Zc * 3 * Hc; e += nthr) {
+    const int j = e / (3 * Hc), rem = e - j * 3 * Hc, c = rem / Hc, u = rem - c * Hc;
+    const long long row = (long long)c * H + r * Hc + u;
+    Ws[e] = (j < n_in) ? ld_operand<MODE>(W_in + row * n_in + j)
+                       : ld_operand<MODE>(W_rec + row * H + (j - n_in));
+  }
+  for (int e = tid; e < BT * Zc; e += nthr) {
+    const int n = e / Zc, j = e - n * Zc, bb = b0 + n;
+    float v = 0.f;
+    if (bb < B) v = (j < n_in) ? ld_operand<MODE>(x + (long long)bb * K * n_in + j)
+                               : ld_operand<MODE>(h0 + (long long)bb * H + (j - n_in));
+    zb[e] = v;
+  }
+  // Every block of the cluster must be running before any block writes into
+  // its shared memory.
+  cluster.sync();
+
+  // thread -> (unit u, column group s) of the dot products
+  const int u = tid % Hc, s = tid / Hc;
+  const bool dot = s < S;
+  const int j0 = (int)((long long)s * Zc / S), j1 = (int)((long long)(s + 1) * Zc / S);
+
+  for (int k = 0; k < K; ++k) {
+    const float* zs = zb + (k & 1) * BT * Zc;
+    float* zn = zb + ((k + 1) & 1) * BT * Zc;
+    if (dot) {
+      float a0[BT], a1[BT], a2[BT];
+#pragma unroll
+      for (int n = 0; n < BT; ++n) { a0[n] = 0.f; a1[n] = 0.f; a2[n] = 0.f; }
+#pragma unroll 4
+      for (int j = j0; j < j1; ++j) {
+        const float* w = Ws + (size_t)j * 3 * Hc + u;
+        const float wf = w[0], wg = w[Hc], wh = w[2 * Hc];
+#pragma unroll
+        for (int n = 0; n < BT; ++n) {
+          const float z = zs[n * Zc + j];
+          a0[n] = fmaf(wf, z, a0[n]);
+          a1[n] = fmaf(wg, z, a1[n]);
+          a2[n] = fmaf(wh, z, a2[n]);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < BT; ++n) {
+        float* p = part + ((size_t)(s * BT + n) * 3) * Hc + u;
+        p[0] = a0[n];
+        p[Hc] = a1[n];
+        p[2 * Hc] = a2[n];
+      }
+    }
+    __syncthreads();
+    // Cell of (sample n, unit u) pairs; partial sums added in the fixed order s = 0..S-1.
+    for (int e = tid; e < BT * Hc; e += nthr) {
+      const int n = e / Hc, uu = e - n * Hc, bb = b0 + n;
+      const int unit = r * Hc + uu;
+      float A[3];
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        float v = bias[c * H + unit];
+        for (int q = 0; q < S; ++q) v += part[((size_t)(q * BT + n) * 3 + c) * Hc + uu];
+        A[c] = v;
+      }
+      const float dtb = (bb < B) ? dt[dt_stride ? bb : 0] : 0.f;
+      const float g = tanhf(A[1]);
+      const float hh = tanhf(A[2]);
+      const float gate = 1.f / (1.f + expf(A[0] * dtb));
+      const float h = gate * g + (1.f - gate) * hh;
+      float hop = 0.f;
+      if (bb < B) {
+        const long long row = (long long)bb * K + k;
+        act[row * H3 + unit] = gate;
+        act[row * H3 + H + unit] = g;
+        act[row * H3 + 2 * H + unit] = hh;
+        stf(h_seq + row * H + unit, h);
+        if constexpr (sizeof(T) == 2) hop = round_bf16(h);   // the stored bf16 state
+        else hop = to_operand<MODE>(h);
+      }
+      const int off = n * Zc + n_in + unit;
+      for (int q = 0; q < C; ++q) cluster.map_shared_rank(zn, q)[off] = hop;
+    }
+    if (k + 1 < K) {
+      for (int e = tid; e < BT * n_in; e += nthr) {
+        const int n = e / n_in, j = e - n * n_in, bb = b0 + n;
+        zn[n * Zc + j] = (bb < B) ? ld_operand<MODE>(x + ((long long)bb * K + k + 1) * n_in + j) : 0.f;
+      }
+    }
+    cluster.sync();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward
+// ---------------------------------------------------------------------------
+template <typename T, typename DT, int MODE, int BT>
+__global__ void __launch_bounds__(kClusterThreads)
+k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
+                  const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H, int S,
+                  const T* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
+                  const float* __restrict__ grad_h_last, const float* __restrict__ y,
+                  const float* __restrict__ act, DT* __restrict__ dA_out,
+                  float* __restrict__ grad_h0, float* __restrict__ grad_x) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int r = (int)cluster.block_rank();
+  const int Hc = H / C, H3 = 3 * H;
+  const int xa = (int)((long long)r * n_in / C), xb = (int)((long long)(r + 1) * n_in / C);
+  const int nx = xb - xa, nJ = nx + Hc;
+  const int nJmax = (n_in + C - 1) / C + Hc;
+  const int b0 = (int)(blockIdx.x / C) * BT;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+
+  extern __shared__ float sm[];
+  float* Wc = sm;                              // [3H][nJmax] columns of W_cat owned here
+  float* dAf = Wc + (size_t)H3 * nJmax;        // [2][BT][3H] dA of all units (operand values)
+  float* carry = dAf + 2 * BT * H3;            // [BT][Hc]
+  float* part = carry + BT * Hc;               // [S][BT][nJmax]
+
+  for (int e = tid; e < H3 * nJmax; e += nthr) {
+    const int row = e / nJmax, jj = e - row * nJmax;
+    float v = 0.f;
+    if (jj < nx) v = ld_operand<MODE>(W_in + (long long)row * n_in + xa + jj);
+    else if (jj < nJ) v = ld_operand<MODE>(W_rec + (long long)row * H + r * Hc + (jj - nx));
+    Wc[e] = v;
+  }
+  for (int e = tid; e < BT * Hc; e += nthr) carry[e] = 0.f;
+  cluster.sync();
+
+  const int jj = tid % nJmax, s = tid / nJmax;
+  const bool dot = (s < S) && (jj < nJ);
+  const int r0 = (int)((long long)s * H3 / S), r1 = (int)((long long)(s + 1) * H3 / S);
+
+  for (int k = K - 1; k >= 0; --k) {
+    float* buf = dAf + (k & 1) * BT * H3;
+    for (int e = tid; e < BT * Hc; e += nthr) {
+      const int n = e / Hc, u = e - n * Hc, bb = b0 + n;
+      const int unit = r * Hc + u;
+      float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+      if (bb < B) {
+        const long long row = (long long)bb * K + k;
+        float delta = carry[e];
+        if (grad_h_seq) delta += grad_h_seq[row * H + unit];
+        if (k == K - 1) {
+          if (grad_h_last) delta += grad_h_last[(long long)bb * H + unit];
+          if (y) delta += ldf(h_seq + row * H + unit) - y[(long long)bb * H + unit];
+        }
+        const float gate = act[row * H3 + unit];
+        const float g = act[row * H3 + H + unit];
+        const float hh = act[row * H3 + 2 * H + unit];
+        const float dtb = dt[dt_stride ? bb : 0];
+        d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
+        d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
+        d0 = to_operand<MODE>(-dtb * delta * (g - hh) * gate * (1.f - gate));
+        stf(dA_out + row * H3 + unit, d0);
+        stf(dA_out + row * H3 + H + unit, d1);
+        stf(dA_out + row * H3 + 2 * H + unit, d2);
+      }
+      const int off = n * H3 + unit;
+      for (int q = 0; q < C; ++q) {
+        float* dst = cluster.map_shared_rank(buf, q);
+        dst[off] = d0;
+        dst[off + H] = d1;
+        dst[off + 2 * H] = d2;
+      }
+    }
+    cluster.sync();
+    if (dot) {
+      float acc[BT];
+#pragma unroll
+      for (int n = 0; n < BT; ++n) acc[n] = 0.f;
+#pragma unroll 4
+      for (int row = r0; row < r1; ++row) {
+        const float w = Wc[(size_t)row * nJmax + jj];
+#pragma unroll
+        for (int n = 0; n < BT; ++n) acc[n] = fmaf(w, buf[n * H3 + row], acc[n]);
+      }
+#pragma unroll
+      for (int n = 0; n < BT; ++n) part[(size_t)(s * BT + n) * nJmax + jj] = acc[n];
+    }
+    __syncthreads();
+    for (int e = tid; e < BT * nJ; e += nthr) {
+      const int n = e / nJ, c = e - n * nJ, bb = b0 + n;
+      float v = 0.f;
+      for (int q = 0; q < S; ++q) v += part[(size_t)(q * BT + n) * nJmax + c];
+      if (c < nx) {
+        if (grad_x && bb < B) grad_x[((long long)bb * K + k) * n_in + xa + c] = v;
+      } else {
+        carry[n * Hc + (c - nx)] = v;
+      }
+    }
+    __syncthreads();
+  }
+  if (grad_h0) {
+    for (int e = tid; e < BT * Hc; e += nthr) {
+      const int n = e / Hc, u = e - n * Hc, bb = b0 + n;
+      if (bb < B) grad_h0[(long long)bb * H + r * Hc + u] = carry[e];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Planning and launch
+// ---------------------------------------------------------------------------
+constexpr size_t kSmemLimit = 200 * 1024;
+
+size_t fwd_smem(const Layout& L, int C, int BT, int S) {
+  const int Hc = L.H / C;
+  return sizeof(float) * ((size_t)L.Zc * 3 * Hc + 2 * (size_t)BT * L.Zc + (size_t)S * BT * 3 * Hc);
+}
+
+size_t bwd_smem(const Layout& L, int C, int BT, int S) {
+  const int Hc = L.H / C;
+  const int nJmax = (L.n_in + C - 1) / C + Hc;
+  return sizeof(float) * ((size_t)L.H3 * nJmax + 2 * (size_t)BT * L.H3 + (size_t)BT * Hc +
+                          (size_t)S * BT * nJmax);
+}
+
+// Cluster size from the hidden size alone (so a sample's arithmetic does not
+// depend on the batch size): about 32 units per block, i.e. the smallest C in
+// {1, 2, 4, 8} with C >= H/32 that divides H and whose slices fit; failing
+// that, the largest C that fits.  Samples per cluster: the smallest BT that
+// keeps the grid within about two blocks per SM.
+bool plan(const Layout& L, bool forward, ClusterPlan* p) {
+  const int Cs[4] = {1, 2, 4, 8};
+  auto valid = [&](int c) {
+    if (L.H % c) return false;
+    const int Hc = L.H / c;
+    if (forward ? (Hc > kClusterThreads) : ((L.n_in + c - 1) / c + Hc > kClusterThreads)) return false;
+    return (forward ? fwd_smem(L, c, 1, 1) : bwd_smem(L, c, 1, 1)) <= kSmemLimit;
+  };
+  const int target = (L.H + 31) / 32;
+  int C = 0, largest = 0;
+  for (int c : Cs) {
+    if (!valid(c)) continue;
+    largest = c;
+    if (!C && c >= target) C = c;
+  }
+  if (!C) C = largest;
+  if (!C) return false;
+  const int Hc = L.H / C;
+  const int width = forward ? Hc : (L.n_in + C - 1) / C + Hc;
+  const int S = std::max(1, std::min(8, kClusterThreads / width));
+  int BT = 16;
+  const int bts[5] = {1, 2, 4, 8, 16};
+  for (int t : bts)
+    if ((long long)(L.B + t - 1) / t * C <= 2 * kNumSMs) { BT = t; break; }
+  auto smem = [&](int bt) { return forward ? fwd_smem(L, C, bt, S) : bwd_smem(L, C, bt, S); };
+  while (BT > 1 && smem(BT) > kSmemLimit) BT /= 2;
+  if (smem(BT) > kSmemLimit) return false;
+  p->C = C;
+  p->BT = BT;
+  p->S = S;
+  p->threads = std::min(kClusterThreads, (width * S + 31) / 32 * 32);
+  p->smem = smem(BT);
+  return true;
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_cluster(Kern kern, const ClusterPlan& p, int B, cudaStream_t s, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((B + p.BT - 1) / p.BT) * p.C), 1, 1);
+  cfg.blockDim = dim3((unsigned)p.threads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename T, int MODE, int BT>
+cudaError_t fwd_bt(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cudaStream_t s) {
+  TraceScope trace("cfc_fwd_cluster", s);
+  return launch_cluster(k_cfc_fwd_cluster<T, MODE, BT>, p, L.B, s,
+                        static_cast<const T*>(a.x), static_cast<const T*>(a.h0),
+                        static_cast<const T*>(a.W_in), static_cast<const T*>(a.W_rec), a.b, a.dt,
+                        a.dt_stride, L.B, L.K, L.n_in, L.H, p.S, static_cast<T*>(a.h_seq),
+                        reinterpret_cast<float*>(a.ws + L.off_act));
+}
+
+template <typename T, typename DT, int MODE, int BT>
+cudaError_t bwd_bt(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cudaStream_t s) {
+  TraceScope trace("cfc_bwd_cluster", s);
+  return launch_cluster(k_cfc_bwd_cluster<T, DT, MODE, BT>, p, L.B, s,
+                        static_cast<const T*>(a.W_in), static_cast<const T*>(a.W_rec), a.dt,
+                        a.dt_stride, L.B, L.K, L.n_in, L.H, p.S, static_cast<const T*>(a.h_seq),
+                        a.grad_h_seq, a.grad_h_last, a.y,
+                        reinterpret_cast<const float*>(a.ws + L.off_act),
+                        reinterpret_cast<DT*>(a.ws + L.off_dA), a.grad_h0, a.grad_x);
+}
+
+template <typename T, int MODE>
+cudaError_t fwd_mode(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cudaStream_t s) {
+  switch (p.BT) {
+    case 1: return fwd_bt<T, MODE, 1>(L, p, a, s);
+    case 2: return fwd_bt<T, MODE, 2>(L, p, a, s);
+    case 4: return fwd_bt<T, MODE, 4>(L, p, a, s);
+    case 8: return fwd_bt<T, MODE, 8>(L, p, a, s);
+    default: return fwd_bt<T, MODE, 16>(L, p, a, s);
+  }
+}
+
+template <typename T, typename DT, int MODE>
+cudaError_t bwd_mode(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cudaStream_t s) {
+  switch (p.BT) {
+    case 1: return bwd_bt<T, DT, MODE, 1>(L, p, a, s);
+    case 2: return bwd_bt<T, DT, MODE, 2>(L, p, a, s);
+    case 4: return bwd_bt<T, DT, MODE, 4>(L, p, a, s);
+    case 8: return bwd_bt<T, DT, MODE, 8>(L, p, a, s);
+    default: return bwd_bt<T, DT, MODE, 16>(L, p, a, s);
+  }
+}
+
+}  // namespace
+
+// Kernel selection for the K loop: CFC_KLOOP_KERNELS=cluster forces the
+// cluster kernels whenever they fit, =simt forces the streaming kernels,
+// anything else ("auto") uses the cluster kernels when their grid stays
+// within about two waves of blocks.  Read on every call.
+namespace {
+int kernel_choice() {
+  const char* v = getenv("CFC_KLOOP_KERNELS");
+  if (v && strcmp(v, "cluster") == 0) return 1;
+  if (v && strcmp(v, "simt") == 0) return 2;
+  return 0;
+}
+
+bool use_cluster(const Layout& L, bool forward, ClusterPlan* p) {
+  const int choice = kernel_choice();
+  if (choice == 2 || !plan(L, forward, p)) return false;
+  if (choice == 1) return true;
+  return (long long)(L.B + p->BT - 1) / p->BT * p->C <= 2 * kNumSMs;
+}
+}  // namespace
+
+cudaError_t launch_forward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  ClusterPlan p;
+  if (!use_cluster(L, true, &p)) return cudaErrorNotSupported;
+  switch (L.math) {
+    case CFC_MATH_FP32: return fwd_mode<float, CFC_MATH_FP32>(L, p, a, s);
+    case CFC_MATH_TF32: return fwd_mode<float, CFC_MATH_TF32>(L, p, a, s);
+    default: return fwd_mode<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+  }
+}
+
+cudaError_t launch_backward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  ClusterPlan p;
+  if (!use_cluster(L, false, &p)) return cudaErrorNotSupported;
+  switch (L.math) {
+    case CFC_MATH_FP32: return bwd_mode<float, float, CFC_MATH_FP32>(L, p, a, s);
+    case CFC_MATH_TF32: return bwd_mode<float, float, CFC_MATH_TF32>(L, p, a, s);
+    default: return bwd_mode<__nv_bfloat16, __nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+  }
+}
+
+}  // namespace cfc

@@ -105,6 +105,12 @@ struct CfcArgs {
 };
 
 cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
+// Cluster kernels (weights resident in shared memory of a block cluster).
+// Return cudaErrorNotSupported, launching nothing, when no cluster plan fits
+// the sizes or (for kernel selection "auto") the plan would need more than
+// about two waves of blocks.
+cudaError_t launch_forward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s);
+cudaError_t launch_backward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s);
 cudaError_t launch_backward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
 cudaError_t launch_wgrad_simt(const Layout& L, const CfcArgs& a, float* out, int n_split,
                               long long rows_per_split, cudaStream_t s);

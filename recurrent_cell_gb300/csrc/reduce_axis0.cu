@@ -56,7 +56,7 @@ __device__ __forceinline__ float* seg_ptr(const ReduceOut& o, long long col) {
 }
 
 template <int VEC>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 3)
 k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, ReduceOut out) {
   using V = Vec<VEC>;
   using T = typename V::T;

@@ -59,6 +59,17 @@ def test_smoke_fp32_scratch_path():
     assert_close(got["per_sample"], ref["per_sample"], w.math, "smoke:per_sample")
 
 
+@pytest.mark.parametrize("kernels", ["cluster", "simt"])
+@pytest.mark.parametrize("w", [wl.TINY, wl.SMOKE, wl.MID.with_(B=128, K=16),
+                               wl.LARGE.with_(B=96, K=4)], ids=lambda w: w.name)
+def test_kernel_families_on_benchmark_shapes(w, kernels, monkeypatch):
+    monkeypatch.setenv("CFC_KLOOP_KERNELS", kernels)
+    inp = wl.make_inputs(w, seed=9)
+    r, got = run(w, inp)
+    ref = oracle_ref(w, inp, per_sample=False, y=inp["y"])
+    check_all(w, got, ref)
+
+
 def test_smoke_fp32_gemm_path_matches():
     w = wl.SMOKE
     inp = wl.make_inputs(w)
@@ -97,9 +108,13 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("kernels", ["auto", "cluster", "simt"])
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("path", [wl.GRAD_SCRATCH, wl.GRAD_GEMM])
-def test_edge_shapes(w, path):
+def test_edge_shapes(w, path, kernels, monkeypatch):
+    """Both K-loop kernel families (cluster-resident weights, streaming
+    weights) and the automatic choice, on ragged shapes."""
+    monkeypatch.setenv("CFC_KLOOP_KERNELS", kernels)
     inp = wl.make_inputs(w, seed=5)
     r, got = run(w, inp, grad_path=path)
     ref = oracle_ref(w, inp, per_sample=(path == wl.GRAD_SCRATCH), y=inp["y"])
