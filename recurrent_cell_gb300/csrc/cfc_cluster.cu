@@ -38,6 +38,9 @@ namespace cfc {
 namespace {
 
 constexpr int kClusterThreads = 256;
+constexpr int kXPerThread = 8;     // forward: x elements per thread prefetched one step ahead
+constexpr int kItemsPerThread = 4; // backward: (sample, unit) items per thread with prefetched activations
+constexpr int kMaxSplit = 8;       // thread groups a dot product is split over
 
 struct ClusterPlan {
   int C = 0, BT = 0, S = 0, threads = 0;
@@ -64,6 +67,8 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
   float* Ws = sm;                              // [Zc][3][Hc] operand values
   float* zb = Ws + (size_t)Zc * 3 * Hc;        // [2][BT][Zc]
   float* part = zb + 2 * BT * Zc;              // [S][BT][3][Hc]
+  float* bs = part + (size_t)S * BT * 3 * Hc;  // [3][Hc] bias of the owned units
+  float* dts = bs + 3 * Hc;                    // [BT] dt of the tile's samples
 
   for (int e = tid; e < Zc * 3 * Hc; e += nthr) {
     const int j = e / (3 * Hc), rem = e - j * 3 * Hc, c = rem / Hc, u = rem - c * Hc;
@@ -78,6 +83,22 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
                                : ld_operand<MODE>(h0 + (long long)bb * H + (j - n_in));
     zb[e] = v;
   }
+  for (int e = tid; e < 3 * Hc; e += nthr) bs[e] = bias[(e / Hc) * H + r * Hc + (e % Hc)];
+  for (int e = tid; e < BT; e += nthr) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+
+  // x of the next step, loaded one step ahead so that its latency overlaps
+  // the current step (the plan guarantees BT*n_in <= kXPerThread * threads).
+  float xr[kXPerThread];
+  auto load_x = [&](int kk) {
+#pragma unroll
+    for (int q = 0; q < kXPerThread; ++q) {
+      const int e = tid + q * nthr;
+      const int n = e / n_in, j = e - n * n_in, bb = b0 + n;
+      xr[q] = (e < BT * n_in && kk < K && bb < B)
+                  ? ld_operand<MODE>(x + ((long long)bb * K + kk) * n_in + j) : 0.f;
+    }
+  };
+  load_x(1);
   // Every block of the cluster must be running before any block writes into
   // its shared memory.
   cluster.sync();
@@ -114,6 +135,14 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
         p[2 * Hc] = a2[n];
       }
     }
+    if (k + 1 < K) {
+#pragma unroll
+      for (int q = 0; q < kXPerThread; ++q) {
+        const int e = tid + q * nthr;
+        if (e < BT * n_in) zn[(e / n_in) * Zc + (e % n_in)] = xr[q];
+      }
+      load_x(k + 2);
+    }
     __syncthreads();
     // Cell of (sample n, unit u) pairs; partial sums added in the fixed order s = 0..S-1.
     for (int e = tid; e < BT * Hc; e += nthr) {
@@ -122,14 +151,19 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
       float A[3];
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
-        float v = bias[c * H + unit];
-        for (int q = 0; q < S; ++q) v += part[((size_t)(q * BT + n) * 3 + c) * Hc + uu];
+        float pv[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+          pv[q] = (q < S) ? part[((size_t)(q * BT + n) * 3 + c) * Hc + uu] : 0.f;
+        float v = bs[c * Hc + uu];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+          if (q < S) v += pv[q];
         A[c] = v;
       }
-      const float dtb = (bb < B) ? dt[dt_stride ? bb : 0] : 0.f;
       const float g = tanhf(A[1]);
       const float hh = tanhf(A[2]);
-      const float gate = 1.f / (1.f + expf(A[0] * dtb));
+      const float gate = 1.f / (1.f + expf(A[0] * dts[n]));
       const float h = gate * g + (1.f - gate) * hh;
       float hop = 0.f;
       if (bb < B) {
@@ -143,12 +177,6 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
       }
       const int off = n * Zc + n_in + unit;
       for (int q = 0; q < C; ++q) cluster.map_shared_rank(zn, q)[off] = hop;
-    }
-    if (k + 1 < K) {
-      for (int e = tid; e < BT * n_in; e += nthr) {
-        const int n = e / n_in, j = e - n * n_in, bb = b0 + n;
-        zn[n * Zc + j] = (bb < B) ? ld_operand<MODE>(x + ((long long)bb * K + k + 1) * n_in + j) : 0.f;
-      }
     }
     cluster.sync();
   }
@@ -178,8 +206,8 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
   extern __shared__ float sm[];
   float* Wc = sm;                              // [3H][nJmax] columns of W_cat owned here
   float* dAf = Wc + (size_t)H3 * nJmax;        // [2][BT][3H] dA of all units (operand values)
-  float* carry = dAf + 2 * BT * H3;            // [BT][Hc]
-  float* part = carry + BT * Hc;               // [S][BT][nJmax]
+  float* part = dAf + 2 * BT * H3;             // [S][BT][nJmax] partial column sums
+  float* dts = part + (size_t)S * BT * nJmax;  // [BT]
 
   for (int e = tid; e < H3 * nJmax; e += nthr) {
     const int row = e / nJmax, jj = e - row * nJmax;
@@ -188,41 +216,91 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
     else if (jj < nJ) v = ld_operand<MODE>(W_rec + (long long)row * H + r * Hc + (jj - nx));
     Wc[e] = v;
   }
-  for (int e = tid; e < BT * Hc; e += nthr) carry[e] = 0.f;
+  for (int e = tid; e < BT; e += nthr) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
   cluster.sync();
 
   const int jj = tid % nJmax, s = tid / nJmax;
   const bool dot = (s < S) && (jj < nJ);
   const int r0 = (int)((long long)s * H3 / S), r1 = (int)((long long)(s + 1) * H3 / S);
 
+  // Saved activations (and per-step upstream gradient) of this thread's
+  // (sample, unit) items, loaded one step ahead (the plan guarantees
+  // BT*Hc <= kItemsPerThread * threads).
+  float pg[kItemsPerThread], pgg[kItemsPerThread], phh[kItemsPerThread], pup[kItemsPerThread];
+  auto load_act = [&](int kk) {
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) {
+      const int e = tid + q * nthr;
+      const int n = e / Hc, uu = e - n * Hc, bb = b0 + n, unit = r * Hc + uu;
+      pg[q] = pgg[q] = phh[q] = pup[q] = 0.f;
+      if (e < BT * Hc && kk >= 0 && bb < B) {
+        const long long row = (long long)bb * K + kk;
+        pg[q] = act[row * H3 + unit];
+        pgg[q] = act[row * H3 + H + unit];
+        phh[q] = act[row * H3 + 2 * H + unit];
+        if (grad_h_seq) pup[q] = grad_h_seq[row * H + unit];
+      }
+    }
+  };
+  load_act(K - 1);
+
+  // Sum of the S partial column sums of the previous contraction (fixed order).
+  auto column_sum = [&](int n, int c) {
+    float pv[kMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q) pv[q] = (q < S) ? part[(size_t)(q * BT + n) * nJmax + c] : 0.f;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q)
+      if (q < S) v += pv[q];
+    return v;
+  };
+  // grad_x of step kk (its x columns), from the contraction held in part.
+  auto finish_grad_x = [&](int kk) {
+    if (!grad_x) return;
+    for (int e = tid; e < BT * nx; e += nthr) {
+      const int n = e / nx, c = e - n * nx, bb = b0 + n;
+      const float v = column_sum(n, c);
+      if (bb < B) grad_x[((long long)bb * K + kk) * n_in + xa + c] = v;
+    }
+  };
+
+  // Per step: (A) finish the previous step's contraction (grad_x columns and
+  // the carry of the owned units), then dA of the owned units, broadcast to
+  // every block; cluster barrier; (B) contract the full dA with the owned
+  // columns into part; block barrier.
   for (int k = K - 1; k >= 0; --k) {
     float* buf = dAf + (k & 1) * BT * H3;
-    for (int e = tid; e < BT * Hc; e += nthr) {
+    float cg_[kItemsPerThread], cgg[kItemsPerThread], chh[kItemsPerThread], cup[kItemsPerThread];
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) { cg_[q] = pg[q]; cgg[q] = pgg[q]; chh[q] = phh[q]; cup[q] = pup[q]; }
+    load_act(k - 1);
+    if (k < K - 1) finish_grad_x(k + 1);
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) {
+      const int e = tid + q * nthr;
+      if (e >= BT * Hc) break;
       const int n = e / Hc, u = e - n * Hc, bb = b0 + n;
       const int unit = r * Hc + u;
       float d0 = 0.f, d1 = 0.f, d2 = 0.f;
       if (bb < B) {
         const long long row = (long long)bb * K + k;
-        float delta = carry[e];
-        if (grad_h_seq) delta += grad_h_seq[row * H + unit];
+        float delta = ((k < K - 1) ? column_sum(n, nx + u) : 0.f) + cup[q];
         if (k == K - 1) {
           if (grad_h_last) delta += grad_h_last[(long long)bb * H + unit];
           if (y) delta += ldf(h_seq + row * H + unit) - y[(long long)bb * H + unit];
         }
-        const float gate = act[row * H3 + unit];
-        const float g = act[row * H3 + H + unit];
-        const float hh = act[row * H3 + 2 * H + unit];
-        const float dtb = dt[dt_stride ? bb : 0];
+        const float gate = cg_[q], g = cgg[q], hh = chh[q];
         d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
         d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
-        d0 = to_operand<MODE>(-dtb * delta * (g - hh) * gate * (1.f - gate));
+        d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
         stf(dA_out + row * H3 + unit, d0);
         stf(dA_out + row * H3 + H + unit, d1);
         stf(dA_out + row * H3 + 2 * H + unit, d2);
       }
       const int off = n * H3 + unit;
-      for (int q = 0; q < C; ++q) {
-        float* dst = cluster.map_shared_rank(buf, q);
+      for (int q2 = 0; q2 < C; ++q2) {
+        float* dst = cluster.map_shared_rank(buf, q2);
         dst[off] = d0;
         dst[off + H] = d1;
         dst[off + 2 * H] = d2;
@@ -230,35 +308,37 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
     }
     cluster.sync();
     if (dot) {
-      float acc[BT];
+      // two interleaved accumulator chains (even / odd rows), added at the end
+      float acc0[BT], acc1[BT];
 #pragma unroll
-      for (int n = 0; n < BT; ++n) acc[n] = 0.f;
-#pragma unroll 4
-      for (int row = r0; row < r1; ++row) {
-        const float w = Wc[(size_t)row * nJmax + jj];
+      for (int n = 0; n < BT; ++n) { acc0[n] = 0.f; acc1[n] = 0.f; }
+      int row = r0;
+#pragma unroll 2
+      for (; row + 1 < r1; row += 2) {
+        const float w0 = Wc[(size_t)row * nJmax + jj];
+        const float w1 = Wc[(size_t)(row + 1) * nJmax + jj];
 #pragma unroll
-        for (int n = 0; n < BT; ++n) acc[n] = fmaf(w, buf[n * H3 + row], acc[n]);
+        for (int n = 0; n < BT; ++n) {
+          acc0[n] = fmaf(w0, buf[n * H3 + row], acc0[n]);
+          acc1[n] = fmaf(w1, buf[n * H3 + row + 1], acc1[n]);
+        }
+      }
+      if (row < r1) {
+        const float w0 = Wc[(size_t)row * nJmax + jj];
+#pragma unroll
+        for (int n = 0; n < BT; ++n) acc0[n] = fmaf(w0, buf[n * H3 + row], acc0[n]);
       }
 #pragma unroll
-      for (int n = 0; n < BT; ++n) part[(size_t)(s * BT + n) * nJmax + jj] = acc[n];
-    }
-    __syncthreads();
-    for (int e = tid; e < BT * nJ; e += nthr) {
-      const int n = e / nJ, c = e - n * nJ, bb = b0 + n;
-      float v = 0.f;
-      for (int q = 0; q < S; ++q) v += part[(size_t)(q * BT + n) * nJmax + c];
-      if (c < nx) {
-        if (grad_x && bb < B) grad_x[((long long)bb * K + k) * n_in + xa + c] = v;
-      } else {
-        carry[n * Hc + (c - nx)] = v;
-      }
+      for (int n = 0; n < BT; ++n) part[(size_t)(s * BT + n) * nJmax + jj] = acc0[n] + acc1[n];
     }
     __syncthreads();
   }
+  finish_grad_x(0);
   if (grad_h0) {
     for (int e = tid; e < BT * Hc; e += nthr) {
       const int n = e / Hc, u = e - n * Hc, bb = b0 + n;
-      if (bb < B) grad_h0[(long long)bb * H + r * Hc + u] = carry[e];
+      const float v = column_sum(n, nx + u);
+      if (bb < B) grad_h0[(long long)bb * H + r * Hc + u] = v;
     }
   }
 }
@@ -270,14 +350,14 @@ constexpr size_t kSmemLimit = 200 * 1024;
 
 size_t fwd_smem(const Layout& L, int C, int BT, int S) {
   const int Hc = L.H / C;
-  return sizeof(float) * ((size_t)L.Zc * 3 * Hc + 2 * (size_t)BT * L.Zc + (size_t)S * BT * 3 * Hc);
+  return sizeof(float) * ((size_t)L.Zc * 3 * Hc + 2 * (size_t)BT * L.Zc + (size_t)S * BT * 3 * Hc +
+                          3 * (size_t)Hc + BT);
 }
 
 size_t bwd_smem(const Layout& L, int C, int BT, int S) {
   const int Hc = L.H / C;
   const int nJmax = (L.n_in + C - 1) / C + Hc;
-  return sizeof(float) * ((size_t)L.H3 * nJmax + 2 * (size_t)BT * L.H3 + (size_t)BT * Hc +
-                          (size_t)S * BT * nJmax);
+  return sizeof(float) * ((size_t)L.H3 * nJmax + 2 * (size_t)BT * L.H3 + (size_t)S * BT * nJmax + BT);
 }
 
 // Cluster size from the hidden size alone (so a sample's arithmetic does not
@@ -304,18 +384,24 @@ bool plan(const Layout& L, bool forward, ClusterPlan* p) {
   if (!C) return false;
   const int Hc = L.H / C;
   const int width = forward ? Hc : (L.n_in + C - 1) / C + Hc;
-  const int S = std::max(1, std::min(8, kClusterThreads / width));
+  const int S = std::max(1, std::min(kMaxSplit, kClusterThreads / width));
   int BT = 16;
   const int bts[5] = {1, 2, 4, 8, 16};
   for (int t : bts)
     if ((long long)(L.B + t - 1) / t * C <= 2 * kNumSMs) { BT = t; break; }
+  const int threads = std::min(kClusterThreads, (width * S + 31) / 32 * 32);
   auto smem = [&](int bt) { return forward ? fwd_smem(L, C, bt, S) : bwd_smem(L, C, bt, S); };
-  while (BT > 1 && smem(BT) > kSmemLimit) BT /= 2;
-  if (smem(BT) > kSmemLimit) return false;
+  auto fits = [&](int bt) {
+    const long long items = forward ? (long long)bt * L.n_in : (long long)bt * Hc;
+    const int per = forward ? kXPerThread : kItemsPerThread;
+    return smem(bt) <= kSmemLimit && items <= (long long)per * threads;
+  };
+  while (BT > 1 && !fits(BT)) BT /= 2;
+  if (!fits(BT)) return false;
   p->C = C;
   p->BT = BT;
   p->S = S;
-  p->threads = std::min(kClusterThreads, (width * S + 31) / 32 * 32);
+  p->threads = threads;
   p->smem = smem(BT);
   return true;
 }
