@@ -72,37 +72,62 @@ def fp32_alu_peak_tflops(sm_mhz):
 # per-kernel algorithmic work (per launch) for the roofline
 # ----------------------------------------------------------------------------
 
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor throughput
+
+
 def kernel_work(name, w, n_split):
-    """(bound, amount per launch, unit) for a kernel of workload w."""
+    """(flops, bytes, flop engine) of one launch of kernel `name` on workload w.
+
+    Bytes are algorithmic: every operand read once and every result written
+    once (saved activations and dA included, they are this path's own data).
+    """
     B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
-    Zc, H3 = n_in + H, 3 * H
+    Zc, H3, R = n_in + H, 3 * H, w.B * w.K
     s = 2 if w.math == wl.MATH_BF16 else 4
-    if name.startswith("cfc_fwd") or name.startswith("cfc_bwd"):
-        return ("flop", 2.0 * B * K * H3 * Zc)
+    N = w.N
+    if name.startswith("cfc_fwd"):
+        flops = 2.0 * R * H3 * Zc
+        byts = R * n_in * s + R * H * s + R * H3 * 4 + B * H * s + H3 * Zc * s
+        return flops, byts, "alu"
+    if name.startswith("cfc_bwd"):
+        flops = 2.0 * R * H3 * Zc
+        byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * Zc * s
+        return flops, byts, "alu"
     if name.startswith("wgrad"):
-        return ("flop", 2.0 * B * K * H3 * (Zc + 1))
+        flops = 2.0 * R * H3 * (Zc + 1)
+        byts = R * H3 * s + R * Zc * s + n_split * N * 4
+        return flops, byts, ("tensor" if name.endswith("_tc") else "alu")
     if name == "reduce_axis0":
-        N = w.N
-        return ("byte", 4.0 * (n_split * N + N))
+        return 0.0, 4.0 * (n_split * N + N), "alu"
     if name == "prep_wt":
-        return ("byte", 2.0 * H3 * Zc * s)
-    return ("byte", 0.0)
+        return 0.0, 2.0 * H3 * Zc * s, "alu"
+    return 0.0, 0.0, "alu"
 
 
-def roofline_for(name, w, n_split, avg_ms, peaks, sustained):
-    kind, amount = kernel_work(name, w, n_split)
-    if kind == "byte":
-        achieved = amount / (avg_ms * 1e-3) / 1e9
-        peak = peaks["hbm"]
-        return dict(kernel=name, bound="hbm", achieved=achieved, peak=peak, unit="GB/s",
-                    frac=achieved / peak, traffic=None, algorithmic_per_launch=amount,
-                    peak_source=f"{peaks['source']} hbm_gbs")
-    achieved = amount / (avg_ms * 1e-3) / 1e12
-    # SIMT kernels run fp32 FFMA on the CUDA cores: ALU bound against the FFMA peak.
-    peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
-    return dict(kernel=name, bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s",
-                frac=achieved / peak, traffic=None, algorithmic_per_launch=amount,
-                peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz")
+def roofline_for(name, w, n_split, avg_ms, peaks, sustained=False):
+    flops, byts, engine = kernel_work(name, w, n_split)
+    t = avg_ms * 1e-3
+    if engine == "tensor":
+        bf16 = peaks["bf16_sust"] if sustained else peaks["bf16"]
+        flop_peak = bf16 * (TF32_OVER_BF16 if w.math == wl.MATH_TF32 else 1.0)
+        flop_src = (f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'}"
+                    + (" x 1.1/2.25 (TF32)" if w.math == wl.MATH_TF32 else ""))
+        flop_bound = "tensor"
+    else:
+        flop_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+        flop_src = f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"
+        flop_bound = "alu"
+    t_flop = flops / (flop_peak * 1e12) if flops else 0.0
+    t_byte = byts / (peaks["hbm"] * 1e9) if byts else 0.0
+    if t_flop >= t_byte and flops:
+        achieved = flops / t / 1e12
+        return dict(kernel=name, bound=flop_bound, achieved=achieved, peak=flop_peak, unit="TFLOP/s",
+                    frac=achieved / flop_peak, traffic=None, algorithmic_flops_per_launch=flops,
+                    algorithmic_bytes_per_launch=byts, peak_source=flop_src)
+    achieved = byts / t / 1e9
+    return dict(kernel=name, bound="hbm", achieved=achieved, peak=peaks["hbm"], unit="GB/s",
+                frac=achieved / peaks["hbm"], traffic=None, algorithmic_flops_per_launch=flops,
+                algorithmic_bytes_per_launch=byts, peak_source=f"{peaks['source']} hbm_gbs")
 
 
 # ----------------------------------------------------------------------------
@@ -193,14 +218,8 @@ class Path:
         self.out_host = [torch.empty(t.shape, dtype=f32).pin_memory() for t in (self.gWi, self.gWr, self.gb)]
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
         self.d2h_bytes = sum(v.numel() * v.element_size() for v in self.out_host)
-        # split count of the GEMM gradient path (as the library computes it)
-        if w.grad_path == wl.GRAD_SCRATCH:
-            self.n_split = B
-        else:
-            tiles = ((3 * H + 63) // 64) * ((n_in + H + 1 + 63) // 64)
-            split = max(1, min(-(-4 * SM_COUNT // tiles), min(B * K, 256)))
-            rps = -(-(B * K) // split)
-            self.n_split = -(-(B * K) // rps)
+        # rows of the gradient partials that reduce_axis0 sums (from the library)
+        self.n_split = cfc.cfc_kloop_grad_splits(B, K, n_in, H, w.math, w.grad_path)
 
     def step(self):
         t, cfc, w = self.t, self.cfc, self.w

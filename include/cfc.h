@@ -94,6 +94,17 @@ long long cfc_per_sample_length(int n_in, int n_hid);
  * passed to the backward of the same inputs. */
 size_t cfc_kloop_workspace_bytes(int B, int K, int n_in, int n_hid, int math, int grad_path);
 
+/* Number of rows S of the gradient partials [S, N] that the backward sums with
+ * reduce_axis0 (B for CFC_GRAD_SCRATCH; a fixed split of the B*K rows for
+ * CFC_GRAD_GEMM).  Host-only; 0 for invalid arguments. */
+int cfc_kloop_grad_splits(int B, int K, int n_in, int n_hid, int math, int grad_path);
+
+/* Device-side error word of the library (host-blocking diagnostic: waits for
+ * all work on the device).  Returns 0 if no kernel has reported an error,
+ * 1 if a tensor-core kernel gave up a bounded wait (its outputs are then not
+ * valid), or CFC_ERR_DEVICE if the word cannot be read.  clear != 0 resets it. */
+int cfc_device_error(int clear);
+
 /* Forward K-loop.
  *   x      [B, K, n_in]      (float or bf16 by `math`)
  *   h0     [B, n_hid]        (float or bf16)

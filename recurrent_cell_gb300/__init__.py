@@ -56,6 +56,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.reduce_axis0.restype = i32
     lib.cfc_kloop_forward_backward_static.argtypes = [vp] * 6 + [i32] * 6 + [vp] * 3 + [vp] * 6 + [vp]
     lib.cfc_kloop_forward_backward_static.restype = i32
+    lib.cfc_kloop_grad_splits.argtypes = [i32] * 6
+    lib.cfc_kloop_grad_splits.restype = i32
+    lib.cfc_device_error.argtypes = [i32]
+    lib.cfc_device_error.restype = i32
     lib.cfc_trace_enable.argtypes = [i32]
     lib.cfc_trace_enable.restype = i32
     lib.cfc_trace_count.argtypes = []
@@ -76,6 +80,15 @@ def cfc_per_sample_length(n_in: int, n_hid: int) -> int:
 
 def cfc_kloop_workspace_bytes(B, K, n_in, n_hid, math, grad_path=GRAD_SCRATCH) -> int:
     return int(load_library().cfc_kloop_workspace_bytes(B, K, n_in, n_hid, math, grad_path))
+
+
+def cfc_kloop_grad_splits(B, K, n_in, n_hid, math, grad_path=GRAD_SCRATCH) -> int:
+    return int(load_library().cfc_kloop_grad_splits(B, K, n_in, n_hid, math, grad_path))
+
+
+def cfc_device_error(clear: bool = False) -> int:
+    """0 unless a kernel reported a device-side error (waits for the device)."""
+    return int(load_library().cfc_device_error(1 if clear else 0))
 
 
 def _torch():

@@ -60,7 +60,7 @@ bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Lay
   if (grad_path == CFC_GRAD_SCRATCH) {
     L->n_split = B;
     L->rows_per_split = K;
-  } else {
+  } else if (math == CFC_MATH_FP32) {
     // Fixed split of the B*K rows into row blocks: about four blocks of the
     // 64 x 64 output tiling per SM.  Depends on the sizes only, so results are
     // reproducible for a given configuration.
@@ -69,6 +69,17 @@ bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Lay
     split = std::max(1ll, std::min(split, std::min<long long>(L->R, 256)));
     L->rows_per_split = (L->R + split - 1) / split;
     L->n_split = (int)((L->R + L->rows_per_split - 1) / L->rows_per_split);
+  } else {
+    // Tensor-core contraction: about two blocks per SM over its 128-row x
+    // N-block tiling; row blocks are whole multiples of 64 rows (one bf16
+    // chunk, two TF32 chunks).
+    const long long tiles = tc_wgrad_blocks(n_in, n_hid);
+    long long split = std::max(1ll, (2ll * kNumSMs + tiles - 1) / tiles);
+    split = std::min(split, std::max(1ll, L->R / 64));
+    long long rps = (L->R + split - 1) / split;
+    rps = (rps + 63) / 64 * 64;
+    L->rows_per_split = rps;
+    L->n_split = (int)((L->R + rps - 1) / rps);
   }
   size_t off = 0;
   L->off_wt = off;   off = align256(off + (size_t)L->Zc * L->H3 * L->elem);
@@ -108,6 +119,14 @@ long long cfc_per_sample_length(int n_in, int n_hid) {
   if (n_in < 1 || n_hid < 1) return 0;
   return 3ll * (n_in + n_hid + 1) * n_hid;
 }
+
+int cfc_kloop_grad_splits(int B, int K, int n_in, int n_hid, int math, int grad_path) {
+  Layout L;
+  if (!make_layout(B, K, n_in, n_hid, math, grad_path, &L)) return 0;
+  return L.n_split;
+}
+
+int cfc_device_error(int clear) { return read_device_error(clear); }
 
 size_t cfc_kloop_workspace_bytes(int B, int K, int n_in, int n_hid, int math, int grad_path) {
   Layout L;
@@ -181,7 +200,8 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;
   float* part = (grad_path == CFC_GRAD_SCRATCH) ? per_sample_scratch
                                                 : reinterpret_cast<float*>(a.ws + L.off_part);
-  e = launch_wgrad_simt(L, a, part, L.n_split, L.rows_per_split, s);
+  e = (math == CFC_MATH_FP32) ? launch_wgrad_simt(L, a, part, L.n_split, L.rows_per_split, s)
+                              : launch_wgrad_tc(L, a, part, s);
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;
   ReduceOut out{};
   out.nseg = 3;

@@ -112,6 +112,13 @@ cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t 
 cudaError_t launch_forward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s);
 cudaError_t launch_backward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s);
 cudaError_t launch_backward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
+// Tensor-core (tcgen05) gradient contraction of the TF32 / bf16 modes.
+cudaError_t launch_wgrad_tc(const Layout& L, const CfcArgs& a, float* out, cudaStream_t s);
+int tc_wgrad_blocks(int n_in, int n_hid);
+// Reads (and optionally clears) the device-side error word of the
+// tensor-core kernels; blocks until the device is idle.
+int read_device_error(int clear);
+
 cudaError_t launch_wgrad_simt(const Layout& L, const CfcArgs& a, float* out, int n_split,
                               long long rows_per_split, cudaStream_t s);
 

@@ -1,0 +1,140 @@
+// tc_common.cuh -- inline-PTX helpers for the 5th-generation tensor cores
+// (tcgen05) of sm_100/sm_103: tensor-memory (TMEM) allocation, shared-memory
+// matrix descriptors, instruction descriptors, MMA issue and completion,
+// TMEM -> register loads, and bounded mbarrier waits.
+//
+// Operand tiles are K-major with the 128-byte swizzle: a tile is a stack of
+// rows of 128 bytes (64 bf16 or 32 tf32 values along K), 8 rows form a
+// 1024-byte atom, and inside each row the 16-byte chunk c of row r is stored
+// at chunk position c ^ (r % 8).  Tiles start on 1024-byte boundaries.  A K
+// extent larger than 128 bytes is a sequence of such tiles ("K atoms").
+#pragma once
+
+#include <stdint.h>
+
+namespace cfc {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of (row, byte-in-row kb) inside a 128B-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t kb) {
+  return row * 128u + ((((kb >> 4) ^ row) & 7u) << 4) + (kb & 15u);
+}
+
+// Shared-memory matrix descriptor of a K-major, 128B-swizzled tile whose
+// first row starts at `saddr` (plus a K step inside the 128-byte row, a
+// multiple of 32 bytes).  Stride between 8-row groups: 1024 bytes.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);   // start address
+  d |= (uint64_t)1u << 16;                   // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1u << 46;                   // descriptor version of sm_100
+  d |= (uint64_t)2u << 61;                   // layout: 128-byte swizzle
+  return d;
+}
+
+// Operand formats of the instruction descriptor.
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+
+// Instruction descriptor of kind::f16 / kind::tf32: fp32 accumulator, A and B
+// K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t fmt) {
+  return (1u << 4)                 // D format: f32
+         | (fmt << 7) | (fmt << 10)  // A, B format
+         | ((N >> 3) << 17)        // N / 8
+         | ((M >> 4) << 24);       // M / 16
+}
+
+// --- mbarrier -----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` to complete, giving up after `max_polls` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_polls) {
+  for (uint32_t i = 0; i < max_polls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// --- TMEM -----------------------------------------------------------------------
+// Executed by one whole warp.  Writes the TMEM base address to *dst (shared).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the tensor cores (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --- MMA ------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+// The mbarrier receives one arrival when all previously issued MMAs of this
+// thread have completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// --- TMEM -> registers ---------------------------------------------------------
+// 32 lanes x 32 bit, 16 consecutive columns: thread t of the warp receives
+// lane (base lane + t), columns [col, col + 16).  The wait for the load is in
+// the same asm statement, so the registers are valid when it returns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace tc
+}  // namespace cfc

@@ -122,6 +122,7 @@ class CfcRun:
     def results(self):
         torch = torch_mod()
         torch.cuda.synchronize()
+        assert cfc.cfc_device_error(clear=True) == 0, "a kernel reported a device-side error"
         out = dict(h_seq=host(self.h_seq), grad_W_in=host(self.gWi), grad_W_rec=host(self.gWr),
                    grad_b=host(self.gb), grad_h0=host(self.gh0), grad_x=host(self.gx))
         if self.scratch is not None:
