@@ -4,6 +4,8 @@
 // anything, then enqueues kernels on the caller's stream.  No allocation, no
 // synchronisation, no host read of device data.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <vector>
 
 #include "cfc_internal.cuh"
@@ -40,6 +42,15 @@ void trace_begin(const char* name, cudaStream_t s) {
 void trace_end(cudaStream_t s) {
   if (!g_trace_on || g_trace.empty()) return;
   cudaEventRecord(g_trace.back().stop, s);
+}
+
+int kernel_choice() {
+  const char* v = getenv("CFC_KLOOP_KERNELS");
+  if (!v) return kAuto;
+  if (strcmp(v, "cluster") == 0) return kCluster;
+  if (strcmp(v, "simt") == 0) return kSimt;
+  if (strcmp(v, "tc") == 0) return kTc;
+  return kAuto;
 }
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -126,7 +137,12 @@ int cfc_kloop_grad_splits(int B, int K, int n_in, int n_hid, int math, int grad_
   return L.n_split;
 }
 
-int cfc_device_error(int clear) { return read_device_error(clear); }
+int cfc_device_error(int clear) {
+  const int a = read_device_error(clear);
+  const int b = read_tc_kloop_error(clear);
+  if (a < 0 || b < 0) return CFC_ERR_DEVICE;
+  return (a || b) ? 1 : 0;
+}
 
 size_t cfc_kloop_workspace_bytes(int B, int K, int n_in, int n_hid, int math, int grad_path) {
   Layout L;
@@ -158,7 +174,8 @@ int cfc_kloop_forward(const void* x, const void* h0, const void* W_in, const voi
   a.x = x; a.h0 = h0; a.W_in = W_in; a.W_rec = W_rec; a.b = b; a.dt = dt; a.dt_stride = dt_stride;
   a.h_seq = h_seq; a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_forward_cluster(L, a, s);
+  cudaError_t e = launch_forward_tc(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_forward_cluster(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_forward_simt(L, a, s);
   return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
 }

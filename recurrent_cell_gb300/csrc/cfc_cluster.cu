@@ -103,6 +103,10 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
   // its shared memory.
   cluster.sync();
 
+  uint32_t peer_zb[8];                // shared::cluster address of zb in every block
+#pragma unroll
+  for (int p = 0; p < 8; ++p) peer_zb[p] = (p < C) ? dsmem_map(smem_addr(zb), (uint32_t)p) : 0u;
+
   // thread -> (unit u, column group s) of the dot products
   const int u = tid % Hc, s = tid / Hc;
   const bool dot = s < S;
@@ -144,8 +148,13 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
       load_x(k + 2);
     }
     __syncthreads();
-    // Cell of (sample n, unit u) pairs; partial sums added in the fixed order s = 0..S-1.
-    for (int e = tid; e < BT * Hc; e += nthr) {
+    // Cell of (sample n, unit u) pairs; partial sums added in the fixed order
+    // s = 0..S-1.  Results stay in registers until after the barrier arrive.
+    float rg[kItemsPerThread], rgg[kItemsPerThread], rhh[kItemsPerThread], rh[kItemsPerThread];
+#pragma unroll
+    for (int it = 0; it < kItemsPerThread; ++it) {
+      const int e = tid + it * nthr;
+      if (e >= BT * Hc) break;
       const int n = e / Hc, uu = e - n * Hc, bb = b0 + n;
       const int unit = r * Hc + uu;
       float A[3];
@@ -165,20 +174,33 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
       const float hh = tanhf(A[2]);
       const float gate = 1.f / (1.f + expf(A[0] * dts[n]));
       const float h = gate * g + (1.f - gate) * hh;
+      rg[it] = gate; rgg[it] = g; rhh[it] = hh; rh[it] = h;
       float hop = 0.f;
       if (bb < B) {
-        const long long row = (long long)bb * K + k;
-        act[row * H3 + unit] = gate;
-        act[row * H3 + H + unit] = g;
-        act[row * H3 + 2 * H + unit] = hh;
-        stf(h_seq + row * H + unit, h);
         if constexpr (sizeof(T) == 2) hop = round_bf16(h);   // the stored bf16 state
         else hop = to_operand<MODE>(h);
       }
-      const int off = n * Zc + n_in + unit;
-      for (int q = 0; q < C; ++q) cluster.map_shared_rank(zn, q)[off] = hop;
+      const uint32_t off = (uint32_t)((((k + 1) & 1) * BT * Zc + n * Zc + n_in + unit) * 4);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < C) dsmem_st(peer_zb[q] + off, hop);
     }
-    cluster.sync();
+    cluster_arrive_release();
+#pragma unroll
+    for (int it = 0; it < kItemsPerThread; ++it) {
+      const int e = tid + it * nthr;
+      if (e >= BT * Hc) break;
+      const int n = e / Hc, uu = e - n * Hc, bb = b0 + n;
+      if (bb < B) {
+        const int unit = r * Hc + uu;
+        const long long row = (long long)bb * K + k;
+        act[row * H3 + unit] = rg[it];
+        act[row * H3 + H + unit] = rgg[it];
+        act[row * H3 + 2 * H + unit] = rhh[it];
+        stf(h_seq + row * H + unit, rh[it]);
+      }
+    }
+    cluster_wait_acquire();
   }
 }
 
@@ -219,6 +241,9 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
   for (int e = tid; e < BT; e += nthr) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
   cluster.sync();
 
+  uint32_t peer_dA[8];                // shared::cluster address of dAf in every block
+#pragma unroll
+  for (int p = 0; p < 8; ++p) peer_dA[p] = (p < C) ? dsmem_map(smem_addr(dAf), (uint32_t)p) : 0u;
   const int jj = tid % nJmax, s = tid / nJmax;
   const bool dot = (s < S) && (jj < nJ);
   const int r0 = (int)((long long)s * H3 / S), r1 = (int)((long long)(s + 1) * H3 / S);
@@ -276,6 +301,7 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
     for (int q = 0; q < kItemsPerThread; ++q) { cg_[q] = pg[q]; cgg[q] = pgg[q]; chh[q] = phh[q]; cup[q] = pup[q]; }
     load_act(k - 1);
     if (k < K - 1) finish_grad_x(k + 1);
+    float rd0[kItemsPerThread], rd1[kItemsPerThread], rd2[kItemsPerThread];
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) {
       const int e = tid + q * nthr;
@@ -294,19 +320,33 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
         d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
         d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
         d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
-        stf(dA_out + row * H3 + unit, d0);
-        stf(dA_out + row * H3 + H + unit, d1);
-        stf(dA_out + row * H3 + 2 * H + unit, d2);
       }
-      const int off = n * H3 + unit;
-      for (int q2 = 0; q2 < C; ++q2) {
-        float* dst = cluster.map_shared_rank(buf, q2);
-        dst[off] = d0;
-        dst[off + H] = d1;
-        dst[off + 2 * H] = d2;
+      rd0[q] = d0; rd1[q] = d1; rd2[q] = d2;
+      const uint32_t off = (uint32_t)(((k & 1) * BT * H3 + n * H3 + unit) * 4);
+#pragma unroll
+      for (int q2 = 0; q2 < 8; ++q2) {
+        if (q2 < C) {
+          dsmem_st(peer_dA[q2] + off, d0);
+          dsmem_st(peer_dA[q2] + off + 4 * H, d1);
+          dsmem_st(peer_dA[q2] + off + 8 * H, d2);
+        }
       }
     }
-    cluster.sync();
+    cluster_arrive_release();
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) {
+      const int e = tid + q * nthr;
+      if (e >= BT * Hc) break;
+      const int n = e / Hc, u = e - n * Hc, bb = b0 + n;
+      if (bb < B) {
+        const int unit = r * Hc + u;
+        const long long row = (long long)bb * K + k;
+        stf(dA_out + row * H3 + unit, rd0[q]);
+        stf(dA_out + row * H3 + H + unit, rd1[q]);
+        stf(dA_out + row * H3 + 2 * H + unit, rd2[q]);
+      }
+    }
+    cluster_wait_acquire();
     if (dot) {
       // two interleaved accumulator chains (even / odd rows), added at the end
       float acc0[BT], acc1[BT];
@@ -394,7 +434,8 @@ bool plan(const Layout& L, bool forward, ClusterPlan* p) {
   auto fits = [&](int bt) {
     const long long items = forward ? (long long)bt * L.n_in : (long long)bt * Hc;
     const int per = forward ? kXPerThread : kItemsPerThread;
-    return smem(bt) <= kSmemLimit && items <= (long long)per * threads;
+    return smem(bt) <= kSmemLimit && items <= (long long)per * threads &&
+           (long long)bt * Hc <= (long long)kItemsPerThread * threads;
   };
   while (BT > 1 && !fits(BT)) BT /= 2;
   if (!fits(BT)) return false;
@@ -470,22 +511,11 @@ cudaError_t bwd_mode(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cu
 
 }  // namespace
 
-// Kernel selection for the K loop: CFC_KLOOP_KERNELS=cluster forces the
-// cluster kernels whenever they fit, =simt forces the streaming kernels,
-// anything else ("auto") uses the cluster kernels when their grid stays
-// within about two waves of blocks.  Read on every call.
 namespace {
-int kernel_choice() {
-  const char* v = getenv("CFC_KLOOP_KERNELS");
-  if (v && strcmp(v, "cluster") == 0) return 1;
-  if (v && strcmp(v, "simt") == 0) return 2;
-  return 0;
-}
-
 bool use_cluster(const Layout& L, bool forward, ClusterPlan* p) {
   const int choice = kernel_choice();
-  if (choice == 2 || !plan(L, forward, p)) return false;
-  if (choice == 1) return true;
+  if (choice == kSimt || choice == kTc || !plan(L, forward, p)) return false;
+  if (choice == kCluster) return true;
   return (long long)(L.B + p->BT - 1) / p->BT * p->C <= 2 * kNumSMs;
 }
 }  // namespace

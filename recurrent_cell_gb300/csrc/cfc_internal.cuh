@@ -54,6 +54,40 @@ __device__ __forceinline__ float ld_operand(const T* p) {
 __device__ __forceinline__ void stf(float* p, float v) { *p = v; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// Distributed shared memory: 32-bit shared::cluster address of the variable at
+// local shared address `local` in block `rank` of the cluster, and stores to it.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void dsmem_st_bf16(uint32_t addr, float v) {
+  const unsigned short b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(b) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Split cluster barrier: arrive with release semantics (orders this thread's
+// earlier writes, e.g. distributed shared-memory stores, before the peers'
+// acquire) and wait with acquire semantics.  Global stores issued between the
+// two are not covered by the release, so the arrive does not wait for them.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets, every region 256-byte aligned).
 // ---------------------------------------------------------------------------
@@ -105,6 +139,17 @@ struct CfcArgs {
 };
 
 cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
+// K-loop kernel family: CFC_KLOOP_KERNELS=tc | cluster | simt forces one
+// family where it supports the sizes (read on every call); anything else
+// selects automatically.
+enum KernelChoice { kAuto = 0, kCluster = 1, kSimt = 2, kTc = 3 };
+int kernel_choice();
+
+// Tensor-core forward (TF32 / bf16 modes); cudaErrorNotSupported, launching
+// nothing, when the sizes do not fit its plan or another family is forced.
+cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
+int read_tc_kloop_error(int clear);
+
 // Cluster kernels (weights resident in shared memory of a block cluster).
 // Return cudaErrorNotSupported, launching nothing, when no cluster plan fits
 // the sizes or (for kernel selection "auto") the plan would need more than

@@ -1,0 +1,439 @@
+// cfc_tc_kloop.cu -- forward K loop of the TF32 / bf16 modes on the tcgen05
+// tensor cores.
+//
+// A cluster of C = H/32 blocks owns a tile of Bt samples for the whole K loop;
+// block r owns hidden units [32r, 32r+32).  Per step the block computes
+//
+//   D[128 x Bt] = Wr[128 x Zc] * Z^T          (one M=128, N=Bt MMA chain)
+//
+// where Wr stacks the W_cat = [W_in | W_rec] rows of its units for the three
+// heads (rows 0-31 f, 32-63 g, 64-95 h~, 96-127 zero) and Z holds the operand
+// rows z_n = [x_k; h_k] of the Bt samples.  Wr stays in shared memory for the
+// whole launch (K-major, 128B-swizzled, 96 KB for Zc*element = 768 B).  Z is
+// double-buffered: while step k reads Z[k&1], every block writes its slice of
+// h_{k+1} (32 units x Bt samples) into Z[(k+1)&1] of every block of the cluster
+// through distributed shared memory, and x_{k+1} (prefetched into registers)
+// locally.  One cluster barrier per step publishes the slices.
+//
+// Epilogue per step: warps w and w+4 read TMEM lane quadrant w (w = 0, 1, 2:
+// the f, g, h~ rows) with tcgen05.ld, stage the pre-activations in padded
+// shared memory, and all threads apply the cell to (unit, sample) items.
+//
+// The MMA waits are bounded; a timeout records an error in the device error
+// word and the launch keeps its barrier schedule so that no block of the
+// cluster is left waiting.
+#include <algorithm>
+#include <cooperative_groups.h>
+
+#include "cfc_internal.cuh"
+#include "tc_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace cfc {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnits = 32;                 // hidden units per block
+constexpr uint32_t kMaxPolls = 1u << 24;
+constexpr size_t kSmemMax = 227 * 1024;
+constexpr int kXRegs = 32;                 // prefetched x values per thread (scalar path)
+constexpr int kXUnits = 4;                 // prefetched 16-byte x units per thread
+
+__device__ int g_tc_kloop_error = 0;
+
+struct TcPlan {
+  int C = 0, Bt = 0, nA = 0;
+  size_t smem = 0, off_z = 0, off_ex = 0, off_bs = 0, off_dt = 0;
+  uint32_t tmem_cols = 0;
+};
+
+template <typename ET>
+__device__ __forceinline__ void st_elem(uint8_t* p, float v) {
+  if constexpr (sizeof(ET) == 4) *reinterpret_cast<float*>(p) = v;
+  else *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+}
+
+// 16 bytes of consecutive K elements starting at p (4 fp32 or 8 bf16), with
+// the mode's operand rounding, as a 16-byte swizzle unit.
+template <int MODE>
+__device__ __forceinline__ uint4 round_unit(uint4 u) {
+  if constexpr (MODE == CFC_MATH_TF32) {
+    u.x = __float_as_uint(round_tf32(__uint_as_float(u.x)));
+    u.y = __float_as_uint(round_tf32(__uint_as_float(u.y)));
+    u.z = __float_as_uint(round_tf32(__uint_as_float(u.z)));
+    u.w = __float_as_uint(round_tf32(__uint_as_float(u.w)));
+  }
+  return u;
+}
+template <typename ET, int MODE>
+__device__ __forceinline__ uint4 load_unit(const ET* p) {
+  uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  if constexpr (MODE == CFC_MATH_TF32) {
+    u.x = __float_as_uint(round_tf32(__uint_as_float(u.x)));
+    u.y = __float_as_uint(round_tf32(__uint_as_float(u.y)));
+    u.z = __float_as_uint(round_tf32(__uint_as_float(u.z)));
+    u.w = __float_as_uint(round_tf32(__uint_as_float(u.w)));
+  }
+  return u;
+}
+
+// Byte offset of operand element (row, kk) in a stack of K atoms of `rows` rows.
+template <typename ET>
+__device__ __forceinline__ uint32_t kmajor_off(int row, int kk, int rows) {
+  const uint32_t kb = (uint32_t)kk * sizeof(ET);
+  return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
+}
+
+template <typename ET, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __restrict__ W_in,
+             const ET* __restrict__ W_rec, const float* __restrict__ bias, const float* __restrict__ dt,
+             int dt_stride, int B, int K, int n_in, int H, int Bt, int nA, uint32_t off_z,
+             uint32_t off_ex, uint32_t off_bs, uint32_t off_dt, uint32_t tmem_cols,
+             ET* __restrict__ h_seq, float* __restrict__ act) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int r = (int)cluster.block_rank();
+  const int Zc = n_in + H, H3 = 3 * H;
+  const int Kpad = nA * (128 / (int)sizeof(ET));
+  const int b0 = (int)(blockIdx.x / C) * Bt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ex_ld = Bt + 1;
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ws = sm;                                  // nA x [128 rows][128 B]
+  uint8_t* Zs = sm + off_z;                          // 2 x nA x [Bt rows][128 B]
+  float* ex = reinterpret_cast<float*>(sm + off_ex); // [3][32][Bt+1]
+  float* bs = reinterpret_cast<float*>(sm + off_bs); // [3][32]
+  float* dts = reinterpret_cast<float*>(sm + off_dt);// [Bt]
+  const uint32_t zbuf_bytes = (uint32_t)nA * Bt * 128;
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
+
+  // Resident A operand: rows (head c, unit u) of W_cat, zero rows 96..127 and
+  // zero K padding.  vec: n_in and H are multiples of one 16-byte unit, so a
+  // unit never straddles W_in / W_rec or x / h and is 16-byte aligned.
+  constexpr int EPU = 16 / (int)sizeof(ET);        // elements per 16-byte unit
+  const bool vec = (n_in % EPU == 0) && (H % EPU == 0);
+  const int upr = Kpad / EPU;                      // units per row
+  if (vec) {
+    for (int e = tid; e < 128 * upr; e += kThreads) {
+      const int i = e / upr, kk = (e - i * upr) * EPU;
+      const int c = i >> 5, u = i & 31;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (c < 3 && kk < Zc) {
+        const long long row = (long long)c * H + r * kUnits + u;
+        v = (kk < n_in) ? load_unit<ET, MODE>(W_in + row * n_in + kk)
+                        : load_unit<ET, MODE>(W_rec + row * H + (kk - n_in));
+      }
+      *reinterpret_cast<uint4*>(Ws + kmajor_off<ET>(i, kk, 128)) = v;
+    }
+    for (int e = tid; e < Bt * upr; e += kThreads) {
+      const int n = e / upr, kk = (e - n * upr) * EPU, bb = b0 + n;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (bb < B && kk < Zc)
+        v = (kk < n_in) ? load_unit<ET, MODE>(x + (long long)bb * K * n_in + kk)
+                        : load_unit<ET, MODE>(h0 + (long long)bb * H + (kk - n_in));
+      *reinterpret_cast<uint4*>(Zs + kmajor_off<ET>(n, kk, Bt)) = v;
+    }
+  } else {
+    for (int e = tid; e < 128 * Kpad; e += kThreads) {
+      const int i = e / Kpad, kk = e - i * Kpad;
+      const int c = i >> 5, u = i & 31;
+      float v = 0.f;
+      if (c < 3 && kk < Zc) {
+        const long long row = (long long)c * H + r * kUnits + u;
+        v = (kk < n_in) ? ld_operand<MODE>(W_in + row * n_in + kk)
+                        : ld_operand<MODE>(W_rec + row * H + (kk - n_in));
+      }
+      st_elem<ET>(Ws + kmajor_off<ET>(i, kk, 128), v);
+    }
+    // Operand rows of step 0: z_n = [x_0; h0], zero padding.
+    for (int e = tid; e < Bt * Kpad; e += kThreads) {
+      const int n = e / Kpad, kk = e - n * Kpad, bb = b0 + n;
+      float v = 0.f;
+      if (bb < B && kk < Zc)
+        v = (kk < n_in) ? ld_operand<MODE>(x + (long long)bb * K * n_in + kk)
+                        : ld_operand<MODE>(h0 + (long long)bb * H + (kk - n_in));
+      st_elem<ET>(Zs + kmajor_off<ET>(n, kk, Bt), v);
+    }
+  }
+  // The second buffer's padding columns stay zero for the whole launch.
+  for (int e = tid; e < Bt * Kpad; e += kThreads) {
+    const int n = e / Kpad, kk = e - n * Kpad;
+    if (kk >= Zc) st_elem<ET>(Zs + zbuf_bytes + kmajor_off<ET>(n, kk, Bt), 0.f);
+  }
+  for (int e = tid; e < 3 * kUnits; e += kThreads) bs[e] = bias[(e >> 5) * H + r * kUnits + (e & 31)];
+  for (int e = tid; e < Bt; e += kThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+
+  asm volatile("fence.proxy.async;" ::: "memory");
+  tc::fence_before_sync();
+  cluster.sync();               // also: every block is running before DSMEM writes
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
+  uint32_t peer_z[8];                 // shared::cluster address of Zs in every block
+#pragma unroll
+  for (int p = 0; p < 8; ++p) peer_z[p] = (p < C) ? dsmem_map(smem_addr(Zs), (uint32_t)p) : 0u;
+  const int nx = Bt * n_in;     // x values staged per step
+
+  for (int k = 0; k < K; ++k) {
+    uint8_t* zc = Zs + (k & 1) * zbuf_bytes;
+    uint8_t* zn = Zs + ((k + 1) & 1) * zbuf_bytes;
+    // x of the next step into registers while the MMAs run (16-byte units when
+    // vec, else single elements); raw bits, rounded when stored.
+    uint4 xu[kXUnits];
+    float xr[kXRegs];
+    if (vec) {
+      const int xupr = n_in / EPU;
+#pragma unroll
+      for (int q = 0; q < kXUnits; ++q) {
+        const int e = tid + q * kThreads;
+        const int n = e / xupr, kk = (e - n * xupr) * EPU, bb = b0 + n;
+        xu[q] = (e < Bt * xupr && k + 1 < K && bb < B)
+                    ? __ldg(reinterpret_cast<const uint4*>(x + ((long long)bb * K + k + 1) * n_in + kk))
+                    : make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kXRegs; ++q) {
+        const int e = tid + q * kThreads;
+        const int n = e / n_in, kk = e - n * n_in, bb = b0 + n;
+        xr[q] = (e < nx && k + 1 < K && bb < B) ? ldf(x + ((long long)bb * K + k + 1) * n_in + kk) : 0.f;
+      }
+    }
+    if (tid == 0) {
+      const uint32_t wa = tc::smem_u32(Ws), za = tc::smem_u32(zc);
+      for (int a = 0; a < nA; ++a) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t ad = tc::sdesc_k_sw128(wa + a * 128 * 128 + 32 * j);
+          const uint64_t bd = tc::sdesc_k_sw128(za + a * Bt * 128 + 32 * j);
+          if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad, bd, id, (a | j) != 0);
+          else tc::mma_bf16(tmem, ad, bd, id, (a | j) != 0);
+        }
+      }
+      tc::mma_commit(&bar);
+    }
+    if (!tc::mbar_wait(&bar, k & 1, kMaxPolls)) err = 1;
+    tc::fence_after_sync();
+    // TMEM -> shared: pre-activations of head w (lane quadrant w), columns split
+    // between warps w and w+4.
+    if ((warp & 3) < 3) {
+      const int c = warp & 3;
+      for (int q = warp >> 2; q < Bt / 16; q += 2) {
+        float v[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(32 * c) << 16) + (uint32_t)(16 * q), v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ex[(c * kUnits + lane) * ex_ld + 16 * q + i] = v[i];
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // Cell of (unit u, sample n) items; lanes of a warp take the 32 units of
+    // one sample (n is warp-uniform).  The results are kept in registers and
+    // written to global memory after the cluster barrier's arrive.
+    constexpr int kItems = 8;                  // items per thread (plan: 32*Bt <= 8*256)
+    float ig[kItems], igg[kItems], ihh[kItems], ih[kItems], hop[kItems];
+    // pass 1: cell math of all items
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      const int e = tid + q * kThreads;
+      hop[q] = 0.f;
+      if (e >= kUnits * Bt) break;
+      const int u = e & 31, n = e >> 5, bb = b0 + n;
+      const float af = ex[(0 * kUnits + u) * ex_ld + n] + bs[u];
+      const float ag = ex[(1 * kUnits + u) * ex_ld + n] + bs[kUnits + u];
+      const float ah = ex[(2 * kUnits + u) * ex_ld + n] + bs[2 * kUnits + u];
+      const float g = tanhf(ag);
+      const float hh = tanhf(ah);
+      const float gate = 1.f / (1.f + expf(af * dts[n]));
+      const float h = gate * g + (1.f - gate) * hh;
+      ig[q] = gate; igg[q] = g; ihh[q] = hh; ih[q] = h;
+      if (bb < B) {
+        if constexpr (sizeof(ET) == 2) hop[q] = round_bf16(h);
+        else hop[q] = round_tf32(h);
+      }
+    }
+    // pass 2: this block's h slice into its own next Z buffer, then (vec) copied
+    // to every other block of the cluster as whole 16-byte chunks.
+    if (k + 1 < K) {
+#pragma unroll
+      for (int q = 0; q < kItems; ++q) {
+        const int e = tid + q * kThreads;
+        if (e >= kUnits * Bt) break;
+        const int u = e & 31, n = e >> 5;
+        const uint32_t off = kmajor_off<ET>(n, n_in + r * kUnits + u, Bt);
+        if (vec) {
+          st_elem<ET>(zn + off, hop[q]);
+        } else {
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            if (p < C) {
+              if constexpr (sizeof(ET) == 4) dsmem_st(peer_z[p] + ((k + 1) & 1) * zbuf_bytes + off, hop[q]);
+              else dsmem_st_bf16(peer_z[p] + ((k + 1) & 1) * zbuf_bytes + off, hop[q]);
+            }
+          }
+        }
+      }
+      if (vec) {
+        __syncthreads();
+        constexpr int kChunksPerRow = kUnits * (int)sizeof(ET) / 16;   // 8 (TF32) or 4 (bf16)
+        for (int c = tid; c < Bt * kChunksPerRow; c += kThreads) {
+          const int n = c / kChunksPerRow, cc = c - n * kChunksPerRow;
+          const uint32_t off = kmajor_off<ET>(n, n_in + r * kUnits + cc * EPU, Bt);
+          const uint4 val = *reinterpret_cast<const uint4*>(zn + off);
+          const uint32_t roff = ((k + 1) & 1) * zbuf_bytes + off;
+#pragma unroll
+          for (int p = 0; p < 8; ++p)
+            if (p < C && p != r) dsmem_st(peer_z[p] + roff, val);
+        }
+      }
+    }
+    if (k + 1 < K) {
+      if (vec) {
+        const int xupr = n_in / EPU;
+#pragma unroll
+        for (int q = 0; q < kXUnits; ++q) {
+          const int e = tid + q * kThreads;
+          if (e < Bt * xupr) {
+            const int n = e / xupr, kk = (e - n * xupr) * EPU;
+            *reinterpret_cast<uint4*>(zn + kmajor_off<ET>(n, kk, Bt)) = round_unit<MODE>(xu[q]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < kXRegs; ++q) {
+          const int e = tid + q * kThreads;
+          if (e < nx) st_elem<ET>(zn + kmajor_off<ET>(e / n_in, e % n_in, Bt), to_operand<MODE>(xr[q]));
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+    tc::fence_before_sync();
+    cluster_arrive_release();
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      const int e = tid + q * kThreads;
+      if (e >= kUnits * Bt) break;
+      const int u = e & 31, n = e >> 5, bb = b0 + n;
+      if (bb < B) {
+        const int unit = r * kUnits + u;
+        const long long row = (long long)bb * K + k;
+        act[row * H3 + unit] = ig[q];
+        act[row * H3 + H + unit] = igg[q];
+        act[row * H3 + 2 * H + unit] = ihh[q];
+        stf(h_seq + row * H + unit, ih[q]);
+      }
+    }
+    cluster_wait_acquire();
+    tc::fence_after_sync();
+  }
+  if (err && tid == 0) atomicExch(&g_tc_kloop_error, 1);
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+bool plan_fwd(const Layout& L, TcPlan* p) {
+  if (L.math == CFC_MATH_FP32) return false;
+  if (L.H % kUnits || L.H / kUnits > 8) return false;
+  const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
+  const int C = L.H / kUnits;
+  const int nA = (L.Zc * es + 127) / 128;
+  auto smem_for = [&](int Bt, TcPlan* q) {
+    size_t off = (size_t)nA * 128 * 128;
+    q->off_z = off;
+    off += 2ull * nA * Bt * 128;
+    q->off_ex = off;
+    off += 3ull * kUnits * (Bt + 1) * 4;
+    q->off_bs = off;
+    off += 3 * kUnits * 4;
+    q->off_dt = off;
+    off += (size_t)Bt * 4;
+    q->smem = off + 1024;  // alignment slack
+    return q->smem;
+  };
+  // Smallest Bt (multiple of 16) whose grid fits in one wave of blocks, or
+  // failing that the largest that fits in shared memory.
+  int best = 0;
+  for (int Bt = 16; Bt <= 128; Bt += 16) {
+    TcPlan q;
+    if (smem_for(Bt, &q) > kSmemMax) break;
+    if ((long long)kUnits * Bt > 8ll * kThreads) break;
+    const int epu = 16 / es;
+    const bool vec = (L.n_in % epu == 0) && (L.H % epu == 0);
+    if (vec ? ((long long)Bt * (L.n_in / epu) > (long long)kXUnits * kThreads)
+            : ((long long)Bt * L.n_in > (long long)kXRegs * kThreads)) break;
+    best = Bt;
+    if ((long long)(L.B + Bt - 1) / Bt * C <= kNumSMs) break;
+  }
+  if (!best) return false;
+  p->C = C;
+  p->Bt = best;
+  p->nA = nA;
+  smem_for(best, p);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)best) cols <<= 1;
+  p->tmem_cols = cols;
+  return true;
+}
+
+template <typename ET, int MODE>
+cudaError_t launch_fwd(const Layout& L, const TcPlan& p, const CfcArgs& a, cudaStream_t s) {
+  auto kern = k_cfc_fwd_tc<ET, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((L.B + p.Bt - 1) / p.Bt) * p.C), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TraceScope trace("cfc_fwd_tc", s);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const ET*>(a.x), static_cast<const ET*>(a.h0),
+                            static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.b, a.dt,
+                            a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt, p.nA, (uint32_t)p.off_z,
+                            (uint32_t)p.off_ex, (uint32_t)p.off_bs, (uint32_t)p.off_dt, p.tmem_cols,
+                            static_cast<ET*>(a.h_seq), reinterpret_cast<float*>(a.ws + L.off_act));
+}
+
+}  // namespace
+
+int read_tc_kloop_error(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_kloop_error, sizeof(int)) != cudaSuccess) return CFC_ERR_DEVICE;
+  if (clear && v) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_tc_kloop_error, &zero, sizeof(int)) != cudaSuccess) return CFC_ERR_DEVICE;
+  }
+  return v;
+}
+
+cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  const int choice = kernel_choice();
+  if (choice == kCluster || choice == kSimt) return cudaErrorNotSupported;
+  TcPlan p;
+  if (!plan_fwd(L, &p)) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32) return launch_fwd<float, CFC_MATH_TF32>(L, p, a, s);
+  return launch_fwd<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+}
+
+}  // namespace cfc

@@ -59,7 +59,7 @@ def test_smoke_fp32_scratch_path():
     assert_close(got["per_sample"], ref["per_sample"], w.math, "smoke:per_sample")
 
 
-@pytest.mark.parametrize("kernels", ["cluster", "simt"])
+@pytest.mark.parametrize("kernels", ["tc", "cluster", "simt"])
 @pytest.mark.parametrize("w", [wl.TINY, wl.SMOKE, wl.MID.with_(B=128, K=16),
                                wl.LARGE.with_(B=96, K=4)], ids=lambda w: w.name)
 def test_kernel_families_on_benchmark_shapes(w, kernels, monkeypatch):
@@ -105,10 +105,15 @@ EDGE = [
     wl.Workload("edge_B3000_K2_bf16", B=3000, K=2, n_in=40, n_hid=72, math=wl.MATH_BF16,
                 grad_path=wl.GRAD_GEMM, dt_per_sample=True),
     wl.Workload("edge_wide_H600", B=3, K=2, n_in=100, n_hid=600),            # units loop (>512 threads)
+    # tensor-core K loop: cluster of H/32 blocks, ragged batch tiles, K padding
+    wl.Workload("edge_tc_tf32_B70_K3", B=70, K=3, n_in=16, n_hid=64, math=wl.MATH_TF32),
+    wl.Workload("edge_tc_bf16_B45_K5", B=45, K=5, n_in=40, n_hid=96, math=wl.MATH_BF16,
+                dt_per_sample=True),
+    wl.Workload("edge_tc_bf16_odd_n_in", B=19, K=4, n_in=7, n_hid=32, math=wl.MATH_BF16),
 ]
 
 
-@pytest.mark.parametrize("kernels", ["auto", "cluster", "simt"])
+@pytest.mark.parametrize("kernels", ["auto", "tc", "cluster", "simt"])
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("path", [wl.GRAD_SCRATCH, wl.GRAD_GEMM])
 def test_edge_shapes(w, path, kernels, monkeypatch):
