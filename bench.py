@@ -85,18 +85,19 @@ def kernel_work(name, w, n_split):
     Zc, H3, R = n_in + H, 3 * H, w.B * w.K
     s = 2 if w.math == wl.MATH_BF16 else 4
     N = w.N
+    engine = "tensor" if name.endswith("_tc") else "alu"
     if name.startswith("cfc_fwd"):
         flops = 2.0 * R * H3 * Zc
         byts = R * n_in * s + R * H * s + R * H3 * 4 + B * H * s + H3 * Zc * s
-        return flops, byts, "alu"
+        return flops, byts, engine
     if name.startswith("cfc_bwd"):
         flops = 2.0 * R * H3 * Zc
         byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * Zc * s
-        return flops, byts, "alu"
+        return flops, byts, engine
     if name.startswith("wgrad"):
         flops = 2.0 * R * H3 * (Zc + 1)
         byts = R * H3 * s + R * Zc * s + n_split * N * 4
-        return flops, byts, ("tensor" if name.endswith("_tc") else "alu")
+        return flops, byts, engine
     if name == "reduce_axis0":
         return 0.0, 4.0 * (n_split * N + N), "alu"
     if name == "prep_wt":

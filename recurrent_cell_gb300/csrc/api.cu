@@ -85,7 +85,7 @@ bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Lay
     // N-block tiling; row blocks are whole multiples of 64 rows (one bf16
     // chunk, two TF32 chunks).
     const long long tiles = tc_wgrad_blocks(n_in, n_hid);
-    long long split = std::max(1ll, (2ll * kNumSMs + tiles - 1) / tiles);
+    long long split = std::max(1ll, (2ll * kNumSMs) / tiles);   // one wave at 2 blocks per SM
     split = std::min(split, std::max(1ll, L->R / 64));
     long long rps = (L->R + split - 1) / split;
     rps = (rps + 63) / 64 * 64;
@@ -98,6 +98,8 @@ bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Lay
   L->off_dA = off;   off = align256(off + (size_t)L->R * L->H3 * L->dA_elem);
   L->off_part = off;
   if (grad_path == CFC_GRAD_GEMM) off = align256(off + (size_t)L->n_split * L->N * sizeof(float));
+  L->off_wtt = off;  // pre-swizzled W_cat^T tiles of the tensor-core backward
+  off = align256(off + tc_bwd_tiles_bytes(n_in, n_hid, math));
   L->total = off;
   return true;
 }
@@ -140,8 +142,9 @@ int cfc_kloop_grad_splits(int B, int K, int n_in, int n_hid, int math, int grad_
 int cfc_device_error(int clear) {
   const int a = read_device_error(clear);
   const int b = read_tc_kloop_error(clear);
-  if (a < 0 || b < 0) return CFC_ERR_DEVICE;
-  return (a || b) ? 1 : 0;
+  const int c = read_tc_bwd_error(clear);
+  if (a < 0 || b < 0 || c < 0) return CFC_ERR_DEVICE;
+  return (a || b || c) ? 1 : 0;
 }
 
 size_t cfc_kloop_workspace_bytes(int B, int K, int n_in, int n_hid, int math, int grad_path) {
@@ -212,7 +215,10 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
   a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  // Cluster kernels when their grid stays within ~2 waves (many steps, fewer
+  // samples), else the tensor-core kernel (streamed weights), else SIMT.
   cudaError_t e = launch_backward_cluster(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_backward_tc(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_backward_simt(L, a, s);
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;
   float* part = (grad_path == CFC_GRAD_SCRATCH) ? per_sample_scratch

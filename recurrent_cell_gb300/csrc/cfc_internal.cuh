@@ -99,7 +99,7 @@ struct Layout {
   long long R;          // B*K rows of the gradient contraction
   int n_split;          // row blocks of the GEMM-path contraction
   long long rows_per_split;
-  size_t off_wt, off_act, off_dA, off_part, total;
+  size_t off_wt, off_act, off_dA, off_part, off_wtt, total;
 };
 
 bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Layout* L);
@@ -149,6 +149,10 @@ int kernel_choice();
 // nothing, when the sizes do not fit its plan or another family is forced.
 cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 int read_tc_kloop_error(int clear);
+// Tensor-core backward (TF32 / bf16 modes), streamed W_cat^T tiles.
+cudaError_t launch_backward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
+size_t tc_bwd_tiles_bytes(int n_in, int n_hid, int math);
+int read_tc_bwd_error(int clear);
 
 // Cluster kernels (weights resident in shared memory of a block cluster).
 // Return cudaErrorNotSupported, launching nothing, when no cluster plan fits

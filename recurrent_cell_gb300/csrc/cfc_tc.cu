@@ -55,38 +55,56 @@ struct Elem<__nv_bfloat16> {
   static constexpr uint32_t kFmt = tc::kFmtBF16;
 };
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return a | (b << 16);
-}
 
-// Vector load of 4 consecutive elements as 4 floats (16 B fp32 or 8 B bf16).
-__device__ __forceinline__ void ld4(const float* p, float (&v)[4]) {
-  const float4 t = __ldg(reinterpret_cast<const float4*>(p));
-  v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-}
-__device__ __forceinline__ void ld4(const __nv_bfloat16* p, float (&v)[4]) {
-  const uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
-  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
-  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
-  v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
-}
-
-// A staging task: 4 columns (m) x PU rows -> 4 units of PU rows each.
+// Raw loaded words of one staging task: PU rows x 4 consecutive columns.
+// fp32: w[i][q] = bits of element (row i, column q); bf16: w[i][0..1] hold
+// the 4 bf16 of row i (2 per word).  Kept raw so that a load is only waited
+// for when the task is stored.
 template <typename ET, int PU>
-struct Block4 {
-  float v[PU][4];
+struct Raw4 {
+  static constexpr int W = sizeof(ET) == 4 ? 4 : 2;
+  uint32_t w[PU][W];
 };
 
-template <int PU>
-__device__ __forceinline__ uint4 unit_of(const float (&v)[PU][4], int col) {
-  if constexpr (PU == 4) {
-    return make_uint4(__float_as_uint(v[0][col]), __float_as_uint(v[1][col]), __float_as_uint(v[2][col]),
-                      __float_as_uint(v[3][col]));
+__device__ __forceinline__ void ld4_raw(const float* p, uint32_t (&w)[4]) {
+  const uint4 t = __ldg(reinterpret_cast<const uint4*>(p));
+  w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+}
+__device__ __forceinline__ void ld4_raw(const __nv_bfloat16* p, uint32_t (&w)[2]) {
+  const uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
+  w[0] = t.x; w[1] = t.y;
+}
+
+// 16-byte swizzle unit of column q (0..3) of a task: PU consecutive rows.
+template <typename ET, int MODE, int PU>
+__device__ __forceinline__ uint4 unit_of(const Raw4<ET, PU>& r, int q) {
+  if constexpr (sizeof(ET) == 4) {
+    uint32_t v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = r.w[i][q];
+      if constexpr (MODE == CFC_MATH_TF32) v[i] = __float_as_uint(round_tf32(__uint_as_float(v[i])));
+    }
+    return make_uint4(v[0], v[1], v[2], v[3]);
   } else {
-    return make_uint4(pack_bf16(v[0][col], v[1][col]), pack_bf16(v[2][col], v[3][col]),
-                      pack_bf16(v[4][col], v[5][col]), pack_bf16(v[6][col], v[7][col]));
+    const int word = q >> 1, sh = (q & 1) * 16;
+    uint32_t v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      v[t] = ((r.w[2 * t][word] >> sh) & 0xFFFFu) | (((r.w[2 * t + 1][word] >> sh) & 0xFFFFu) << 16);
+    return make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+template <typename ET>
+__device__ __forceinline__ void set_row(uint32_t (&w)[Raw4<ET, 1>::W], float a, float b, float c, float d) {
+  if constexpr (sizeof(ET) == 4) {
+    w[0] = __float_as_uint(a); w[1] = __float_as_uint(b); w[2] = __float_as_uint(c); w[3] = __float_as_uint(d);
+  } else {
+    w[0] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+    w[1] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(c)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d)) << 16);
   }
 }
 
@@ -133,10 +151,8 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
   const int nbq = NB / 4;
   const int b_tasks = nbq * G;
   constexpr int kBPer = (kMaxNB / 4 * G + kTcThreads - 1) / kTcThreads;  // 2
-  Block4<ET, PU> ra, rb[kBPer];
+  Raw4<ET, PU> ra, rb[kBPer];
 
-  // z source row pointers of the PU rows starting at row0 (h part): h0 of the
-  // sample for the first step, else the previous h_seq row.
   auto load_chunk = [&](int c) {
     const long long rc = r_begin + (long long)c * KC;
     {  // A: dA rows (m contiguous)
@@ -146,12 +162,13 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
       for (int i = 0; i < PU; ++i) {
         const long long row = rc + g * PU + i;
         if (VEC) {
-          if (row < r_end && m < H3) ld4(dA + row * H3 + m, ra.v[i]);
-          else ra.v[i][0] = ra.v[i][1] = ra.v[i][2] = ra.v[i][3] = 0.f;
+          if (row < r_end && m < H3) ld4_raw(dA + row * H3 + m, ra.w[i]);
+          else set_row<ET>(ra.w[i], 0.f, 0.f, 0.f, 0.f);
         } else {
+          float v[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            ra.v[i][q] = (row < r_end && m + q < H3) ? ldf(dA + row * H3 + m + q) : 0.f;
+          for (int q = 0; q < 4; ++q) v[q] = (row < r_end && m + q < H3) ? ldf(dA + row * H3 + m + q) : 0.f;
+          set_row<ET>(ra.w[i], v[0], v[1], v[2], v[3]);
         }
       }
     }
@@ -166,23 +183,15 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
 #pragma unroll
       for (int i = 0; i < PU; ++i) {
         const long long row = row0 + i;
-        float (&v)[4] = rb[t].v[i];
-        v[0] = v[1] = v[2] = v[3] = 0.f;
+        bool done_row = false;
         if (row < r_end) {
           const ET* hrow = (k == 0) ? (h0 + b * H) : (h_seq + (row - 1) * H);
           if (VEC) {
-            if (j < n_in) {
-              ld4(x + row * n_in + j, v);
-            } else if (j < Zc) {
-              ld4(hrow + (j - n_in), v);
-            } else if (j == Zc) {
-              v[0] = 1.f;
-            }
-            if constexpr (MODE == CFC_MATH_TF32) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) v[q] = round_tf32(v[q]);
-            }
+            if (j < n_in) { ld4_raw(x + row * n_in + j, rb[t].w[i]); done_row = true; }
+            else if (j < Zc) { ld4_raw(hrow + (j - n_in), rb[t].w[i]); done_row = true; }
+            else if (j == Zc) { set_row<ET>(rb[t].w[i], 1.f, 0.f, 0.f, 0.f); done_row = true; }
           } else {
+            float v[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int jj = j + q;
@@ -192,8 +201,11 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
               else if (jj == Zc) val = 1.f;
               v[q] = val;
             }
+            set_row<ET>(rb[t].w[i], v[0], v[1], v[2], v[3]);
+            done_row = true;
           }
         }
+        if (!done_row) set_row<ET>(rb[t].w[i], 0.f, 0.f, 0.f, 0.f);
         if (++k == K) { k = 0; ++b; }
       }
     }
@@ -205,7 +217,7 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
       const int mq = tid & 31, g = tid >> 5;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(a + tc::sw128_offset(4 * mq + q, 16 * g)) = unit_of<PU>(ra.v, q);
+        *reinterpret_cast<uint4*>(a + tc::sw128_offset(4 * mq + q, 16 * g)) = unit_of<ET, CFC_MATH_FP32, PU>(ra, q);
     }
 #pragma unroll
     for (int t = 0; t < kBPer; ++t) {
@@ -214,7 +226,7 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
         const int jq = task % nbq, g = task / nbq;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(bb + tc::sw128_offset(4 * jq + q, 16 * g)) = unit_of<PU>(rb[t].v, q);
+          *reinterpret_cast<uint4*>(bb + tc::sw128_offset(4 * jq + q, 16 * g)) = unit_of<ET, MODE, PU>(rb[t], q);
       }
     }
   };

@@ -226,7 +226,10 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
       }
       tc::mma_commit(&bar);
     }
-    if (!tc::mbar_wait(&bar, k & 1, kMaxPolls)) err = 1;
+    // One thread waits for the MMAs; the others meet it at the block barrier.
+    if (tid == 0 && !tc::mbar_wait(&bar, k & 1, kMaxPolls)) err = 1;
+    tc::fence_before_sync();
+    __syncthreads();
     tc::fence_after_sync();
     // TMEM -> shared: pre-activations of head w (lane quadrant w), columns split
     // between warps w and w+4.
