@@ -39,7 +39,8 @@ namespace {
 
 constexpr int kClusterThreads = 256;
 constexpr int kXPerThread = 8;     // forward: x elements per thread prefetched one step ahead
-constexpr int kItemsPerThread = 4; // backward: (sample, unit) items per thread with prefetched activations
+// (sample, unit) items per thread kept in registers, by samples per cluster.
+__host__ __device__ constexpr int items_per_thread(int bt) { return bt <= 4 ? 2 : (bt <= 8 ? 4 : 8); }
 constexpr int kMaxSplit = 8;       // thread groups a dot product is split over
 
 struct ClusterPlan {
@@ -56,6 +57,7 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
                   const T* __restrict__ W_rec, const float* __restrict__ bias,
                   const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H, int S,
                   T* __restrict__ h_seq, float* __restrict__ act) {
+  constexpr int kItemsPerThread = items_per_thread(BT);
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int r = (int)cluster.block_rank();
@@ -215,6 +217,7 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
                   const float* __restrict__ grad_h_last, const float* __restrict__ y,
                   const float* __restrict__ act, DT* __restrict__ dA_out,
                   float* __restrict__ grad_h0, float* __restrict__ grad_x) {
+  constexpr int kItemsPerThread = items_per_thread(BT);
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int r = (int)cluster.block_rank();
@@ -425,20 +428,27 @@ bool plan(const Layout& L, bool forward, ClusterPlan* p) {
   const int Hc = L.H / C;
   const int width = forward ? Hc : (L.n_in + C - 1) / C + Hc;
   const int S = std::max(1, std::min(kMaxSplit, kClusterThreads / width));
-  int BT = 16;
-  const int bts[5] = {1, 2, 4, 8, 16};
-  for (int t : bts)
-    if ((long long)(L.B + t - 1) / t * C <= 2 * kNumSMs) { BT = t; break; }
   const int threads = std::min(kClusterThreads, (width * S + 31) / 32 * 32);
   auto smem = [&](int bt) { return forward ? fwd_smem(L, C, bt, S) : bwd_smem(L, C, bt, S); };
   auto fits = [&](int bt) {
     const long long items = forward ? (long long)bt * L.n_in : (long long)bt * Hc;
-    const int per = forward ? kXPerThread : kItemsPerThread;
+    const int per = forward ? kXPerThread : items_per_thread(bt);
     return smem(bt) <= kSmemLimit && items <= (long long)per * threads &&
-           (long long)bt * Hc <= (long long)kItemsPerThread * threads;
+           (long long)bt * Hc <= (long long)items_per_thread(bt) * threads;
   };
-  while (BT > 1 && !fits(BT)) BT /= 2;
-  if (!fits(BT)) return false;
+  // Samples per cluster: the smallest BT whose grid fits in one wave (blocks
+  // per SM from the shared-memory size); else the largest that fits.
+  const int bts[6] = {1, 2, 4, 8, 16, 32};
+  const int nbt = forward ? 5 : 6;
+  int BT = 0;
+  for (int i = 0; i < nbt; ++i) {
+    const int t = bts[i];
+    if (!fits(t)) break;
+    BT = t;
+    const long long per_sm = std::max<long long>(1, (long long)(227 * 1024) / (long long)smem(t));
+    if ((long long)(L.B + t - 1) / t * C <= per_sm * kNumSMs) break;
+  }
+  if (!BT) return false;
   p->C = C;
   p->BT = BT;
   p->S = S;
@@ -505,7 +515,8 @@ cudaError_t bwd_mode(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cu
     case 2: return bwd_bt<T, DT, MODE, 2>(L, p, a, s);
     case 4: return bwd_bt<T, DT, MODE, 4>(L, p, a, s);
     case 8: return bwd_bt<T, DT, MODE, 8>(L, p, a, s);
-    default: return bwd_bt<T, DT, MODE, 16>(L, p, a, s);
+    case 16: return bwd_bt<T, DT, MODE, 16>(L, p, a, s);
+    default: return bwd_bt<T, DT, MODE, 32>(L, p, a, s);
   }
 }
 
