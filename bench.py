@@ -100,7 +100,7 @@ def kernel_work(name, w, n_split):
         return flops, byts, engine
     if name == "reduce_axis0":
         return 0.0, 4.0 * (n_split * N + N), "alu"
-    if name == "prep_wt":
+    if name.startswith("prep_w"):
         return 0.0, 2.0 * H3 * Zc * s, "alu"
     return 0.0, 0.0, "alu"
 

@@ -50,6 +50,7 @@ int kernel_choice() {
   if (strcmp(v, "cluster") == 0) return kCluster;
   if (strcmp(v, "simt") == 0) return kSimt;
   if (strcmp(v, "tc") == 0) return kTc;
+  if (strcmp(v, "tcs") == 0) return kTcStream;
   return kAuto;
 }
 
@@ -177,7 +178,11 @@ int cfc_kloop_forward(const void* x, const void* h0, const void* W_in, const voi
   a.x = x; a.h0 = h0; a.W_in = W_in; a.W_rec = W_rec; a.b = b; a.dt = dt; a.dt_stride = dt_stride;
   a.h_seq = h_seq; a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Tensor-core cluster kernel (weights resident) while its grid fits one
+  // wave, else the tensor-core kernel with streamed weights, else the SIMT
+  // cluster kernel (FP32), else the plain SIMT kernel.
   cudaError_t e = launch_forward_tc(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_forward_tc_stream(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_forward_cluster(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_forward_simt(L, a, s);
   return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;

@@ -525,7 +525,7 @@ cudaError_t bwd_mode(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cu
 namespace {
 bool use_cluster(const Layout& L, bool forward, ClusterPlan* p) {
   const int choice = kernel_choice();
-  if (choice == kSimt || choice == kTc || !plan(L, forward, p)) return false;
+  if (choice == kSimt || choice == kTc || choice == kTcStream || !plan(L, forward, p)) return false;
   if (choice == kCluster) return true;
   return (long long)(L.B + p->BT - 1) / p->BT * p->C <= 2 * kNumSMs;
 }

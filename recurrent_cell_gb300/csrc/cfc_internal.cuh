@@ -142,13 +142,15 @@ cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t 
 // K-loop kernel family: CFC_KLOOP_KERNELS=tc | cluster | simt forces one
 // family where it supports the sizes (read on every call); anything else
 // selects automatically.
-enum KernelChoice { kAuto = 0, kCluster = 1, kSimt = 2, kTc = 3 };
+enum KernelChoice { kAuto = 0, kCluster = 1, kSimt = 2, kTc = 3, kTcStream = 4 };
 int kernel_choice();
 
 // Tensor-core forward (TF32 / bf16 modes); cudaErrorNotSupported, launching
 // nothing, when the sizes do not fit its plan or another family is forced.
 cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 int read_tc_kloop_error(int clear);
+// Tensor-core forward with streamed W_cat tiles (TF32 / bf16 modes).
+cudaError_t launch_forward_tc_stream(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core backward (TF32 / bf16 modes), streamed W_cat^T tiles.
 cudaError_t launch_backward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 size_t tc_bwd_tiles_bytes(int n_in, int n_hid, int math);

@@ -248,14 +248,12 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) {
-      const uint32_t a_addr = tc::smem_u32(As + st * kATile);
-      const uint32_t b_addr = tc::smem_u32(Bs + st * kBTile);
+      const uint64_t ad = tc::sdesc_k_sw128(tc::smem_u32(As + st * kATile));
+      const uint64_t bd = tc::sdesc_k_sw128(tc::smem_u32(Bs + st * kBTile));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint64_t ad = tc::sdesc_k_sw128(a_addr + 32 * k);
-        const uint64_t bd = tc::sdesc_k_sw128(b_addr + 32 * k);
-        if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad, bd, id, (c | k) != 0);
-        else tc::mma_bf16(tmem, ad, bd, id, (c | k) != 0);
+        if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad + 2 * k, bd + 2 * k, id, (c | k) != 0);
+        else tc::mma_bf16(tmem, ad + 2 * k, bd + 2 * k, id, (c | k) != 0);
       }
       tc::mma_commit(&bars[st]);
     }

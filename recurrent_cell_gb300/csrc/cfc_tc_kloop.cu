@@ -214,15 +214,16 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
       }
     }
     if (tid == 0) {
-      const uint32_t wa = tc::smem_u32(Ws), za = tc::smem_u32(zc);
+      uint64_t ad = tc::sdesc_k_sw128(tc::smem_u32(Ws)), bd = tc::sdesc_k_sw128(tc::smem_u32(zc));
+      const uint32_t b_step = (uint32_t)Bt * 128;
       for (int a = 0; a < nA; ++a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint64_t ad = tc::sdesc_k_sw128(wa + a * 128 * 128 + 32 * j);
-          const uint64_t bd = tc::sdesc_k_sw128(za + a * Bt * 128 + 32 * j);
-          if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad, bd, id, (a | j) != 0);
-          else tc::mma_bf16(tmem, ad, bd, id, (a | j) != 0);
+          if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+          else tc::mma_bf16(tmem, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
         }
+        ad = tc::sdesc_advance(ad, 128 * 128);
+        bd = tc::sdesc_advance(bd, b_step);
       }
       tc::mma_commit(&bar);
     }
@@ -432,9 +433,11 @@ int read_tc_kloop_error(int clear) {
 
 cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s) {
   const int choice = kernel_choice();
-  if (choice == kCluster || choice == kSimt) return cudaErrorNotSupported;
+  if (choice == kCluster || choice == kSimt || choice == kTcStream) return cudaErrorNotSupported;
   TcPlan p;
   if (!plan_fwd(L, &p)) return cudaErrorNotSupported;
+  // Beyond one wave of clusters the streamed-weight kernel is faster.
+  if (choice == kAuto && (long long)(L.B + p.Bt - 1) / p.Bt * p.C > kNumSMs) return cudaErrorNotSupported;
   if (L.math == CFC_MATH_TF32) return launch_fwd<float, CFC_MATH_TF32>(L, p, a, s);
   return launch_fwd<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
 }

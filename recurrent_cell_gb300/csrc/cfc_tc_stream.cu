@@ -1,0 +1,792 @@
+// cfc_tc_stream.cu -- forward and backward K loops of the TF32 / bf16 modes on
+// the tcgen05 tensor cores with streamed weights, one block per tile of Bt
+// samples (no cluster).
+//
+// Forward, per step k:  D [3H x Bt] = W_cat [3H x Zc] * Z_k^T  with M tiles of
+// 128 rows ordered (f, g, h~) per block of 128 units, so the three
+// pre-activations of a unit sit in the same TMEM lane of three consecutive
+// tiles and the thread that reads them applies the whole cell.  W_cat is
+// streamed as pre-swizzled 16 KB tiles (like W_cat^T below); Z_k = [x_k; h_k]
+// of the block's samples is a K-major swizzled shared-memory tile that the
+// epilogue overwrites with h_{k+1} once the step's MMAs are complete.
+//
+// Backward, per step k (reverse): the block computes the gradient reaching
+// z_k = [x_k; h_k]
+//
+//   dz^T [Zc x Bt] = W_cat^T [Zc x 3H] * dA_k^T [3H x Bt]
+//
+// as nM = ceil(Zc/128) MMA row tiles (M = 128 z-columns, N = Bt samples,
+// K = 3H).  The A operand, W_cat^T, is the same for every step and every
+// block: it is prepared once per call as pre-swizzled 16 KB tiles (128 rows x
+// 128 bytes of K) in the workspace and streamed through a ring of shared-memory
+// stages with TMA bulk copies (cp.async.bulk, mbarrier transaction counts).
+// The tile sequence repeats every step, so the copies for the next step's
+// first tiles run while the block computes the next dA.  The B operand, dA_k
+// of the Bt samples, is computed by the block itself into a K-major swizzled
+// shared-memory tile.
+//
+// Elementwise phase of step k: thread <-> z-column j = 128*mt + 32*(warp%4) +
+// lane (the TMEM lane quadrant rule).  It reads dz of step k+1 for its column
+// from TMEM: x columns become grad_x[:, k+1], h columns the carry of unit
+// j - n_in, from which (with the saved activations) it forms the three dA
+// values of that unit for every sample of the tile.  After step 0 the same
+// read gives grad_x[:, 0] and grad_h0.
+//
+// Waits are bounded; a timeout records an error in the device error word.
+#include <algorithm>
+
+#include "cfc_internal.cuh"
+#include "tc_common.cuh"
+
+namespace cfc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxStages = 6;    // ring of streamed A tiles (runtime count: nst)
+constexpr uint32_t kTile = 128 * 128;      // bytes of one streamed A tile
+constexpr uint32_t kMaxPolls = 1u << 24;
+constexpr size_t kSmemMax = 227 * 1024;
+
+__device__ int g_tc_bwd_error = 0;
+
+__device__ __forceinline__ void expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+// Multicast forms: one copy lands at the same shared-memory offset of every
+// CTA in `mask` and completes the transaction bytes on each one's mbarrier;
+// one MMA completion arrives on the mbarrier of every CTA in `mask`.
+__device__ __forceinline__ void bulk_g2s_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                            uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(tc::smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   tc::smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+template <typename ET>
+__device__ __forceinline__ void st_elem(uint8_t* p, float v) {
+  if constexpr (sizeof(ET) == 4) *reinterpret_cast<float*>(p) = v;
+  else *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+}
+
+template <typename ET>
+__device__ __forceinline__ uint32_t kmajor_off(int row, int kk, int rows) {
+  const uint32_t kb = (uint32_t)kk * sizeof(ET);
+  return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
+}
+
+// W_cat^T tiles: tile (mt, a) holds rows j = 128*mt .. 128*mt+127 (z columns)
+// and K elements a*EPA .. a*EPA+EPA-1 (EPA = 128 bytes / element), at byte
+// offset ((a * nM) + mt) * kTile, swizzled exactly as in shared memory.
+template <typename ET, int MODE>
+__global__ void k_prep_wt_tiles(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, int n_in,
+                                int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
+  constexpr int EPA = 128 / sizeof(ET);
+  const int Zc = n_in + H, H3 = 3 * H;
+  const long long total = (long long)nM * nAk * 128 * EPA;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int kl = (int)(e % EPA);
+    const long long rest = e / EPA;
+    const int i = (int)(rest % 128);
+    const long long t = rest / 128;            // tile index = a * nM + mt
+    const int mt = (int)(t % nM), a = (int)(t / nM);
+    const int j = mt * 128 + i, kk = a * EPA + kl;
+    float v = 0.f;
+    if (j < Zc && kk < H3)
+      v = (j < n_in) ? ld_operand<MODE>(W_in + (long long)kk * n_in + j)
+                     : ld_operand<MODE>(W_rec + (long long)kk * H + (j - n_in));
+    st_elem<ET>(tiles + t * kTile + tc::sw128_offset(i, kl * sizeof(ET)), v);
+  }
+}
+
+template <typename ET, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, int dt_stride, int B,
+              int K, int n_in, int H, int Bt, int nM, int nAk, int nst, uint32_t tmem_cols,
+              const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
+              const float* __restrict__ grad_h_last, const float* __restrict__ y,
+              const float* __restrict__ act, ET* __restrict__ dA_out, float* __restrict__ grad_h0,
+              float* __restrict__ grad_x) {
+  const int Zc = n_in + H, H3 = 3 * H;
+  const int b0 = blockIdx.x * Bt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
+  const int T = nAk * nM;                       // streamed tiles per step
+  const long long total_tiles = (long long)K * T;
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage = sm;                                   // nst x 16 KB
+  uint8_t* dAs = sm + (size_t)nst * kTile;               // nAk x [Bt rows][128 B]
+  float* dts = reinterpret_cast<float*>(dAs + (size_t)nAk * Bt * 128);   // [Bt]
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    tc::mbar_init(&done, 1);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
+  for (int e = tid; e < Bt; e += kThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+  // dA tile padding (K beyond 3H) stays zero for the whole launch.
+  {
+    constexpr int EPA = 128 / sizeof(ET);
+    const int Kpad = nAk * EPA;
+    for (int e = tid; e < Bt * (Kpad - H3); e += kThreads) {
+      const int n = e / (Kpad - H3), kk = H3 + e % (Kpad - H3);
+      st_elem<ET>(dAs + kmajor_off<ET>(n, kk, Bt), 0.f);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
+
+  // Ring positions (thread 0).  Stage indices and barrier phases advance by
+  // increments: integer division on this path costs more than the MMAs.
+  long long copies_left = total_tiles;
+  int pst = 0, pt = 0;          // producer: stage, tile of the per-step sequence
+  uint32_t pwrap = 0;           // producer: completed passes over the ring
+  int cst = 0;                  // consumer: stage
+  uint32_t cwrap = 0;           // consumer: completed passes over the ring
+  auto issue_copy = [&]() {
+    // stage reuse: the MMAs of the tile nst copies back must be complete
+    if (pwrap > 0 && !tc::mbar_wait(&empty[pst], (pwrap - 1) & 1u, kMaxPolls)) err = 1;
+    expect_tx(&full[pst], kTile);
+    bulk_g2s(stage + pst * kTile, wtiles + (size_t)pt * kTile, kTile, &full[pst]);
+    if (++pt == T) pt = 0;
+    if (++pst == nst) {
+      pst = 0;
+      ++pwrap;
+    }
+    --copies_left;
+  };
+  if (tid == 0) {
+    for (int i = 0; i < nst - 2 && copies_left > 0; ++i) issue_copy();
+  }
+
+  // rows of z handled by this thread: j = 128*mt + 32*quad + lane for mt = warp/4, warp/4 + 2, ...
+  for (int step = 0; step <= K; ++step) {
+    const int k = K - 1 - step;                  // step == K: final read-out only
+    // ---- elementwise phase: dz of step k+1 from TMEM -> grad_x / carry -> dA_k
+    for (int mt = warp >> 2; mt < nM; mt += kThreads / 128) {
+      const int j = mt * 128 + quad * 32 + lane;
+      for (int n0 = 0; n0 < Bt; n0 += 16) {
+        float dz[16];
+        if (step > 0) {
+          tc::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * Bt + n0), dz);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dz[i] = 0.f;
+        }
+        if (j < n_in) {
+          if (step > 0 && grad_x) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int bb = b0 + n0 + i;
+              if (bb < B) grad_x[((long long)bb * K + (k + 1)) * n_in + j] = dz[i];
+            }
+          }
+        } else if (j < Zc) {
+          const int u = j - n_in;
+          if (k < 0) {                           // after step 0: grad_h0
+            if (grad_h0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int bb = b0 + n0 + i;
+                if (bb < B) grad_h0[(long long)bb * H + u] = dz[i];
+              }
+            }
+          } else {
+            float ga[16], gg[16], gh[16], up[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int bb = b0 + n0 + i;
+              ga[i] = gg[i] = gh[i] = up[i] = 0.f;
+              if (bb < B) {
+                const long long row = (long long)bb * K + k;
+                ga[i] = act[row * H3 + u];
+                gg[i] = act[row * H3 + H + u];
+                gh[i] = act[row * H3 + 2 * H + u];
+                if (grad_h_seq) up[i] = grad_h_seq[row * H + u];
+                if (k == K - 1) {
+                  if (grad_h_last) up[i] += grad_h_last[(long long)bb * H + u];
+                  if (y) up[i] += ldf(h_seq + row * H + u) - y[(long long)bb * H + u];
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int n = n0 + i, bb = b0 + n;
+              float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+              if (bb < B) {
+                const float delta = dz[i] + up[i];
+                const float gate = ga[i], g = gg[i], hh = gh[i];
+                d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
+                d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
+                d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
+                const long long row = (long long)bb * K + k;
+                stf(dA_out + row * H3 + u, d0);
+                stf(dA_out + row * H3 + H + u, d1);
+                stf(dA_out + row * H3 + 2 * H + u, d2);
+              }
+              st_elem<ET>(dAs + kmajor_off<ET>(n, u, Bt), d0);
+              st_elem<ET>(dAs + kmajor_off<ET>(n, H + u, Bt), d1);
+              st_elem<ET>(dAs + kmajor_off<ET>(n, 2 * H + u, Bt), d2);
+            }
+          }
+        }
+      }
+    }
+    if (k < 0) break;
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // ---- MMA phase (thread 0): stream W_cat^T tiles, dz_k = W^T dA_k into TMEM
+    if (tid == 0) {
+      const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
+      const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(dAs));
+      for (int a = 0; a < nAk; ++a) {
+        const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+        uint32_t d = tmem;
+        for (int mt = 0; mt < nM; ++mt, d += (uint32_t)Bt) {
+          if (!tc::mbar_wait(&full[cst], cwrap & 1u, kMaxPolls)) err = 1;
+          tc::fence_after_sync();
+          const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kTile);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+            else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+          }
+          tc::mma_commit(&empty[cst]);
+          if (++cst == nst) {
+            cst = 0;
+            ++cwrap;
+          }
+          if (copies_left > 0) issue_copy();
+        }
+      }
+      tc::mma_commit(&done);
+      // Only this thread waits on the MMA completion; the others wait at the
+      // block barrier (polling threads would compete with the barrier traffic
+      // of the tile stream).
+      if (!tc::mbar_wait(&done, (uint32_t)(step & 1), kMaxPolls)) err = 1;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+  }
+  if (err) atomicExch(&g_tc_bwd_error, 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+// W_cat tiles of the forward: tile (a, m), m = 3*ub + c, holds the rows of
+// head c for units 128*ub + i (i = 0..127) and K elements a*EPA .. +EPA-1 of z,
+// at byte offset (a * nM + m) * kTile, swizzled as in shared memory.
+template <typename ET, int MODE>
+__global__ void k_prep_w_tiles_fwd(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, int n_in,
+                                   int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
+  constexpr int EPA = 128 / sizeof(ET);
+  const int Zc = n_in + H;
+  const long long total = (long long)nM * nAk * 128 * EPA;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int kl = (int)(e % EPA);
+    const long long rest = e / EPA;
+    const int i = (int)(rest % 128);
+    const long long t = rest / 128;            // a * nM + m
+    const int m = (int)(t % nM), a = (int)(t / nM);
+    const int c = m % 3, ub = m / 3;
+    const int unit = ub * 128 + i, kk = a * EPA + kl;
+    float v = 0.f;
+    if (unit < H && kk < Zc) {
+      const long long row = (long long)c * H + unit;
+      v = (kk < n_in) ? ld_operand<MODE>(W_in + row * n_in + kk) : ld_operand<MODE>(W_rec + row * H + (kk - n_in));
+    }
+    st_elem<ET>(tiles + t * kTile + tc::sw128_offset(i, kl * sizeof(ET)), v);
+  }
+}
+
+constexpr int kXUnits = 4;                 // prefetched 16-byte x units per epilogue thread
+constexpr int kFwdConsumers = 256;         // cell epilogue: warps 0..7
+constexpr int kFwdProducerWarp = 8;        // W_cat tile stream
+constexpr int kFwdMmaWarp = 9;             // MMA issue
+constexpr int kFwdThreads = kFwdConsumers + 64;
+constexpr int kFwdMaxStages = 12;
+
+// Named barrier of the epilogue warps and the MMA warp (the producer warp runs ahead).
+__device__ __forceinline__ void step_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFwdConsumers + 32) : "memory");
+}
+
+// Bounded mbarrier wait executed by a whole warp: lane 0's observation
+// decides for all lanes, so the warp stays converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t max_polls) {
+  for (uint32_t i = 0; i < max_polls; ++i) {
+    const int ok = tc::mbar_try_wait(bar, parity) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, ok, 0)) return true;
+  }
+  return false;
+}
+
+// The cell's three nonlinearities in the tensor-core modes, from
+// tanh(a) = 1 - 2 / (1 + exp(2a)) and gate = 1 / (1 + exp(z)), z = A_f dt:
+// with p1 = 1 + exp(2 A_g), p2 = 1 + exp(2 A_h~), p3 = 1 + exp(z) and one
+// reciprocal r = 1 / (p1 p2 p3), 1/p1 = r p2 p3 and so on.  The exponent
+// arguments are capped at 28 so the product stays finite (p^3 < e^85); at
+// the cap tanh is 1 and the gate below 7e-13, both within an fp32 ulp of the
+// uncapped values' contribution.  Absolute error: a few fp32 ulps of 1, far
+// below the TF32 / bf16 rounding these modes apply.
+struct CellAct {
+  float gate, g, hh;
+};
+__device__ __forceinline__ CellAct cell_act(float a_f, float a_g, float a_h, float dt) {
+  constexpr float kCap = 28.f;
+  const float p1 = 1.f + __expf(fminf(2.f * a_g, kCap));
+  const float p2 = 1.f + __expf(fminf(2.f * a_h, kCap));
+  const float p3 = 1.f + __expf(fminf(a_f * dt, kCap));
+  const float p12 = p1 * p2;
+  const float r = __fdividef(1.f, p12 * p3);
+  const float rp3 = r * p3;
+  CellAct c;
+  c.g = fmaf(-2.f, rp3 * p2, 1.f);
+  c.hh = fmaf(-2.f, rp3 * p1, 1.f);
+  c.gate = r * p12;
+  return c;
+}
+
+template <typename ET, int MODE>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, const ET* __restrict__ h0,
+              const float* __restrict__ bias, const float* __restrict__ dt, int dt_stride, int B, int K,
+              int n_in, int H, int Bt, int nUB, int nAk, int nst, uint32_t tmem_cols, int C,
+              ET* __restrict__ h_seq, float* __restrict__ act) {
+  constexpr int EPU = 16 / (int)sizeof(ET);
+  constexpr int EPA = 128 / (int)sizeof(ET);
+  const int Zc = n_in + H, H3 = 3 * H;
+  const int nM = 3 * nUB;
+  const uint32_t rank = (C > 1) ? cluster_rank() : 0u;
+  const uint16_t cmask = (uint16_t)((1u << C) - 1u);
+  const int Kpad = nAk * EPA;
+  const int b0 = blockIdx.x * Bt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
+  const int T = nAk * nM;
+  const long long total_tiles = (long long)K * T;
+  const bool vec = (n_in % EPU == 0) && (H % EPU == 0);
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage = sm;                                       // nst x 16 KB
+  uint8_t* Zs = sm + (size_t)nst * kTile;                    // nAk x [Bt rows][128 B]
+  float* bs = reinterpret_cast<float*>(Zs + (size_t)nAk * Bt * 128);   // [3H]
+  float* dts = bs + H3;                                      // [Bt]
+  __shared__ uint64_t full[kFwdMaxStages], empty[kFwdMaxStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], C);   // one MMA completion of every CTA of the cluster
+    }
+    tc::mbar_init(&done, 1);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
+  for (int e = tid; e < H3; e += kFwdThreads) bs[e] = bias[e];
+  for (int e = tid; e < Bt; e += kFwdThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+  // z rows of step 0 = [x_0; h0], zero K padding.
+  for (int e = tid; e < Bt * Kpad; e += kFwdThreads) {
+    const int n = e / Kpad, kk = e - n * Kpad, bb = b0 + n;
+    float v = 0.f;
+    if (bb < B && kk < Zc)
+      v = (kk < n_in) ? ld_operand<MODE>(x + (long long)bb * K * n_in + kk)
+                      : ld_operand<MODE>(h0 + (long long)bb * H + (kk - n_in));
+    st_elem<ET>(Zs + kmajor_off<ET>(n, kk, Bt), v);
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (C > 1) {   // every CTA's barriers are initialised before any remote arrival
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  volatile int* err_flag = &err;
+
+  if (warp == kFwdProducerWarp) {
+    // ---- producer warp: the W_cat tile sequence of every step through the ring.
+    // In a cluster of C CTAs tile g is fetched once, by CTA g % C, and
+    // multicast to all; a stage is refilled once every CTA's MMAs released it.
+    int st = 0, t = 0, issuer = 0;
+    uint32_t wrap = 0;
+    for (long long g = 0; g < total_tiles; ++g) {
+      if (__shfl_sync(0xffffffffu, *err_flag, 0)) break;
+      if (wrap > 0 && !mbar_wait_warp(&empty[st], (wrap - 1) & 1u, kMaxPolls)) {
+        if (lane == 0) *err_flag = 1;
+        break;
+      }
+      if (lane == 0) {
+        expect_tx(&full[st], kTile);
+        const uint8_t* src = wtiles + (size_t)t * kTile;
+        if (C == 1) bulk_g2s(stage + st * kTile, src, kTile, &full[st]);
+        else if ((uint32_t)issuer == rank) bulk_g2s_mc(stage + st * kTile, src, kTile, &full[st], cmask);
+      }
+      __syncwarp();
+      if (++t == T) t = 0;
+      if (++issuer == C) issuer = 0;
+      if (++st == nst) {
+        st = 0;
+        ++wrap;
+      }
+    }
+  } else if (warp == kFwdMmaWarp) {
+    // ---- MMA warp: D[m] (TMEM columns m*Bt ..) = W_cat tile rows x Z_k^T.
+    // After a timed-out wait nothing more is issued (the remaining waits would
+    // each run to their limit); the steps finish on stale data and the host
+    // sees the device error word.
+    const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
+    const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
+    const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(Zs));
+    int cst = 0;
+    uint32_t cwrap = 0;
+    bool ok = true;
+    for (int k = 0; k < K; ++k) {
+      if (k > 0) step_sync();             // Z_k written by the epilogue of step k-1
+      tc::fence_after_sync();
+      if (ok && __shfl_sync(0xffffffffu, *err_flag, 0) == 0) {
+        for (int a = 0; a < nAk && ok; ++a) {
+          const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+          uint32_t d = tmem;
+          for (int m = 0; m < nM; ++m, d += (uint32_t)Bt) {
+            if (!mbar_wait_warp(&full[cst], cwrap & 1u, kMaxPolls)) {
+              if (lane == 0) *err_flag = 1;
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            if (lane == 0) {
+              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kTile);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+                else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+              }
+              if (C == 1) tc::mma_commit(&empty[cst]);
+              else mma_commit_mc(&empty[cst], cmask);
+            }
+            __syncwarp();
+            if (++cst == nst) {
+              cst = 0;
+              ++cwrap;
+            }
+          }
+        }
+        if (ok) {
+          if (lane == 0) tc::mma_commit(&done);
+          __syncwarp();
+          if (!mbar_wait_warp(&done, (uint32_t)(k & 1), kMaxPolls)) {
+            if (lane == 0) *err_flag = 1;
+            ok = false;
+          }
+        }
+      }
+      tc::fence_before_sync();
+      step_sync();                        // D_k complete: release the epilogue
+    }
+  } else {
+    // ---- epilogue warps
+    const int xupr = vec ? n_in / EPU : 0;
+    const long long sample_stride_act = (long long)K * H3, sample_stride_h = (long long)K * H;
+    for (int k = 0; k < K; ++k) {
+      // x of the next step: raw 16-byte units, stored into Z after the MMAs.
+      uint4 xu[kXUnits];
+      if (vec) {
+#pragma unroll
+        for (int q = 0; q < kXUnits; ++q) {
+          const int e = tid + q * kFwdConsumers;
+          const int n = (xupr > 0) ? e / xupr : 0, kk = (e - n * xupr) * EPU, bb = b0 + n;
+          xu[q] = (e < Bt * xupr && k + 1 < K && bb < B)
+                      ? __ldg(reinterpret_cast<const uint4*>(x + ((long long)bb * K + k + 1) * n_in + kk))
+                      : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      step_sync();
+      tc::fence_after_sync();
+      // thread <-> unit 128*ub + 32*quad + lane, 16 samples per pass;
+      // (ub, sample chunk) pairs alternate between the two warp halves.
+      const int nchunk = Bt / 16;
+      for (int pidx = half; pidx < nUB * nchunk; pidx += 2) {
+        const int ub = pidx / nchunk, n0 = (pidx - ub * nchunk) * 16;
+        const int u = ub * 128 + quad * 32 + lane;
+        float af[16], ag[16], ah[16];
+        const uint32_t t0 = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(3 * ub * Bt + n0);
+        tc::tmem_ld16x3(t0, t0 + (uint32_t)Bt, t0 + 2u * (uint32_t)Bt, af, ag, ah);
+        if (u < H) {
+          const float bf = bs[u], bg = bs[H + u], bh = bs[2 * H + u];
+          const int nvalid = min(16, B - (b0 + n0));
+          float* ap = act + ((long long)(b0 + n0) * K + k) * H3 + u;
+          ET* hp = h_seq + ((long long)(b0 + n0) * K + k) * H + u;
+          uint8_t* zp = Zs + (size_t)((n_in + u) * (int)sizeof(ET) >> 7) * Bt * 128;
+          const uint32_t kb = (uint32_t)(((n_in + u) * (int)sizeof(ET)) & 127);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + i;
+            const CellAct c = cell_act(af[i] + bf, ag[i] + bg, ah[i] + bh, dts[n]);
+            const float gate = c.gate, g = c.g, hh = c.hh;
+            const float h = fmaf(gate, g - hh, hh);
+            float hop = 0.f;
+            if (i < nvalid) {
+              ap[0] = gate;
+              ap[H] = g;
+              ap[2 * H] = hh;
+              stf(hp, h);
+              if constexpr (sizeof(ET) == 2) hop = round_bf16(h);
+              else hop = round_tf32(h);
+            }
+            ap += sample_stride_act;
+            hp += sample_stride_h;
+            if (k + 1 < K) st_elem<ET>(zp + tc::sw128_offset(n, kb), hop);
+          }
+        }
+      }
+      if (k + 1 < K) {
+        if (vec) {
+#pragma unroll
+          for (int q = 0; q < kXUnits; ++q) {
+            const int e = tid + q * kFwdConsumers;
+            if (e < Bt * xupr) {
+              const int n = e / xupr, kk = (e - n * xupr) * EPU;
+              uint4 v = xu[q];
+              if constexpr (MODE == CFC_MATH_TF32) {
+                v.x = __float_as_uint(round_tf32(__uint_as_float(v.x)));
+                v.y = __float_as_uint(round_tf32(__uint_as_float(v.y)));
+                v.z = __float_as_uint(round_tf32(__uint_as_float(v.z)));
+                v.w = __float_as_uint(round_tf32(__uint_as_float(v.w)));
+              }
+              *reinterpret_cast<uint4*>(Zs + kmajor_off<ET>(n, kk, Bt)) = v;
+            }
+          }
+        } else {
+          for (int e = tid; e < Bt * n_in; e += kFwdConsumers) {
+            const int n = e / n_in, kk = e - n * n_in, bb = b0 + n;
+            const float v = (bb < B) ? ld_operand<MODE>(x + ((long long)bb * K + k + 1) * n_in + kk) : 0.f;
+            st_elem<ET>(Zs + kmajor_off<ET>(n, kk, Bt), v);
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        step_sync();                      // Z_{k+1} ready, TMEM reads of step k done
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (C > 1) {   // no CTA leaves while a peer may still signal its barriers
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
+  if (err) atomicExch(&g_tc_bwd_error, 1);
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+struct FwdPlan {
+  int Bt = 0, nUB = 0, nAk = 0, nst = 0, C = 1;
+  uint32_t tmem_cols = 0;
+  size_t smem = 0;
+};
+
+bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
+  if (L.math == CFC_MATH_FP32) return false;
+  const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
+  const int epu = 16 / es;
+  const int nUB = (L.H + 127) / 128, nM = 3 * nUB;
+  const int nAk = (L.Zc * es + 127) / 128;
+  int Bt = (int)(((long long)L.B + kNumSMs - 1) / kNumSMs);
+  Bt = std::min(128, std::max(32, (Bt + 15) / 16 * 16));
+  auto fixed_for = [&](int bt) { return 1024 + (size_t)nAk * bt * 128 + (size_t)(3 * L.H + bt) * 4 + 256; };
+  auto ok = [&](int bt) {
+    const bool vec = (L.n_in % epu == 0) && (L.H % epu == 0);
+    return fixed_for(bt) + 4 * (size_t)kTile <= kSmemMax && (long long)nM * bt <= 512 &&
+           (!vec || (long long)bt * (L.n_in / epu) <= (long long)kXUnits * kFwdConsumers);
+  };
+  while (Bt > 16 && !ok(Bt)) Bt -= 16;
+  if (!ok(Bt)) return false;
+  int nst = (int)std::min<size_t>(kFwdMaxStages, (kSmemMax - fixed_for(Bt)) / kTile);
+  p->Bt = Bt;
+  p->nUB = nUB;
+  p->nAk = nAk;
+  p->nst = nst;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(nM * Bt)) cols <<= 1;
+  p->tmem_cols = cols;
+  p->smem = fixed_for(Bt) + (size_t)nst * kTile;
+  p->C = 4;
+  if (const char* v = getenv("CFC_TC_CLUSTER")) p->C = std::max(1, std::min(8, atoi(v)));
+  return true;
+}
+
+template <typename ET, int MODE>
+cudaError_t launch_fwd_stream(const Layout& L, const FwdPlan& p, const CfcArgs& a, cudaStream_t s) {
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
+  {
+    const long long total = (long long)3 * p.nUB * p.nAk * 128 * (128 / sizeof(ET));
+    const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
+    TraceScope trace("prep_w", s);
+    k_prep_w_tiles_fwd<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_in),
+                                                        static_cast<const ET*>(a.W_rec), L.n_in, L.H,
+                                                        3 * p.nUB, p.nAk, tiles);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = k_cfc_fwd_tcb<ET, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  const int blocks = (L.B + p.Bt - 1) / p.Bt;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((blocks + p.C - 1) / p.C * p.C), 1, 1);   // whole clusters
+  cfg.blockDim = dim3(kFwdThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TraceScope trace("cfc_fwd_stream_tc", s);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(tiles), static_cast<const ET*>(a.x),
+                            static_cast<const ET*>(a.h0), a.b, a.dt, a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt,
+                            p.nUB, p.nAk, p.nst, p.tmem_cols, p.C, static_cast<ET*>(a.h_seq),
+                            reinterpret_cast<float*>(a.ws + L.off_act));
+}
+
+
+struct BwdPlan {
+  int Bt = 0, nM = 0, nAk = 0, nst = 0;
+  uint32_t tmem_cols = 0;
+  size_t smem = 0;
+};
+
+bool plan_bwd(const Layout& L, BwdPlan* p) {
+  if (L.math == CFC_MATH_FP32) return false;
+  const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
+  const int nM = (L.Zc + 127) / 128;
+  const int nAk = (L.H3 * es + 127) / 128;
+  // Bt: samples per block, the MMA's N: about one block per SM, at least 32.
+  int Bt = (int)(((long long)L.B + kNumSMs - 1) / kNumSMs);
+  Bt = std::min(128, std::max(32, (Bt + 15) / 16 * 16));
+  auto fixed_for = [&](int bt) { return 1024 + (size_t)nAk * bt * 128 + bt * 4 + 256; };
+  while (Bt > 16 && (fixed_for(Bt) + 4 * (size_t)kTile > kSmemMax || (long long)nM * Bt > 512)) Bt -= 16;
+  if (fixed_for(Bt) + 4 * (size_t)kTile > kSmemMax || (long long)nM * Bt > 512) return false;
+  // as many stages as fit (the stream is latency-bound: more tiles in flight)
+  const int nst = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed_for(Bt)) / kTile);
+  p->Bt = Bt;
+  p->nM = nM;
+  p->nAk = nAk;
+  p->nst = nst;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(nM * Bt)) cols <<= 1;
+  p->tmem_cols = cols;
+  p->smem = fixed_for(Bt) + (size_t)nst * kTile;
+  return true;
+}
+
+template <typename ET, int MODE>
+cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cudaStream_t s) {
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
+  {
+    const long long total = (long long)p.nM * p.nAk * 128 * (128 / sizeof(ET));
+    const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
+    TraceScope trace("prep_wt_tiles", s);
+    k_prep_wt_tiles<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_in),
+                                                     static_cast<const ET*>(a.W_rec), L.n_in, L.H, p.nM,
+                                                     p.nAk, tiles);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = k_cfc_bwd_tcb<ET, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (L.B + p.Bt - 1) / p.Bt;
+  TraceScope trace("cfc_bwd_tc", s);
+  kern<<<grid, kThreads, p.smem, s>>>(tiles, a.dt, a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt, p.nM, p.nAk,
+                                      p.nst, p.tmem_cols, static_cast<const ET*>(a.h_seq), a.grad_h_seq,
+                                      a.grad_h_last, a.y, reinterpret_cast<const float*>(a.ws + L.off_act),
+                                      reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0, a.grad_x);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tc_bwd_tiles_bytes(int n_in, int n_hid, int math) {
+  if (math == CFC_MATH_FP32) return 0;
+  const int es = (math == CFC_MATH_TF32) ? 4 : 2;
+  // backward: W_cat^T tiles; forward: W_cat tiles (the two are never live at once)
+  const size_t bwd = (size_t)((n_in + n_hid + 127) / 128) * ((3 * n_hid * es + 127) / 128) * kTile;
+  const size_t fwd = (size_t)(3 * ((n_hid + 127) / 128)) * (((n_in + n_hid) * es + 127) / 128) * kTile;
+  return std::max(bwd, fwd);
+}
+
+cudaError_t launch_forward_tc_stream(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  const int choice = kernel_choice();
+  if (choice == kCluster || choice == kSimt || choice == kTc) return cudaErrorNotSupported;
+  FwdPlan p;
+  if (!plan_fwd_stream(L, &p)) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32) return launch_fwd_stream<float, CFC_MATH_TF32>(L, p, a, s);
+  return launch_fwd_stream<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+}
+
+int read_tc_bwd_error(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_bwd_error, sizeof(int)) != cudaSuccess) return CFC_ERR_DEVICE;
+  if (clear && v) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_tc_bwd_error, &zero, sizeof(int)) != cudaSuccess) return CFC_ERR_DEVICE;
+  }
+  return v;
+}
+
+cudaError_t launch_backward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  const int choice = kernel_choice();
+  if (choice == kCluster || choice == kSimt) return cudaErrorNotSupported;
+  BwdPlan p;
+  if (!plan_bwd(L, &p)) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32) return launch_bwd<float, CFC_MATH_TF32>(L, p, a, s);
+  return launch_bwd<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+}
+
+}  // namespace cfc

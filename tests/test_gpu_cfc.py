@@ -59,12 +59,26 @@ def test_smoke_fp32_scratch_path():
     assert_close(got["per_sample"], ref["per_sample"], w.math, "smoke:per_sample")
 
 
-@pytest.mark.parametrize("kernels", ["tc", "cluster", "simt"])
+@pytest.mark.parametrize("kernels", ["tc", "tcs", "cluster", "simt"])
 @pytest.mark.parametrize("w", [wl.TINY, wl.SMOKE, wl.MID.with_(B=128, K=16),
                                wl.LARGE.with_(B=96, K=4)], ids=lambda w: w.name)
 def test_kernel_families_on_benchmark_shapes(w, kernels, monkeypatch):
     monkeypatch.setenv("CFC_KLOOP_KERNELS", kernels)
     inp = wl.make_inputs(w, seed=9)
+    r, got = run(w, inp)
+    ref = oracle_ref(w, inp, per_sample=False, y=inp["y"])
+    check_all(w, got, ref)
+
+
+@pytest.mark.parametrize("cluster", ["1", "2", "4"])
+@pytest.mark.parametrize("w", [wl.LARGE.with_(B=300, K=3), wl.MID.with_(B=70, K=5)],
+                         ids=lambda w: f"{w.name.split('_')[0]}_B{w.B}_K{w.K}")
+def test_streamed_forward_cluster_multicast(w, cluster, monkeypatch):
+    """Streamed-weight forward with its weight tiles fetched once per cluster
+    and multicast (cluster sizes 1, 2, 4; grids padded to whole clusters)."""
+    monkeypatch.setenv("CFC_KLOOP_KERNELS", "tcs")
+    monkeypatch.setenv("CFC_TC_CLUSTER", cluster)
+    inp = wl.make_inputs(w, seed=13)
     r, got = run(w, inp)
     ref = oracle_ref(w, inp, per_sample=False, y=inp["y"])
     check_all(w, got, ref)
@@ -113,7 +127,7 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("kernels", ["auto", "tc", "cluster", "simt"])
+@pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt"])
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("path", [wl.GRAD_SCRATCH, wl.GRAD_GEMM])
 def test_edge_shapes(w, path, kernels, monkeypatch):
