@@ -81,6 +81,10 @@ bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Lay
     split = std::max(1ll, std::min(split, std::min<long long>(L->R, 256)));
     L->rows_per_split = (L->R + split - 1) / split;
     L->n_split = (int)((L->R + L->rows_per_split - 1) / L->rows_per_split);
+  } else if (const int tma_splits = tma_wgrad_splits(B, K, n_in, n_hid, math, grad_path)) {
+    // TMA-fed tensor-core contraction: one block per SM, (3H / 128) x splits.
+    L->n_split = tma_splits;
+    L->rows_per_split = (L->R + tma_splits - 1) / tma_splits;
   } else {
     // Tensor-core contraction: about two blocks per SM over its 128-row x
     // N-block tiling; row blocks are whole multiples of 64 rows (one bf16

@@ -164,6 +164,9 @@ cudaError_t launch_forward_cluster(const Layout& L, const CfcArgs& a, cudaStream
 cudaError_t launch_backward_cluster(const Layout& L, const CfcArgs& a, cudaStream_t s);
 cudaError_t launch_backward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core (tcgen05) gradient contraction of the TF32 / bf16 modes.
+// Splits of the TMA-fed contraction (bf16, GEMM path) for these sizes, or 0
+// when it does not apply (then the register-staged contraction is used).
+int tma_wgrad_splits(int B, int K, int n_in, int n_hid, int math, int grad_path);
 cudaError_t launch_wgrad_tc(const Layout& L, const CfcArgs& a, float* out, cudaStream_t s);
 int tc_wgrad_blocks(int n_in, int n_hid);
 // Reads (and optionally clears) the device-side error word of the

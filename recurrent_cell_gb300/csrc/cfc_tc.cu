@@ -23,7 +23,10 @@
 // Every mbarrier wait is bounded; on timeout the kernel records an error in
 // g_cfc_device_error, stops issuing work, waits (bounded) for MMAs already in
 // flight and frees its TMEM.
+#include <cuda.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "cfc_internal.cuh"
 #include "tc_common.cuh"
@@ -320,6 +323,486 @@ cudaError_t launch_mode(const Layout& L, const CfcArgs& a, float* out, cudaStrea
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// TMA-fed contraction (bf16 mode, GEMM path).
+//
+// The rows r = (b, k) are the contraction index and the outer index of every
+// operand in HBM, so the operands are loaded as MN-major tiles: for a chunk of
+// 64 rows, a 64-column block of dA, x or h_seq is one TMA box of 64 rows x
+// 128 bytes, 128-byte swizzled, and the MMA reads it with an MN-major
+// descriptor (leading byte offset = the next 64-column block, stride byte
+// offset = the next 8 rows).  No staging threads, no transposition.
+//
+// Tensor maps are 3-D (columns, K, B) so a chunk is a box of kb steps x nb
+// samples (whole samples when K <= 64, 64 steps of one sample when K is a
+// multiple of 64).  The state entering row (b, k) is h_seq[b][k-1]: the h
+// boxes are loaded at step coordinate k0 - 1, so the rows with k = 0 come back
+// zero-filled (out of bounds) and a patch warp writes h0[b] into them before
+// the MMAs read the stage.  The bias gradient is the contraction with a ones
+// column: a constant 64-column block after the h blocks holds 1 in its first
+// column, written once per stage (the TMA never touches it).
+//
+// Block = (M tile of 128 rows of 3H, split s of the chunk sequence).  Warp 0
+// issues the TMA boxes of each chunk into a ring of stages, warp 2 patches the
+// k = 0 rows, warp 1 issues the MMAs (N pieces of at most 256 columns; the
+// accumulator D[128 x Ntot] lives in TMEM), and all eight warps write D into
+// the packed partial row of split s at the end.  Waits are bounded.
+//
+// The M tiles of one split form a thread-block cluster (up to 8): every tile
+// needs the same z blocks, so each z block of a chunk is fetched by one CTA
+// and multicast to all; a stage is refilled once the MMAs of every CTA of the
+// cluster have released it (MMA completion multicast to every CTA's `empty`
+// barrier).  This cuts the L2 -> SM traffic of z by the cluster size.
+// ---------------------------------------------------------------------------
+constexpr int kTmaRows = 64;                    // rows (MMA K) per chunk
+constexpr int kTmaBlock = kTmaRows * 128;       // one 64-column block of a chunk
+constexpr int kTmaMaxStages = 4;
+constexpr int kTmaWarpProducer = 0, kTmaWarpMma = 1, kTmaWarpPatch = 2;
+constexpr uint32_t kTmaTmemCols = 512;
+
+struct TmaWgradPlan {
+  int C = 1;             // cluster size (M tiles sharing z by multicast)
+  int nx = 0, nh = 0;    // 64-column blocks of x and of h
+  int Ntot = 0;          // accumulator columns: Zc + 1 rounded up to 16
+  int nMt = 0, S = 0, chunks = 0, stages = 0;
+  int kb = 0, nb = 0;    // chunk = kb steps x nb samples
+  size_t stage_bytes = 0, smem = 0;
+};
+
+__global__ void k_wgrad_tma(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                            const __grid_constant__ CUtensorMap, const __nv_bfloat16*, int, int, int, int, int,
+                            int, int, int, int, int, float*);
+
+// Clusters of C blocks (kTcThreads threads, smem bytes each) of k_wgrad_tma
+// resident at once on the current device; 0 if it cannot be queried.
+int max_active_clusters(int C, size_t smem) {
+  static std::mutex mu;
+  static int cached_dev = -1, cached_C = 0, cached_n = 0;
+  static size_t cached_smem = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev == cached_dev && C == cached_C && smem == cached_smem) return cached_n;
+  if (cudaFuncSetAttribute(k_wgrad_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C, 64, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_wgrad_tma, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached_dev = dev;
+  cached_C = C;
+  cached_smem = smem;
+  cached_n = n;
+  return n;
+}
+
+bool plan_tma_wgrad(int B, int K, int n_in, int H, int math, int grad_path, TmaWgradPlan* p) {
+  if (math != CFC_MATH_BF16 || grad_path != CFC_GRAD_GEMM) return false;
+  if (n_in % 64 || H % 64) return false;
+  int kb, nb;
+  if (K <= kTmaRows && kTmaRows % K == 0) {
+    kb = K;
+    nb = kTmaRows / K;
+    if (B % nb) return false;
+  } else if (K % kTmaRows == 0) {
+    kb = kTmaRows;
+    nb = 1;
+  } else {
+    return false;
+  }
+  const int Zc = n_in + H;
+  const int Ntot = (Zc + 1 + 15) / 16 * 16;
+  if (Ntot > (int)kTmaTmemCols) return false;
+  p->nx = n_in / 64;
+  p->nh = H / 64;
+  p->Ntot = Ntot;
+  p->nMt = (3 * H + 127) / 128;
+  p->chunks = (int)((long long)B * K / kTmaRows);
+  p->kb = kb;
+  p->nb = nb;
+  p->stage_bytes = (size_t)(2 + p->nx + p->nh + 1) * kTmaBlock;
+  p->stages = (int)std::min<size_t>(kTmaMaxStages, (227 * 1024 - 1024) / p->stage_bytes);
+  if (p->stages < 2) return false;
+  p->smem = 1024 + (size_t)p->stages * p->stage_bytes;
+  // z multicast across the M tiles of a split (CFC_WGRAD_MULTICAST): measured
+  // slower than one CTA per tile (the cluster advances at its slowest CTA's
+  // pace and fewer clusters fit), so off by default.
+  p->C = (p->nMt <= 8 && getenv("CFC_WGRAD_MULTICAST")) ? p->nMt : 1;
+  // One wave: as many splits as clusters of C CTAs fit at once (clusters live
+  // inside one GPC, so this can be below 152 / C); 152 / nMt without a
+  // device or without clusters.
+  int fit = kNumSMs / p->nMt;
+  if (p->C > 1) {
+    const int q = max_active_clusters(p->C, p->smem);
+    if (q > 0) fit = q;
+  }
+  p->S = std::max(1, std::min(p->chunks, fit));
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+// The same box delivered to every CTA of the cluster in `mask` (same
+// shared-memory offset, each CTA's own mbarrier at the same offset).
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3, %4}], [%5], %6;" ::"r"(tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(tc::smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   tc::smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t cta_rank_in_cluster() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void expect_tx_bytes(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+// Bounded wait by a whole warp; lane 0's observation decides for all lanes.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    const int ok = tc::mbar_try_wait(bar, parity) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, ok, 0)) return true;
+  }
+  return false;
+}
+// MN-major, 128-byte-swizzled operand: 64-column blocks kTmaBlock apart,
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((uint32_t)kTmaBlock >> 4) << 16;   // leading byte offset: next MN block
+  d |= (uint64_t)(1024u >> 4) << 32;                 // stride byte offset: next 8 rows
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+__device__ __forceinline__ void chunk_origin(int c, int K, int nb, int* b0, int* k0) {
+  if (nb > 1) {
+    *b0 = c * nb;
+    *k0 = 0;
+  } else {
+    const int per = K / kTmaRows;
+    *b0 = c / per;
+    *k0 = (c - *b0 * per) * kTmaRows;
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ CUtensorMap map_x,
+            const __grid_constant__ CUtensorMap map_h, const __nv_bfloat16* __restrict__ h0, int K, int n_in,
+            int H, int chunks, int S, int stages, int kb, int nb, int Ntot, int C, float* __restrict__ out) {
+  const int mt = blockIdx.x, s = blockIdx.y;
+  const uint32_t rank = (C > 1) ? cta_rank_in_cluster() : 0u;
+  const uint16_t cmask = (uint16_t)((1u << C) - 1u);
+  const int c_begin = (int)((long long)chunks * s / S), c_end = (int)((long long)chunks * (s + 1) / S);
+  const int nx = n_in / 64, nh = H / 64;
+  const int H3 = 3 * H, Zc = n_in + H;
+  const uint32_t stage_bytes = (uint32_t)(2 + nx + nh + 1) * kTmaBlock;
+  const uint32_t tx_bytes = (uint32_t)(2 + nx + nh) * kTmaBlock;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kTmaMaxStages], ready[kTmaMaxStages], empty[kTmaMaxStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+  volatile int* errp = &err;
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&ready[i], 1);
+      tc::mbar_init(&empty[i], C);   // MMA completion of every CTA of the cluster
+    }
+    tc::mbar_init(&done, 1);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmaTmemCols);
+  // The ones block of every stage: element 0 of each row (logical 16-byte
+  // chunk 0, stored at chunk position row % 8) is bf16 1.0.
+  for (int st = 0; st < stages; ++st) {
+    uint8_t* cb = sm + (size_t)st * stage_bytes + (size_t)(2 + nx + nh) * kTmaBlock;
+    for (int e = tid; e < kTmaBlock / 16; e += kTcThreads) {
+      const int r = e >> 3, q = e & 7;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (q == (r & 7)) v.x = 0x3F80u;
+      *reinterpret_cast<uint4*>(cb + (size_t)e * 16) = v;
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (C > 1) {   // every CTA's barriers are initialised before any multicast lands
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == kTmaWarpProducer) {
+    int st = 0;
+    uint32_t wrap = 0;
+    for (int c = c_begin; c < c_end; ++c) {
+      if (__shfl_sync(0xffffffffu, *errp, 0)) break;
+      if (wrap > 0 && !wait_warp(&empty[st], (wrap - 1) & 1u)) {
+        if (lane == 0) *errp = 1;
+        break;
+      }
+      if (lane == 0) {
+        int b0, k0;
+        chunk_origin(c, K, nb, &b0, &k0);
+        uint8_t* base = sm + (size_t)st * stage_bytes;
+        expect_tx_bytes(&full[st], tx_bytes);
+        tma_load_3d(base, &map_dA, mt * 128, k0, b0, &full[st]);
+        tma_load_3d(base + kTmaBlock, &map_dA, mt * 128 + 64, k0, b0, &full[st]);
+        // z blocks: block j by CTA j % C, multicast to the cluster
+        for (int j = 0; j < nx + nh; ++j) {
+          if (C > 1 && (uint32_t)(j % C) != rank) continue;
+          uint8_t* dst = base + (size_t)(2 + j) * kTmaBlock;
+          const CUtensorMap* map = (j < nx) ? &map_x : &map_h;
+          const int col = (j < nx) ? 64 * j : 64 * (j - nx);
+          const int kc = (j < nx) ? k0 : k0 - 1;
+          if (C > 1) tma_load_3d_mc(dst, map, col, kc, b0, &full[st], cmask);
+          else tma_load_3d(dst, map, col, kc, b0, &full[st]);
+        }
+      }
+      __syncwarp();
+      if (++st == stages) {
+        st = 0;
+        ++wrap;
+      }
+    }
+  } else if (warp == kTmaWarpPatch) {
+    // rows n*kb of a chunk starting at step 0 hold k = 0 of sample b0 + n:
+    // h0[b0 + n] goes into the h blocks.  The h0 rows of the next chunk are
+    // loaded while this chunk's stage is patched (up to kPatchRegs 16-byte
+    // units per lane; the rest are loaded when needed).
+    constexpr int kPatchRegs = 8;
+    const int items = nb * nh * 8;
+    uint4 pre[kPatchRegs];
+    auto prefetch = [&](int c) {
+      int b0, k0;
+      chunk_origin(c, K, nb, &b0, &k0);
+#pragma unroll
+      for (int i = 0; i < kPatchRegs; ++i) {
+        const int e = lane + 32 * i;
+        const int q = e & 7, j = (e >> 3) % nh, n = (e >> 3) / nh;
+        pre[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < c_end && k0 == 0 && e < items)
+          asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(pre[i].x), "=r"(pre[i].y), "=r"(pre[i].z), "=r"(pre[i].w)
+                       : "l"(h0 + (long long)(b0 + n) * H + 64 * j + 8 * q));
+      }
+    };
+    prefetch(c_begin);
+    int st = 0;
+    uint32_t wrap = 0;
+    for (int c = c_begin; c < c_end; ++c) {
+      int b0, k0;
+      chunk_origin(c, K, nb, &b0, &k0);
+      if (!wait_warp(&full[st], wrap & 1u)) {
+        if (lane == 0) *errp = 1;
+        break;
+      }
+      if (k0 == 0) {
+        uint8_t* hb = sm + (size_t)st * stage_bytes + (size_t)(2 + nx) * kTmaBlock;
+        auto put = [&](int e, const uint4& v) {
+          const int q = e & 7, j = (e >> 3) % nh, n = (e >> 3) / nh;
+          const int r = n * kb;
+          *reinterpret_cast<uint4*>(hb + (size_t)j * kTmaBlock + r * 128 + ((q ^ (r & 7)) << 4)) = v;
+        };
+#pragma unroll
+        for (int i = 0; i < kPatchRegs; ++i)
+          if (lane + 32 * i < items) put(lane + 32 * i, pre[i]);
+        for (int e = lane + 32 * kPatchRegs; e < items; e += 32) {
+          const int q = e & 7, j = (e >> 3) % nh, n = (e >> 3) / nh;
+          put(e, *reinterpret_cast<const uint4*>(h0 + (long long)(b0 + n) * H + 64 * j + 8 * q));
+        }
+        tc::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[st]);
+      prefetch(c + 1);
+      if (++st == stages) {
+        st = 0;
+        ++wrap;
+      }
+    }
+  } else if (warp == kTmaWarpMma) {
+    const uint64_t a_desc = sdesc_mn_sw128(tc::smem_u32(sm));
+    const uint64_t b_desc = sdesc_mn_sw128(tc::smem_u32(sm + 2 * kTmaBlock));
+    const int n1 = Ntot > 256 ? 256 : Ntot, n2 = Ntot - n1;   // N pieces
+    constexpr uint32_t kMN = (1u << 15) | (1u << 16);          // A and B MN-major
+    const uint32_t id1 = tc::idesc(128, (uint32_t)n1, tc::kFmtBF16) | kMN;
+    const uint32_t id2 = tc::idesc(128, (uint32_t)(n2 > 0 ? n2 : 16), tc::kFmtBF16) | kMN;
+    int st = 0;
+    uint32_t wrap = 0;
+    bool ok = true;
+    for (int c = c_begin; c < c_end; ++c) {
+      if (!wait_warp(&ready[st], wrap & 1u)) {
+        if (lane == 0) *errp = 1;
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t so = (uint32_t)st * stage_bytes;
+#pragma unroll
+        for (int ks = 0; ks < kTmaRows / 16; ++ks) {
+          const uint32_t acc = (c > c_begin || ks > 0) ? 1u : 0u;
+          const uint64_t ad = tc::sdesc_advance(a_desc, so + ks * 2048);
+          const uint64_t bd = tc::sdesc_advance(b_desc, so + ks * 2048);
+          tc::mma_bf16(tmem, ad, bd, id1, acc);
+          if (n2 > 0) tc::mma_bf16(tmem + 256, ad, tc::sdesc_advance(bd, 4 * kTmaBlock), id2, acc);
+        }
+        if (C > 1) mma_commit_multicast(&empty[st], cmask);
+        else tc::mma_commit(&empty[st]);
+      }
+      __syncwarp();
+      if (++st == stages) {
+        st = 0;
+        ++wrap;
+      }
+    }
+    if (ok && c_end > c_begin && lane == 0) tc::mma_commit(&done);
+    __syncwarp();
+  }
+
+  // ---- epilogue: D[m][j] -> packed partial row of split s
+  if (tid == 0 && c_end > c_begin && *errp == 0 && !tc::mbar_wait(&done, 0, kMaxPolls)) *errp = 1;
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool have = (c_end > c_begin) && *errp == 0;
+  float* o = out + (long long)s * (3ll * (Zc + 1) * H);
+  const long long off_rec = (long long)H3 * n_in, off_b = (long long)H3 * Zc;
+  const int quad = warp & 3, half = warp >> 2;
+  const int m = mt * 128 + quad * 32 + lane;
+  const int ng = Ntot / 16, gh = (ng + 1) / 2;
+  for (int g = half * gh; g < ng && g < (half + 1) * gh; ++g) {
+    float v[16];
+    if (have) {
+      tc::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 16), v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+    if (m < H3) {
+      const int j0 = g * 16;
+      float* dst = nullptr;
+      if (j0 + 16 <= n_in) dst = o + (long long)m * n_in + j0;
+      else if (j0 >= n_in && j0 + 16 <= Zc) dst = o + off_rec + (long long)m * H + (j0 - n_in);
+      if (dst) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      } else if (j0 == Zc) {
+        o[off_b + m] = v[0];
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (C > 1) {   // no CTA leaves while a peer may still signal its barriers
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
+  if (*errp) atomicExch(&g_cfc_device_error, 1);
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmaTmemCols);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map (columns, K, B) of a dense [B][K][cols] array; box 64 x kb x nb.
+bool encode_bkc(CUtensorMap* m, const void* base, int cols, int K, int B, int kb, int nb) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)K, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * K};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)kb, (cuuint32_t)nb};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_wgrad_tma(const Layout& L, const TmaWgradPlan& p, const CfcArgs& a, float* out,
+                             cudaStream_t s) {
+  CUtensorMap mdA, mx, mh;
+  if (!encode_bkc(&mdA, a.ws + L.off_dA, L.H3, L.K, L.B, p.kb, p.nb) ||
+      !encode_bkc(&mx, a.x, L.n_in, L.K, L.B, p.kb, p.nb) ||
+      !encode_bkc(&mh, a.h_seq, L.H, L.K, L.B, p.kb, p.nb))
+    return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(k_wgrad_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  const int C = p.C;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.nMt, (unsigned)p.S, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TraceScope trace("wgrad_tma_tc", s);
+  return cudaLaunchKernelEx(&cfg, k_wgrad_tma, mdA, mx, mh, static_cast<const __nv_bfloat16*>(a.h0), L.K, L.n_in,
+                            L.H, p.chunks, p.S, p.stages, p.kb, p.nb, p.Ntot, C, out);
+}
+
 }  // namespace
 
 int read_device_error(int clear) {
@@ -337,7 +820,19 @@ int tc_wgrad_blocks(int n_in, int n_hid) {
   return ((3 * n_hid + 127) / 128) * ((Zb + kMaxNB - 1) / kMaxNB);
 }
 
+int tma_wgrad_splits(int B, int K, int n_in, int n_hid, int math, int grad_path) {
+  if (getenv("CFC_WGRAD_STAGED")) return 0;   // force the register-staged contraction
+  TmaWgradPlan p;
+  return plan_tma_wgrad(B, K, n_in, n_hid, math, grad_path, &p) ? p.S : 0;
+}
+
 cudaError_t launch_wgrad_tc(const Layout& L, const CfcArgs& a, float* out, cudaStream_t s) {
+  TmaWgradPlan p;
+  if (tma_wgrad_splits(L.B, L.K, L.n_in, L.H, L.math, L.grad_path) == L.n_split &&
+      plan_tma_wgrad(L.B, L.K, L.n_in, L.H, L.math, L.grad_path, &p)) {
+    cudaError_t e = launch_wgrad_tma(L, p, a, out, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (L.math == CFC_MATH_TF32) return launch_mode<float, CFC_MATH_TF32>(L, a, out, s);
   if (L.math == CFC_MATH_BF16) return launch_mode<__nv_bfloat16, CFC_MATH_BF16>(L, a, out, s);
   return cudaErrorNotSupported;

@@ -84,6 +84,22 @@ def test_streamed_forward_cluster_multicast(w, cluster, monkeypatch):
     check_all(w, got, ref)
 
 
+@pytest.mark.parametrize("variant", ["tma_multicast", "tma_single", "staged"])
+def test_large_weight_gradient_contractions(variant, monkeypatch):
+    """The TMA-fed weight-gradient contraction (z blocks multicast across the
+    cluster of M tiles, or one CTA per tile) and the register-staged one, on
+    the large shape with fewer samples."""
+    if variant == "staged":
+        monkeypatch.setenv("CFC_WGRAD_STAGED", "1")
+    if variant == "tma_multicast":
+        monkeypatch.setenv("CFC_WGRAD_MULTICAST", "1")
+    w = wl.LARGE.with_(B=512)
+    inp = wl.make_inputs(w, seed=21)
+    r, got = run(w, inp)
+    ref = oracle_ref(w, inp, per_sample=False, y=inp["y"])
+    check_all(w, got, ref)
+
+
 def test_smoke_fp32_gemm_path_matches():
     w = wl.SMOKE
     inp = wl.make_inputs(w)
@@ -124,6 +140,12 @@ EDGE = [
     wl.Workload("edge_tc_bf16_B45_K5", B=45, K=5, n_in=40, n_hid=96, math=wl.MATH_BF16,
                 dt_per_sample=True),
     wl.Workload("edge_tc_bf16_odd_n_in", B=19, K=4, n_in=7, n_hid=32, math=wl.MATH_BF16),
+    # TMA-fed weight gradient (bf16, GEMM path): 64 steps of one sample per
+    # chunk with a ragged 3H tile, and whole samples per chunk
+    wl.Workload("edge_tma_K128_H64", B=3, K=128, n_in=64, n_hid=64, math=wl.MATH_BF16,
+                grad_path=wl.GRAD_GEMM),
+    wl.Workload("edge_tma_B40_K8", B=40, K=8, n_in=64, n_hid=128, math=wl.MATH_BF16,
+                grad_path=wl.GRAD_GEMM, dt_per_sample=True),
 ]
 
 
