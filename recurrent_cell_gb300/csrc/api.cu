@@ -224,9 +224,12 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
   a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // Cluster kernels when their grid stays within ~2 waves (many steps, fewer
-  // samples), else the tensor-core kernel (streamed weights), else SIMT.
-  cudaError_t e = launch_backward_cluster(L, a, s);
+  // TF32 / bf16: the tensor-core cluster kernel while its grid fits one wave;
+  // then the CUDA-core cluster kernel while its grid stays within ~2 waves
+  // (many steps, fewer samples), else the tensor-core kernel with streamed
+  // weights, else SIMT.
+  cudaError_t e = launch_backward_cluster_tc(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_backward_cluster(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_backward_tc(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_backward_simt(L, a, s);
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;

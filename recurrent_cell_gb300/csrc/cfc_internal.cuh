@@ -149,6 +149,8 @@ int kernel_choice();
 // nothing, when the sizes do not fit its plan or another family is forced.
 cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 int read_tc_kloop_error(int clear);
+// Tensor-core backward, cluster split by units (TF32 / bf16 modes).
+cudaError_t launch_backward_cluster_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core forward with streamed W_cat tiles (TF32 / bf16 modes).
 cudaError_t launch_forward_tc_stream(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core backward (TF32 / bf16 modes), streamed W_cat^T tiles.

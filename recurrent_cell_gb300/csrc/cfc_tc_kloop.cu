@@ -419,6 +419,296 @@ cudaError_t launch_fwd(const Layout& L, const TcPlan& p, const CfcArgs& a, cudaS
                             static_cast<ET*>(a.h_seq), reinterpret_cast<float*>(a.ws + L.off_act));
 }
 
+// ---------------------------------------------------------------------------
+// Backward K loop on the tensor cores, the cluster split by hidden units.
+//
+// Block r of the cluster owns units U_r = [32r, 32r+32) and the x columns
+// X_r = [r*xs, (r+1)*xs), xs = n_in / C.  Per step k (reverse) it
+//   1. forms dA of its units for the Bt samples from its carry (the gradient
+//      reaching its units' h columns, summed at the end of the previous step),
+//      the saved activations (loaded one step ahead) and the upstream seeds;
+//      writes dA to global memory (operand type) and into the K-major B tile
+//      (rows = samples, K = (head, unit) = 96);
+//   2. computes its partial dz_r^T [Zc x Bt] = W_cat[rows of U_r]^T dA_r^T:
+//      nMt M=128 MMA chains, A = its 96 columns of W_cat^T resident in shared
+//      memory (K-major, 128B swizzle), accumulators in TMEM;
+//   3. sends each partial column j to the block that owns j (an x column or a
+//      unit) through distributed shared memory: receive buffer [source block]
+//      [column][sample], double-buffered by step parity;
+//   4. after one cluster barrier, sums the C partials of its own columns in
+//      block order (deterministic): x columns -> grad_x[:, k], unit columns ->
+//      the carry of step k-1, or grad_h0 after step 0.
+// Only partial sums cross the cluster; dA never leaves the block that made it.
+// ---------------------------------------------------------------------------
+constexpr int kBwdMaxItems = 16;        // (unit, sample) items per thread: 32*Bt <= 16*256
+
+struct TcBwdPlan {
+  int C = 0, Bt = 0, nMt = 0, nAk = 0, xs = 0;
+  size_t smem = 0, off_da = 0, off_recv = 0, off_carry = 0, off_dt = 0;
+  uint32_t tmem_cols = 0;
+};
+
+template <typename ET, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const float* __restrict__ dt,
+             int dt_stride, int B, int K, int n_in, int H, int Bt, int nMt, int nAk, int xs, uint32_t off_da,
+             uint32_t off_recv, uint32_t off_carry, uint32_t off_dt, uint32_t tmem_cols,
+             const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
+             const float* __restrict__ grad_h_last, const float* __restrict__ y, const float* __restrict__ act,
+             ET* __restrict__ dA_out, float* __restrict__ grad_h0, float* __restrict__ grad_x) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int r = (int)cluster.block_rank();
+  const int Zc = n_in + H, H3 = 3 * H;
+  const int Mrows = nMt * 128;
+  const int Kpad = nAk * (128 / (int)sizeof(ET));
+  const int cpo = xs + kUnits;                       // columns owned by one block
+  const int b0 = (int)(blockIdx.x / C) * Bt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nitems = kUnits * Bt;
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Wt = sm;                                        // nAk x [Mrows][128 B]
+  uint8_t* dAs = sm + off_da;                              // nAk x [Bt][128 B]
+  float* recv = reinterpret_cast<float*>(sm + off_recv);   // [2][C][cpo][Bt]
+  float* carry = reinterpret_cast<float*>(sm + off_carry); // [Bt][33]
+  float* dts = reinterpret_cast<float*>(sm + off_dt);      // [Bt]
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
+  // A operand: row j (z column), K index kap = c*32 + u -> W_cat[c*H + 32r + u][j].
+  for (int e = tid; e < Mrows * Kpad; e += kThreads) {
+    const int kap = e / Mrows, j = e - kap * Mrows;
+    float v = 0.f;
+    if (j < Zc && kap < 3 * kUnits) {
+      const long long row = (long long)(kap >> 5) * H + r * kUnits + (kap & 31);
+      v = (j < n_in) ? ld_operand<MODE>(W_in + row * n_in + j) : ld_operand<MODE>(W_rec + row * H + (j - n_in));
+    }
+    st_elem<ET>(Wt + kmajor_off<ET>(j, kap, Mrows), v);
+  }
+  for (int e = tid; e < nAk * Bt * 32; e += kThreads) reinterpret_cast<float*>(dAs)[e] = 0.f;
+  for (int e = tid; e < Bt * 33; e += kThreads) carry[e] = 0.f;
+  for (int e = tid; e < Bt; e += kThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+  const uint32_t recv_addr = smem_addr(recv);
+
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc::fence_before_sync();
+  cluster.sync();               // every block is running before DSMEM writes
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
+
+  // Saved activations of step k (items: lanes = the 32 units of one sample).
+  float pa[3][kBwdMaxItems], pu[kBwdMaxItems];
+  auto load_step = [&](int k) {
+#pragma unroll
+    for (int q = 0; q < kBwdMaxItems; ++q) {
+      const int e = tid + q * kThreads;
+      pa[0][q] = pa[1][q] = pa[2][q] = pu[q] = 0.f;
+      if (e < nitems && k >= 0) {
+        const int u = e & 31, n = e >> 5, bb = b0 + n;
+        if (bb < B) {
+          const long long row = (long long)bb * K + k;
+          const int unit = r * kUnits + u;
+          pa[0][q] = act[row * H3 + unit];
+          pa[1][q] = act[row * H3 + H + unit];
+          pa[2][q] = act[row * H3 + 2 * H + unit];
+          if (grad_h_seq) pu[q] = grad_h_seq[row * H + unit];
+        }
+      }
+    }
+  };
+  load_step(K - 1);
+
+  for (int step = 0; step < K; ++step) {
+    const int k = K - 1 - step;
+    const int buf = k & 1;
+    {
+      // ---- 1. dA of this block's units -> global dA and the B tile
+#pragma unroll
+      for (int q = 0; q < kBwdMaxItems; ++q) {
+        const int e = tid + q * kThreads;
+        if (e >= nitems) break;
+        const int u = e & 31, n = e >> 5, bb = b0 + n;
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+        if (bb < B) {
+          const int unit = r * kUnits + u;
+          float delta = carry[n * 33 + u] + pu[q];
+          if (k == K - 1) {
+            if (grad_h_last) delta += grad_h_last[(long long)bb * H + unit];
+            if (y) delta += ldf(h_seq + ((long long)bb * K + k) * H + unit) - y[(long long)bb * H + unit];
+          }
+          const float gate = pa[0][q], g = pa[1][q], hh = pa[2][q];
+          d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
+          d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
+          d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
+          const long long row = (long long)bb * K + k;
+          stf(dA_out + row * H3 + unit, d0);
+          stf(dA_out + row * H3 + H + unit, d1);
+          stf(dA_out + row * H3 + 2 * H + unit, d2);
+        }
+        st_elem<ET>(dAs + kmajor_off<ET>(n, u, Bt), d0);
+        st_elem<ET>(dAs + kmajor_off<ET>(n, kUnits + u, Bt), d1);
+        st_elem<ET>(dAs + kmajor_off<ET>(n, 2 * kUnits + u, Bt), d2);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      // ---- 2. partial dz (thread 0 issues; the next step's activations load meanwhile)
+      if (tid == 0) {
+        const uint64_t a0 = tc::sdesc_k_sw128(tc::smem_u32(Wt)), b0d = tc::sdesc_k_sw128(tc::smem_u32(dAs));
+        for (int mt = 0; mt < nMt; ++mt) {
+          for (int a = 0; a < nAk; ++a) {
+            const uint64_t ad = tc::sdesc_advance(a0, (uint32_t)(a * Mrows + mt * 128) * 128u);
+            const uint64_t bd = tc::sdesc_advance(b0d, (uint32_t)(a * Bt) * 128u);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if constexpr (sizeof(ET) == 4)
+                tc::mma_tf32(tmem + (uint32_t)(mt * Bt), ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+              else tc::mma_bf16(tmem + (uint32_t)(mt * Bt), ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+            }
+          }
+        }
+        tc::mma_commit(&bar);
+      }
+      load_step(k - 1);
+      if (tid == 0 && !tc::mbar_wait(&bar, (uint32_t)(step & 1), kMaxPolls)) err = 1;
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      // ---- 3. partial column j -> its owner's receive buffer [buf][r][jl][n]
+      const int qd = warp & 3, half = warp >> 2, nch = Bt / 16;
+      for (int pidx = half; pidx < nMt * nch; pidx += 2) {
+        const int mt = pidx / nch, n0 = (pidx - mt * nch) * 16;
+        const int j = mt * 128 + qd * 32 + lane;
+        float v[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(mt * Bt + n0), v);
+        if (j < Zc) {
+          int owner, jl;
+          if (j < n_in) {
+            owner = j / xs;
+            jl = j - owner * xs;
+          } else {
+            owner = (j - n_in) >> 5;
+            jl = xs + ((j - n_in) & 31);
+          }
+          const uint32_t off = (uint32_t)((((buf * C + r) * cpo + jl) * Bt + n0) * 4);
+          const uint32_t dst = (owner == r) ? 0u : dsmem_map(recv_addr, (uint32_t)owner);
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const uint4 w = make_uint4(__float_as_uint(v[i]), __float_as_uint(v[i + 1]), __float_as_uint(v[i + 2]),
+                                       __float_as_uint(v[i + 3]));
+            if (owner == r) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(recv) + off + 4 * i) = w;
+            else dsmem_st(dst + off + 4 * i, w);
+          }
+        }
+      }
+    }
+    // ---- 4. one barrier publishes the partials; owners sum them
+    tc::fence_before_sync();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    tc::fence_after_sync();
+    for (int e = tid; e < cpo * Bt; e += kThreads) {
+      const int jl = e / Bt, n = e - jl * Bt, bb = b0 + n;
+      float sum = 0.f;
+      for (int src = 0; src < C; ++src) sum += recv[((buf * C + src) * cpo + jl) * Bt + n];
+      if (jl < xs) {
+        if (grad_x && bb < B) grad_x[((long long)bb * K + k) * n_in + r * xs + jl] = sum;
+      } else {
+        const int u = jl - xs;
+        if (k > 0) carry[n * 33 + u] = sum;
+        else if (grad_h0 && bb < B) grad_h0[(long long)bb * H + r * kUnits + u] = sum;
+      }
+    }
+    __syncthreads();
+  }
+  if (err && tid == 0) atomicExch(&g_tc_kloop_error, 1);
+  tc::fence_before_sync();
+  cluster.sync();               // no block leaves while peers may still write its buffers
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+bool plan_bwd_cluster(const Layout& L, TcBwdPlan* p) {
+  if (L.math == CFC_MATH_FP32) return false;
+  if (L.H % kUnits || L.H / kUnits > 8) return false;
+  const int C = L.H / kUnits;
+  if (L.n_in % C) return false;
+  const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
+  const int nMt = (L.Zc + 127) / 128;
+  const int nAk = (3 * kUnits * es + 127) / 128;
+  const int xs = L.n_in / C, cpo = xs + kUnits;
+  auto smem_for = [&](int Bt, TcBwdPlan* q) {
+    size_t off = (size_t)nAk * nMt * 128 * 128;
+    q->off_da = off;
+    off += (size_t)nAk * Bt * 128;
+    q->off_recv = off;
+    off += 2ull * C * cpo * Bt * 4;
+    q->off_carry = off;
+    off += (size_t)Bt * 33 * 4;
+    q->off_dt = off;
+    off += (size_t)Bt * 4;
+    q->smem = off + 1024;
+    return q->smem;
+  };
+  // Smallest Bt (multiple of 16) whose grid fits one wave of blocks.
+  int best = 0;
+  for (int Bt = 16; Bt <= 128; Bt += 16) {
+    TcBwdPlan q;
+    if (smem_for(Bt, &q) > kSmemMax) break;
+    if ((long long)kUnits * Bt > (long long)kBwdMaxItems * kThreads) break;
+    if ((long long)nMt * Bt > 512) break;
+    best = Bt;
+    if ((long long)(L.B + Bt - 1) / Bt * C <= kNumSMs) break;
+  }
+  if (!best) return false;
+  p->C = C;
+  p->Bt = best;
+  p->nMt = nMt;
+  p->nAk = nAk;
+  p->xs = xs;
+  smem_for(best, p);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(nMt * best)) cols <<= 1;
+  p->tmem_cols = cols;
+  return true;
+}
+
+template <typename ET, int MODE>
+cudaError_t launch_bwd_cluster(const Layout& L, const TcBwdPlan& p, const CfcArgs& a, cudaStream_t s) {
+  auto kern = k_cfc_bwd_tc<ET, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((L.B + p.Bt - 1) / p.Bt) * p.C), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TraceScope trace("cfc_bwd_cluster_tc", s);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.dt,
+                            a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt, p.nMt, p.nAk, p.xs, (uint32_t)p.off_da,
+                            (uint32_t)p.off_recv, (uint32_t)p.off_carry, (uint32_t)p.off_dt, p.tmem_cols,
+                            static_cast<const ET*>(a.h_seq), a.grad_h_seq, a.grad_h_last, a.y,
+                            reinterpret_cast<const float*>(a.ws + L.off_act),
+                            reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0, a.grad_x);
+}
+
 }  // namespace
 
 int read_tc_kloop_error(int clear) {
@@ -440,6 +730,16 @@ cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s)
   if (choice == kAuto && (long long)(L.B + p.Bt - 1) / p.Bt * p.C > kNumSMs) return cudaErrorNotSupported;
   if (L.math == CFC_MATH_TF32) return launch_fwd<float, CFC_MATH_TF32>(L, p, a, s);
   return launch_fwd<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+}
+
+cudaError_t launch_backward_cluster_tc(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  const int choice = kernel_choice();
+  if (choice == kCluster || choice == kSimt || choice == kTcStream) return cudaErrorNotSupported;
+  TcBwdPlan p;
+  if (!plan_bwd_cluster(L, &p)) return cudaErrorNotSupported;
+  if (choice == kAuto && (long long)(L.B + p.Bt - 1) / p.Bt * p.C > kNumSMs) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32) return launch_bwd_cluster<float, CFC_MATH_TF32>(L, p, a, s);
+  return launch_bwd_cluster<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
 }
 
 }  // namespace cfc
