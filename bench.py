@@ -91,9 +91,16 @@ def kernel_work(name, w, n_split):
         byts = R * n_in * s + R * H * s + R * H3 * 4 + B * H * s + H3 * Zc * s
         return flops, byts, engine
     if name.startswith("cfc_bwd"):
-        flops = 2.0 * R * H3 * Zc
-        byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * Zc * s
+        if engine == "tensor":
+            # the tensor-core K loops carry W_rec^T dA only; grad_x is grad_x_tc
+            flops = 2.0 * R * H3 * H
+            byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * H * s
+        else:
+            flops = 2.0 * R * H3 * Zc
+            byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * Zc * s
         return flops, byts, engine
+    if name.startswith("grad_x"):
+        return 2.0 * R * H3 * n_in, R * H3 * s + R * n_in * 4 + H3 * n_in * s, engine
     if name.startswith("wgrad"):
         flops = 2.0 * R * H3 * (Zc + 1)
         byts = R * H3 * s + R * Zc * s + n_split * N * 4

@@ -803,6 +803,230 @@ cudaError_t launch_wgrad_tma(const Layout& L, const TmaWgradPlan& p, const CfcAr
                             L.H, p.chunks, p.S, p.stages, p.kb, p.nb, p.Ntot, C, out);
 }
 
+// ---------------------------------------------------------------------------
+// grad_x of the tensor-core backward kernels as one GEMM after the K loop:
+//
+//   grad_x[r][i] = sum_m dA[r][m] * W_in[m][i]      (r over B*K rows, m over 3H)
+//
+// grad_x does not feed the recurrence, so the K-loop kernels only carry
+// W_rec^T dA and this kernel does the rest with the dA they saved.  A = dA
+// rows (K-major: m is dA's contiguous index) arrive as 128-row x 128-byte TMA
+// boxes (2-D map, 128B swizzle) through a ring of stages; B = W_in^T (the
+// block's part of NW columns, K-major, mode-rounded) is staged once per block
+// and stays resident.  Blocks are persistent over 128-row tiles; the
+// accumulator is double-buffered in TMEM so the epilogue of one tile overlaps
+// the MMAs of the next.  Warp 0: TMA producer, warp 1: MMA issue, warps 4-7:
+// epilogue (TMEM lane quadrants), warps 2-3 idle after staging.
+// ---------------------------------------------------------------------------
+constexpr int kGxMaxStages = 8;
+
+struct GradXPlan {
+  int nAk = 0, NW = 0, nN = 0, G = 0, nst = 0, tiles = 0;
+  uint32_t tmem_cols = 0;
+  size_t smem = 0;
+};
+
+bool plan_grad_x(const Layout& L, GradXPlan* p) {
+  if (L.math == CFC_MATH_FP32) return false;
+  const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
+  if ((L.H3 * es) % 16) return false;                  // TMA row stride
+  p->nAk = (L.H3 * es + 127) / 128;
+  const int nw_max = std::min(256, (int)((110 * 1024) / ((size_t)p->nAk * 128)) / 16 * 16);
+  if (nw_max < 16) return false;
+  p->nN = (L.n_in + nw_max - 1) / nw_max;
+  p->NW = ((L.n_in + p->nN - 1) / p->nN + 15) / 16 * 16;
+  const size_t b_bytes = (size_t)p->nAk * p->NW * 128;
+  p->nst = (int)std::min<size_t>(kGxMaxStages, (227 * 1024 - 1024 - b_bytes) / (128 * 128));
+  if (p->nst < 2) return false;
+  p->smem = 1024 + b_bytes + (size_t)p->nst * 128 * 128;
+  p->tiles = (int)((L.R + 127) / 128);
+  p->G = std::max(1, std::min(p->tiles, kNumSMs / p->nN));
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * p->NW)) cols <<= 1;
+  p->tmem_cols = cols;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+template <typename ET, int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_grad_x_tc(const __grid_constant__ CUtensorMap map_dA, const ET* __restrict__ W_in, int H3, int n_in, long long R,
+            int nAk, int NW, int nN, int G, int nst, int tiles, uint32_t tmem_cols, float* __restrict__ grad_x) {
+  constexpr int EPA = 128 / (int)sizeof(ET);
+  const int np = blockIdx.x % nN, g = blockIdx.x / nN;
+  const int n0 = np * NW;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Bs = sm;                                             // nAk x [NW rows][128 B]
+  uint8_t* As = sm + (size_t)nAk * NW * 128;                    // nst x [128 rows][128 B]
+  __shared__ uint64_t full[kGxMaxStages], empty[kGxMaxStages], dfull[2], dempty[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+  volatile int* errp = &err;
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&dfull[i], 1);
+      tc::mbar_init(&dempty[i], 4);     // one arrival per epilogue warp
+    }
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
+  // B[n][m] = W_in[m][n0 + n] (W_in stacked as [3H][n_in]), zero padding.
+  const int Kpad = nAk * EPA;
+  for (int e = tid; e < NW * Kpad; e += kTcThreads) {
+    const int m = e / NW, n = e - m * NW;
+    float v = 0.f;
+    if (m < H3 && n0 + n < n_in) v = ld_operand<MODE>(W_in + (long long)m * n_in + n0 + n);
+    const uint32_t kb = (uint32_t)m * sizeof(ET);
+    uint8_t* dst = Bs + (kb >> 7) * (uint32_t)NW * 128u + tc::sw128_offset(n, kb & 127u);
+    if constexpr (sizeof(ET) == 4) *reinterpret_cast<float*>(dst) = v;
+    else *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(v);
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ---- producer: the nAk boxes of every tile of this block
+    int st = 0;
+    uint32_t wrap = 0;
+    for (int t = g; t < tiles; t += G) {
+      for (int a = 0; a < nAk; ++a) {
+        if (__shfl_sync(0xffffffffu, *errp, 0)) break;
+        if (wrap > 0 && !wait_warp(&empty[st], (wrap - 1) & 1u)) {
+          if (lane == 0) *errp = 1;
+          break;
+        }
+        if (lane == 0) {
+          expect_tx_bytes(&full[st], 128 * 128);
+          tma_load_2d(As + (size_t)st * 128 * 128, &map_dA, a * EPA, t * 128, &full[st]);
+        }
+        __syncwarp();
+        if (++st == nst) {
+          st = 0;
+          ++wrap;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue: D[buf] (columns buf*NW ...) = A tile x B part
+    const uint32_t id = tc::idesc(128, (uint32_t)NW, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
+    const uint64_t a0 = tc::sdesc_k_sw128(tc::smem_u32(As)), b0 = tc::sdesc_k_sw128(tc::smem_u32(Bs));
+    int st = 0, i = 0;
+    uint32_t wrap = 0;
+    bool ok = true;
+    for (int t = g; t < tiles && ok; t += G, ++i) {
+      const int buf = i & 1;
+      if (i >= 2 && !wait_warp(&dempty[buf], (uint32_t)(((i - 2) >> 1) & 1))) {
+        if (lane == 0) *errp = 1;
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      for (int a = 0; a < nAk; ++a) {
+        if (!wait_warp(&full[st], wrap & 1u)) {
+          if (lane == 0) *errp = 1;
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const uint64_t ad = tc::sdesc_advance(a0, (uint32_t)st * 128 * 128);
+          const uint64_t bd = tc::sdesc_advance(b0, (uint32_t)a * NW * 128);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if constexpr (sizeof(ET) == 4)
+              tc::mma_tf32(tmem + (uint32_t)(buf * NW), ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+            else tc::mma_bf16(tmem + (uint32_t)(buf * NW), ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+          }
+          tc::mma_commit(&empty[st]);
+        }
+        __syncwarp();
+        if (++st == nst) {
+          st = 0;
+          ++wrap;
+        }
+      }
+      if (ok && lane == 0) tc::mma_commit(&dfull[buf]);
+      __syncwarp();
+    }
+  } else if (warp >= 4) {
+    // ---- epilogue: lane quadrant = warp - 4, 16 columns per load
+    const int qd = warp - 4;
+    int i = 0;
+    for (int t = g; t < tiles; t += G, ++i) {
+      const int buf = i & 1;
+      if (!wait_warp(&dfull[buf], (uint32_t)((i >> 1) & 1))) {
+        if (lane == 0) *errp = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const long long row = (long long)t * 128 + qd * 32 + lane;
+      for (int c0 = 0; c0 < NW; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * NW + c0), v);
+        if (row < R) {
+          float* dst = grad_x + row * n_in + n0 + c0;
+          const int left = n_in - (n0 + c0);
+          if (left >= 16 && (n_in & 3) == 0) {
+#pragma unroll
+            for (int q = 0; q < 16; q += 4) *reinterpret_cast<float4*>(dst + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              if (q < left) dst[q] = v[q];
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dempty[buf]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*errp) atomicExch(&g_cfc_device_error, 1);
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+template <typename ET, int MODE>
+cudaError_t launch_grad_x(const Layout& L, const GradXPlan& p, const CfcArgs& a, cudaStream_t s) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)L.H3, (cuuint64_t)L.R};
+  const cuuint64_t strides[1] = {(cuuint64_t)L.H3 * sizeof(ET)};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(ET)), 128u};
+  const cuuint32_t es[2] = {1u, 1u};
+  if (fn(&map, sizeof(ET) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+         a.ws + L.off_dA, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorNotSupported;
+  auto kern = k_grad_x_tc<ET, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  TraceScope trace("grad_x_tc", s);
+  kern<<<p.nN * p.G, kTcThreads, p.smem, s>>>(map, static_cast<const ET*>(a.W_in), L.H3, L.n_in, L.R, p.nAk, p.NW,
+                                               p.nN, p.G, p.nst, p.tiles, p.tmem_cols, a.grad_x);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int read_device_error(int clear) {
@@ -836,6 +1060,18 @@ cudaError_t launch_wgrad_tc(const Layout& L, const CfcArgs& a, float* out, cudaS
   if (L.math == CFC_MATH_TF32) return launch_mode<float, CFC_MATH_TF32>(L, a, out, s);
   if (L.math == CFC_MATH_BF16) return launch_mode<__nv_bfloat16, CFC_MATH_BF16>(L, a, out, s);
   return cudaErrorNotSupported;
+}
+
+bool grad_x_gemm_applies(const Layout& L) {
+  GradXPlan p;
+  return plan_grad_x(L, &p) && encode_fn() != nullptr;
+}
+
+cudaError_t launch_grad_x_tc(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  GradXPlan p;
+  if (!a.grad_x || !plan_grad_x(L, &p)) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32) return launch_grad_x<float, CFC_MATH_TF32>(L, p, a, s);
+  return launch_grad_x<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
 }
 
 }  // namespace cfc

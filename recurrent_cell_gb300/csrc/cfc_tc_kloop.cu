@@ -422,28 +422,30 @@ cudaError_t launch_fwd(const Layout& L, const TcPlan& p, const CfcArgs& a, cudaS
 // ---------------------------------------------------------------------------
 // Backward K loop on the tensor cores, the cluster split by hidden units.
 //
-// Block r of the cluster owns units U_r = [32r, 32r+32) and the x columns
-// X_r = [r*xs, (r+1)*xs), xs = n_in / C.  Per step k (reverse) it
+// Block r of the cluster owns units U_r = [32r, 32r+32).  Per step k
+// (reverse) it
 //   1. forms dA of its units for the Bt samples from its carry (the gradient
 //      reaching its units' h columns, summed at the end of the previous step),
 //      the saved activations (loaded one step ahead) and the upstream seeds;
 //      writes dA to global memory (operand type) and into the K-major B tile
 //      (rows = samples, K = (head, unit) = 96);
-//   2. computes its partial dz_r^T [Zc x Bt] = W_cat[rows of U_r]^T dA_r^T:
-//      nMt M=128 MMA chains, A = its 96 columns of W_cat^T resident in shared
+//   2. computes its partial carry^T [H x Bt] = W_rec[rows of U_r]^T dA_r^T:
+//      nMt M=128 MMA chains, A = its 96 columns of W_rec^T resident in shared
 //      memory (K-major, 128B swizzle), accumulators in TMEM;
-//   3. sends each partial column j to the block that owns j (an x column or a
-//      unit) through distributed shared memory: receive buffer [source block]
-//      [column][sample], double-buffered by step parity;
-//   4. after one cluster barrier, sums the C partials of its own columns in
-//      block order (deterministic): x columns -> grad_x[:, k], unit columns ->
-//      the carry of step k-1, or grad_h0 after step 0.
+//   3. sends each partial unit column j to the block that owns unit j through
+//      distributed shared memory: receive buffer [source block][unit][sample],
+//      double-buffered by step parity;
+//   4. after one cluster barrier, sums the C partials of its own units in
+//      block order (deterministic): the carry of step k-1, or grad_h0 after
+//      step 0.
 // Only partial sums cross the cluster; dA never leaves the block that made it.
+// grad_x = dA W_in does not feed the recurrence: it is one GEMM over all B*K
+// rows after the loop (launch_grad_x_tc).
 // ---------------------------------------------------------------------------
-constexpr int kBwdMaxItems = 16;        // (unit, sample) items per thread: 32*Bt <= 16*256
+constexpr int kBwdMaxItems = 8;         // (unit, sample) items per thread: 32*Bt <= 8*256
 
 struct TcBwdPlan {
-  int C = 0, Bt = 0, nMt = 0, nAk = 0, xs = 0;
+  int C = 0, Bt = 0, nMt = 0, nAk = 0;
   size_t smem = 0, off_da = 0, off_recv = 0, off_carry = 0, off_dt = 0;
   uint32_t tmem_cols = 0;
 };
@@ -451,18 +453,18 @@ struct TcBwdPlan {
 template <typename ET, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const float* __restrict__ dt,
-             int dt_stride, int B, int K, int n_in, int H, int Bt, int nMt, int nAk, int xs, uint32_t off_da,
-             uint32_t off_recv, uint32_t off_carry, uint32_t off_dt, uint32_t tmem_cols,
-             const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
-             const float* __restrict__ grad_h_last, const float* __restrict__ y, const float* __restrict__ act,
-             ET* __restrict__ dA_out, float* __restrict__ grad_h0, float* __restrict__ grad_x) {
+             int dt_stride, int B, int K, int H, int Bt, int nMt, int nAk, uint32_t off_da, uint32_t off_recv,
+             uint32_t off_carry, uint32_t off_dt, uint32_t tmem_cols, const ET* __restrict__ h_seq,
+             const float* __restrict__ grad_h_seq, const float* __restrict__ grad_h_last,
+             const float* __restrict__ y, const float* __restrict__ act, ET* __restrict__ dA_out,
+             float* __restrict__ grad_h0) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int r = (int)cluster.block_rank();
-  const int Zc = n_in + H, H3 = 3 * H;
+  const int H3 = 3 * H;
   const int Mrows = nMt * 128;
   const int Kpad = nAk * (128 / (int)sizeof(ET));
-  const int cpo = xs + kUnits;                       // columns owned by one block
+  constexpr int cpo = kUnits;                        // columns owned by one block
   const int b0 = (int)(blockIdx.x / C) * Bt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nitems = kUnits * Bt;
@@ -471,7 +473,7 @@ k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const fl
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t* Wt = sm;                                        // nAk x [Mrows][128 B]
   uint8_t* dAs = sm + off_da;                              // nAk x [Bt][128 B]
-  float* recv = reinterpret_cast<float*>(sm + off_recv);   // [2][C][cpo][Bt]
+  float* recv = reinterpret_cast<float*>(sm + off_recv);   // [2][C][32][Bt]
   float* carry = reinterpret_cast<float*>(sm + off_carry); // [Bt][33]
   float* dts = reinterpret_cast<float*>(sm + off_dt);      // [Bt]
   __shared__ uint64_t bar;
@@ -484,13 +486,13 @@ k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const fl
     err = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
-  // A operand: row j (z column), K index kap = c*32 + u -> W_cat[c*H + 32r + u][j].
+  // A operand: row j (unit), K index kap = c*32 + u -> W_rec[c*H + 32r + u][j].
   for (int e = tid; e < Mrows * Kpad; e += kThreads) {
     const int kap = e / Mrows, j = e - kap * Mrows;
     float v = 0.f;
-    if (j < Zc && kap < 3 * kUnits) {
+    if (j < H && kap < 3 * kUnits) {
       const long long row = (long long)(kap >> 5) * H + r * kUnits + (kap & 31);
-      v = (j < n_in) ? ld_operand<MODE>(W_in + row * n_in + j) : ld_operand<MODE>(W_rec + row * H + (j - n_in));
+      v = ld_operand<MODE>(W_rec + row * H + j);
     }
     st_elem<ET>(Wt + kmajor_off<ET>(j, kap, Mrows), v);
   }
@@ -585,22 +587,15 @@ k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const fl
       tc::fence_before_sync();
       __syncthreads();
       tc::fence_after_sync();
-      // ---- 3. partial column j -> its owner's receive buffer [buf][r][jl][n]
+      // ---- 3. partial unit column j -> its owner's receive buffer [buf][r][jl][n]
       const int qd = warp & 3, half = warp >> 2, nch = Bt / 16;
       for (int pidx = half; pidx < nMt * nch; pidx += 2) {
         const int mt = pidx / nch, n0 = (pidx - mt * nch) * 16;
         const int j = mt * 128 + qd * 32 + lane;
         float v[16];
         tc::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(mt * Bt + n0), v);
-        if (j < Zc) {
-          int owner, jl;
-          if (j < n_in) {
-            owner = j / xs;
-            jl = j - owner * xs;
-          } else {
-            owner = (j - n_in) >> 5;
-            jl = xs + ((j - n_in) & 31);
-          }
+        if (j < H) {
+          const int owner = j >> 5, jl = j & 31;
           const uint32_t off = (uint32_t)((((buf * C + r) * cpo + jl) * Bt + n0) * 4);
           const uint32_t dst = (owner == r) ? 0u : dsmem_map(recv_addr, (uint32_t)owner);
 #pragma unroll
@@ -619,16 +614,11 @@ k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const fl
     cluster_wait_acquire();
     tc::fence_after_sync();
     for (int e = tid; e < cpo * Bt; e += kThreads) {
-      const int jl = e / Bt, n = e - jl * Bt, bb = b0 + n;
+      const int u = e / Bt, n = e - u * Bt, bb = b0 + n;
       float sum = 0.f;
-      for (int src = 0; src < C; ++src) sum += recv[((buf * C + src) * cpo + jl) * Bt + n];
-      if (jl < xs) {
-        if (grad_x && bb < B) grad_x[((long long)bb * K + k) * n_in + r * xs + jl] = sum;
-      } else {
-        const int u = jl - xs;
-        if (k > 0) carry[n * 33 + u] = sum;
-        else if (grad_h0 && bb < B) grad_h0[(long long)bb * H + r * kUnits + u] = sum;
-      }
+      for (int src = 0; src < C; ++src) sum += recv[((buf * C + src) * cpo + u) * Bt + n];
+      if (k > 0) carry[n * 33 + u] = sum;
+      else if (grad_h0 && bb < B) grad_h0[(long long)bb * H + r * kUnits + u] = sum;
     }
     __syncthreads();
   }
@@ -642,11 +632,10 @@ bool plan_bwd_cluster(const Layout& L, TcBwdPlan* p) {
   if (L.math == CFC_MATH_FP32) return false;
   if (L.H % kUnits || L.H / kUnits > 8) return false;
   const int C = L.H / kUnits;
-  if (L.n_in % C) return false;
   const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
-  const int nMt = (L.Zc + 127) / 128;
+  const int nMt = (L.H + 127) / 128;
   const int nAk = (3 * kUnits * es + 127) / 128;
-  const int xs = L.n_in / C, cpo = xs + kUnits;
+  const int cpo = kUnits;
   auto smem_for = [&](int Bt, TcBwdPlan* q) {
     size_t off = (size_t)nAk * nMt * 128 * 128;
     q->off_da = off;
@@ -675,7 +664,6 @@ bool plan_bwd_cluster(const Layout& L, TcBwdPlan* p) {
   p->Bt = best;
   p->nMt = nMt;
   p->nAk = nAk;
-  p->xs = xs;
   smem_for(best, p);
   uint32_t cols = 32;
   while (cols < (uint32_t)(nMt * best)) cols <<= 1;
@@ -700,13 +688,17 @@ cudaError_t launch_bwd_cluster(const Layout& L, const TcBwdPlan& p, const CfcArg
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  TraceScope trace("cfc_bwd_cluster_tc", s);
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.dt,
-                            a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt, p.nMt, p.nAk, p.xs, (uint32_t)p.off_da,
-                            (uint32_t)p.off_recv, (uint32_t)p.off_carry, (uint32_t)p.off_dt, p.tmem_cols,
-                            static_cast<const ET*>(a.h_seq), a.grad_h_seq, a.grad_h_last, a.y,
-                            reinterpret_cast<const float*>(a.ws + L.off_act),
-                            reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0, a.grad_x);
+  {
+    TraceScope trace("cfc_bwd_cluster_tc", s);
+    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.dt,
+                           a.dt_stride, L.B, L.K, L.H, p.Bt, p.nMt, p.nAk, (uint32_t)p.off_da,
+                           (uint32_t)p.off_recv, (uint32_t)p.off_carry, (uint32_t)p.off_dt, p.tmem_cols,
+                           static_cast<const ET*>(a.h_seq), a.grad_h_seq, a.grad_h_last, a.y,
+                           reinterpret_cast<const float*>(a.ws + L.off_act), reinterpret_cast<ET*>(a.ws + L.off_dA),
+                           a.grad_h0);
+  }
+  if (e != cudaSuccess || !a.grad_x) return e;
+  return launch_grad_x_tc(L, a, s);
 }
 
 }  // namespace
@@ -737,6 +729,7 @@ cudaError_t launch_backward_cluster_tc(const Layout& L, const CfcArgs& a, cudaSt
   if (choice == kCluster || choice == kSimt || choice == kTcStream) return cudaErrorNotSupported;
   TcBwdPlan p;
   if (!plan_bwd_cluster(L, &p)) return cudaErrorNotSupported;
+  if (a.grad_x && !grad_x_gemm_applies(L)) return cudaErrorNotSupported;
   if (choice == kAuto && (long long)(L.B + p.Bt - 1) / p.Bt * p.C > kNumSMs) return cudaErrorNotSupported;
   if (L.math == CFC_MATH_TF32) return launch_bwd_cluster<float, CFC_MATH_TF32>(L, p, a, s);
   return launch_bwd_cluster<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);

@@ -11,26 +11,27 @@
 // epilogue overwrites with h_{k+1} once the step's MMAs are complete.
 //
 // Backward, per step k (reverse): the block computes the gradient reaching
-// z_k = [x_k; h_k]
+// h_k (the carry)
 //
-//   dz^T [Zc x Bt] = W_cat^T [Zc x 3H] * dA_k^T [3H x Bt]
+//   carry^T [H x Bt] = W_rec^T [H x 3H] * dA_k^T [3H x Bt]
 //
-// as nM = ceil(Zc/128) MMA row tiles (M = 128 z-columns, N = Bt samples,
-// K = 3H).  The A operand, W_cat^T, is the same for every step and every
-// block: it is prepared once per call as pre-swizzled 16 KB tiles (128 rows x
-// 128 bytes of K) in the workspace and streamed through a ring of shared-memory
-// stages with TMA bulk copies (cp.async.bulk, mbarrier transaction counts).
+// as nM = ceil(H/128) MMA row tiles (M = 128 units, N = Bt samples, K = 3H).
+// (grad_x = dA W_in does not feed the recurrence; it is one GEMM over all B*K
+// rows after the loop.)  The A operand, W_rec^T, is the same for every step
+// and every block: it is prepared once per call as pre-swizzled 16 KB tiles
+// (128 rows x 128 bytes of K) in the workspace and streamed through a ring of
+// shared-memory stages with TMA bulk copies (cp.async.bulk, mbarrier
+// transaction counts).
 // The tile sequence repeats every step, so the copies for the next step's
 // first tiles run while the block computes the next dA.  The B operand, dA_k
 // of the Bt samples, is computed by the block itself into a K-major swizzled
 // shared-memory tile.
 //
-// Elementwise phase of step k: thread <-> z-column j = 128*mt + 32*(warp%4) +
-// lane (the TMEM lane quadrant rule).  It reads dz of step k+1 for its column
-// from TMEM: x columns become grad_x[:, k+1], h columns the carry of unit
-// j - n_in, from which (with the saved activations) it forms the three dA
-// values of that unit for every sample of the tile.  After step 0 the same
-// read gives grad_x[:, 0] and grad_h0.
+// Elementwise phase of step k: thread <-> unit j = 128*mt + 32*(warp%4) + lane
+// (the TMEM lane quadrant rule).  It reads the carry of step k+1 for its unit
+// from TMEM and forms (with the saved activations) the three dA values of
+// that unit for every sample of the tile.  After step 0 the same read gives
+// grad_h0.
 //
 // Waits are bounded; a timeout records an error in the device error word.
 #include <algorithm>
@@ -95,14 +96,13 @@ __device__ __forceinline__ uint32_t kmajor_off(int row, int kk, int rows) {
   return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
 }
 
-// W_cat^T tiles: tile (mt, a) holds rows j = 128*mt .. 128*mt+127 (z columns)
+// W_rec^T tiles: tile (mt, a) holds rows j = 128*mt .. 128*mt+127 (units)
 // and K elements a*EPA .. a*EPA+EPA-1 (EPA = 128 bytes / element), at byte
 // offset ((a * nM) + mt) * kTile, swizzled exactly as in shared memory.
 template <typename ET, int MODE>
-__global__ void k_prep_wt_tiles(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, int n_in,
-                                int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
+__global__ void k_prep_wt_tiles(const ET* __restrict__ W_rec, int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
   constexpr int EPA = 128 / sizeof(ET);
-  const int Zc = n_in + H, H3 = 3 * H;
+  const int H3 = 3 * H;
   const long long total = (long long)nM * nAk * 128 * EPA;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -113,9 +113,7 @@ __global__ void k_prep_wt_tiles(const ET* __restrict__ W_in, const ET* __restric
     const int mt = (int)(t % nM), a = (int)(t / nM);
     const int j = mt * 128 + i, kk = a * EPA + kl;
     float v = 0.f;
-    if (j < Zc && kk < H3)
-      v = (j < n_in) ? ld_operand<MODE>(W_in + (long long)kk * n_in + j)
-                     : ld_operand<MODE>(W_rec + (long long)kk * H + (j - n_in));
+    if (j < H && kk < H3) v = ld_operand<MODE>(W_rec + (long long)kk * H + j);
     st_elem<ET>(tiles + t * kTile + tc::sw128_offset(i, kl * sizeof(ET)), v);
   }
 }
@@ -123,12 +121,11 @@ __global__ void k_prep_wt_tiles(const ET* __restrict__ W_in, const ET* __restric
 template <typename ET, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, int dt_stride, int B,
-              int K, int n_in, int H, int Bt, int nM, int nAk, int nst, uint32_t tmem_cols,
+              int K, int H, int Bt, int nM, int nAk, int nst, uint32_t tmem_cols,
               const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
               const float* __restrict__ grad_h_last, const float* __restrict__ y,
-              const float* __restrict__ act, ET* __restrict__ dA_out, float* __restrict__ grad_h0,
-              float* __restrict__ grad_x) {
-  const int Zc = n_in + H, H3 = 3 * H;
+              const float* __restrict__ act, ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
+  const int H3 = 3 * H;
   const int b0 = blockIdx.x * Bt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
   const int T = nAk * nM;                       // streamed tiles per step
@@ -192,10 +189,10 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
     for (int i = 0; i < nst - 2 && copies_left > 0; ++i) issue_copy();
   }
 
-  // rows of z handled by this thread: j = 128*mt + 32*quad + lane for mt = warp/4, warp/4 + 2, ...
+  // units handled by this thread: j = 128*mt + 32*quad + lane for mt = warp/4, warp/4 + 2, ...
   for (int step = 0; step <= K; ++step) {
     const int k = K - 1 - step;                  // step == K: final read-out only
-    // ---- elementwise phase: dz of step k+1 from TMEM -> grad_x / carry -> dA_k
+    // ---- elementwise phase: carry of step k+1 from TMEM -> dA_k
     for (int mt = warp >> 2; mt < nM; mt += kThreads / 128) {
       const int j = mt * 128 + quad * 32 + lane;
       for (int n0 = 0; n0 < Bt; n0 += 16) {
@@ -206,16 +203,8 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
 #pragma unroll
           for (int i = 0; i < 16; ++i) dz[i] = 0.f;
         }
-        if (j < n_in) {
-          if (step > 0 && grad_x) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int bb = b0 + n0 + i;
-              if (bb < B) grad_x[((long long)bb * K + (k + 1)) * n_in + j] = dz[i];
-            }
-          }
-        } else if (j < Zc) {
-          const int u = j - n_in;
+        if (j < H) {
+          const int u = j;
           if (k < 0) {                           // after step 0: grad_h0
             if (grad_h0) {
 #pragma unroll
@@ -270,7 +259,7 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    // ---- MMA phase (thread 0): stream W_cat^T tiles, dz_k = W^T dA_k into TMEM
+    // ---- MMA phase (thread 0): stream W_rec^T tiles, carry_k = W_rec^T dA_k into TMEM
     if (tid == 0) {
       const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
       const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(dAs));
@@ -704,7 +693,7 @@ struct BwdPlan {
 bool plan_bwd(const Layout& L, BwdPlan* p) {
   if (L.math == CFC_MATH_FP32) return false;
   const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
-  const int nM = (L.Zc + 127) / 128;
+  const int nM = (L.H + 127) / 128;
   const int nAk = (L.H3 * es + 127) / 128;
   // Bt: samples per block, the MMA's N: about one block per SM, at least 32.
   int Bt = (int)(((long long)L.B + kNumSMs - 1) / kNumSMs);
@@ -732,9 +721,7 @@ cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cuda
     const long long total = (long long)p.nM * p.nAk * 128 * (128 / sizeof(ET));
     const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
     TraceScope trace("prep_wt_tiles", s);
-    k_prep_wt_tiles<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_in),
-                                                     static_cast<const ET*>(a.W_rec), L.n_in, L.H, p.nM,
-                                                     p.nAk, tiles);
+    k_prep_wt_tiles<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_rec), L.H, p.nM, p.nAk, tiles);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -742,12 +729,16 @@ cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cuda
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
   const int grid = (L.B + p.Bt - 1) / p.Bt;
-  TraceScope trace("cfc_bwd_tc", s);
-  kern<<<grid, kThreads, p.smem, s>>>(tiles, a.dt, a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt, p.nM, p.nAk,
-                                      p.nst, p.tmem_cols, static_cast<const ET*>(a.h_seq), a.grad_h_seq,
-                                      a.grad_h_last, a.y, reinterpret_cast<const float*>(a.ws + L.off_act),
-                                      reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0, a.grad_x);
-  return cudaGetLastError();
+  {
+    TraceScope trace("cfc_bwd_tc", s);
+    kern<<<grid, kThreads, p.smem, s>>>(tiles, a.dt, a.dt_stride, L.B, L.K, L.H, p.Bt, p.nM, p.nAk, p.nst,
+                                        p.tmem_cols, static_cast<const ET*>(a.h_seq), a.grad_h_seq, a.grad_h_last,
+                                        a.y, reinterpret_cast<const float*>(a.ws + L.off_act),
+                                        reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess || !a.grad_x) return e;
+  return launch_grad_x_tc(L, a, s);
 }
 
 }  // namespace
@@ -755,8 +746,8 @@ cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cuda
 size_t tc_bwd_tiles_bytes(int n_in, int n_hid, int math) {
   if (math == CFC_MATH_FP32) return 0;
   const int es = (math == CFC_MATH_TF32) ? 4 : 2;
-  // backward: W_cat^T tiles; forward: W_cat tiles (the two are never live at once)
-  const size_t bwd = (size_t)((n_in + n_hid + 127) / 128) * ((3 * n_hid * es + 127) / 128) * kTile;
+  // backward: W_rec^T tiles; forward: W_cat tiles (the two are never live at once)
+  const size_t bwd = (size_t)((n_hid + 127) / 128) * ((3 * n_hid * es + 127) / 128) * kTile;
   const size_t fwd = (size_t)(3 * ((n_hid + 127) / 128)) * (((n_in + n_hid) * es + 127) / 128) * kTile;
   return std::max(bwd, fwd);
 }
@@ -785,6 +776,7 @@ cudaError_t launch_backward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s
   if (choice == kCluster || choice == kSimt) return cudaErrorNotSupported;
   BwdPlan p;
   if (!plan_bwd(L, &p)) return cudaErrorNotSupported;
+  if (a.grad_x && !grad_x_gemm_applies(L)) return cudaErrorNotSupported;
   if (L.math == CFC_MATH_TF32) return launch_bwd<float, CFC_MATH_TF32>(L, p, a, s);
   return launch_bwd<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
 }
