@@ -91,8 +91,9 @@ def kernel_work(name, w, n_split):
         byts = R * n_in * s + R * H * s + R * H3 * 4 + B * H * s + H3 * Zc * s
         return flops, byts, engine
     if name.startswith("cfc_bwd"):
-        if engine == "tensor":
-            # the tensor-core K loops carry W_rec^T dA only; grad_x is grad_x_tc
+        if name != "cfc_bwd_simt":
+            # the cluster and tensor-core K loops carry W_rec^T dA only; grad_x
+            # (when requested) is its own GEMM
             flops = 2.0 * R * H3 * H
             byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * H * s
         else:

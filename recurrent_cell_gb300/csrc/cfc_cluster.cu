@@ -14,13 +14,13 @@
 // slices; the operand buffer is double-buffered so that no second barrier is
 // needed.
 //
-// Backward: block r owns the same units for the elementwise dA and a set of
-// output columns of dz = W_cat^T dA: a slice of the x columns (grad_x) and the
-// h columns of its own units (the carry of its own units, which it needs next
-// step).  It keeps the columns of W_cat for that set in shared memory,
-// [3H][nJ].  Each step it computes dA of its units, broadcasts it to every
+// Backward: block r owns the same units for the elementwise dA and the
+// matching columns of the carry W_rec^T dA (the carry of its own units, which
+// it needs next step).  It keeps those columns of W_rec in shared memory,
+// [3H][Hc].  Each step it computes dA of its units, broadcasts it to every
 // block of the cluster (distributed shared memory, double-buffered), and after
-// the cluster barrier contracts the full dA vector with its columns.
+// the cluster barrier contracts the full dA vector with its columns.  grad_x =
+// dA W_in does not feed the recurrence and is one GEMM after the loop.
 //
 // Every kernel here reads the weights from HBM once per block per launch; the
 // K loop runs on chip.  No spin waits: the only synchronisation is the
@@ -216,30 +216,25 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
                   const T* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
                   const float* __restrict__ grad_h_last, const float* __restrict__ y,
                   const float* __restrict__ act, DT* __restrict__ dA_out,
-                  float* __restrict__ grad_h0, float* __restrict__ grad_x) {
+                  float* __restrict__ grad_h0) {
   constexpr int kItemsPerThread = items_per_thread(BT);
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int r = (int)cluster.block_rank();
   const int Hc = H / C, H3 = 3 * H;
-  const int xa = (int)((long long)r * n_in / C), xb = (int)((long long)(r + 1) * n_in / C);
-  const int nx = xb - xa, nJ = nx + Hc;
-  const int nJmax = (n_in + C - 1) / C + Hc;
+  const int nJ = Hc, nJmax = Hc;
   const int b0 = (int)(blockIdx.x / C) * BT;
   const int tid = threadIdx.x, nthr = blockDim.x;
 
   extern __shared__ float sm[];
-  float* Wc = sm;                              // [3H][nJmax] columns of W_cat owned here
+  float* Wc = sm;                              // [3H][Hc] columns of W_rec owned here
   float* dAf = Wc + (size_t)H3 * nJmax;        // [2][BT][3H] dA of all units (operand values)
   float* part = dAf + 2 * BT * H3;             // [S][BT][nJmax] partial column sums
   float* dts = part + (size_t)S * BT * nJmax;  // [BT]
 
   for (int e = tid; e < H3 * nJmax; e += nthr) {
     const int row = e / nJmax, jj = e - row * nJmax;
-    float v = 0.f;
-    if (jj < nx) v = ld_operand<MODE>(W_in + (long long)row * n_in + xa + jj);
-    else if (jj < nJ) v = ld_operand<MODE>(W_rec + (long long)row * H + r * Hc + (jj - nx));
-    Wc[e] = v;
+    Wc[e] = ld_operand<MODE>(W_rec + (long long)row * H + r * Hc + jj);
   }
   for (int e = tid; e < BT; e += nthr) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
   cluster.sync();
@@ -283,27 +278,15 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
       if (q < S) v += pv[q];
     return v;
   };
-  // grad_x of step kk (its x columns), from the contraction held in part.
-  auto finish_grad_x = [&](int kk) {
-    if (!grad_x) return;
-    for (int e = tid; e < BT * nx; e += nthr) {
-      const int n = e / nx, c = e - n * nx, bb = b0 + n;
-      const float v = column_sum(n, c);
-      if (bb < B) grad_x[((long long)bb * K + kk) * n_in + xa + c] = v;
-    }
-  };
-
-  // Per step: (A) finish the previous step's contraction (grad_x columns and
-  // the carry of the owned units), then dA of the owned units, broadcast to
-  // every block; cluster barrier; (B) contract the full dA with the owned
-  // columns into part; block barrier.
+  // Per step: (A) dA of the owned units from the previous step's carry
+  // (summed from part), broadcast to every block; cluster barrier; (B)
+  // contract the full dA with the owned columns into part; block barrier.
   for (int k = K - 1; k >= 0; --k) {
     float* buf = dAf + (k & 1) * BT * H3;
     float cg_[kItemsPerThread], cgg[kItemsPerThread], chh[kItemsPerThread], cup[kItemsPerThread];
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) { cg_[q] = pg[q]; cgg[q] = pgg[q]; chh[q] = phh[q]; cup[q] = pup[q]; }
     load_act(k - 1);
-    if (k < K - 1) finish_grad_x(k + 1);
     float rd0[kItemsPerThread], rd1[kItemsPerThread], rd2[kItemsPerThread];
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) {
@@ -314,7 +297,7 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
       float d0 = 0.f, d1 = 0.f, d2 = 0.f;
       if (bb < B) {
         const long long row = (long long)bb * K + k;
-        float delta = ((k < K - 1) ? column_sum(n, nx + u) : 0.f) + cup[q];
+        float delta = ((k < K - 1) ? column_sum(n, u) : 0.f) + cup[q];
         if (k == K - 1) {
           if (grad_h_last) delta += grad_h_last[(long long)bb * H + unit];
           if (y) delta += ldf(h_seq + row * H + unit) - y[(long long)bb * H + unit];
@@ -376,11 +359,10 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
     }
     __syncthreads();
   }
-  finish_grad_x(0);
   if (grad_h0) {
     for (int e = tid; e < BT * Hc; e += nthr) {
       const int n = e / Hc, u = e - n * Hc, bb = b0 + n;
-      const float v = column_sum(n, nx + u);
+      const float v = column_sum(n, u);
       if (bb < B) grad_h0[(long long)bb * H + r * Hc + u] = v;
     }
   }
@@ -399,7 +381,7 @@ size_t fwd_smem(const Layout& L, int C, int BT, int S) {
 
 size_t bwd_smem(const Layout& L, int C, int BT, int S) {
   const int Hc = L.H / C;
-  const int nJmax = (L.n_in + C - 1) / C + Hc;
+  const int nJmax = Hc;
   return sizeof(float) * ((size_t)L.H3 * nJmax + 2 * (size_t)BT * L.H3 + (size_t)S * BT * nJmax + BT);
 }
 
@@ -413,7 +395,7 @@ bool plan(const Layout& L, bool forward, ClusterPlan* p) {
   auto valid = [&](int c) {
     if (L.H % c) return false;
     const int Hc = L.H / c;
-    if (forward ? (Hc > kClusterThreads) : ((L.n_in + c - 1) / c + Hc > kClusterThreads)) return false;
+    if (Hc > kClusterThreads) return false;
     return (forward ? fwd_smem(L, c, 1, 1) : bwd_smem(L, c, 1, 1)) <= kSmemLimit;
   };
   const int target = (L.H + 31) / 32;
@@ -426,7 +408,7 @@ bool plan(const Layout& L, bool forward, ClusterPlan* p) {
   if (!C) C = largest;
   if (!C) return false;
   const int Hc = L.H / C;
-  const int width = forward ? Hc : (L.n_in + C - 1) / C + Hc;
+  const int width = Hc;
   const int S = std::max(1, std::min(kMaxSplit, kClusterThreads / width));
   const int threads = std::min(kClusterThreads, (width * S + 31) / 32 * 32);
   auto smem = [&](int bt) { return forward ? fwd_smem(L, C, bt, S) : bwd_smem(L, C, bt, S); };
@@ -488,13 +470,18 @@ cudaError_t fwd_bt(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cuda
 
 template <typename T, typename DT, int MODE, int BT>
 cudaError_t bwd_bt(const Layout& L, const ClusterPlan& p, const CfcArgs& a, cudaStream_t s) {
-  TraceScope trace("cfc_bwd_cluster", s);
-  return launch_cluster(k_cfc_bwd_cluster<T, DT, MODE, BT>, p, L.B, s,
-                        static_cast<const T*>(a.W_in), static_cast<const T*>(a.W_rec), a.dt,
-                        a.dt_stride, L.B, L.K, L.n_in, L.H, p.S, static_cast<const T*>(a.h_seq),
-                        a.grad_h_seq, a.grad_h_last, a.y,
-                        reinterpret_cast<const float*>(a.ws + L.off_act),
-                        reinterpret_cast<DT*>(a.ws + L.off_dA), a.grad_h0, a.grad_x);
+  cudaError_t e;
+  {
+    TraceScope trace("cfc_bwd_cluster", s);
+    e = launch_cluster(k_cfc_bwd_cluster<T, DT, MODE, BT>, p, L.B, s,
+                       static_cast<const T*>(a.W_in), static_cast<const T*>(a.W_rec), a.dt,
+                       a.dt_stride, L.B, L.K, L.n_in, L.H, p.S, static_cast<const T*>(a.h_seq),
+                       a.grad_h_seq, a.grad_h_last, a.y,
+                       reinterpret_cast<const float*>(a.ws + L.off_act),
+                       reinterpret_cast<DT*>(a.ws + L.off_dA), a.grad_h0);
+  }
+  if (e != cudaSuccess) return e;
+  return launch_grad_x_simt(L, a, s);
 }
 
 template <typename T, int MODE>

@@ -149,6 +149,8 @@ int kernel_choice();
 // nothing, when the sizes do not fit its plan or another family is forced.
 cudaError_t launch_forward_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 int read_tc_kloop_error(int clear);
+// grad_x = dA W_in on CUDA cores after the cluster K loop (any mode).
+cudaError_t launch_grad_x_simt(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // grad_x = dA W_in for the tensor-core K-loop kernels (which carry only
 // W_rec^T dA): one TMA-fed tcgen05 GEMM over the B*K rows after the loop.
 bool grad_x_gemm_applies(const Layout& L);

@@ -388,6 +388,70 @@ cudaError_t wgrad_mode(const Layout& L, const CfcArgs& a, float* out, int n_spli
   return cudaGetLastError();
 }
 
+// grad_x[r][i] = sum_m dA[r][m] * W_in[m][i] over the B*K rows r (W_in stacked
+// as [3H][n_in], operand-rounded), for the K-loop kernels that leave grad_x
+// out of the recurrence.  64 x 64 output tiles, m in chunks of 32 through
+// shared memory, 4 x 4 outputs per thread; every output sums m in ascending
+// order (deterministic).
+constexpr int kGxTile = 64, kGxK = 32;
+
+template <typename T, typename DT, int MODE>
+__global__ void __launch_bounds__(256)
+k_grad_x_simt(const DT* __restrict__ dA, const T* __restrict__ W_in, long long R, int H3, int n_in,
+              float* __restrict__ grad_x) {
+  __shared__ float As[kGxK][kGxTile + 1];     // [m][row]
+  __shared__ float Bs[kGxK][kGxTile];         // [m][col]
+  const long long r0 = (long long)blockIdx.x * kGxTile;
+  const int c0 = blockIdx.y * kGxTile;
+  const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+  float acc[4][4] = {};
+  for (int m0 = 0; m0 < H3; m0 += kGxK) {
+    for (int e = tid; e < kGxTile * kGxK; e += 256) {
+      const int rr = e / kGxK, mm = e - rr * kGxK;
+      const long long row = r0 + rr;
+      As[mm][rr] = (row < R && m0 + mm < H3) ? ldf(dA + row * H3 + m0 + mm) : 0.f;
+    }
+    for (int e = tid; e < kGxTile * kGxK; e += 256) {
+      const int mm = e / kGxTile, cc = e - mm * kGxTile;
+      Bs[mm][cc] = (m0 + mm < H3 && c0 + cc < n_in) ? ld_operand<MODE>(W_in + (long long)(m0 + mm) * n_in + c0 + cc)
+                                                      : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int mm = 0; mm < kGxK; ++mm) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[mm][tr * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[mm][tc * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long row = r0 + tr * 4 + i;
+    if (row >= R) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = c0 + tc * 4 + j;
+      if (col < n_in) grad_x[row * n_in + col] = acc[i][j];
+    }
+  }
+}
+
+template <typename T, typename DT, int MODE>
+cudaError_t grad_x_mode(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  dim3 grid((unsigned)((L.R + kGxTile - 1) / kGxTile), (unsigned)((L.n_in + kGxTile - 1) / kGxTile));
+  TraceScope trace("grad_x_simt", s);
+  k_grad_x_simt<T, DT, MODE><<<grid, 256, 0, s>>>(reinterpret_cast<const DT*>(a.ws + L.off_dA),
+                                                  static_cast<const T*>(a.W_in), L.R, L.H3, L.n_in, a.grad_x);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t s) {
@@ -412,6 +476,15 @@ cudaError_t launch_wgrad_simt(const Layout& L, const CfcArgs& a, float* out, int
     case CFC_MATH_FP32: return wgrad_mode<float, float, CFC_MATH_FP32>(L, a, out, n_split, rows_per_split, s);
     case CFC_MATH_TF32: return wgrad_mode<float, float, CFC_MATH_TF32>(L, a, out, n_split, rows_per_split, s);
     default: return wgrad_mode<__nv_bfloat16, __nv_bfloat16, CFC_MATH_BF16>(L, a, out, n_split, rows_per_split, s);
+  }
+}
+
+cudaError_t launch_grad_x_simt(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  if (!a.grad_x) return cudaSuccess;
+  switch (L.math) {
+    case CFC_MATH_FP32: return grad_x_mode<float, float, CFC_MATH_FP32>(L, a, s);
+    case CFC_MATH_TF32: return grad_x_mode<float, float, CFC_MATH_TF32>(L, a, s);
+    default: return grad_x_mode<__nv_bfloat16, __nv_bfloat16, CFC_MATH_BF16>(L, a, s);
   }
 }
 
