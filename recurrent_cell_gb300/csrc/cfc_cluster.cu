@@ -226,16 +226,19 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
   const int b0 = (int)(blockIdx.x / C) * BT;
   const int tid = threadIdx.x, nthr = blockDim.x;
 
+  const int H3p = (H3 + 3) & ~3;                // dA row length, zero-padded
+  const int ldw = (H3p % 8 == 0) ? H3p + 4 : H3p;  // weight row stride (ldw/4 odd)
   extern __shared__ float sm[];
-  float* Wc = sm;                              // [3H][Hc] columns of W_rec owned here
-  float* dAf = Wc + (size_t)H3 * nJmax;        // [2][BT][3H] dA of all units (operand values)
-  float* part = dAf + 2 * BT * H3;             // [S][BT][nJmax] partial column sums
+  float* Wc = sm;                              // [Hc][ldw]: W_rec columns owned here, transposed
+  float* dAf = Wc + (size_t)Hc * ldw;          // [2][BT][H3p] dA of all units (operand values)
+  float* part = dAf + 2 * BT * H3p;            // [S][BT][nJmax] partial column sums
   float* dts = part + (size_t)S * BT * nJmax;  // [BT]
 
-  for (int e = tid; e < H3 * nJmax; e += nthr) {
-    const int row = e / nJmax, jj = e - row * nJmax;
-    Wc[e] = ld_operand<MODE>(W_rec + (long long)row * H + r * Hc + jj);
+  for (int e = tid; e < Hc * ldw; e += nthr) {
+    const int jj = e / ldw, row = e - jj * ldw;
+    Wc[e] = (row < H3) ? ld_operand<MODE>(W_rec + (long long)row * H + r * Hc + jj) : 0.f;
   }
+  for (int e = tid; e < 2 * BT * H3p; e += nthr) dAf[e] = 0.f;   // padding stays zero
   for (int e = tid; e < BT; e += nthr) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
   cluster.sync();
 
@@ -244,7 +247,9 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
   for (int p = 0; p < 8; ++p) peer_dA[p] = (p < C) ? dsmem_map(smem_addr(dAf), (uint32_t)p) : 0u;
   const int jj = tid % nJmax, s = tid / nJmax;
   const bool dot = (s < S) && (jj < nJ);
-  const int r0 = (int)((long long)s * H3 / S), r1 = (int)((long long)(s + 1) * H3 / S);
+  const int nq = H3p / 4;
+  const int q0 = (int)((long long)s * nq / S), q1 = (int)((long long)(s + 1) * nq / S);
+  const float4* wc4 = reinterpret_cast<const float4*>(Wc + (size_t)jj * ldw);
 
   // Saved activations (and per-step upstream gradient) of this thread's
   // (sample, unit) items, loaded one step ahead (the plan guarantees
@@ -282,7 +287,7 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
   // (summed from part), broadcast to every block; cluster barrier; (B)
   // contract the full dA with the owned columns into part; block barrier.
   for (int k = K - 1; k >= 0; --k) {
-    float* buf = dAf + (k & 1) * BT * H3;
+    float* buf = dAf + (k & 1) * BT * H3p;
     float cg_[kItemsPerThread], cgg[kItemsPerThread], chh[kItemsPerThread], cup[kItemsPerThread];
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) { cg_[q] = pg[q]; cgg[q] = pgg[q]; chh[q] = phh[q]; cup[q] = pup[q]; }
@@ -308,7 +313,7 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
         d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
       }
       rd0[q] = d0; rd1[q] = d1; rd2[q] = d2;
-      const uint32_t off = (uint32_t)(((k & 1) * BT * H3 + n * H3 + unit) * 4);
+      const uint32_t off = (uint32_t)(((k & 1) * BT * H3p + n * H3p + unit) * 4);
 #pragma unroll
       for (int q2 = 0; q2 < 8; ++q2) {
         if (q2 < C) {
@@ -338,21 +343,18 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
       float acc0[BT], acc1[BT];
 #pragma unroll
       for (int n = 0; n < BT; ++n) { acc0[n] = 0.f; acc1[n] = 0.f; }
-      int row = r0;
-#pragma unroll 2
-      for (; row + 1 < r1; row += 2) {
-        const float w0 = Wc[(size_t)row * nJmax + jj];
-        const float w1 = Wc[(size_t)(row + 1) * nJmax + jj];
+      constexpr int kUnroll = BT <= 4 ? 2 : 1;   // larger tiles: registers go to the BT chains
+#pragma unroll(kUnroll)
+      for (int q = q0; q < q1; ++q) {
+        const float4 w = wc4[q];
 #pragma unroll
         for (int n = 0; n < BT; ++n) {
-          acc0[n] = fmaf(w0, buf[n * H3 + row], acc0[n]);
-          acc1[n] = fmaf(w1, buf[n * H3 + row + 1], acc1[n]);
+          const float4 d = reinterpret_cast<const float4*>(buf + n * H3p)[q];
+          acc0[n] = fmaf(w.x, d.x, acc0[n]);
+          acc1[n] = fmaf(w.y, d.y, acc1[n]);
+          acc0[n] = fmaf(w.z, d.z, acc0[n]);
+          acc1[n] = fmaf(w.w, d.w, acc1[n]);
         }
-      }
-      if (row < r1) {
-        const float w0 = Wc[(size_t)row * nJmax + jj];
-#pragma unroll
-        for (int n = 0; n < BT; ++n) acc0[n] = fmaf(w0, buf[n * H3 + row], acc0[n]);
       }
 #pragma unroll
       for (int n = 0; n < BT; ++n) part[(size_t)(s * BT + n) * nJmax + jj] = acc0[n] + acc1[n];
@@ -382,7 +384,8 @@ size_t fwd_smem(const Layout& L, int C, int BT, int S) {
 size_t bwd_smem(const Layout& L, int C, int BT, int S) {
   const int Hc = L.H / C;
   const int nJmax = Hc;
-  return sizeof(float) * ((size_t)L.H3 * nJmax + 2 * (size_t)BT * L.H3 + (size_t)S * BT * nJmax + BT);
+  const int H3p = (L.H3 + 3) & ~3, ldw = (H3p % 8 == 0) ? H3p + 4 : H3p;
+  return sizeof(float) * ((size_t)Hc * ldw + 2 * (size_t)BT * H3p + (size_t)S * BT * nJmax + BT);
 }
 
 // Cluster size from the hidden size alone (so a sample's arithmetic does not
