@@ -54,6 +54,32 @@ __device__ __forceinline__ float ld_operand(const T* p) {
 __device__ __forceinline__ void stf(float* p, float v) { *p = v; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// The cell's three nonlinearities in the tensor-core modes, from
+// tanh(a) = 1 - 2 / (1 + exp(2a)) and gate = 1 / (1 + exp(z)), z = A_f dt:
+// with p1 = 1 + exp(2 A_g), p2 = 1 + exp(2 A_h~), p3 = 1 + exp(z) and one
+// reciprocal r = 1 / (p1 p2 p3), 1/p1 = r p2 p3 and so on.  The exponent
+// arguments are capped at 28 so the product stays finite (p^3 < e^85); at
+// the cap tanh is 1 and the gate below 7e-13, both within an fp32 ulp of the
+// uncapped values' contribution.  Absolute error: a few fp32 ulps of 1, far
+// below the TF32 / bf16 rounding these modes apply.
+struct CellAct {
+  float gate, g, hh;
+};
+__device__ __forceinline__ CellAct cell_act(float a_f, float a_g, float a_h, float dt) {
+  constexpr float kCap = 28.f;
+  const float p1 = 1.f + __expf(fminf(2.f * a_g, kCap));
+  const float p2 = 1.f + __expf(fminf(2.f * a_h, kCap));
+  const float p3 = 1.f + __expf(fminf(a_f * dt, kCap));
+  const float p12 = p1 * p2;
+  const float r = __fdividef(1.f, p12 * p3);
+  const float rp3 = r * p3;
+  CellAct c;
+  c.g = fmaf(-2.f, rp3 * p2, 1.f);
+  c.hh = fmaf(-2.f, rp3 * p1, 1.f);
+  c.gate = r * p12;
+  return c;
+}
+
 // Distributed shared memory: 32-bit shared::cluster address of the variable at
 // local shared address `local` in block `rank` of the cluster, and stores to it.
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {

@@ -188,6 +188,28 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
   for (int p = 0; p < 8; ++p) peer_z[p] = (p < C) ? dsmem_map(smem_addr(Zs), (uint32_t)p) : 0u;
   const int nx = Bt * n_in;     // x values staged per step
 
+  // Cell results of (unit u, sample n) items; lanes of a warp take the 32
+  // units of one sample (n is warp-uniform).  Step k's results are written to
+  // global memory while step k+1's MMAs run.
+  constexpr int kItems = 8;                    // items per thread (plan: 32*Bt <= 8*256)
+  float ig[kItems], igg[kItems], ihh[kItems], ih[kItems];
+  auto store_results = [&](int kk) {
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      const int e = tid + q * kThreads;
+      if (e >= kUnits * Bt) break;
+      const int u = e & 31, n = e >> 5, bb = b0 + n;
+      if (bb < B) {
+        const int unit = r * kUnits + u;
+        const long long row = (long long)bb * K + kk;
+        act[row * H3 + unit] = ig[q];
+        act[row * H3 + H + unit] = igg[q];
+        act[row * H3 + 2 * H + unit] = ihh[q];
+        stf(h_seq + row * H + unit, ih[q]);
+      }
+    }
+  };
+
   for (int k = 0; k < K; ++k) {
     uint8_t* zc = Zs + (k & 1) * zbuf_bytes;
     uint8_t* zn = Zs + ((k + 1) & 1) * zbuf_bytes;
@@ -227,6 +249,7 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
       }
       tc::mma_commit(&bar);
     }
+    if (k > 0) store_results(k - 1);
     // One thread waits for the MMAs; the others meet it at the block barrier.
     if (tid == 0 && !tc::mbar_wait(&bar, k & 1, kMaxPolls)) err = 1;
     tc::fence_before_sync();
@@ -246,11 +269,7 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    // Cell of (unit u, sample n) items; lanes of a warp take the 32 units of
-    // one sample (n is warp-uniform).  The results are kept in registers and
-    // written to global memory after the cluster barrier's arrive.
-    constexpr int kItems = 8;                  // items per thread (plan: 32*Bt <= 8*256)
-    float ig[kItems], igg[kItems], ihh[kItems], ih[kItems], hop[kItems];
+    float hop[kItems];
     // pass 1: cell math of all items
 #pragma unroll
     for (int q = 0; q < kItems; ++q) {
@@ -261,10 +280,9 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
       const float af = ex[(0 * kUnits + u) * ex_ld + n] + bs[u];
       const float ag = ex[(1 * kUnits + u) * ex_ld + n] + bs[kUnits + u];
       const float ah = ex[(2 * kUnits + u) * ex_ld + n] + bs[2 * kUnits + u];
-      const float g = tanhf(ag);
-      const float hh = tanhf(ah);
-      const float gate = 1.f / (1.f + expf(af * dts[n]));
-      const float h = gate * g + (1.f - gate) * hh;
+      const CellAct ca = cell_act(af, ag, ah, dts[n]);
+      const float gate = ca.gate, g = ca.g, hh = ca.hh;
+      const float h = fmaf(gate, g - hh, hh);
       ig[q] = gate; igg[q] = g; ihh[q] = hh; ih[q] = h;
       if (bb < B) {
         if constexpr (sizeof(ET) == 2) hop[q] = round_bf16(h);
@@ -328,23 +346,10 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
     tc::fence_before_sync();
     cluster_arrive_release();
-#pragma unroll
-    for (int q = 0; q < kItems; ++q) {
-      const int e = tid + q * kThreads;
-      if (e >= kUnits * Bt) break;
-      const int u = e & 31, n = e >> 5, bb = b0 + n;
-      if (bb < B) {
-        const int unit = r * kUnits + u;
-        const long long row = (long long)bb * K + k;
-        act[row * H3 + unit] = ig[q];
-        act[row * H3 + H + unit] = igg[q];
-        act[row * H3 + 2 * H + unit] = ihh[q];
-        stf(h_seq + row * H + unit, ih[q]);
-      }
-    }
     cluster_wait_acquire();
     tc::fence_after_sync();
   }
+  store_results(K - 1);
   if (err && tid == 0) atomicExch(&g_tc_kloop_error, 1);
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
