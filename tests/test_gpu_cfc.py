@@ -85,15 +85,17 @@ def test_streamed_forward_cluster_multicast(w, cluster, monkeypatch):
 
 
 @pytest.mark.parametrize("variant", ["tma_multicast", "tma_single", "staged"])
-def test_large_weight_gradient_contractions(variant, monkeypatch):
+@pytest.mark.parametrize("base", [wl.LARGE.with_(B=512), wl.MID.with_(B=96, K=32)],
+                         ids=lambda w: w.name.split("_")[0])
+def test_weight_gradient_contractions(base, variant, monkeypatch):
     """The TMA-fed weight-gradient contraction (z blocks multicast across the
     cluster of M tiles, or one CTA per tile) and the register-staged one, on
-    the large shape with fewer samples."""
+    the large (bf16) and mid (TF32) shapes with fewer samples."""
     if variant == "staged":
         monkeypatch.setenv("CFC_WGRAD_STAGED", "1")
     if variant == "tma_multicast":
         monkeypatch.setenv("CFC_WGRAD_MULTICAST", "1")
-    w = wl.LARGE.with_(B=512)
+    w = base
     inp = wl.make_inputs(w, seed=21)
     r, got = run(w, inp)
     ref = oracle_ref(w, inp, per_sample=False, y=inp["y"])
@@ -146,6 +148,12 @@ EDGE = [
                 grad_path=wl.GRAD_GEMM),
     wl.Workload("edge_tma_B40_K8", B=40, K=8, n_in=64, n_hid=128, math=wl.MATH_BF16,
                 grad_path=wl.GRAD_GEMM, dt_per_sample=True),
+    # the same in TF32 (32-row chunks, rounding warps): whole samples per chunk
+    # with a ragged 3H tile, and 32 steps of one sample per chunk
+    wl.Workload("edge_tma_tf32_B40_K8", B=40, K=8, n_in=32, n_hid=64, math=wl.MATH_TF32,
+                grad_path=wl.GRAD_GEMM, dt_per_sample=True),
+    wl.Workload("edge_tma_tf32_K64_H32", B=3, K=64, n_in=32, n_hid=32, math=wl.MATH_TF32,
+                grad_path=wl.GRAD_GEMM),
 ]
 
 
