@@ -44,7 +44,15 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxStages = 6;    // ring of streamed A tiles (runtime count: nst)
-constexpr uint32_t kTile = 128 * 128;      // bytes of one streamed A tile
+constexpr uint32_t kTile = 128 * 128;      // bytes of one A tile (128 rows x one 128-byte K atom)
+// A stage holds the tiles of two consecutive K atoms of one M tile (32 KB):
+// one full-barrier wait and one commit per 8 MMAs.
+constexpr uint32_t kStage = 2 * kTile;
+// Byte offset of the tile of K atom a, M tile m in the streamed sequence
+// (stage (a/2, m), in stage order a/2-major).
+__host__ __device__ __forceinline__ size_t tile_offset(int a, int m, int nM) {
+  return ((size_t)(a >> 1) * nM + m) * kStage + (size_t)(a & 1) * kTile;
+}
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr size_t kSmemMax = 227 * 1024;
 
@@ -98,7 +106,7 @@ __device__ __forceinline__ uint32_t kmajor_off(int row, int kk, int rows) {
 
 // W_rec^T tiles: tile (mt, a) holds rows j = 128*mt .. 128*mt+127 (units)
 // and K elements a*EPA .. a*EPA+EPA-1 (EPA = 128 bytes / element), at byte
-// offset ((a * nM) + mt) * kTile, swizzled exactly as in shared memory.
+// offset tile_offset(a, mt, nM), swizzled exactly as in shared memory.
 template <typename ET, int MODE>
 __global__ void k_prep_wt_tiles(const ET* __restrict__ W_rec, int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
   constexpr int EPA = 128 / sizeof(ET);
@@ -109,12 +117,12 @@ __global__ void k_prep_wt_tiles(const ET* __restrict__ W_rec, int H, int nM, int
     const int kl = (int)(e % EPA);
     const long long rest = e / EPA;
     const int i = (int)(rest % 128);
-    const long long t = rest / 128;            // tile index = a * nM + mt
+    const long long t = rest / 128;            // a * nM + mt
     const int mt = (int)(t % nM), a = (int)(t / nM);
     const int j = mt * 128 + i, kk = a * EPA + kl;
     float v = 0.f;
     if (j < H && kk < H3) v = ld_operand<MODE>(W_rec + (long long)kk * H + j);
-    st_elem<ET>(tiles + t * kTile + tc::sw128_offset(i, kl * sizeof(ET)), v);
+    st_elem<ET>(tiles + tile_offset(a, mt, nM) + tc::sw128_offset(i, kl * sizeof(ET)), v);
   }
 }
 
@@ -128,13 +136,14 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
   const int H3 = 3 * H;
   const int b0 = blockIdx.x * Bt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
-  const int T = nAk * nM;                       // streamed tiles per step
+  const int nP = (nAk + 1) / 2;                 // K-atom pairs
+  const int T = nP * nM;                        // streamed stages per step
   const long long total_tiles = (long long)K * T;
 
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stage = sm;                                   // nst x 16 KB
-  uint8_t* dAs = sm + (size_t)nst * kTile;               // nAk x [Bt rows][128 B]
+  uint8_t* stage = sm;                                   // nst x 32 KB
+  uint8_t* dAs = sm + (size_t)nst * kStage;              // nAk x [Bt rows][128 B]
   float* dts = reinterpret_cast<float*>(dAs + (size_t)nAk * Bt * 128);   // [Bt]
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
   __shared__ uint32_t tmem_base;
@@ -176,8 +185,8 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
   auto issue_copy = [&]() {
     // stage reuse: the MMAs of the tile nst copies back must be complete
     if (pwrap > 0 && !tc::mbar_wait(&empty[pst], (pwrap - 1) & 1u, kMaxPolls)) err = 1;
-    expect_tx(&full[pst], kTile);
-    bulk_g2s(stage + pst * kTile, wtiles + (size_t)pt * kTile, kTile, &full[pst]);
+    expect_tx(&full[pst], kStage);
+    bulk_g2s(stage + (size_t)pst * kStage, wtiles + (size_t)pt * kStage, kStage, &full[pst]);
     if (++pt == T) pt = 0;
     if (++pst == nst) {
       pst = 0;
@@ -263,17 +272,23 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
     if (tid == 0) {
       const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
       const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(dAs));
-      for (int a = 0; a < nAk; ++a) {
-        const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+      for (int pa = 0; pa < nP; ++pa) {
         uint32_t d = tmem;
         for (int mt = 0; mt < nM; ++mt, d += (uint32_t)Bt) {
           if (!tc::mbar_wait(&full[cst], cwrap & 1u, kMaxPolls)) err = 1;
           tc::fence_after_sync();
-          const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kTile);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-            else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+          for (int sub = 0; sub < 2; ++sub) {
+            const int a = 2 * pa + sub;
+            if (a < nAk) {
+              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
+              const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+                else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+              }
+            }
           }
           tc::mma_commit(&empty[cst]);
           if (++cst == nst) {
@@ -301,7 +316,7 @@ k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, 
 
 // W_cat tiles of the forward: tile (a, m), m = 3*ub + c, holds the rows of
 // head c for units 128*ub + i (i = 0..127) and K elements a*EPA .. +EPA-1 of z,
-// at byte offset (a * nM + m) * kTile, swizzled as in shared memory.
+// at byte offset tile_offset(a, m, nM), swizzled as in shared memory.
 template <typename ET, int MODE>
 __global__ void k_prep_w_tiles_fwd(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, int n_in,
                                    int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
@@ -322,7 +337,7 @@ __global__ void k_prep_w_tiles_fwd(const ET* __restrict__ W_in, const ET* __rest
       const long long row = (long long)c * H + unit;
       v = (kk < n_in) ? ld_operand<MODE>(W_in + row * n_in + kk) : ld_operand<MODE>(W_rec + row * H + (kk - n_in));
     }
-    st_elem<ET>(tiles + t * kTile + tc::sw128_offset(i, kl * sizeof(ET)), v);
+    st_elem<ET>(tiles + tile_offset(a, m, nM) + tc::sw128_offset(i, kl * sizeof(ET)), v);
   }
 }
 
@@ -363,14 +378,15 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
   const int Kpad = nAk * EPA;
   const int b0 = blockIdx.x * Bt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
-  const int T = nAk * nM;
+  const int nP = (nAk + 1) / 2;                 // K-atom pairs
+  const int T = nP * nM;                        // streamed stages per step
   const long long total_tiles = (long long)K * T;
   const bool vec = (n_in % EPU == 0) && (H % EPU == 0);
 
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stage = sm;                                       // nst x 16 KB
-  uint8_t* Zs = sm + (size_t)nst * kTile;                    // nAk x [Bt rows][128 B]
+  uint8_t* stage = sm;                                       // nst x 32 KB
+  uint8_t* Zs = sm + (size_t)nst * kStage;                   // nAk x [Bt rows][128 B]
   float* bs = reinterpret_cast<float*>(Zs + (size_t)nAk * Bt * 128);   // [3H]
   float* dts = bs + H3;                                      // [Bt]
   __shared__ uint64_t full[kFwdMaxStages], empty[kFwdMaxStages], done;
@@ -422,10 +438,10 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
         break;
       }
       if (lane == 0) {
-        expect_tx(&full[st], kTile);
-        const uint8_t* src = wtiles + (size_t)t * kTile;
-        if (C == 1) bulk_g2s(stage + st * kTile, src, kTile, &full[st]);
-        else if ((uint32_t)issuer == rank) bulk_g2s_mc(stage + st * kTile, src, kTile, &full[st], cmask);
+        expect_tx(&full[st], kStage);
+        const uint8_t* src = wtiles + (size_t)t * kStage;
+        if (C == 1) bulk_g2s(stage + (size_t)st * kStage, src, kStage, &full[st]);
+        else if ((uint32_t)issuer == rank) bulk_g2s_mc(stage + (size_t)st * kStage, src, kStage, &full[st], cmask);
       }
       __syncwarp();
       if (++t == T) t = 0;
@@ -450,8 +466,7 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
       if (k > 0) step_sync();             // Z_k written by the epilogue of step k-1
       tc::fence_after_sync();
       if (ok && __shfl_sync(0xffffffffu, *err_flag, 0) == 0) {
-        for (int a = 0; a < nAk && ok; ++a) {
-          const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+        for (int pa = 0; pa < nP && ok; ++pa) {
           uint32_t d = tmem;
           for (int m = 0; m < nM; ++m, d += (uint32_t)Bt) {
             if (!mbar_wait_warp(&full[cst], cwrap & 1u, kMaxPolls)) {
@@ -461,11 +476,18 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
             }
             tc::fence_after_sync();
             if (lane == 0) {
-              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kTile);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-                else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+              for (int sub = 0; sub < 2; ++sub) {
+                const int a = 2 * pa + sub;
+                if (a < nAk) {
+                  const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
+                  const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+                    else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+                  }
+                }
               }
               if (C == 1) tc::mma_commit(&empty[cst]);
               else mma_commit_mc(&empty[cst], cmask);
@@ -602,12 +624,12 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
   auto fixed_for = [&](int bt) { return 1024 + (size_t)nAk * bt * 128 + (size_t)(3 * L.H + bt) * 4 + 256; };
   auto ok = [&](int bt) {
     const bool vec = (L.n_in % epu == 0) && (L.H % epu == 0);
-    return fixed_for(bt) + 4 * (size_t)kTile <= kSmemMax && (long long)nM * bt <= 512 &&
+    return fixed_for(bt) + 3 * (size_t)kStage <= kSmemMax && (long long)nM * bt <= 512 &&
            (!vec || (long long)bt * (L.n_in / epu) <= (long long)kXUnits * kFwdConsumers);
   };
   while (Bt > 16 && !ok(Bt)) Bt -= 16;
   if (!ok(Bt)) return false;
-  int nst = (int)std::min<size_t>(kFwdMaxStages, (kSmemMax - fixed_for(Bt)) / kTile);
+  int nst = (int)std::min<size_t>(kFwdMaxStages, (kSmemMax - fixed_for(Bt)) / kStage);
   p->Bt = Bt;
   p->nUB = nUB;
   p->nAk = nAk;
@@ -615,8 +637,10 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
   uint32_t cols = 32;
   while (cols < (uint32_t)(nM * Bt)) cols <<= 1;
   p->tmem_cols = cols;
-  p->smem = fixed_for(Bt) + (size_t)nst * kTile;
-  p->C = 4;
+  p->smem = fixed_for(Bt) + (size_t)nst * kStage;
+  // Tile multicast across a cluster (CFC_TC_CLUSTER = cluster size) measured
+  // no faster than one CTA per sample tile; off by default.
+  p->C = 1;
   if (const char* v = getenv("CFC_TC_CLUSTER")) p->C = std::max(1, std::min(8, atoi(v)));
   return true;
 }
@@ -673,10 +697,10 @@ bool plan_bwd(const Layout& L, BwdPlan* p) {
   int Bt = (int)(((long long)L.B + kNumSMs - 1) / kNumSMs);
   Bt = std::min(128, std::max(32, (Bt + 15) / 16 * 16));
   auto fixed_for = [&](int bt) { return 1024 + (size_t)nAk * bt * 128 + bt * 4 + 256; };
-  while (Bt > 16 && (fixed_for(Bt) + 4 * (size_t)kTile > kSmemMax || (long long)nM * Bt > 512)) Bt -= 16;
-  if (fixed_for(Bt) + 4 * (size_t)kTile > kSmemMax || (long long)nM * Bt > 512) return false;
+  while (Bt > 16 && (fixed_for(Bt) + 3 * (size_t)kStage > kSmemMax || (long long)nM * Bt > 512)) Bt -= 16;
+  if (fixed_for(Bt) + 3 * (size_t)kStage > kSmemMax || (long long)nM * Bt > 512) return false;
   // as many stages as fit (the stream is latency-bound: more tiles in flight)
-  const int nst = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed_for(Bt)) / kTile);
+  const int nst = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed_for(Bt)) / kStage);
   p->Bt = Bt;
   p->nM = nM;
   p->nAk = nAk;
@@ -684,7 +708,7 @@ bool plan_bwd(const Layout& L, BwdPlan* p) {
   uint32_t cols = 32;
   while (cols < (uint32_t)(nM * Bt)) cols <<= 1;
   p->tmem_cols = cols;
-  p->smem = fixed_for(Bt) + (size_t)nst * kTile;
+  p->smem = fixed_for(Bt) + (size_t)nst * kStage;
   return true;
 }
 
@@ -721,8 +745,8 @@ size_t tc_bwd_tiles_bytes(int n_in, int n_hid, int math) {
   if (math == CFC_MATH_FP32) return 0;
   const int es = (math == CFC_MATH_TF32) ? 4 : 2;
   // backward: W_rec^T tiles; forward: W_cat tiles (the two are never live at once)
-  const size_t bwd = (size_t)((n_hid + 127) / 128) * ((3 * n_hid * es + 127) / 128) * kTile;
-  const size_t fwd = (size_t)(3 * ((n_hid + 127) / 128)) * (((n_in + n_hid) * es + 127) / 128) * kTile;
+  const size_t bwd = (size_t)((n_hid + 127) / 128) * (((3 * n_hid * es + 127) / 128 + 1) / 2) * kStage;
+  const size_t fwd = (size_t)(3 * ((n_hid + 127) / 128)) * ((((n_in + n_hid) * es + 127) / 128 + 1) / 2) * kStage;
   return std::max(bwd, fwd);
 }
 
