@@ -221,15 +221,46 @@ __global__ void __launch_bounds__(256)
 k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict__ h0,
         const T* __restrict__ h_seq, int K, int n_in, int H, long long R,
         long long rows_per_split, float* __restrict__ out) {
-  __shared__ float sA[kTR][kTM + 4];
-  __shared__ float sZ[kTR][kTN + 4];
+  // Thread (ty, tx) owns outputs m = m0 + 4*ty + p, j = j0 + 4*tx + q (p, q < 4):
+  // per row one 128-bit shared load of dA and one of z feed 16 FMAs.  The
+  // next row chunk is loaded into registers while the current one is used.
+  __shared__ __align__(16) float sA[2][kTR][kTM];
+  __shared__ __align__(16) float sZ[2][kTR][kTN];
   const int H3 = 3 * H, Zc = n_in + H, Zb = Zc + 1;
   const long long N = (long long)H3 * Zb;
   const int m0 = blockIdx.x * kTM, j0 = blockIdx.y * kTN;
   const long long s = blockIdx.z;
-  const long long r_begin = s * rows_per_split;
-  const long long r_end = min(R, r_begin + rows_per_split);
+  const int r_begin = (int)(s * rows_per_split);            // B*K < 2^31
+  const int r_end = (int)min(R, (long long)r_begin + rows_per_split);
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  constexpr int kPer = (kTR * kTM) / 256;                   // elements per thread per chunk
+
+  float ra[kPer], rz[kPer];
+  auto load_chunk = [&](int r) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * 256;
+      const int rr = e / kTM, cc = e - rr * kTM;
+      const int row = r + rr;
+      const int m = m0 + cc, j = j0 + cc;
+      float a = 0.f, z = 0.f;
+      if (row < r_end) {
+        if (m < H3) a = ldf(dA + (long long)row * H3 + m);
+        if (j < n_in) {
+          z = ld_operand<MODE>(x + (long long)row * n_in + j);
+        } else if (j < Zc) {
+          const int kk = row % K;
+          const int u = j - n_in;
+          z = (kk == 0) ? ld_operand<MODE>(h0 + (long long)(row / K) * H + u)
+                        : ld_operand<MODE>(h_seq + (long long)(row - 1) * H + u);
+        } else if (j == Zc) {
+          z = 1.f;
+        }
+      }
+      ra[q] = a;
+      rz[q] = z;
+    }
+  };
 
   float acc[4][4];
 #pragma unroll
@@ -237,56 +268,41 @@ k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict_
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
 
-  for (long long r = r_begin; r < r_end; r += kTR) {
+  if (r_begin < r_end) load_chunk(r_begin);
+  int buf = 0;
+  for (int r = r_begin; r < r_end; r += kTR, buf ^= 1) {
 #pragma unroll
-    for (int q = 0; q < (kTR * kTM) / 256; ++q) {
+    for (int q = 0; q < kPer; ++q) {
       const int e = tid + q * 256;
       const int rr = e / kTM, cc = e - rr * kTM;
-      const long long row = r + rr;
-      const int m = m0 + cc, j = j0 + cc;
-      float a = 0.f, z = 0.f;
-      if (row < r_end) {
-        if (m < H3) a = ldf(dA + row * H3 + m);
-        if (j < n_in) {
-          z = ld_operand<MODE>(x + row * n_in + j);
-        } else if (j < Zc) {
-          const long long bidx = row / K;
-          const int kk = (int)(row - bidx * K);
-          const int u = j - n_in;
-          z = (kk == 0) ? ld_operand<MODE>(h0 + bidx * H + u)
-                        : ld_operand<MODE>(h_seq + (row - 1) * H + u);
-        } else if (j == Zc) {
-          z = 1.f;
-        }
-      }
-      sA[rr][cc] = a;
-      sZ[rr][cc] = z;
+      sA[buf][rr][cc] = ra[q];
+      sZ[buf][rr][cc] = rz[q];
     }
     __syncthreads();
+    if (r + kTR < r_end) load_chunk(r + kTR);
 #pragma unroll
     for (int rr = 0; rr < kTR; ++rr) {
-      float av[4], zv[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) av[p] = sA[rr][ty + 16 * p];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) zv[q] = sZ[rr][tx + 16 * q];
+      const float4 av = *reinterpret_cast<const float4*>(&sA[buf][rr][4 * ty]);
+      const float4 zv = *reinterpret_cast<const float4*>(&sZ[buf][rr][4 * tx]);
+      const float a4[4] = {av.x, av.y, av.z, av.w}, z4[4] = {zv.x, zv.y, zv.z, zv.w};
 #pragma unroll
       for (int p = 0; p < 4; ++p)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(av[p], zv[q], acc[p][q]);
+        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a4[p], z4[q], acc[p][q]);
     }
-    __syncthreads();
+    // The buffer written next iteration is the other one; the barrier at the
+    // top of the iteration after that orders its reuse.
   }
   float* o = out + s * N;
   const long long off_rec = (long long)H3 * n_in;
   const long long off_b = (long long)H3 * Zc;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    const int m = m0 + ty + 16 * p;
+    const int m = m0 + 4 * ty + p;
     if (m >= H3) continue;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int j = j0 + tx + 16 * q;
+      const int j = j0 + 4 * tx + q;
       if (j < n_in) o[(long long)m * n_in + j] = acc[p][q];
       else if (j < Zc) o[off_rec + (long long)m * H + (j - n_in)] = acc[p][q];
       else if (j == Zc) o[off_b + m] = acc[p][q];
