@@ -804,6 +804,390 @@ cudaError_t launch_wgrad_tma(const Layout& L, const TmaWgradPlan& p, const CfcAr
 }
 
 // ---------------------------------------------------------------------------
+// TMA-fed contraction, TF32 mode (GEMM path).
+//
+// kind::tf32 MMAs read K-major operands only, while dA, x and h_seq keep the
+// contraction index r outermost.  The operands arrive as in the bf16 kernel --
+// 3-D TMA boxes of 32 rows x 128 bytes (32 fp32 columns), 128-byte swizzled --
+// in a raw stage, and transposer warps turn each block of 4 rows x 4 columns
+// (one 16-byte unit in each of 4 rows) into 4 units of the K-major tile (4
+// columns x 4 rows), rounding x and h to TF32 on the way (dA is stored
+// rounded).  A chunk is 32 rows: one 128-byte K atom, 4 MMAs with K = 8.
+//
+// A thread's block is (box, kq, mq): raw rows 4kq..4kq+3, unit mq.  16-byte
+// shared accesses are served per quarter warp, so the 8 lanes l of a quarter
+// q take mq = l ^ 2(q/2), kq = l/2 + 4(q%2): their raw reads (position
+// mq ^ (row % 8)) and their K-major writes (position kq ^ (row % 8)) each hit 8
+// distinct 16-byte positions, and the 8 quarters of a box cover its 64
+// blocks once.
+//
+// Warps: 0 TMA producer, 1 MMA issue, 2 h0 patch (the rows with k = 0, as in
+// the bf16 kernel), 3..9 transposers.  Raw stages go full (TMA) -> ready
+// (patched) -> rfree (transposers done); K-major stages kfull (transposers
+// done, after their proxy fences) -> kempty (MMA completion).  Block = (M
+// tile of 128 rows of 3H, split s); accumulator D[128 x Ntot] in TMEM.
+// ---------------------------------------------------------------------------
+constexpr int kT32Rows = 32;                     // rows (MMA K) per chunk
+constexpr int kT32Box = kT32Rows * 128;          // one 32-column box of a chunk
+constexpr int kT32Threads = 320;
+constexpr int kT32WarpProducer = 0, kT32WarpMma = 1, kT32WarpPatch = 2, kT32FirstTr = 3;
+constexpr int kT32Tr = kT32Threads / 32 - kT32FirstTr;   // transposer warps
+constexpr int kT32MaxRaw = 4, kT32KStages = 2;
+constexpr uint32_t kT32TmemCols = 256;
+
+struct Tf32WgradPlan {
+  int nx = 0, nh = 0;    // 32-column boxes of x and of h
+  int Ntot = 0;          // accumulator columns: Zc + 1 rounded up to 16
+  int nMt = 0, S = 0, chunks = 0, raw_stages = 0;
+  int kb = 0, nb = 0;    // chunk = kb steps x nb samples
+  size_t raw_bytes = 0, k_bytes = 0, smem = 0;
+};
+
+bool plan_tf32_wgrad(int B, int K, int n_in, int H, int math, int grad_path, Tf32WgradPlan* p) {
+  if (math != CFC_MATH_TF32 || grad_path != CFC_GRAD_GEMM) return false;
+  if (n_in % 32 || H % 32) return false;
+  int kb, nb;
+  if (K <= kT32Rows && kT32Rows % K == 0) {
+    kb = K;
+    nb = kT32Rows / K;
+    if (B % nb) return false;
+  } else if (K % kT32Rows == 0) {
+    kb = kT32Rows;
+    nb = 1;
+  } else {
+    return false;
+  }
+  const int Zc = n_in + H;
+  const int Ntot = (Zc + 1 + 15) / 16 * 16;
+  if (Ntot > 256) return false;   // one MMA of N <= 256
+  p->nx = n_in / 32;
+  p->nh = H / 32;
+  p->Ntot = Ntot;
+  p->nMt = (3 * H + 127) / 128;
+  p->chunks = (int)((long long)B * K / kT32Rows);
+  p->kb = kb;
+  p->nb = nb;
+  p->raw_bytes = (size_t)(4 + p->nx + p->nh) * kT32Box;
+  p->k_bytes = 128 * 128 + (size_t)Ntot * 128;
+  const size_t fixed = 1024 + kT32KStages * p->k_bytes;
+  if (fixed + 2 * p->raw_bytes > 227 * 1024) return false;
+  p->raw_stages = (int)std::min<size_t>(kT32MaxRaw, (227 * 1024 - fixed) / p->raw_bytes);
+  p->smem = fixed + (size_t)p->raw_stages * p->raw_bytes;
+  p->S = std::max(1, std::min(p->chunks, kNumSMs / p->nMt));
+  return true;
+}
+
+__device__ __forceinline__ void chunk_origin_rows(int c, int K, int nb, int rows, int* b0, int* k0) {
+  if (nb > 1) {
+    *b0 = c * nb;
+    *k0 = 0;
+  } else {
+    const int per = K / rows;
+    *b0 = c / per;
+    *k0 = (c - *b0 * per) * rows;
+  }
+}
+
+__device__ __forceinline__ uint32_t tf32_bits(uint32_t u) { return (u + 0x1000u) & 0xFFFFE000u; }
+
+__global__ void __launch_bounds__(kT32Threads, 1)
+k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ CUtensorMap map_x,
+                 const __grid_constant__ CUtensorMap map_h, const float* __restrict__ h0, int K, int n_in,
+                 int H, int chunks, int S, int raw_stages, int kb, int nb, int Ntot, float* __restrict__ out) {
+  const int mt = blockIdx.x, s = blockIdx.y;
+  const int c_begin = (int)((long long)chunks * s / S), c_end = (int)((long long)chunks * (s + 1) / S);
+  const int nx = n_in / 32, nh = H / 32, nbox = 4 + nx + nh;
+  const int H3 = 3 * H, Zc = n_in + H;
+  const uint32_t raw_bytes = (uint32_t)nbox * kT32Box;
+  const uint32_t k_bytes = 128u * 128u + (uint32_t)Ntot * 128u;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = sm;                                        // [raw_stages][nbox][32 rows][128 B]
+  uint8_t* kst = sm + (size_t)raw_stages * raw_bytes;       // [2][A 128 rows | B Ntot rows][128 B]
+  __shared__ uint64_t full[kT32MaxRaw], ready[kT32MaxRaw], rfree[kT32MaxRaw];
+  __shared__ uint64_t kfull[kT32KStages], kempty[kT32KStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+  volatile int* errp = &err;
+
+  if (tid == 0) {
+    for (int i = 0; i < raw_stages; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&ready[i], 1);
+      tc::mbar_init(&rfree[i], kT32Tr);
+    }
+    for (int i = 0; i < kT32KStages; ++i) {
+      tc::mbar_init(&kfull[i], kT32Tr);
+      tc::mbar_init(&kempty[i], 1);
+    }
+    tc::mbar_init(&done, 1);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kT32TmemCols);
+  // Rows Zc .. Ntot-1 of every K-major B tile never change: row Zc is the ones
+  // column of the bias gradient, the rest zero padding.
+  for (int ks = 0; ks < kT32KStages; ++ks) {
+    uint8_t* bt = kst + (size_t)ks * k_bytes + 128 * 128;
+    for (int e = tid; e < (Ntot - Zc) * 8; e += kT32Threads) {
+      const int row = Zc + (e >> 3), q = e & 7;
+      const uint32_t one = (row == Zc) ? 0x3F800000u : 0u;
+      *reinterpret_cast<uint4*>(bt + row * 128 + ((q ^ (row & 7)) << 4)) = make_uint4(one, one, one, one);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == kT32WarpProducer) {
+    int st = 0;
+    uint32_t wrap = 0;
+    for (int c = c_begin; c < c_end; ++c) {
+      if (__shfl_sync(0xffffffffu, *errp, 0)) break;
+      if (wrap > 0 && !wait_warp(&rfree[st], (wrap - 1) & 1u)) {
+        if (lane == 0) *errp = 1;
+        break;
+      }
+      if (lane == 0) {
+        int b0, k0;
+        chunk_origin_rows(c, K, nb, kT32Rows, &b0, &k0);
+        uint8_t* base = raw + (size_t)st * raw_bytes;
+        expect_tx_bytes(&full[st], raw_bytes);
+        for (int i = 0; i < 4; ++i) tma_load_3d(base + i * kT32Box, &map_dA, mt * 128 + 32 * i, k0, b0, &full[st]);
+        for (int j = 0; j < nx; ++j) tma_load_3d(base + (4 + j) * kT32Box, &map_x, 32 * j, k0, b0, &full[st]);
+        for (int j = 0; j < nh; ++j)
+          tma_load_3d(base + (4 + nx + j) * kT32Box, &map_h, 32 * j, k0 - 1, b0, &full[st]);
+      }
+      __syncwarp();
+      if (++st == raw_stages) {
+        st = 0;
+        ++wrap;
+      }
+    }
+  } else if (warp == kT32WarpPatch) {
+    // Rows n*kb of a chunk that starts at step 0 hold k = 0 of sample b0 + n:
+    // h0[b0 + n] replaces the zero-filled h rows.  The next chunk's h0 units
+    // are loaded while this chunk is patched (kPatchRegs per lane; any rest
+    // is loaded when needed).
+    constexpr int kPatchRegs = 4;
+    const int items = nb * nh * 8;
+    uint4 pre[kPatchRegs];
+    auto prefetch = [&](int c) {
+      int b0, k0;
+      chunk_origin_rows(c, K, nb, kT32Rows, &b0, &k0);
+#pragma unroll
+      for (int i = 0; i < kPatchRegs; ++i) {
+        const int e = lane + 32 * i;
+        const int q = e & 7, j = (e >> 3) % nh, n = (e >> 3) / nh;
+        pre[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < c_end && k0 == 0 && e < items)
+          asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(pre[i].x), "=r"(pre[i].y), "=r"(pre[i].z), "=r"(pre[i].w)
+                       : "l"(h0 + (long long)(b0 + n) * H + 32 * j + 4 * q));
+      }
+    };
+    prefetch(c_begin);
+    int st = 0;
+    uint32_t wrap = 0;
+    for (int c = c_begin; c < c_end; ++c) {
+      int b0, k0;
+      chunk_origin_rows(c, K, nb, kT32Rows, &b0, &k0);
+      if (!wait_warp(&full[st], wrap & 1u)) {
+        if (lane == 0) *errp = 1;
+        break;
+      }
+      if (k0 == 0) {
+        uint8_t* hb = raw + (size_t)st * raw_bytes + (size_t)(4 + nx) * kT32Box;
+        auto put = [&](int e, const uint4& v) {
+          const int q = e & 7, j = (e >> 3) % nh, n = (e >> 3) / nh;
+          const int r = n * kb;
+          *reinterpret_cast<uint4*>(hb + (size_t)j * kT32Box + r * 128 + ((q ^ (r & 7)) << 4)) = v;
+        };
+#pragma unroll
+        for (int i = 0; i < kPatchRegs; ++i)
+          if (lane + 32 * i < items) put(lane + 32 * i, pre[i]);
+        for (int e = lane + 32 * kPatchRegs; e < items; e += 32) {
+          const int q = e & 7, j = (e >> 3) % nh, n = (e >> 3) / nh;
+          put(e, *reinterpret_cast<const uint4*>(h0 + (long long)(b0 + n) * H + 32 * j + 4 * q));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[st]);
+      prefetch(c + 1);
+      if (++st == raw_stages) {
+        st = 0;
+        ++wrap;
+      }
+    }
+  } else if (warp >= kT32FirstTr) {
+    const int tw = warp - kT32FirstTr;
+    const int ntask = nbox * 64;
+    int rs = 0, ks = 0;
+    uint32_t rwrap = 0, kwrap = 0;
+    for (int c = c_begin; c < c_end; ++c) {
+      if (!wait_warp(&ready[rs], rwrap & 1u) || (kwrap > 0 && !wait_warp(&kempty[ks], (kwrap - 1) & 1u))) {
+        if (lane == 0) *errp = 1;
+        break;
+      }
+      const uint8_t* rb = raw + (size_t)rs * raw_bytes;
+      uint8_t* ka = kst + (size_t)ks * k_bytes;
+      uint8_t* kbt = ka + 128 * 128;
+      for (int task = tw * 32 + lane; task < ntask; task += kT32Tr * 32) {
+        const int box = task >> 6, q4 = (task >> 3) & 7, l = task & 7;
+        const int mq = l ^ (2 * (q4 >> 1)), kq = (l >> 1) + 4 * (q4 & 1);
+        const uint8_t* src = rb + (size_t)box * kT32Box;
+        uint32_t w[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * kq + i;
+          const uint4 u = *reinterpret_cast<const uint4*>(src + r * 128 + ((mq ^ (r & 7)) << 4));
+          w[i][0] = u.x; w[i][1] = u.y; w[i][2] = u.z; w[i][3] = u.w;
+        }
+        uint8_t* dst;
+        int row0;
+        const bool rnd = box >= 4;
+        if (box < 4) {
+          dst = ka;
+          row0 = 32 * box + 4 * mq;
+        } else if (box < 4 + nx) {
+          dst = kbt;
+          row0 = 32 * (box - 4) + 4 * mq;
+        } else {
+          dst = kbt;
+          row0 = n_in + 32 * (box - 4 - nx) + 4 * mq;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int row = row0 + j;
+          uint4 v = make_uint4(w[0][j], w[1][j], w[2][j], w[3][j]);
+          if (rnd) v = make_uint4(tf32_bits(v.x), tf32_bits(v.y), tf32_bits(v.z), tf32_bits(v.w));
+          *reinterpret_cast<uint4*>(dst + row * 128 + ((kq ^ (row & 7)) << 4)) = v;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&rfree[rs]);
+        mbar_arrive(&kfull[ks]);
+      }
+      if (++rs == raw_stages) {
+        rs = 0;
+        ++rwrap;
+      }
+      if (++ks == kT32KStages) {
+        ks = 0;
+        ++kwrap;
+      }
+    }
+  } else if (warp == kT32WarpMma) {
+    const uint32_t id = tc::idesc(128, (uint32_t)Ntot, tc::kFmtTF32);
+    const uint64_t a_desc = tc::sdesc_k_sw128(tc::smem_u32(kst));
+    const uint64_t b_desc = tc::sdesc_k_sw128(tc::smem_u32(kst + 128 * 128));
+    int ks = 0;
+    uint32_t wrap = 0;
+    bool ok = true;
+    for (int c = c_begin; c < c_end; ++c) {
+      if (!wait_warp(&kfull[ks], wrap & 1u)) {
+        if (lane == 0) *errp = 1;
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t so = (uint32_t)ks * k_bytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (c > c_begin || kk > 0) ? 1u : 0u;
+          tc::mma_tf32(tmem, tc::sdesc_advance(a_desc, so + 32 * kk), tc::sdesc_advance(b_desc, so + 32 * kk), id,
+                       acc);
+        }
+        tc::mma_commit(&kempty[ks]);
+      }
+      __syncwarp();
+      if (++ks == kT32KStages) {
+        ks = 0;
+        ++wrap;
+      }
+    }
+    if (ok && c_end > c_begin && lane == 0) tc::mma_commit(&done);
+    __syncwarp();
+  }
+
+  // ---- epilogue: D[m][j] -> packed partial row of split s (warps 0..7)
+  if (tid == 0 && c_end > c_begin && *errp == 0 && !tc::mbar_wait(&done, 0, kMaxPolls)) *errp = 1;
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool have = (c_end > c_begin) && *errp == 0;
+  if (warp < 8) {
+    float* o = out + (long long)s * (3ll * (Zc + 1) * H);
+    const long long off_rec = (long long)H3 * n_in, off_b = (long long)H3 * Zc;
+    const int quad = warp & 3, half = warp >> 2;
+    const int m = mt * 128 + quad * 32 + lane;
+    const int ng = Ntot / 16, gh = (ng + 1) / 2;
+    for (int g = half * gh; g < ng && g < (half + 1) * gh; ++g) {
+      float v[16];
+      if (have) {
+        tc::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(g * 16), v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+      if (m < H3) {
+        const int j0 = g * 16;
+        float* dst = nullptr;
+        if (j0 + 16 <= n_in) dst = o + (long long)m * n_in + j0;
+        else if (j0 >= n_in && j0 + 16 <= Zc) dst = o + off_rec + (long long)m * H + (j0 - n_in);
+        if (dst) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else if (j0 == Zc) {
+          o[off_b + m] = v[0];
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*errp) atomicExch(&g_cfc_device_error, 1);
+  if (warp == 0) tc::tmem_dealloc(tmem, kT32TmemCols);
+}
+
+// 3-D fp32 map (columns, K, B) of a dense [B][K][cols] array; box 32 x kb x nb.
+bool encode_bkc_f32(CUtensorMap* m, const void* base, int cols, int K, int B, int kb, int nb) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)K, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * 4 * K};
+  const cuuint32_t box[3] = {32u, (cuuint32_t)kb, (cuuint32_t)nb};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_wgrad_tma_tf32(const Layout& L, const Tf32WgradPlan& p, const CfcArgs& a, float* out,
+                                  cudaStream_t s) {
+  CUtensorMap mdA, mx, mh;
+  if (!encode_bkc_f32(&mdA, a.ws + L.off_dA, L.H3, L.K, L.B, p.kb, p.nb) ||
+      !encode_bkc_f32(&mx, a.x, L.n_in, L.K, L.B, p.kb, p.nb) ||
+      !encode_bkc_f32(&mh, a.h_seq, L.H, L.K, L.B, p.kb, p.nb))
+    return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(k_wgrad_tma_tf32, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  TraceScope trace("wgrad_tma_tf32", s);
+  k_wgrad_tma_tf32<<<dim3((unsigned)p.nMt, (unsigned)p.S, 1), kT32Threads, p.smem, s>>>(
+      mdA, mx, mh, static_cast<const float*>(a.h0), L.K, L.n_in, L.H, p.chunks, p.S, p.raw_stages, p.kb, p.nb,
+      p.Ntot, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // grad_x of the tensor-core backward kernels as one GEMM after the K loop:
 //
 //   grad_x[r][i] = sum_m dA[r][m] * W_in[m][i]      (r over B*K rows, m over 3H)
@@ -1047,14 +1431,22 @@ int tc_wgrad_blocks(int n_in, int n_hid) {
 int tma_wgrad_splits(int B, int K, int n_in, int n_hid, int math, int grad_path) {
   if (getenv("CFC_WGRAD_STAGED")) return 0;   // force the register-staged contraction
   TmaWgradPlan p;
-  return plan_tma_wgrad(B, K, n_in, n_hid, math, grad_path, &p) ? p.S : 0;
+  if (plan_tma_wgrad(B, K, n_in, n_hid, math, grad_path, &p)) return p.S;
+  Tf32WgradPlan q;
+  if (plan_tf32_wgrad(B, K, n_in, n_hid, math, grad_path, &q)) return q.S;
+  return 0;
 }
 
 cudaError_t launch_wgrad_tc(const Layout& L, const CfcArgs& a, float* out, cudaStream_t s) {
+  const int splits = tma_wgrad_splits(L.B, L.K, L.n_in, L.H, L.math, L.grad_path);
   TmaWgradPlan p;
-  if (tma_wgrad_splits(L.B, L.K, L.n_in, L.H, L.math, L.grad_path) == L.n_split &&
-      plan_tma_wgrad(L.B, L.K, L.n_in, L.H, L.math, L.grad_path, &p)) {
+  if (splits == L.n_split && plan_tma_wgrad(L.B, L.K, L.n_in, L.H, L.math, L.grad_path, &p)) {
     cudaError_t e = launch_wgrad_tma(L, p, a, out, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  Tf32WgradPlan q;
+  if (splits == L.n_split && plan_tf32_wgrad(L.B, L.K, L.n_in, L.H, L.math, L.grad_path, &q)) {
+    cudaError_t e = launch_wgrad_tma_tf32(L, q, a, out, s);
     if (e != cudaErrorNotSupported) return e;
   }
   if (L.math == CFC_MATH_TF32) return launch_mode<float, CFC_MATH_TF32>(L, a, out, s);

@@ -49,7 +49,8 @@ def test_standalone_configs_bit_exact(B, N):
     np.testing.assert_array_equal(bits(got), bits(oracle.reduce_axis0(a)))
 
 
-@pytest.mark.parametrize("B, N", [(1, 5), (2, 3), (7, 1), (31, 129), (255, 130), (257, 131),
+@pytest.mark.parametrize("B, N", [(1, 5), (2, 3), (7, 1), (31, 129), (33, 38), (64, 33), (100, 515),
+                                  (128, 1027), (129, 5), (255, 130), (257, 131),
                                   (300, 4), (513, 1000), (1000, 4096), (2049, 77), (4100, 256)])
 def test_edge_shapes_bit_exact(B, N):
     a = wl.make_reduce_input(B, N, seed=7 * B + N)
