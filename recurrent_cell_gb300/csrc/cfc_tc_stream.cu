@@ -347,10 +347,31 @@ constexpr int kFwdProducerWarp = 8;        // W_cat tile stream
 constexpr int kFwdMmaWarp = 9;             // MMA issue
 constexpr int kFwdThreads = kFwdConsumers + 64;
 constexpr int kFwdMaxStages = 12;
+constexpr int kMaxSched = 256;             // streamed stages per step
 
-// Named barrier of the epilogue warps and the MMA warp (the producer warp runs ahead).
-__device__ __forceinline__ void step_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kFwdConsumers + 32) : "memory");
+// Order of the streamed stages of one step.  The units are split into two
+// halves U0 (unit blocks ub < nU0) and U1 (the rest), each with its own TMEM
+// accumulators, so that the epilogue of one half overlaps the MMAs of the
+// other:
+//   epilogue(k): [acc0] U0 cell, h(U0) -> Z  --zlo-->  [acc1] x_{k+1} -> Z
+//                --zx-->  U1 cell, h(U1) -> Z  --zhi-->
+//   MMAs(k+1):   U0 stages ordered by the signal their Z atoms need (zlo, zx,
+//                zhi), then U1 stages (which also need U1's accumulators
+//                read, i.e. zhi); the U1 stages that read atoms holding h(U0)
+//                come first, and acc0 is committed right after them, so the
+//                U0 epilogue never overwrites Z atoms that an MMA of the step
+//                still has to read.
+// lvl: 1, 2, 3 = the stage waits for zlo, zx, zhi of the previous step;
+// first: the stage is the first of its M tile in the step (the MMA
+// overwrites the accumulator).
+struct FwdSchedule {
+  int T = 0, nacc0 = 0, nU0 = 0;
+  uint8_t pa[kMaxSched], m[kMaxSched], lvl[kMaxSched], first[kMaxSched];
+};
+
+// Named barrier of the epilogue warps only.
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFwdConsumers) : "memory");
 }
 
 // Bounded mbarrier wait executed by a whole warp: lane 0's observation
@@ -362,13 +383,16 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, u
   }
   return false;
 }
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
 
 template <typename ET, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, const ET* __restrict__ h0,
-              const float* __restrict__ bias, const float* __restrict__ dt, int dt_stride, int B, int K,
-              int n_in, int H, int Bt, int nUB, int nAk, int nst, uint32_t tmem_cols, int C,
-              ET* __restrict__ h_seq, float* __restrict__ act) {
+k_cfc_fwd_tcb(const __grid_constant__ FwdSchedule sched, const uint8_t* __restrict__ wtiles,
+              const ET* __restrict__ x, const ET* __restrict__ h0, const float* __restrict__ bias,
+              const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H, int Bt, int nUB,
+              int nAk, int nst, uint32_t tmem_cols, int C, ET* __restrict__ h_seq, float* __restrict__ act) {
   constexpr int EPU = 16 / (int)sizeof(ET);
   constexpr int EPA = 128 / (int)sizeof(ET);
   const int Zc = n_in + H, H3 = 3 * H;
@@ -378,10 +402,10 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
   const int Kpad = nAk * EPA;
   const int b0 = blockIdx.x * Bt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
-  const int nP = (nAk + 1) / 2;                 // K-atom pairs
-  const int T = nP * nM;                        // streamed stages per step
+  const int T = sched.T;
   const long long total_tiles = (long long)K * T;
   const bool vec = (n_in % EPU == 0) && (H % EPU == 0);
+  const int nU0 = sched.nU0;
 
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
@@ -389,7 +413,8 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
   uint8_t* Zs = sm + (size_t)nst * kStage;                   // nAk x [Bt rows][128 B]
   float* bs = reinterpret_cast<float*>(Zs + (size_t)nAk * Bt * 128);   // [3H]
   float* dts = bs + H3;                                      // [Bt]
-  __shared__ uint64_t full[kFwdMaxStages], empty[kFwdMaxStages], done;
+  __shared__ uint64_t full[kFwdMaxStages], empty[kFwdMaxStages];
+  __shared__ uint64_t acc0, acc1, zsig[3];                   // zsig: zlo, zx, zhi
   __shared__ uint32_t tmem_base;
   __shared__ int err;
 
@@ -398,23 +423,13 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&empty[i], C);   // one MMA completion of every CTA of the cluster
     }
-    tc::mbar_init(&done, 1);
+    tc::mbar_init(&acc0, 1);
+    tc::mbar_init(&acc1, 1);
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&zsig[i], kFwdConsumers / 32);
     tc::mbar_init_fence();
     err = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
-  for (int e = tid; e < H3; e += kFwdThreads) bs[e] = bias[e];
-  for (int e = tid; e < Bt; e += kFwdThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
-  // z rows of step 0 = [x_0; h0], zero K padding.
-  for (int e = tid; e < Bt * Kpad; e += kFwdThreads) {
-    const int n = e / Kpad, kk = e - n * Kpad, bb = b0 + n;
-    float v = 0.f;
-    if (bb < B && kk < Zc)
-      v = (kk < n_in) ? ld_operand<MODE>(x + (long long)bb * K * n_in + kk)
-                      : ld_operand<MODE>(h0 + (long long)bb * H + (kk - n_in));
-    st_elem<ET>(Zs + kmajor_off<ET>(n, kk, Bt), v);
-  }
-  tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   if (C > 1) {   // every CTA's barriers are initialised before any remote arrival
@@ -424,11 +439,49 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
   volatile int* err_flag = &err;
+  if (warp != kFwdProducerWarp) {
+    // While the producer starts the tile stream: bias, dt and the z rows of
+    // step 0 = [x_0; h0] with zero K padding (16-byte units when vec), then
+    // the epilogue and MMA warps meet at named barrier 2.
+    constexpr int kPro = kFwdConsumers + 32;
+    const int ptid = (warp == kFwdMmaWarp) ? kFwdConsumers + lane : tid;   // 0 .. kPro-1
+    for (int e = ptid; e < H3; e += kPro) bs[e] = bias[e];
+    for (int e = ptid; e < Bt; e += kPro) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+    if (vec) {
+      const int upr = Kpad / EPU;
+      for (int e = ptid; e < Bt * upr; e += kPro) {
+        const int n = e / upr, kk = (e - n * upr) * EPU, bb = b0 + n;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (bb < B && kk < Zc)
+          v = __ldg(reinterpret_cast<const uint4*>((kk < n_in) ? x + (long long)bb * K * n_in + kk
+                                                              : h0 + (long long)bb * H + (kk - n_in)));
+        if constexpr (MODE == CFC_MATH_TF32) {
+          v.x = __float_as_uint(round_tf32(__uint_as_float(v.x)));
+          v.y = __float_as_uint(round_tf32(__uint_as_float(v.y)));
+          v.z = __float_as_uint(round_tf32(__uint_as_float(v.z)));
+          v.w = __float_as_uint(round_tf32(__uint_as_float(v.w)));
+        }
+        *reinterpret_cast<uint4*>(Zs + kmajor_off<ET>(n, kk, Bt)) = v;
+      }
+    } else {
+      for (int e = ptid; e < Bt * Kpad; e += kPro) {
+        const int n = e / Kpad, kk = e - n * Kpad, bb = b0 + n;
+        float v = 0.f;
+        if (bb < B && kk < Zc)
+          v = (kk < n_in) ? ld_operand<MODE>(x + (long long)bb * K * n_in + kk)
+                          : ld_operand<MODE>(h0 + (long long)bb * H + (kk - n_in));
+        st_elem<ET>(Zs + kmajor_off<ET>(n, kk, Bt), v);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    asm volatile("bar.sync 2, %0;" ::"n"(kPro) : "memory");
+  }
 
   if (warp == kFwdProducerWarp) {
-    // ---- producer warp: the W_cat tile sequence of every step through the ring.
-    // In a cluster of C CTAs tile g is fetched once, by CTA g % C, and
-    // multicast to all; a stage is refilled once every CTA's MMAs released it.
+    // ---- producer warp: the W_cat stages of every step, in schedule order,
+    // through the ring.  In a cluster of C CTAs stage g is fetched once, by
+    // CTA g % C, and multicast to all; a slot is refilled once every CTA's
+    // MMAs released it.
     int st = 0, t = 0, issuer = 0;
     uint32_t wrap = 0;
     for (long long g = 0; g < total_tiles; ++g) {
@@ -439,7 +492,7 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
       }
       if (lane == 0) {
         expect_tx(&full[st], kStage);
-        const uint8_t* src = wtiles + (size_t)t * kStage;
+        const uint8_t* src = wtiles + ((size_t)sched.pa[t] * nM + sched.m[t]) * kStage;
         if (C == 1) bulk_g2s(stage + (size_t)st * kStage, src, kStage, &full[st]);
         else if ((uint32_t)issuer == rank) bulk_g2s_mc(stage + (size_t)st * kStage, src, kStage, &full[st], cmask);
       }
@@ -452,88 +505,68 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
       }
     }
   } else if (warp == kFwdMmaWarp) {
-    // ---- MMA warp: D[m] (TMEM columns m*Bt ..) = W_cat tile rows x Z_k^T.
-    // After a timed-out wait nothing more is issued (the remaining waits would
-    // each run to their limit); the steps finish on stale data and the host
-    // sees the device error word.
+    // ---- MMA warp: D[m] (TMEM columns m*Bt ..) += W_cat stage rows x Z_k^T.
+    // After a timed-out wait nothing more is issued; the epilogue's own waits
+    // then run out and the host sees the device error word.
     const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
     const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
     const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(Zs));
     int cst = 0;
     uint32_t cwrap = 0;
     bool ok = true;
-    for (int k = 0; k < K; ++k) {
-      if (k > 0) step_sync();             // Z_k written by the epilogue of step k-1
-      tc::fence_after_sync();
-      if (ok && __shfl_sync(0xffffffffu, *err_flag, 0) == 0) {
-        for (int pa = 0; pa < nP && ok; ++pa) {
-          uint32_t d = tmem;
-          for (int m = 0; m < nM; ++m, d += (uint32_t)Bt) {
-            if (!mbar_wait_warp(&full[cst], cwrap & 1u, kMaxPolls)) {
-              if (lane == 0) *err_flag = 1;
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            if (lane == 0) {
-#pragma unroll
-              for (int sub = 0; sub < 2; ++sub) {
-                const int a = 2 * pa + sub;
-                if (a < nAk) {
-                  const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
-                  const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) {
-                    if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-                    else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-                  }
-                }
-              }
-              if (C == 1) tc::mma_commit(&empty[cst]);
-              else mma_commit_mc(&empty[cst], cmask);
-            }
-            __syncwarp();
-            if (++cst == nst) {
-              cst = 0;
-              ++cwrap;
-            }
-          }
+    for (int k = 0; k < K && ok; ++k) {
+      int waited = (k == 0) ? 3 : 0;
+      for (int t = 0; t < T && ok; ++t) {
+        while (waited < sched.lvl[t]) {
+          if (!mbar_wait_warp(&zsig[waited], (uint32_t)((k - 1) & 1), kMaxPolls)) ok = false;
+          ++waited;
         }
-        if (ok) {
-          if (lane == 0) tc::mma_commit(&done);
-          __syncwarp();
-          if (!mbar_wait_warp(&done, (uint32_t)(k & 1), kMaxPolls)) {
-            if (lane == 0) *err_flag = 1;
-            ok = false;
+        if (ok && !mbar_wait_warp(&full[cst], cwrap & 1u, kMaxPolls)) ok = false;
+        if (!ok) {
+          if (lane == 0) *err_flag = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const int pa = sched.pa[t];
+          const uint32_t d = tmem + (uint32_t)sched.m[t] * (uint32_t)Bt;
+          const bool first = sched.first[t] != 0;
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            const int a = 2 * pa + sub;
+            if (a < nAk) {
+              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
+              const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t accum = (first && sub == 0 && q == 0) ? 0u : 1u;
+                if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, accum);
+                else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, accum);
+              }
+            }
           }
+          if (C == 1) tc::mma_commit(&empty[cst]);
+          else mma_commit_mc(&empty[cst], cmask);
+          if (t == sched.nacc0 - 1) tc::mma_commit(&acc0);
+          if (t == T - 1) tc::mma_commit(&acc1);
+        }
+        __syncwarp();
+        if (++cst == nst) {
+          cst = 0;
+          ++cwrap;
         }
       }
-      tc::fence_before_sync();
-      step_sync();                        // D_k complete: release the epilogue
     }
   } else {
     // ---- epilogue warps
     const int xupr = vec ? n_in / EPU : 0;
     const long long sample_stride_act = (long long)K * H3, sample_stride_h = (long long)K * H;
-    for (int k = 0; k < K; ++k) {
-      // x of the next step: raw 16-byte units, stored into Z after the MMAs.
-      uint4 xu[kXUnits];
-      if (vec) {
-#pragma unroll
-        for (int q = 0; q < kXUnits; ++q) {
-          const int e = tid + q * kFwdConsumers;
-          const int n = (xupr > 0) ? e / xupr : 0, kk = (e - n * xupr) * EPU, bb = b0 + n;
-          xu[q] = (e < Bt * xupr && k + 1 < K && bb < B)
-                      ? __ldg(reinterpret_cast<const uint4*>(x + ((long long)bb * K + k + 1) * n_in + kk))
-                      : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      step_sync();
-      tc::fence_after_sync();
-      // thread <-> unit 128*ub + 32*quad + lane, 16 samples per pass;
-      // (ub, sample chunk) pairs alternate between the two warp halves.
-      const int nchunk = Bt / 16;
-      for (int pidx = half; pidx < nUB * nchunk; pidx += 2) {
+    const int nchunk = Bt / 16;
+    bool ok = true;
+    // thread <-> unit 128*ub + 32*quad + lane, 16 samples per pass; (ub, sample
+    // chunk) pairs of units [ub_lo, ub_hi) alternate between the two warp halves.
+    auto cell_pass = [&](int k, int ub_lo, int ub_hi) {
+      for (int pidx = ub_lo * nchunk + half; pidx < ub_hi * nchunk; pidx += 2) {
         const int ub = pidx / nchunk, n0 = (pidx - ub * nchunk) * 16;
         const int u = ub * 128 + quad * 32 + lane;
         float af[16], ag[16], ah[16];
@@ -567,6 +600,42 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
           }
         }
       }
+    };
+    // Z writes (generic proxy) become visible to the MMAs (async proxy), the
+    // TMEM reads are ordered before the signal, then one arrival per warp.
+    auto signal = [&](uint64_t* bar) {
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar);
+    };
+    // One warp polls the MMA completion (polling threads slow the tile
+    // stream), the epilogue warps meet it at a named barrier.
+    auto wait_acc = [&](uint64_t* bar, uint32_t parity) {
+      if (warp == 0 && ok && !mbar_wait_warp(bar, parity, kMaxPolls) && lane == 0) *err_flag = 1;
+      epi_sync();
+      ok = ok && *err_flag == 0;
+      tc::fence_after_sync();
+    };
+    for (int k = 0; k < K; ++k) {
+      // x of the next step: raw 16-byte units, stored into Z after all MMAs of step k.
+      uint4 xu[kXUnits];
+      if (vec) {
+#pragma unroll
+        for (int q = 0; q < kXUnits; ++q) {
+          const int e = tid + q * kFwdConsumers;
+          const int n = (xupr > 0) ? e / xupr : 0, kk = (e - n * xupr) * EPU, bb = b0 + n;
+          xu[q] = (e < Bt * xupr && k + 1 < K && bb < B)
+                      ? __ldg(reinterpret_cast<const uint4*>(x + ((long long)bb * K + k + 1) * n_in + kk))
+                      : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // ---- first half of the units
+      wait_acc(&acc0, (uint32_t)(k & 1));
+      if (ok) cell_pass(k, 0, nU0);
+      if (k + 1 < K) signal(&zsig[0]);
+      // ---- all MMAs of step k done: x_{k+1}, then the second half
+      wait_acc(&acc1, (uint32_t)(k & 1));
       if (k + 1 < K) {
         if (vec) {
 #pragma unroll
@@ -591,10 +660,10 @@ k_cfc_fwd_tcb(const uint8_t* __restrict__ wtiles, const ET* __restrict__ x, cons
             st_elem<ET>(Zs + kmajor_off<ET>(n, kk, Bt), v);
           }
         }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        step_sync();                      // Z_{k+1} ready, TMEM reads of step k done
+        signal(&zsig[1]);
       }
+      if (ok) cell_pass(k, nU0, nUB);
+      if (k + 1 < K) signal(&zsig[2]);
     }
   }
   tc::fence_before_sync();
@@ -611,7 +680,55 @@ struct FwdPlan {
   int Bt = 0, nUB = 0, nAk = 0, nst = 0, C = 1;
   uint32_t tmem_cols = 0;
   size_t smem = 0;
+  FwdSchedule sched;
 };
+
+// The stage order of one step (see FwdSchedule).  Atom levels: x -> 2 (zx),
+// h of U0 -> 1 (zlo), h of U1 -> 3 (zhi), K padding -> 0; a stage (atom
+// pair) takes the highest level of its atoms.
+bool make_fwd_schedule(int n_in, int H, int es, int nUB, int nAk, FwdSchedule* s) {
+  const int nP = (nAk + 1) / 2, nM = 3 * nUB;
+  if (nP * nM > kMaxSched) return false;
+  const int nU0 = std::max(1, nUB / 2);
+  const int H0 = std::min(H, 128 * nU0);
+  const int epa = 128 / es;
+  int lvl[kMaxSched / 2 + 1];
+  bool has_u0h[kMaxSched / 2 + 1];
+  for (int pa = 0; pa < nP; ++pa) {
+    lvl[pa] = 0;
+    has_u0h[pa] = false;
+    for (int kk = 2 * pa * epa; kk < std::min(2 * (pa + 1) * epa, n_in + H); ++kk) {
+      const int l = kk < n_in ? 2 : (kk < n_in + H0 ? 1 : 3);
+      lvl[pa] = std::max(lvl[pa], l);
+      has_u0h[pa] = has_u0h[pa] || l == 1;
+    }
+  }
+  int t = 0;
+  bool seen[3 * 64] = {};
+  auto push = [&](int pa, int m, int l) {
+    s->pa[t] = (uint8_t)pa;
+    s->m[t] = (uint8_t)m;
+    s->lvl[t] = (uint8_t)l;
+    s->first[t] = seen[m] ? 0 : 1;
+    seen[m] = true;
+    ++t;
+  };
+  if (nM > 3 * 64 || nP > 255) return false;
+  for (int l = 0; l <= 3; ++l)
+    for (int pa = 0; pa < nP; ++pa)
+      if (lvl[pa] == l)
+        for (int m = 0; m < 3 * nU0; ++m) push(pa, m, std::max(l, 1));
+  for (int pa = 0; pa < nP; ++pa)
+    if (has_u0h[pa])
+      for (int m = 3 * nU0; m < nM; ++m) push(pa, m, 3);
+  s->nacc0 = t;
+  for (int pa = 0; pa < nP; ++pa)
+    if (!has_u0h[pa])
+      for (int m = 3 * nU0; m < nM; ++m) push(pa, m, 3);
+  s->T = t;
+  s->nU0 = nU0;
+  return t == nP * nM;
+}
 
 bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
   if (L.math == CFC_MATH_FP32) return false;
@@ -629,6 +746,7 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
   };
   while (Bt > 16 && !ok(Bt)) Bt -= 16;
   if (!ok(Bt)) return false;
+  if (!make_fwd_schedule(L.n_in, L.H, es, nUB, nAk, &p->sched)) return false;
   int nst = (int)std::min<size_t>(kFwdMaxStages, (kSmemMax - fixed_for(Bt)) / kStage);
   p->Bt = Bt;
   p->nUB = nUB;
@@ -675,7 +793,7 @@ cudaError_t launch_fwd_stream(const Layout& L, const FwdPlan& p, const CfcArgs& 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   TraceScope trace("cfc_fwd_stream_tc", s);
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(tiles), static_cast<const ET*>(a.x),
+  return cudaLaunchKernelEx(&cfg, kern, p.sched, static_cast<const uint8_t*>(tiles), static_cast<const ET*>(a.x),
                             static_cast<const ET*>(a.h0), a.b, a.dt, a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt,
                             p.nUB, p.nAk, p.nst, p.tmem_cols, p.C, static_cast<ET*>(a.h_seq),
                             reinterpret_cast<float*>(a.ws + L.off_act));
