@@ -349,6 +349,43 @@ def measure_workload(w, steps, warmup, device, peaks, flush, dist_ctx=None, with
     return out
 
 
+def measure_graph(w, steps, device):
+    """The same step launched eagerly and replayed from one CUDA graph captured
+    through the C ABI (the calls allocate nothing and never synchronise)."""
+    import torch
+    p = Path(w, device)
+    for _ in range(3):
+        p.step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        p.step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        p.step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    def batch(fn):
+        # back to back, no L2 flush: the host's launch rate is part of the time
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / steps
+
+    out = dict(eager_ms=batch(p.step), graph_ms=batch(g.replay), steps=steps,
+               timing="back-to-back steps, no L2 flush")
+    del g, p
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_reduce(B, N, steps, device, peaks, flush):
     import torch
     import recurrent_cell_gb300 as cfc
@@ -499,6 +536,8 @@ def main():
         red = [measure_reduce(B, N, 20, device, peaks, flush)
                for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
         secondary["reduce_axis0"] = red
+        secondary["cuda_graph"] = {wl.SHORT_NAMES[n].name: measure_graph(wl.SHORT_NAMES[n], 50, device)
+                                   for n in ("tiny", "smoke")}
     if rank == 0 and world == 1:
         cpu, _ = time_oracle(w, seconds=args.cpu_seconds)
     if rank != 0:
