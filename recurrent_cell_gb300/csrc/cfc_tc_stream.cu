@@ -22,19 +22,20 @@
 // (128 rows x 128 bytes of K) in the workspace and streamed through a ring of
 // shared-memory stages with TMA bulk copies (cp.async.bulk, mbarrier
 // transaction counts).
-// The tile sequence repeats every step, so the copies for the next step's
-// first tiles run while the block computes the next dA.  The B operand, dA_k
-// of the Bt samples, is computed by the block itself into a K-major swizzled
-// shared-memory tile.
+// The B operand, dA_k of the Bt samples, is computed by the block itself
+// into a K-major swizzled shared-memory tile.
 //
-// Elementwise phase of step k: thread <-> unit j = 128*mt + 32*(warp%4) + lane
-// (the TMEM lane quadrant rule).  It reads the carry of step k+1 for its unit
-// from TMEM and forms (with the saved activations) the three dA values of
-// that unit for every sample of the tile.  After step 0 the same read gives
-// grad_h0.
+// Both kernels are warp-specialised: a producer warp streams the tiles, an
+// MMA warp issues the MMAs, eight warps do the cell / elementwise work.  The
+// units are split into two halves with their own TMEM accumulators, and the
+// stages of a step are ordered so that each half's elementwise work overlaps
+// MMAs of the other half (TileSchedule).  Thread <-> unit 128*mt +
+// 32*(warp%4) + lane (the TMEM lane quadrant rule).  After step 0 the
+// backward's carry read gives grad_h0.
 //
 // Waits are bounded; a timeout records an error in the device error word.
 #include <algorithm>
+#include <vector>
 
 #include "cfc_internal.cuh"
 #include "tc_common.cuh"
@@ -42,8 +43,6 @@
 namespace cfc {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxStages = 6;    // ring of streamed A tiles (runtime count: nst)
 constexpr uint32_t kTile = 128 * 128;      // bytes of one A tile (128 rows x one 128-byte K atom)
 // A stage holds the tiles of two consecutive K atoms of one M tile (32 KB):
 // one full-barrier wait and one commit per 8 MMAs.
@@ -126,194 +125,6 @@ __global__ void k_prep_wt_tiles(const ET* __restrict__ W_rec, int H, int nM, int
   }
 }
 
-template <typename ET, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-k_cfc_bwd_tcb(const uint8_t* __restrict__ wtiles, const float* __restrict__ dt, int dt_stride, int B,
-              int K, int H, int Bt, int nM, int nAk, int nst, uint32_t tmem_cols,
-              const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
-              const float* __restrict__ grad_h_last, const float* __restrict__ y,
-              const float* __restrict__ act, ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
-  const int H3 = 3 * H;
-  const int b0 = blockIdx.x * Bt;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
-  const int nP = (nAk + 1) / 2;                 // K-atom pairs
-  const int T = nP * nM;                        // streamed stages per step
-  const long long total_tiles = (long long)K * T;
-
-  extern __shared__ uint8_t smraw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stage = sm;                                   // nst x 32 KB
-  uint8_t* dAs = sm + (size_t)nst * kStage;              // nAk x [Bt rows][128 B]
-  float* dts = reinterpret_cast<float*>(dAs + (size_t)nAk * Bt * 128);   // [Bt]
-  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
-  __shared__ uint32_t tmem_base;
-  __shared__ int err;
-
-  if (tid == 0) {
-    for (int i = 0; i < nst; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
-    }
-    tc::mbar_init(&done, 1);
-    tc::mbar_init_fence();
-    err = 0;
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
-  for (int e = tid; e < Bt; e += kThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
-  // dA tile padding (K beyond 3H) stays zero for the whole launch.
-  {
-    constexpr int EPA = 128 / sizeof(ET);
-    const int Kpad = nAk * EPA;
-    for (int e = tid; e < Bt * (Kpad - H3); e += kThreads) {
-      const int n = e / (Kpad - H3), kk = H3 + e % (Kpad - H3);
-      st_elem<ET>(dAs + kmajor_off<ET>(n, kk, Bt), 0.f);
-    }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
-
-  // Ring positions (thread 0).  Stage indices and barrier phases advance by
-  // increments: integer division on this path costs more than the MMAs.
-  long long copies_left = total_tiles;
-  int pst = 0, pt = 0;          // producer: stage, tile of the per-step sequence
-  uint32_t pwrap = 0;           // producer: completed passes over the ring
-  int cst = 0;                  // consumer: stage
-  uint32_t cwrap = 0;           // consumer: completed passes over the ring
-  auto issue_copy = [&]() {
-    // stage reuse: the MMAs of the tile nst copies back must be complete
-    if (pwrap > 0 && !tc::mbar_wait(&empty[pst], (pwrap - 1) & 1u, kMaxPolls)) err = 1;
-    expect_tx(&full[pst], kStage);
-    bulk_g2s(stage + (size_t)pst * kStage, wtiles + (size_t)pt * kStage, kStage, &full[pst]);
-    if (++pt == T) pt = 0;
-    if (++pst == nst) {
-      pst = 0;
-      ++pwrap;
-    }
-    --copies_left;
-  };
-  if (tid == 0) {
-    for (int i = 0; i < nst - 2 && copies_left > 0; ++i) issue_copy();
-  }
-
-  // units handled by this thread: j = 128*mt + 32*quad + lane for mt = warp/4, warp/4 + 2, ...
-  for (int step = 0; step <= K; ++step) {
-    const int k = K - 1 - step;                  // step == K: final read-out only
-    // ---- elementwise phase: carry of step k+1 from TMEM -> dA_k
-    for (int mt = warp >> 2; mt < nM; mt += kThreads / 128) {
-      const int j = mt * 128 + quad * 32 + lane;
-      for (int n0 = 0; n0 < Bt; n0 += 16) {
-        float dz[16];
-        if (step > 0) {
-          tc::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * Bt + n0), dz);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) dz[i] = 0.f;
-        }
-        if (j < H) {
-          const int u = j;
-          if (k < 0) {                           // after step 0: grad_h0
-            if (grad_h0) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int bb = b0 + n0 + i;
-                if (bb < B) grad_h0[(long long)bb * H + u] = dz[i];
-              }
-            }
-          } else {
-            float ga[16], gg[16], gh[16], up[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int bb = b0 + n0 + i;
-              ga[i] = gg[i] = gh[i] = up[i] = 0.f;
-              if (bb < B) {
-                const long long row = (long long)bb * K + k;
-                ga[i] = act[row * H3 + u];
-                gg[i] = act[row * H3 + H + u];
-                gh[i] = act[row * H3 + 2 * H + u];
-                if (grad_h_seq) up[i] = grad_h_seq[row * H + u];
-                if (k == K - 1) {
-                  if (grad_h_last) up[i] += grad_h_last[(long long)bb * H + u];
-                  if (y) up[i] += ldf(h_seq + row * H + u) - y[(long long)bb * H + u];
-                }
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int n = n0 + i, bb = b0 + n;
-              float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-              if (bb < B) {
-                const float delta = dz[i] + up[i];
-                const float gate = ga[i], g = gg[i], hh = gh[i];
-                d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
-                d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
-                d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
-                const long long row = (long long)bb * K + k;
-                stf(dA_out + row * H3 + u, d0);
-                stf(dA_out + row * H3 + H + u, d1);
-                stf(dA_out + row * H3 + 2 * H + u, d2);
-              }
-              st_elem<ET>(dAs + kmajor_off<ET>(n, u, Bt), d0);
-              st_elem<ET>(dAs + kmajor_off<ET>(n, H + u, Bt), d1);
-              st_elem<ET>(dAs + kmajor_off<ET>(n, 2 * H + u, Bt), d2);
-            }
-          }
-        }
-      }
-    }
-    if (k < 0) break;
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    // ---- MMA phase (thread 0): stream W_rec^T tiles, carry_k = W_rec^T dA_k into TMEM
-    if (tid == 0) {
-      const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
-      const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(dAs));
-      for (int pa = 0; pa < nP; ++pa) {
-        uint32_t d = tmem;
-        for (int mt = 0; mt < nM; ++mt, d += (uint32_t)Bt) {
-          if (!tc::mbar_wait(&full[cst], cwrap & 1u, kMaxPolls)) err = 1;
-          tc::fence_after_sync();
-#pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const int a = 2 * pa + sub;
-            if (a < nAk) {
-              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
-              const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-                else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-              }
-            }
-          }
-          tc::mma_commit(&empty[cst]);
-          if (++cst == nst) {
-            cst = 0;
-            ++cwrap;
-          }
-          if (copies_left > 0) issue_copy();
-        }
-      }
-      tc::mma_commit(&done);
-      // Only this thread waits on the MMA completion; the others wait at the
-      // block barrier (polling threads would compete with the barrier traffic
-      // of the tile stream).
-      if (!tc::mbar_wait(&done, (uint32_t)(step & 1), kMaxPolls)) err = 1;
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-  }
-  if (err) atomicExch(&g_tc_bwd_error, 1);
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
-}
-
 // W_cat tiles of the forward: tile (a, m), m = 3*ub + c, holds the rows of
 // head c for units 128*ub + i (i = 0..127) and K elements a*EPA .. +EPA-1 of z,
 // at byte offset tile_offset(a, m, nM), swizzled as in shared memory.
@@ -364,7 +175,7 @@ constexpr int kMaxSched = 256;             // streamed stages per step
 // lvl: 1, 2, 3 = the stage waits for zlo, zx, zhi of the previous step;
 // first: the stage is the first of its M tile in the step (the MMA
 // overwrites the accumulator).
-struct FwdSchedule {
+struct TileSchedule {
   int T = 0, nacc0 = 0, nU0 = 0;
   uint8_t pa[kMaxSched], m[kMaxSched], lvl[kMaxSched], first[kMaxSched];
 };
@@ -389,7 +200,7 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
 
 template <typename ET, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-k_cfc_fwd_tcb(const __grid_constant__ FwdSchedule sched, const uint8_t* __restrict__ wtiles,
+k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restrict__ wtiles,
               const ET* __restrict__ x, const ET* __restrict__ h0, const float* __restrict__ bias,
               const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H, int Bt, int nUB,
               int nAk, int nst, uint32_t tmem_cols, int C, ET* __restrict__ h_seq, float* __restrict__ act) {
@@ -680,13 +491,13 @@ struct FwdPlan {
   int Bt = 0, nUB = 0, nAk = 0, nst = 0, C = 1;
   uint32_t tmem_cols = 0;
   size_t smem = 0;
-  FwdSchedule sched;
+  TileSchedule sched;
 };
 
-// The stage order of one step (see FwdSchedule).  Atom levels: x -> 2 (zx),
+// The stage order of one step (see TileSchedule).  Atom levels: x -> 2 (zx),
 // h of U0 -> 1 (zlo), h of U1 -> 3 (zhi), K padding -> 0; a stage (atom
 // pair) takes the highest level of its atoms.
-bool make_fwd_schedule(int n_in, int H, int es, int nUB, int nAk, FwdSchedule* s) {
+bool make_fwd_schedule(int n_in, int H, int es, int nUB, int nAk, TileSchedule* s) {
   const int nP = (nAk + 1) / 2, nM = 3 * nUB;
   if (nP * nM > kMaxSched) return false;
   const int nU0 = std::max(1, nUB / 2);
@@ -763,6 +574,320 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// Backward K loop with streamed W_rec^T tiles (large batches): one CTA per
+// tile of Bt samples.  Per step k (reverse) the elementwise warps turn the
+// carry of step k+1 (TMEM) into dA_k of their units -- written to global
+// memory and into the K-major B tile dAs (K index c*H + u) -- and the MMAs
+// compute carry_k^T = W_rec^T dA_k^T (M tiles of 128 units, N = Bt, K = 3H)
+// from the streamed tiles.
+//
+// Warp-specialised like the forward: warp 8 streams tiles, warp 9 issues the
+// MMAs, warps 0..7 do the elementwise work, the units split into halves U0
+// (M tiles < nU0) and U1 with their own accumulators:
+//   elementwise(s): [acc0 of s-1] U0: carry -> dA_k(U0)  --dlo-->
+//                   [acc1 of s-1] U1: carry -> dA_k(U1)  --dhi-->
+//   MMAs(s):        U0 stages over atoms of U0 units only (dlo), the other U0
+//                   stages (dhi), U1 stages over atoms holding U0 units, acc0,
+//                   the remaining U1 stages, acc1.
+// So U1's elementwise work overlaps the first U0 MMAs of the step, and U0's
+// elementwise work of the next step overlaps the last U1 MMAs.
+// ---------------------------------------------------------------------------
+constexpr int kBwdElem = 256;              // elementwise warps 0..7
+constexpr int kBwdProducerWarp = 8;
+constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdThreads = kBwdElem + 64;
+
+template <typename ET, int MODE>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restrict__ wtiles,
+              const float* __restrict__ dt, int dt_stride, int B, int K, int H, int Bt, int nM, int nAk, int nst,
+              uint32_t tmem_cols, const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
+              const float* __restrict__ grad_h_last, const float* __restrict__ y,
+              const float* __restrict__ act, ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
+  const int H3 = 3 * H;
+  const int b0 = blockIdx.x * Bt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
+  const int T = sched.T;
+  const long long total_tiles = (long long)K * T;
+  const int nM0 = sched.nU0;
+
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage = sm;                                   // nst x 32 KB
+  uint8_t* dAs = sm + (size_t)nst * kStage;              // nAk x [Bt rows][128 B]
+  float* dts = reinterpret_cast<float*>(dAs + (size_t)nAk * Bt * 128);   // [Bt]
+  __shared__ uint64_t full[kFwdMaxStages], empty[kFwdMaxStages];
+  __shared__ uint64_t acc0, acc1, dsig[2];               // dsig: dlo, dhi
+  __shared__ uint32_t tmem_base;
+  __shared__ int err;
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    tc::mbar_init(&acc0, 1);
+    tc::mbar_init(&acc1, 1);
+    for (int i = 0; i < 2; ++i) tc::mbar_init(&dsig[i], kBwdElem / 32);
+    tc::mbar_init_fence();
+    err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
+  for (int e = tid; e < Bt; e += kBwdThreads) dts[e] = (b0 + e < B) ? dt[dt_stride ? b0 + e : 0] : 0.f;
+  // dA tile padding (K beyond 3H) stays zero for the whole launch.
+  {
+    constexpr int EPA = 128 / sizeof(ET);
+    const int Kpad = nAk * EPA;
+    for (int e = tid; e < Bt * (Kpad - H3); e += kBwdThreads) {
+      const int n = e / (Kpad - H3), kk = H3 + e % (Kpad - H3);
+      st_elem<ET>(dAs + kmajor_off<ET>(n, kk, Bt), 0.f);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  volatile int* err_flag = &err;
+
+  if (warp == kBwdProducerWarp) {
+    int st = 0, t = 0;
+    uint32_t wrap = 0;
+    for (long long g = 0; g < total_tiles; ++g) {
+      if (__shfl_sync(0xffffffffu, *err_flag, 0)) break;
+      if (wrap > 0 && !mbar_wait_warp(&empty[st], (wrap - 1) & 1u, kMaxPolls)) {
+        if (lane == 0) *err_flag = 1;
+        break;
+      }
+      if (lane == 0) {
+        expect_tx(&full[st], kStage);
+        bulk_g2s(stage + (size_t)st * kStage, wtiles + ((size_t)sched.pa[t] * nM + sched.m[t]) * kStage, kStage,
+                 &full[st]);
+      }
+      __syncwarp();
+      if (++t == T) t = 0;
+      if (++st == nst) {
+        st = 0;
+        ++wrap;
+      }
+    }
+  } else if (warp == kBwdMmaWarp) {
+    const uint32_t id = tc::idesc(128, (uint32_t)Bt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
+    const uint64_t a_desc0 = tc::sdesc_k_sw128(tc::smem_u32(stage));
+    const uint64_t b_desc0 = tc::sdesc_k_sw128(tc::smem_u32(dAs));
+    int cst = 0;
+    uint32_t cwrap = 0;
+    bool ok = true;
+    for (int s = 0; s < K && ok; ++s) {
+      int waited = 0;
+      for (int t = 0; t < T && ok; ++t) {
+        while (waited < sched.lvl[t]) {
+          if (!mbar_wait_warp(&dsig[waited], (uint32_t)(s & 1), kMaxPolls)) ok = false;
+          ++waited;
+        }
+        if (ok && !mbar_wait_warp(&full[cst], cwrap & 1u, kMaxPolls)) ok = false;
+        if (!ok) {
+          if (lane == 0) *err_flag = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const int pa = sched.pa[t];
+          const uint32_t d = tmem + (uint32_t)sched.m[t] * (uint32_t)Bt;
+          const bool first = sched.first[t] != 0;
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            const int a = 2 * pa + sub;
+            if (a < nAk) {
+              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
+              const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t accum = (first && sub == 0 && q == 0) ? 0u : 1u;
+                if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, accum);
+                else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, accum);
+              }
+            }
+          }
+          tc::mma_commit(&empty[cst]);
+          if (t == sched.nacc0 - 1) tc::mma_commit(&acc0);
+          if (t == T - 1) tc::mma_commit(&acc1);
+        }
+        __syncwarp();
+        if (++cst == nst) {
+          cst = 0;
+          ++cwrap;
+        }
+      }
+    }
+  } else {
+    // ---- elementwise warps: thread <-> unit 128*mt + 32*quad + lane, 8
+    // samples per pass; (M tile, sample chunk) pairs alternate between the
+    // two warp halves.
+    constexpr int kP = 8;                        // samples per pass
+    const int nchunk = Bt / kP;
+    bool ok = true;
+    auto wait_acc = [&](uint64_t* bar, uint32_t parity) {
+      if (warp == 0 && ok && !mbar_wait_warp(bar, parity, kMaxPolls) && lane == 0) *err_flag = 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(kBwdElem) : "memory");
+      ok = ok && *err_flag == 0;
+      tc::fence_after_sync();
+    };
+    auto signal = [&](uint64_t* bar) {
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar);
+    };
+    // Saved activations of one pass, loaded one pass ahead of their use.
+    using VP = float[kP];
+    const long long sample_stride = (long long)K * H3;   // act / dA rows of one sample
+    auto load_pass = [&](int k, int pidx, VP& ga, VP& gg, VP& gh) {
+      const int mt = pidx / nchunk, n0 = (pidx - mt * nchunk) * kP;
+      const int u = mt * 128 + quad * 32 + lane;
+      const float* ap = act + ((long long)(b0 + n0) * K + k) * H3 + u;
+      const int nvalid = (u < H && k >= 0) ? min(kP, B - (b0 + n0)) : 0;
+#pragma unroll
+      for (int i = 0; i < kP; ++i) {
+        ga[i] = gg[i] = gh[i] = 0.f;
+        if (i < nvalid) {
+          ga[i] = ap[0];
+          gg[i] = ap[H];
+          gh[i] = ap[2 * H];
+        }
+        ap += sample_stride;
+      }
+    };
+    auto run_pass = [&](int s, int pidx, const VP& ga, const VP& gg, const VP& gh) {
+      const int k = K - 1 - s;                   // k < 0: grad_h0 read-out
+      const int mt = pidx / nchunk, n0 = (pidx - mt * nchunk) * kP;
+      const int u = mt * 128 + quad * 32 + lane;
+      float dz[kP];
+      if (s > 0) {
+        tc::tmem_ld8(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * Bt + n0), dz);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kP; ++i) dz[i] = 0.f;
+      }
+      if (u >= H) return;
+      const int nvalid = min(kP, B - (b0 + n0));
+      if (k < 0) {
+        if (grad_h0) {
+#pragma unroll
+          for (int i = 0; i < kP; ++i)
+            if (i < nvalid) grad_h0[(long long)(b0 + n0 + i) * H + u] = dz[i];
+        }
+        return;
+      }
+      // upstream gradient of h_k (only the per-step seeds and the last step's)
+      if (grad_h_seq || k == K - 1) {
+#pragma unroll
+        for (int i = 0; i < kP; ++i) {
+          const int bb = b0 + n0 + i;
+          if (i < nvalid) {
+            const long long row = (long long)bb * K + k;
+            float up = grad_h_seq ? grad_h_seq[row * H + u] : 0.f;
+            if (k == K - 1) {
+              if (grad_h_last) up += grad_h_last[(long long)bb * H + u];
+              if (y) up += ldf(h_seq + row * H + u) - y[(long long)bb * H + u];
+            }
+            dz[i] += up;
+          }
+        }
+      }
+      ET* dp = dA_out + ((long long)(b0 + n0) * K + k) * H3 + u;
+#pragma unroll
+      for (int i = 0; i < kP; ++i) {
+        const int n = n0 + i;
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+        if (i < nvalid) {
+          const float delta = dz[i];
+          const float gate = ga[i], g = gg[i], hh = gh[i];
+          d1 = to_operand<MODE>(delta * gate * (1.f - g * g));
+          d2 = to_operand<MODE>(delta * (1.f - gate) * (1.f - hh * hh));
+          d0 = to_operand<MODE>(-dts[n] * delta * (g - hh) * gate * (1.f - gate));
+          stf(dp, d0);
+          stf(dp + H, d1);
+          stf(dp + 2 * H, d2);
+        }
+        dp += sample_stride;
+        st_elem<ET>(dAs + kmajor_off<ET>(n, u, Bt), d0);
+        st_elem<ET>(dAs + kmajor_off<ET>(n, H + u, Bt), d1);
+        st_elem<ET>(dAs + kmajor_off<ET>(n, 2 * H + u, Bt), d2);
+      }
+    };
+    // This thread's passes of M tiles [mt_lo, mt_hi): pidx = mt_lo*nchunk +
+    // half, +2, ...; two input buffers, the next pass always in flight.
+    auto elem = [&](int s, int mt_lo, int mt_hi) {
+      const int k = K - 1 - s;
+      const int end = mt_hi * nchunk;
+      float ga0[kP], gg0[kP], gh0[kP], ga1[kP], gg1[kP], gh1[kP];
+      int p = mt_lo * nchunk + half;
+      if (p < end) load_pass(k, p, ga0, gg0, gh0);
+      for (; p < end; p += 4) {
+        if (p + 2 < end) load_pass(k, p + 2, ga1, gg1, gh1);
+        run_pass(s, p, ga0, gg0, gh0);
+        if (p + 4 < end) load_pass(k, p + 4, ga0, gg0, gh0);
+        if (p + 2 < end) run_pass(s, p + 2, ga1, gg1, gh1);
+      }
+    };
+    for (int s = 0; s <= K; ++s) {
+      if (s > 0) wait_acc(&acc0, (uint32_t)((s - 1) & 1));
+      if (ok) elem(s, 0, nM0);
+      if (s < K) signal(&dsig[0]);
+      if (s > 0) wait_acc(&acc1, (uint32_t)((s - 1) & 1));
+      if (ok) elem(s, nM0, nM);
+      if (s < K) signal(&dsig[1]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (err) atomicExch(&g_tc_bwd_error, 1);
+  if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+// Stage order of one backward step (see k_cfc_bwd_tcb).  K index kk of dA is
+// unit kk % H; an atom pair has level 1 if all its units are in U0, else 2.
+bool make_bwd_schedule(int H, int es, int nM, int nAk, TileSchedule* s) {
+  const int nP = (nAk + 1) / 2;
+  if (nP * nM > kMaxSched || nM > 255 || nP > 255) return false;
+  const int nM0 = std::max(1, nM / 2);
+  const int H0 = std::min(H, 128 * nM0);
+  const int epa = 128 / es;
+  std::vector<int> lvl(nP, 0);
+  std::vector<char> has_u0(nP, 0), seen(nM, 0);
+  for (int pa = 0; pa < nP; ++pa)
+    for (int kk = 2 * pa * epa; kk < std::min(2 * (pa + 1) * epa, 3 * H); ++kk) {
+      const int l = (kk % H) < H0 ? 1 : 2;
+      lvl[pa] = std::max(lvl[pa], l);
+      if (l == 1) has_u0[pa] = 1;
+    }
+  int t = 0;
+  auto push = [&](int pa, int m, int l) {
+    s->pa[t] = (uint8_t)pa;
+    s->m[t] = (uint8_t)m;
+    s->lvl[t] = (uint8_t)l;
+    s->first[t] = seen[m] ? 0 : 1;
+    seen[m] = 1;
+    ++t;
+  };
+  for (int l = 0; l <= 2; ++l)
+    for (int pa = 0; pa < nP; ++pa)
+      if (lvl[pa] == l)
+        for (int m = 0; m < nM0; ++m) push(pa, m, std::max(l, 1));
+  for (int pa = 0; pa < nP; ++pa)
+    if (has_u0[pa])
+      for (int m = nM0; m < nM; ++m) push(pa, m, 2);
+  s->nacc0 = t;
+  for (int pa = 0; pa < nP; ++pa)
+    if (!has_u0[pa])
+      for (int m = nM0; m < nM; ++m) push(pa, m, 2);
+  s->T = t;
+  s->nU0 = nM0;
+  return t == nP * nM;
+}
+
 template <typename ET, int MODE>
 cudaError_t launch_fwd_stream(const Layout& L, const FwdPlan& p, const CfcArgs& a, cudaStream_t s) {
   uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
@@ -804,6 +929,7 @@ struct BwdPlan {
   int Bt = 0, nM = 0, nAk = 0, nst = 0;
   uint32_t tmem_cols = 0;
   size_t smem = 0;
+  TileSchedule sched;
 };
 
 bool plan_bwd(const Layout& L, BwdPlan* p) {
@@ -818,7 +944,8 @@ bool plan_bwd(const Layout& L, BwdPlan* p) {
   while (Bt > 16 && (fixed_for(Bt) + 3 * (size_t)kStage > kSmemMax || (long long)nM * Bt > 512)) Bt -= 16;
   if (fixed_for(Bt) + 3 * (size_t)kStage > kSmemMax || (long long)nM * Bt > 512) return false;
   // as many stages as fit (the stream is latency-bound: more tiles in flight)
-  const int nst = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed_for(Bt)) / kStage);
+  const int nst = (int)std::min<size_t>(kFwdMaxStages, (kSmemMax - fixed_for(Bt)) / kStage);
+  if (!make_bwd_schedule(L.H, es, nM, nAk, &p->sched)) return false;
   p->Bt = Bt;
   p->nM = nM;
   p->nAk = nAk;
@@ -847,7 +974,7 @@ cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cuda
   const int grid = (L.B + p.Bt - 1) / p.Bt;
   {
     TraceScope trace("cfc_bwd_tc", s);
-    kern<<<grid, kThreads, p.smem, s>>>(tiles, a.dt, a.dt_stride, L.B, L.K, L.H, p.Bt, p.nM, p.nAk, p.nst,
+    kern<<<grid, kBwdThreads, p.smem, s>>>(p.sched, tiles, a.dt, a.dt_stride, L.B, L.K, L.H, p.Bt, p.nM, p.nAk, p.nst,
                                         p.tmem_cols, static_cast<const ET*>(a.h_seq), a.grad_h_seq, a.grad_h_last,
                                         a.y, reinterpret_cast<const float*>(a.ws + L.off_act),
                                         reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0);

@@ -142,6 +142,11 @@ EDGE = [
     wl.Workload("edge_tc_bf16_B45_K5", B=45, K=5, n_in=40, n_hid=96, math=wl.MATH_BF16,
                 dt_per_sample=True),
     wl.Workload("edge_tc_bf16_odd_n_in", B=19, K=4, n_in=7, n_hid=32, math=wl.MATH_BF16),
+    # streamed-weight K loops with two unit halves: H0 = 128 not on an atom
+    # pair boundary, x / h atoms shared, a short second half
+    wl.Workload("edge_tcs_bf16_H200", B=150, K=3, n_in=40, n_hid=200, math=wl.MATH_BF16,
+                dt_per_sample=True),
+    wl.Workload("edge_tcs_tf32_H160", B=70, K=4, n_in=24, n_hid=160, math=wl.MATH_TF32),
     # TMA-fed weight gradient (bf16, GEMM path): 64 steps of one sample per
     # chunk with a ragged 3H tile, and whole samples per chunk
     wl.Workload("edge_tma_K128_H64", B=3, K=128, n_in=64, n_hid=64, math=wl.MATH_BF16,
