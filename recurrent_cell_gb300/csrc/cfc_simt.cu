@@ -217,7 +217,7 @@ k_cfc_bwd(const T* __restrict__ W_in, const T* __restrict__ W_rec,
 constexpr int kTM = 64, kTN = 64, kTR = 16;
 
 template <typename T, typename DT, int MODE>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 5)
 k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict__ h0,
         const T* __restrict__ h_seq, int K, int n_in, int H, long long R,
         long long rows_per_split, float* __restrict__ out) {
@@ -235,46 +235,65 @@ k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict_
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   constexpr int kPer = (kTR * kTM) / 256;                   // elements per thread per chunk
 
+  // Row of element q of a chunk: r + tid/kTM + q*(256/kTM).  Its step index
+  // (row mod K) and sample (row / K) advance by kTR rows per chunk, kept
+  // incrementally (no integer division in the loop).
+  constexpr int kRowStep = 256 / kTM;
+  int kq[kPer], bq[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int row = r_begin + tid / kTM + q * kRowStep;
+    bq[q] = row / K;
+    kq[q] = row - bq[q] * K;
+  }
   float ra[kPer], rz[kPer];
+  const int cc = tid % kTM;
+  const int m = m0 + cc, j = j0 + cc;
   auto load_chunk = [&](int r) {
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
-      const int e = tid + q * 256;
-      const int rr = e / kTM, cc = e - rr * kTM;
-      const int row = r + rr;
-      const int m = m0 + cc, j = j0 + cc;
+      const int row = r + tid / kTM + q * kRowStep;
       float a = 0.f, z = 0.f;
       if (row < r_end) {
         if (m < H3) a = ldf(dA + (long long)row * H3 + m);
         if (j < n_in) {
           z = ld_operand<MODE>(x + (long long)row * n_in + j);
         } else if (j < Zc) {
-          const int kk = row % K;
           const int u = j - n_in;
-          z = (kk == 0) ? ld_operand<MODE>(h0 + (long long)(row / K) * H + u)
-                        : ld_operand<MODE>(h_seq + (long long)(row - 1) * H + u);
+          z = (kq[q] == 0) ? ld_operand<MODE>(h0 + (long long)bq[q] * H + u)
+                           : ld_operand<MODE>(h_seq + (long long)(row - 1) * H + u);
         } else if (j == Zc) {
           z = 1.f;
         }
       }
       ra[q] = a;
       rz[q] = z;
+      // the same element of the next chunk: kTR rows further
+      kq[q] += kTR;
+      while (kq[q] >= K) {
+        kq[q] -= K;
+        ++bq[q];
+      }
     }
   };
 
-  float acc[4][4];
+  // When Zc is a multiple of kTN the bias column would be a tile of its own;
+  // the block whose tile ends at Zc sums it instead (accb, one per m row).
+  const bool fold_bias = (Zc % kTN == 0) && (j0 + kTN == Zc);
+  float acc[4][4], accb[4];
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
+  for (int p = 0; p < 4; ++p) {
+    accb[p] = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
+  }
 
   if (r_begin < r_end) load_chunk(r_begin);
   int buf = 0;
   for (int r = r_begin; r < r_end; r += kTR, buf ^= 1) {
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
-      const int e = tid + q * 256;
-      const int rr = e / kTM, cc = e - rr * kTM;
+      const int rr = tid / kTM + q * kRowStep;
       sA[buf][rr][cc] = ra[q];
       sZ[buf][rr][cc] = rz[q];
     }
@@ -289,6 +308,10 @@ k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict_
       for (int p = 0; p < 4; ++p)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a4[p], z4[q], acc[p][q]);
+      if (fold_bias) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) accb[p] += a4[p];
+      }
     }
     // The buffer written next iteration is the other one; the barrier at the
     // top of the iteration after that orders its reuse.
@@ -307,6 +330,7 @@ k_wgrad(const DT* __restrict__ dA, const T* __restrict__ x, const T* __restrict_
       else if (j < Zc) o[off_rec + (long long)m * H + (j - n_in)] = acc[p][q];
       else if (j == Zc) o[off_b + m] = acc[p][q];
     }
+    if (fold_bias && tx == 0) o[off_b + m] = accb[p];
   }
 }
 
@@ -395,7 +419,10 @@ cudaError_t backward_mode(const Layout& L, const CfcArgs& a, cudaStream_t s) {
 template <typename T, typename DT, int MODE>
 cudaError_t wgrad_mode(const Layout& L, const CfcArgs& a, float* out, int n_split,
                        long long rows_per_split, cudaStream_t s) {
-  dim3 grid((L.H3 + kTM - 1) / kTM, (L.Zc + 1 + kTN - 1) / kTN, n_split);
+  // Column tiles of z = [x; h; 1]; a bias column alone in a last tile is
+  // folded into the tile before it.
+  const int ntn = (L.Zc % kTN == 0) ? L.Zc / kTN : (L.Zc + 1 + kTN - 1) / kTN;
+  dim3 grid((L.H3 + kTM - 1) / kTM, ntn, n_split);
   TraceScope trace("wgrad_simt", s);
   k_wgrad<T, DT, MODE><<<grid, 256, 0, s>>>(
       reinterpret_cast<const DT*>(a.ws + L.off_dA), static_cast<const T*>(a.x),
