@@ -119,16 +119,17 @@ def kernel_work(name, w, n_split):
 # sources they were taken from: KERNEL_SOURCE_HASH is the hash of
 # recurrent_cell_gb300/csrc/* and include/* at capture time, and any change to
 # those files makes `traffic` null until the captures are repeated.
-KERNEL_SOURCE_HASH = "4c47ec4ce271117b"
+KERNEL_SOURCE_HASH = "c4b27f74e97d06f4"
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): 885504,
+    ("smoke", "cfc_fwd_cluster"): 885248,
     ("smoke", "cfc_bwd_cluster"): 3412224,
-    ("mid", "cfc_fwd_tc"): 91352064,
-    ("mid", "cfc_bwd_cluster_tc"): 159193088,
-    ("mid", "wgrad_tc"): 154695936,
-    ("large", "cfc_fwd_stream_tc"): 196251392,
-    ("large", "cfc_bwd_tc"): 288088064,
-    ("large", "wgrad_tma_tc"): 154810624,
+    ("smoke", "wgrad_simt"): 4748544,
+    ("mid", "cfc_fwd_tc"): 91625216,
+    ("mid", "cfc_bwd_cluster_tc"): 159102464,
+    ("mid", "wgrad_tma_tf32"): 154297600,
+    ("large", "cfc_fwd_stream_tc"): 195872256,
+    ("large", "cfc_bwd_tc"): 287868672,
+    ("large", "wgrad_tma_tc"): 154775808,
 }
 
 
