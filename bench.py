@@ -119,7 +119,7 @@ def kernel_work(name, w, n_split):
 # sources they were taken from: KERNEL_SOURCE_HASH is the hash of
 # recurrent_cell_gb300/csrc/* and include/* at capture time, and any change to
 # those files makes `traffic` null until the captures are repeated.
-KERNEL_SOURCE_HASH = "c4b27f74e97d06f4"
+KERNEL_SOURCE_HASH = "0cd39563f54f148a"
 PROFILED_TRAFFIC = {
     ("smoke", "cfc_fwd_cluster"): 885248,
     ("smoke", "cfc_bwd_cluster"): 3412224,
@@ -350,6 +350,35 @@ def measure_workload(w, steps, warmup, device, peaks, flush, dist_ctx=None, with
     return out
 
 
+def measure_reduce_multi(steps, device, peaks, flush, B=32, count=17):
+    """count reducer calls of one training step (the pages' step makes 17, one
+    per scratch buffer) as count single reduce_axis0 launches and as one
+    reduce_axis0_multi call; [B, N_i] fp32 ~ N(0, 1), N_i in 4096 .. 20481."""
+    import torch
+    import recurrent_cell_gb300 as cfc
+    Ns = [4096 * (1 + i % 5) + (i % 3) for i in range(count)]
+    mats = [torch.from_numpy(wl.make_reduce_input(B, N, seed=1000 + i)).to(device) for i, N in enumerate(Ns)]
+    outs = [torch.empty(N, device=device) for N in Ns]
+
+    def singles():
+        for a, o in zip(mats, outs):
+            cfc.reduce_axis0(a, o)
+
+    def multi():
+        cfc.reduce_axis0_multi(mats, outs)
+
+    for _ in range(3):
+        singles()
+        multi()
+    torch.cuda.synchronize()
+    t1 = timed(torch, singles, steps, flush)
+    t2 = timed(torch, multi, steps, flush)
+    byts = 4.0 * sum(B * N + N for N in Ns)
+    ms1, ms2 = sum(t1) / len(t1), sum(t2) / len(t2)
+    return dict(B=B, count=count, N=Ns, bytes=byts, singles_ms=ms1, multi_ms=ms2,
+                multi_GBps=byts / (ms2 * 1e-3) / 1e9, frac_of_hbm=byts / (ms2 * 1e-3) / 1e9 / peaks["hbm"])
+
+
 def measure_graph(w, steps, device):
     """The same step launched eagerly and replayed from one CUDA graph captured
     through the C ABI (the calls allocate nothing and never synchronise)."""
@@ -537,6 +566,7 @@ def main():
         red = [measure_reduce(B, N, 20, device, peaks, flush)
                for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
         secondary["reduce_axis0"] = red
+        secondary["reduce_axis0_multi"] = measure_reduce_multi(20, device, peaks, flush)
         secondary["cuda_graph"] = {wl.SHORT_NAMES[n].name: measure_graph(wl.SHORT_NAMES[n], 50, device)
                                    for n in ("tiny", "smoke")}
     if rank == 0 and world == 1:

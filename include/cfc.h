@@ -7,7 +7,8 @@
  *                       run over K steps for B independent samples;
  *   cfc_kloop_backward  backward through time: parameter gradients summed over
  *                       the batch, grad_h0 and (optionally) grad_x;
- *   reduce_axis0        deterministic, atomic-free column sum [B, N] -> [N].
+ *   reduce_axis0        deterministic, atomic-free column sum [B, N] -> [N];
+ *   reduce_axis0_multi  the same for a list of matrices in few launches.
  *
  * Cell (per sample, step k = 0..K-1, heads c = f, g, h~ in that order):
  *   A_c    = b[c] + W_in[c] x_k + W_rec[c] h_k
@@ -156,6 +157,18 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
  * out must be 4-byte aligned and must not overlap (16-byte alignment and
  * n_tail % 4 == 0 select the float4 path; otherwise scalar, same order). */
 int reduce_axis0(const float* per_batch, int n_batch, long long n_tail, float* out, void* stream);
+
+/* reduce_axis0 for `count` independent matrices with one launch per kernel
+ * configuration (the pages' training step calls the reducer 17 times, once per
+ * scratch buffer: "K-loop Parallelization Implementation Plan", Self-Review).
+ * per_batch, n_batch, n_tail and out are HOST arrays of `count` entries; entry
+ * i is a device matrix [n_batch[i], n_tail[i]] and its device output
+ * out[i][n_tail[i]] (overwrite), with the rules of reduce_axis0.  Every out[i]
+ * receives exactly the bits reduce_axis0 would write.  0 <= count <= 4096;
+ * entries with n_tail 0 are skipped; matrices and outputs must not overlap.
+ * All entries are checked before anything is launched. */
+int reduce_axis0_multi(const float* const* per_batch, const int* n_batch, const long long* n_tail,
+                       float* const* out, int count, void* stream);
 
 /* Forward + backward without allocation.  This entry point has no counterpart
  * in the pages; it exists for callers that cannot allocate device memory

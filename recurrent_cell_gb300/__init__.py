@@ -54,6 +54,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cfc_kloop_backward.restype = i32
     lib.reduce_axis0.argtypes = [vp, i32, i64, vp, vp]
     lib.reduce_axis0.restype = i32
+    lib.reduce_axis0_multi.argtypes = [vp, vp, vp, vp, i32, vp]
+    lib.reduce_axis0_multi.restype = i32
     lib.cfc_kloop_forward_backward_static.argtypes = [vp] * 6 + [i32] * 6 + [vp] * 3 + [vp] * 6 + [vp]
     lib.cfc_kloop_forward_backward_static.restype = i32
     lib.cfc_kloop_grad_splits.argtypes = [i32] * 6
@@ -189,6 +191,29 @@ def reduce_axis0(per_batch, out, stream=None):
         _ptr(per_batch, "per_batch", torch.float32), B, N,
         _ptr(out, "out", torch.float32, (N,)), _stream(stream))
     _check("reduce_axis0", status)
+
+
+def reduce_axis0_multi(per_batch, out, stream=None):
+    """out[i][N_i] = column sums of per_batch[i][B_i, N_i] for every i, in few
+    launches; the same bits as reduce_axis0 on each pair."""
+    torch = _torch()
+    per_batch, out = list(per_batch), list(out)
+    if len(per_batch) != len(out):
+        raise ValueError("per_batch and out must have the same length")
+    n = len(per_batch)
+    ins = (ctypes.c_void_p * max(n, 1))()
+    outs = (ctypes.c_void_p * max(n, 1))()
+    nb = (ctypes.c_int * max(n, 1))()
+    nt = (ctypes.c_longlong * max(n, 1))()
+    for i, (a, o) in enumerate(zip(per_batch, out)):
+        if a.dim() != 2:
+            raise ValueError(f"per_batch[{i}] must be 2-D")
+        B, N = a.shape
+        ins[i] = _ptr(a, f"per_batch[{i}]", torch.float32)
+        outs[i] = _ptr(o, f"out[{i}]", torch.float32, (N,))
+        nb[i], nt[i] = B, N
+    status = load_library().reduce_axis0_multi(ins, nb, nt, outs, n, _stream(stream))
+    _check("reduce_axis0_multi", status)
 
 
 def cfc_kloop_forward_backward_static(x, h0, W_in, W_rec, b, dt, h_seq, grad_W_in, grad_W_rec,

@@ -280,4 +280,19 @@ int reduce_axis0(const float* per_batch, int n_batch, long long n_tail, float* o
   return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
 }
 
+int reduce_axis0_multi(const float* const* per_batch, const int* n_batch, const long long* n_tail,
+                       float* const* out, int count, void* stream) {
+  if (count < 0 || count > 4096) return CFC_ERR_SHAPE;
+  if (count == 0) return CFC_OK;
+  if (!per_batch || !n_batch || !n_tail || !out) return CFC_ERR_NULL;
+  for (int i = 0; i < count; ++i) {
+    if (n_batch[i] < 0 || n_tail[i] < 0 || n_tail[i] > (1ll << 35)) return CFC_ERR_SHAPE;
+    if (n_tail[i] == 0) continue;
+    if (!out[i] || (n_batch[i] > 0 && !per_batch[i])) return CFC_ERR_NULL;
+    if (!al4(out[i]) || (per_batch[i] && !al4(per_batch[i]))) return CFC_ERR_ALIGN;
+  }
+  cudaError_t e = launch_reduce_multi(per_batch, n_batch, n_tail, out, count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
+}
+
 }  // extern "C"

@@ -153,6 +153,10 @@ struct ReduceOut {
 
 cudaError_t launch_reduce(const float* in, int n_batch, long long n_tail, long long ld,
                           const ReduceOut& out, cudaStream_t stream);
+// count matrices (host arrays of device pointers and sizes, already checked),
+// one launch per kernel configuration and up to 32 matrices.
+cudaError_t launch_reduce_multi(const float* const* in, const int* n_batch, const long long* n_tail,
+                                float* const* out, int count, cudaStream_t stream);
 
 struct CfcArgs {
   const void* x; const void* h0; const void* W_in; const void* W_rec;

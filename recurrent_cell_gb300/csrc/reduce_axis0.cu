@@ -34,6 +34,7 @@ namespace cfc {
 namespace {
 
 constexpr int kWarps = 8;      // subtrees per block
+constexpr int kMultiMax = 32;  // matrices per launch of the multi-matrix kernel
 
 template <int VEC> struct Vec;
 template <> struct Vec<4> {
@@ -75,8 +76,8 @@ __device__ __forceinline__ float4 shfl_down(float4 v, int d) {
 // full 256-leaf tree.  Small batches therefore use small NL and spend the
 // lanes on more columns instead.
 template <int VEC, int LG, int LPG, int CPL>
-__global__ void __launch_bounds__(kWarps * 32, 3)
-k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, ReduceOut out) {
+__device__ __forceinline__ void reduce_block(const float* __restrict__ in, int B, long long N, long long ld,
+                                             const ReduceOut& out, long long block) {
   using V = Vec<VEC>;
   using T = typename V::T;
   constexpr int GW = 32 / LG;                 // column groups per warp and column set
@@ -96,7 +97,7 @@ k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, R
     for (int m = 0; m < LPG; ++m) t[m] = (int)(__brev((unsigned)(((w * LG + lg) * LPG + m) * LS)) >> 24);
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-      const long long col = (((long long)blockIdx.x * CPL + c) * GW + cg) * VEC;
+      const long long col = ((block * CPL + c) * GW + cg) * VEC;
 #pragma unroll
       for (int m = 0; m < LPG; ++m) {
         v[c][m] = V::zero();
@@ -110,7 +111,7 @@ k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, R
       for (int off = 256; off < B; off += 256) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          const long long col = (((long long)blockIdx.x * CPL + c) * GW + cg) * VEC;
+          const long long col = ((block * CPL + c) * GW + cg) * VEC;
 #pragma unroll
           for (int m = 0; m < LPG; ++m)
             if (col < N && t[m] + off < B) v[c][m] = V::add(v[c][m], V::load(in + (long long)(t[m] + off) * ld + col));
@@ -144,7 +145,7 @@ k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, R
   __syncthreads();
   // The 8 warps' subtrees.
   for (int e = threadIdx.x; e < GW * CPL; e += kWarps * 32) {
-    const long long col = ((long long)blockIdx.x * CPL * GW + e) * VEC;
+    const long long col = (block * CPL * GW + e) * VEC;
     if (col < N) {
       T s01 = V::add(part[0][e], part[1][e]);
       T s23 = V::add(part[2][e], part[3][e]);
@@ -153,6 +154,37 @@ k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, R
       *reinterpret_cast<T*>(seg_ptr(out, col)) = V::add(V::add(s01, s23), V::add(s45, s67));
     }
   }
+}
+
+template <int VEC, int LG, int LPG, int CPL>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+k_reduce_axis0(const float* __restrict__ in, int B, long long N, long long ld, ReduceOut out) {
+  reduce_block<VEC, LG, LPG, CPL>(in, B, N, ld, out, blockIdx.x);
+}
+
+// Several matrices in one launch: block b belongs to the matrix i with
+// block_begin[i] <= b < block_begin[i+1] and runs that matrix's block
+// b - block_begin[i], exactly as a single-matrix launch would.
+struct MultiTable {
+  int count;
+  long long block_begin[kMultiMax + 1];
+  const float* in[kMultiMax];
+  float* out[kMultiMax];
+  long long N[kMultiMax];
+  int B[kMultiMax];
+};
+
+template <int VEC, int LG, int LPG, int CPL>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+k_reduce_axis0_multi(const __grid_constant__ MultiTable t) {
+  const long long b = blockIdx.x;
+  int i = 0;
+  while (i + 1 < t.count && t.block_begin[i + 1] <= b) ++i;
+  ReduceOut o{};
+  o.nseg = 1;
+  o.ptr[0] = t.out[i];
+  o.begin[0] = 0;
+  reduce_block<VEC, LG, LPG, CPL>(t.in[i], t.B[i], t.N[i], t.N[i], o, b - t.block_begin[i]);
 }
 
 template <int VEC, int LG, int LPG, int CPL>
@@ -167,6 +199,35 @@ cudaError_t launch_cfg(const float* in, int n_batch, long long n_tail, long long
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+template <int VEC_, int LG_, int LPG_, int CPL_>
+struct Cfg {
+  static constexpr int VEC = VEC_, LG = LG_, LPG = LPG_, CPL = CPL_;
+};
+
+// Kernel configuration for a batch of n_batch rows: visited leaves NL >= B
+// (all 256 beyond 128 rows), 8 or more loads per lane in flight.  0-3: float4
+// rows; 4-7: scalar loads for ragged or unaligned rows.  The ragged choices
+// were measured (B = 1024, N = 40961: 4 lane groups of 8 leaves and 2 column
+// sets, 58 us, against 67-82 us for one 32-leaf group or 2 groups of 16).
+int reduce_config(int n_batch, bool vec) {
+  const int band = n_batch > 128 ? 0 : n_batch > 64 ? 1 : n_batch > 32 ? 2 : 3;
+  return (vec ? 0 : 4) + band;
+}
+
+template <typename F>
+cudaError_t with_config(int cfg, F&& f) {
+  switch (cfg) {
+    case 0: return f(Cfg<4, 4, 8, 1>{});
+    case 1: return f(Cfg<4, 4, 4, 2>{});
+    case 2: return f(Cfg<4, 4, 2, 4>{});
+    case 3: return f(Cfg<4, 4, 1, 8>{});
+    case 4: return f(Cfg<1, 4, 8, 2>{});
+    case 5: return f(Cfg<1, 1, 16, 1>{});
+    case 6: return f(Cfg<1, 1, 8, 1>{});
+    default: return f(Cfg<1, 1, 4, 2>{});
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_reduce(const float* in, int n_batch, long long n_tail, long long ld,
@@ -175,20 +236,51 @@ cudaError_t launch_reduce(const float* in, int n_batch, long long n_tail, long l
   bool vec = (n_tail % 4 == 0) && (ld % 4 == 0) && aligned16(in);
   for (int s = 0; s < out.nseg; ++s) vec = vec && aligned16(out.ptr[s]) && (out.begin[s] % 4 == 0);
   TraceScope trace("reduce_axis0", stream);
-  // Visited leaves NL >= B (all 256 beyond 128 rows); 8 or more loads per lane in flight.
-  if (vec) {
-    if (n_batch > 128) return launch_cfg<4, 4, 8, 1>(in, n_batch, n_tail, ld, out, stream);
-    if (n_batch > 64) return launch_cfg<4, 4, 4, 2>(in, n_batch, n_tail, ld, out, stream);
-    if (n_batch > 32) return launch_cfg<4, 4, 2, 4>(in, n_batch, n_tail, ld, out, stream);
-    return launch_cfg<4, 4, 1, 8>(in, n_batch, n_tail, ld, out, stream);
+  return with_config(reduce_config(n_batch, vec), [&](auto c) {
+    using C = decltype(c);
+    return launch_cfg<C::VEC, C::LG, C::LPG, C::CPL>(in, n_batch, n_tail, ld, out, stream);
+  });
+}
+
+cudaError_t launch_reduce_multi(const float* const* in, const int* n_batch, const long long* n_tail,
+                                float* const* out, int count, cudaStream_t stream) {
+  // Matrices grouped by kernel configuration, in their given order; each group
+  // in launches of up to kMultiMax matrices (and fewer than 2^31 blocks).
+  TraceScope trace("reduce_axis0_multi", stream);
+  for (int cfg = 0; cfg < 8; ++cfg) {
+    cudaError_t e = with_config(cfg, [&](auto c) -> cudaError_t {
+      using C = decltype(c);
+      constexpr int GW = 32 / C::LG;
+      MultiTable t{};
+      auto flush = [&]() -> cudaError_t {
+        if (t.count == 0) return cudaSuccess;
+        const long long blocks = t.block_begin[t.count];
+        k_reduce_axis0_multi<C::VEC, C::LG, C::LPG, C::CPL><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(t);
+        t.count = 0;
+        return cudaGetLastError();
+      };
+      for (int i = 0; i < count; ++i) {
+        if (n_tail[i] <= 0) continue;
+        const bool vec = (n_tail[i] % 4 == 0) && aligned16(in[i]) && aligned16(out[i]);
+        if (reduce_config(n_batch[i], vec) != cfg) continue;
+        const long long groups = (n_tail[i] + C::VEC - 1) / C::VEC;
+        const long long blocks = (groups + (long long)GW * C::CPL - 1) / ((long long)GW * C::CPL);
+        if (t.count == kMultiMax || t.block_begin[t.count] + blocks > 0x7fffffffll) {
+          cudaError_t fe = flush();
+          if (fe != cudaSuccess) return fe;
+        }
+        const int j = t.count++;
+        t.in[j] = in[i];
+        t.out[j] = out[i];
+        t.N[j] = n_tail[i];
+        t.B[j] = n_batch[i];
+        t.block_begin[j + 1] = t.block_begin[j] + blocks;
+      }
+      return flush();
+    });
+    if (e != cudaSuccess) return e;
   }
-  // Ragged rows (scalar loads).  The configurations were chosen by measurement
-  // (B = 1024, N = 40961: 4 lane groups of 8 leaves and 2 column sets, 58 us,
-  // against 67-82 us for one 32-leaf group or 2 groups of 16).
-  if (n_batch > 128) return launch_cfg<1, 4, 8, 2>(in, n_batch, n_tail, ld, out, stream);
-  if (n_batch > 64) return launch_cfg<1, 1, 16, 1>(in, n_batch, n_tail, ld, out, stream);
-  if (n_batch > 32) return launch_cfg<1, 1, 8, 1>(in, n_batch, n_tail, ld, out, stream);
-  return launch_cfg<1, 1, 4, 2>(in, n_batch, n_tail, ld, out, stream);
+  return cudaSuccess;
 }
 
 }  // namespace cfc

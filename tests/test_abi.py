@@ -117,3 +117,25 @@ def test_reduce_argument_validation(lib):
     assert lib.reduce_axis0(None, 4, 10, P, None) == ERR_NULL
     assert lib.reduce_axis0(P, 4, 10, None, None) == ERR_NULL
     assert lib.reduce_axis0(P + 2, 4, 10, P, None) == ERR_ALIGN
+
+
+def test_reduce_multi_argument_validation(lib):
+    """Every entry is checked before anything is launched (no GPU needed)."""
+    def call(ins, nbs, nts, outs, count=None):
+        n = len(ins)
+        a_in = (ctypes.c_void_p * max(n, 1))(*ins)
+        a_out = (ctypes.c_void_p * max(n, 1))(*outs)
+        a_nb = (ctypes.c_int * max(n, 1))(*nbs)
+        a_nt = (ctypes.c_longlong * max(n, 1))(*nts)
+        return lib.reduce_axis0_multi(a_in, a_nb, a_nt, a_out, n if count is None else count, None)
+    assert call([], [], [], []) == 0                                   # nothing to do
+    assert call([P], [4], [0], [P]) == 0                               # empty tail: skipped
+    assert call([P], [4], [10], [P], count=-1) == ERR_SHAPE
+    assert call([P], [4], [10], [P], count=5000) == ERR_SHAPE
+    assert lib.reduce_axis0_multi(None, None, None, None, 1, None) == ERR_NULL
+    assert call([P, P], [4, -1], [10, 10], [P, P]) == ERR_SHAPE        # second entry bad
+    assert call([P, P], [4, 4], [10, (1 << 35) + 1], [P, P]) == ERR_SHAPE
+    assert call([P, None], [4, 4], [10, 10], [P, P]) == ERR_NULL
+    assert call([P, P], [4, 4], [10, 10], [P, None]) == ERR_NULL
+    assert call([P, P + 2], [4, 4], [10, 10], [P, P]) == ERR_ALIGN
+    assert call([P, P], [4, 4], [10, 10], [P, P + 1]) == ERR_ALIGN

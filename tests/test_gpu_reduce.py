@@ -100,3 +100,38 @@ def test_run_to_run_bit_identical():
             ref = cur
         else:
             np.testing.assert_array_equal(cur, ref)
+
+
+MULTI_SHAPES = [(1024, 40960), (256, 40961), (32, 4096), (0, 100), (7, 1), (300, 131), (129, 5),
+                (64, 1027), (1, 37), (2049, 77), (33, 4), (100, 515), (1031, 8)]
+
+
+@pytest.mark.parametrize("repeat", [1, 4])          # 13 or 52 matrices (more than one launch's table)
+def test_multi_matches_single_calls_bitwise(repeat):
+    """reduce_axis0_multi over a mixed list (float4 and scalar configurations,
+    every batch band, empty batch, ragged and unaligned rows) gives, for every
+    matrix, the oracle's bits."""
+    torch = torch_mod()
+    shapes = MULTI_SHAPES * repeat
+    mats, outs, refs = [], [], []
+    for i, (B, N) in enumerate(shapes):
+        a = wl.make_reduce_input(B, N, seed=97 * i + B)
+        off = i % 3                                      # some inputs not 16-byte aligned
+        flat = torch.full((off + B * N,), float("nan"), device="cuda")
+        flat[off:] = dev(a.reshape(-1))
+        mats.append(flat[off:].view(B, N))
+        outs.append(torch.full((N,), float("nan"), device="cuda"))
+        refs.append(oracle.reduce_axis0(a))
+    cfc.reduce_axis0_multi(mats, outs)
+    torch.cuda.synchronize()
+    for i, (o, ref) in enumerate(zip(outs, refs)):
+        np.testing.assert_array_equal(bits(o.cpu().numpy()), bits(ref), err_msg=f"matrix {i} {shapes[i]}")
+
+
+def test_multi_empty_list_and_single_entry():
+    torch = torch_mod()
+    cfc.reduce_axis0_multi([], [])
+    a = wl.make_reduce_input(256, 40960, seed=1)
+    out = torch.empty(40960, device="cuda")
+    cfc.reduce_axis0_multi([dev(a)], [out])
+    np.testing.assert_array_equal(bits(out.cpu().numpy()), bits(oracle.reduce_axis0(a)))
