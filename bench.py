@@ -119,7 +119,7 @@ def kernel_work(name, w, n_split):
 # sources they were taken from: KERNEL_SOURCE_HASH is the hash of
 # recurrent_cell_gb300/csrc/* and include/* at capture time, and any change to
 # those files makes `traffic` null until the captures are repeated.
-KERNEL_SOURCE_HASH = "0cd39563f54f148a"
+KERNEL_SOURCE_HASH = "c59d05a080876dc4"
 PROFILED_TRAFFIC = {
     ("smoke", "cfc_fwd_cluster"): 885248,
     ("smoke", "cfc_bwd_cluster"): 3412224,
@@ -350,6 +350,48 @@ def measure_workload(w, steps, warmup, device, peaks, flush, dist_ctx=None, with
     return out
 
 
+def measure_tau(w, steps, warmup, device, peaks, flush):
+    """The pages' single-head tau-cell K loop (FP32): forward + backward with
+    the y loss seed, per-sample rows summed by reduce_axis0.  Roofline of the
+    dominant kernel against the FFMA peak: forward 2 H (n_in + H) flop per
+    sample-step; backward 2 H (n_in + H) (gradient rows) + 2 H H (carry)."""
+    import torch
+    import recurrent_cell_gb300 as cfc
+    inp = wl.make_tau_inputs(w)
+    t = {k: torch.from_numpy(v).to(device) for k, v in inp.items()}
+    B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+    ws = torch.empty(cfc.cfc_tau_kloop_workspace_bytes(B, K, n_in, H), dtype=torch.uint8, device=device)
+    h_seq = torch.empty(B, K, H, device=device)
+    g = [torch.empty(H, n_in, device=device), torch.empty(H, H, device=device), torch.empty(H, device=device),
+         torch.empty(H, device=device)]
+    scratch = torch.empty(B, cfc.cfc_tau_per_sample_length(n_in, H), device=device)
+
+    def step():
+        cfc.cfc_tau_kloop_forward(t["x"], t["h0"], t["W_in"], t["W_rec"], t["b"], t["tau"], t["dt"], h_seq, ws)
+        cfc.cfc_tau_kloop_backward(t["x"], t["h0"], t["W_in"], t["W_rec"], t["b"], t["tau"], t["dt"], h_seq,
+                                   *g, scratch, ws, y=t["y"])
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    cfc.cfc_trace_enable(True)
+    ms = timed(torch, step, steps, flush)
+    records = cfc.cfc_trace_records()
+    cfc.cfc_trace_enable(False)
+    kernels = summarize_trace(records, steps)
+    ms_step = sum(ms) / len(ms)
+    Zc = n_in + H
+    flops = {"tau_fwd": 2.0 * H * Zc * B * K, "tau_bwd": (2.0 * H * Zc + 2.0 * H * H) * B * K}
+    top = max((n for n in kernels if n in flops), key=lambda n: kernels[n]["ms_total"])
+    achieved = flops[top] / (kernels[top]["avg_ms"] * 1e-3) / 1e12
+    peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+    return dict(workload=w.name, value=B * K / (ms_step * 1e-3), unit=UNIT, ms_per_step=ms_step,
+                kernels=kernels,
+                roofline=dict(kernel=top, bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s",
+                              frac=achieved / peak,
+                              peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"))
+
+
 def measure_reduce_multi(steps, device, peaks, flush, B=32, count=17):
     """count reducer calls of one training step (the pages' step makes 17, one
     per scratch buffer) as count single reduce_axis0 launches and as one
@@ -567,6 +609,7 @@ def main():
                for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
         secondary["reduce_axis0"] = red
         secondary["reduce_axis0_multi"] = measure_reduce_multi(20, device, peaks, flush)
+        secondary["tau_cell"] = measure_tau(wl.TAU_SMOKE, 30, 3, device, peaks, flush)
         secondary["cuda_graph"] = {wl.SHORT_NAMES[n].name: measure_graph(wl.SHORT_NAMES[n], 50, device)
                                    for n in ("tiny", "smoke")}
     if rank == 0 and world == 1:

@@ -8,7 +8,8 @@
  *   cfc_kloop_backward  backward through time: parameter gradients summed over
  *                       the batch, grad_h0 and (optionally) grad_x;
  *   reduce_axis0        deterministic, atomic-free column sum [B, N] -> [N];
- *   reduce_axis0_multi  the same for a list of matrices in few launches.
+ *   reduce_axis0_multi  the same for a list of matrices in few launches;
+ *   cfc_tau_kloop_*     the pages' single-head tau-cell K loop (FP32).
  *
  * Cell (per sample, step k = 0..K-1, heads c = f, g, h~ in that order):
  *   A_c    = b[c] + W_in[c] x_k + W_rec[c] h_k
@@ -157,6 +158,50 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
  * out must be 4-byte aligned and must not overlap (16-byte alignment and
  * n_tail % 4 == 0 select the float4 path; otherwise scalar, same order). */
 int reduce_axis0(const float* per_batch, int n_batch, long long n_tail, float* out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The pages' single-head tau-cell ("K-loop Parallelization Implementation
+ * Plan", Task 2: cfc_step_batched, Task 3: cfc_step_backward_batched), FP32:
+ *   pre = b + W_in x_k + W_rec h_k,  s = tanh(pre),
+ *   decay_i = exp(-dt / max(tau_i, 1e-6)),  h_{k+1} = h_k * decay + (1 - decay) * s,
+ *   h_seq[:, k] = h_{k+1}.
+ * Backward (dh = gradient reaching h_{k+1}): d_pre = dh (1 - decay)(1 - s^2);
+ * gb += d_pre, gW_in += d_pre (x) x_k, gW_rec += d_pre (x) h_k,
+ * gtau += dh (h_k - s) decay dt / max(tau, 1e-6)^2 where tau > 1e-6 (else 0);
+ * grad h_k = W_rec^T d_pre + dh decay, grad x_k = W_in^T d_pre.
+ * Shapes: x [B, K, n_in], h0 [B, n_hid], W_in [n_hid, n_in], W_rec [n_hid, n_hid],
+ * b [n_hid], tau [n_hid], dt [B] (dt_stride 1) or [1] (dt_stride 0).  Every
+ * pointer 16-byte aligned.  Sizes: 1 <= n_in, n_hid <= 1024 and the sample's
+ * weights and gradient, 2 n_hid ((n_in + n_hid) | 1) floats, within one SM's
+ * shared memory (about 28 K floats each; n_in = 64, n_hid = 128 fits) —
+ * otherwise CFC_ERR_SHAPE. */
+
+/* Packed per-sample gradient length (n_in + n_hid + 2) * n_hid, layout
+ * [gW_in (i, j) | gW_rec (i, j) | gb (i) | gtau (i)]; 0 if unsupported. */
+long long cfc_tau_per_sample_length(int n_in, int n_hid);
+
+/* Workspace bytes of the tau-cell forward/backward pair (the saved s values),
+ * 0 for unsupported sizes. */
+size_t cfc_tau_kloop_workspace_bytes(int B, int K, int n_in, int n_hid);
+
+/* Forward K loop: h_seq [B, K, n_hid] (overwrite) and s in the workspace. */
+int cfc_tau_kloop_forward(const float* x, const float* h0, const float* W_in, const float* W_rec, const float* b,
+                          const float* tau, const float* dt, int dt_stride, int B, int K, int n_in, int n_hid,
+                          float* h_seq, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward through the K loop of the forward that filled `workspace`.
+ * Upstream gradients as for cfc_kloop_backward (at least one of grad_h_seq
+ * [B, K, n_hid], grad_h_last [B, n_hid], y [B, n_hid]).  Outputs (overwrite):
+ * grad_W_in [n_hid, n_in], grad_W_rec [n_hid, n_hid], grad_b [n_hid],
+ * grad_tau [n_hid] summed over the batch by reduce_axis0 from
+ * per_sample_scratch [B, cfc_tau_per_sample_length] (written, required);
+ * grad_h0 [B, n_hid] and grad_x [B, K, n_in] optional (NULL). */
+int cfc_tau_kloop_backward(const float* x, const float* h0, const float* W_in, const float* W_rec,
+                           const float* b, const float* tau, const float* dt, int dt_stride, int B, int K,
+                           int n_in, int n_hid, const float* h_seq, const float* grad_h_seq,
+                           const float* grad_h_last, const float* y, float* grad_W_in, float* grad_W_rec,
+                           float* grad_b, float* grad_tau, float* grad_h0, float* grad_x,
+                           float* per_sample_scratch, void* workspace, size_t workspace_bytes, void* stream);
 
 /* reduce_axis0 for `count` independent matrices with one launch per kernel
  * configuration (the pages' training step calls the reducer 17 times, once per

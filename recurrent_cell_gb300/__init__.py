@@ -56,6 +56,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.reduce_axis0.restype = i32
     lib.reduce_axis0_multi.argtypes = [vp, vp, vp, vp, i32, vp]
     lib.reduce_axis0_multi.restype = i32
+    lib.cfc_tau_per_sample_length.argtypes = [i32, i32]
+    lib.cfc_tau_per_sample_length.restype = i64
+    lib.cfc_tau_kloop_workspace_bytes.argtypes = [i32] * 4
+    lib.cfc_tau_kloop_workspace_bytes.restype = sz
+    lib.cfc_tau_kloop_forward.argtypes = [vp] * 7 + [i32] * 5 + [vp, vp, sz, vp]
+    lib.cfc_tau_kloop_forward.restype = i32
+    lib.cfc_tau_kloop_backward.argtypes = [vp] * 7 + [i32] * 5 + [vp] * 4 + [vp] * 7 + [vp, sz, vp]
+    lib.cfc_tau_kloop_backward.restype = i32
     lib.cfc_kloop_forward_backward_static.argtypes = [vp] * 6 + [i32] * 6 + [vp] * 3 + [vp] * 6 + [vp]
     lib.cfc_kloop_forward_backward_static.restype = i32
     lib.cfc_kloop_grad_splits.argtypes = [i32] * 6
@@ -191,6 +199,58 @@ def reduce_axis0(per_batch, out, stream=None):
         _ptr(per_batch, "per_batch", torch.float32), B, N,
         _ptr(out, "out", torch.float32, (N,)), _stream(stream))
     _check("reduce_axis0", status)
+
+
+def cfc_tau_per_sample_length(n_in: int, n_hid: int) -> int:
+    return int(load_library().cfc_tau_per_sample_length(n_in, n_hid))
+
+
+def cfc_tau_kloop_workspace_bytes(B: int, K: int, n_in: int, n_hid: int) -> int:
+    return int(load_library().cfc_tau_kloop_workspace_bytes(B, K, n_in, n_hid))
+
+
+def cfc_tau_kloop_forward(x, h0, W_in, W_rec, b, tau, dt, h_seq, workspace, stream=None):
+    """tau-cell forward K loop (float32): writes h_seq [B, K, n_hid] and the
+    saved activations in ``workspace``."""
+    torch = _torch()
+    f32 = torch.float32
+    B, K, n_in = x.shape
+    H = h0.shape[1]
+    dt_stride = 0 if dt.numel() == 1 else 1
+    status = load_library().cfc_tau_kloop_forward(
+        _ptr(x, "x", f32, (B, K, n_in)), _ptr(h0, "h0", f32, (B, H)), _ptr(W_in, "W_in", f32, (H, n_in)),
+        _ptr(W_rec, "W_rec", f32, (H, H)), _ptr(b, "b", f32, (H,)), _ptr(tau, "tau", f32, (H,)),
+        _ptr(dt, "dt", f32, (B,) if dt_stride else None), dt_stride, B, K, n_in, H,
+        _ptr(h_seq, "h_seq", f32, (B, K, H)), _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check("cfc_tau_kloop_forward", status)
+
+
+def cfc_tau_kloop_backward(x, h0, W_in, W_rec, b, tau, dt, h_seq, grad_W_in, grad_W_rec, grad_b, grad_tau,
+                           per_sample_scratch, workspace, grad_h_seq=None, grad_h_last=None, y=None,
+                           grad_h0=None, grad_x=None, stream=None):
+    """Backward through the tau-cell K loop of the forward that filled ``workspace``."""
+    torch = _torch()
+    f32 = torch.float32
+    B, K, n_in = x.shape
+    H = h0.shape[1]
+    N = (n_in + H + 2) * H
+    dt_stride = 0 if dt.numel() == 1 else 1
+    status = load_library().cfc_tau_kloop_backward(
+        _ptr(x, "x", f32, (B, K, n_in)), _ptr(h0, "h0", f32, (B, H)), _ptr(W_in, "W_in", f32, (H, n_in)),
+        _ptr(W_rec, "W_rec", f32, (H, H)), _ptr(b, "b", f32, (H,)), _ptr(tau, "tau", f32, (H,)),
+        _ptr(dt, "dt", f32, (B,) if dt_stride else None), dt_stride, B, K, n_in, H,
+        _ptr(h_seq, "h_seq", f32, (B, K, H)),
+        _ptr(grad_h_seq, "grad_h_seq", f32, (B, K, H), optional=True),
+        _ptr(grad_h_last, "grad_h_last", f32, (B, H), optional=True),
+        _ptr(y, "y", f32, (B, H), optional=True),
+        _ptr(grad_W_in, "grad_W_in", f32, (H, n_in)), _ptr(grad_W_rec, "grad_W_rec", f32, (H, H)),
+        _ptr(grad_b, "grad_b", f32, (H,)), _ptr(grad_tau, "grad_tau", f32, (H,)),
+        _ptr(grad_h0, "grad_h0", f32, (B, H), optional=True),
+        _ptr(grad_x, "grad_x", f32, (B, K, n_in), optional=True),
+        _ptr(per_sample_scratch, "per_sample_scratch", f32, (B, N)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check("cfc_tau_kloop_backward", status)
 
 
 def reduce_axis0_multi(per_batch, out, stream=None):

@@ -280,6 +280,62 @@ int reduce_axis0(const float* per_batch, int n_batch, long long n_tail, float* o
   return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
 }
 
+long long cfc_tau_per_sample_length(int n_in, int n_hid) {
+  if (!tau_shape_supported(n_in, n_hid)) return 0;
+  return (long long)(n_in + n_hid + 2) * n_hid;
+}
+
+size_t cfc_tau_kloop_workspace_bytes(int B, int K, int n_in, int n_hid) {
+  if (B < 1 || K < 1 || !tau_shape_supported(n_in, n_hid)) return 0;
+  return align256((size_t)B * K * n_hid * sizeof(float));
+}
+
+static int tau_check(const void* const* ptrs, int n, int B, int K, int n_in, int n_hid, int dt_stride,
+                     const void* workspace, size_t workspace_bytes) {
+  if (B < 1 || K < 1 || !tau_shape_supported(n_in, n_hid)) return CFC_ERR_SHAPE;
+  if ((long long)B * K * (n_in > n_hid ? n_in : n_hid) > (1ll << 40)) return CFC_ERR_SHAPE;
+  if (dt_stride != 0 && dt_stride != 1) return CFC_ERR_SHAPE;
+  for (int i = 0; i < n; ++i)
+    if (!ptrs[i]) return CFC_ERR_NULL;
+  for (int i = 0; i < n; ++i)
+    if (!al16(ptrs[i])) return CFC_ERR_ALIGN;
+  if (!workspace || workspace_bytes < cfc_tau_kloop_workspace_bytes(B, K, n_in, n_hid)) return CFC_ERR_WORKSPACE;
+  if (!al16(workspace)) return CFC_ERR_ALIGN;
+  return CFC_OK;
+}
+
+int cfc_tau_kloop_forward(const float* x, const float* h0, const float* W_in, const float* W_rec, const float* b,
+                          const float* tau, const float* dt, int dt_stride, int B, int K, int n_in, int n_hid,
+                          float* h_seq, void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {x, h0, W_in, W_rec, b, tau, dt, h_seq};
+  const int st = tau_check(ptrs, 8, B, K, n_in, n_hid, dt_stride, workspace, workspace_bytes);
+  if (st != CFC_OK) return st;
+  cudaError_t e = launch_tau_forward(x, h0, W_in, W_rec, b, tau, dt, dt_stride, B, K, n_in, n_hid, h_seq,
+                                     static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
+}
+
+int cfc_tau_kloop_backward(const float* x, const float* h0, const float* W_in, const float* W_rec,
+                           const float* b, const float* tau, const float* dt, int dt_stride, int B, int K,
+                           int n_in, int n_hid, const float* h_seq, const float* grad_h_seq,
+                           const float* grad_h_last, const float* y, float* grad_W_in, float* grad_W_rec,
+                           float* grad_b, float* grad_tau, float* grad_h0, float* grad_x,
+                           float* per_sample_scratch, void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {x, h0, W_in, W_rec, b, tau, dt, h_seq, grad_W_in, grad_W_rec, grad_b, grad_tau,
+                        per_sample_scratch};
+  const int st = tau_check(ptrs, 13, B, K, n_in, n_hid, dt_stride, workspace, workspace_bytes);
+  if (st != CFC_OK) return st;
+  if (!grad_h_seq && !grad_h_last && !y) return CFC_ERR_NULL;
+  const void* opt[] = {grad_h_seq, grad_h_last, y, grad_h0, grad_x};
+  for (const void* p : opt)
+    if (p && !al16(p)) return CFC_ERR_ALIGN;
+  cudaError_t e = launch_tau_backward(x, h0, W_in, W_rec, tau, dt, dt_stride, B, K, n_in, n_hid, h_seq,
+                                      static_cast<const float*>(workspace), grad_h_seq, grad_h_last, y,
+                                      per_sample_scratch, grad_h0, grad_x, grad_W_in, grad_W_rec, grad_b,
+                                      grad_tau, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
+}
+
 int reduce_axis0_multi(const float* const* per_batch, const int* n_batch, const long long* n_tail,
                        float* const* out, int count, void* stream) {
   if (count < 0 || count > 4096) return CFC_ERR_SHAPE;

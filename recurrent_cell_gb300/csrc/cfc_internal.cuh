@@ -146,13 +146,25 @@ struct TraceScope {
 // Launchers (return cudaError_t of the launch).
 // ---------------------------------------------------------------------------
 struct ReduceOut {
-  float* ptr[3];
-  long long begin[3];
+  float* ptr[4];
+  long long begin[4];
   int nseg;
 };
 
 cudaError_t launch_reduce(const float* in, int n_batch, long long n_tail, long long ld,
                           const ReduceOut& out, cudaStream_t stream);
+// tau-cell K loop (cfc_tau.cu), FP32.
+bool tau_shape_supported(int n_in, int n_hid);
+cudaError_t launch_tau_forward(const float* x, const float* h0, const float* W_in, const float* W_rec,
+                               const float* b, const float* tau, const float* dt, int dt_stride, int B, int K,
+                               int n_in, int H, float* h_seq, float* s_ws, cudaStream_t s);
+cudaError_t launch_tau_backward(const float* x, const float* h0, const float* W_in, const float* W_rec,
+                                const float* tau, const float* dt, int dt_stride, int B, int K, int n_in, int H,
+                                const float* h_seq, const float* s_ws, const float* grad_h_seq,
+                                const float* grad_h_last, const float* y, float* per_sample, float* grad_h0,
+                                float* grad_x, float* grad_W_in, float* grad_W_rec, float* grad_b,
+                                float* grad_tau, cudaStream_t s);
+
 // count matrices (host arrays of device pointers and sizes, already checked),
 // one launch per kernel configuration and up to 32 matrices.
 cudaError_t launch_reduce_multi(const float* const* in, const int* n_batch, const long long* n_tail,

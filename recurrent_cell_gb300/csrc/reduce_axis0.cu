@@ -58,6 +58,7 @@ __device__ __forceinline__ float* seg_ptr(const ReduceOut& o, long long col) {
   int s = 0;
   if (o.nseg > 1 && col >= o.begin[1]) s = 1;
   if (o.nseg > 2 && col >= o.begin[2]) s = 2;
+  if (o.nseg > 3 && col >= o.begin[3]) s = 3;
   return o.ptr[s] + (col - o.begin[s]);
 }
 

@@ -106,3 +106,29 @@ def make_reduce_input(B: int, N: int, seed: int = 0) -> np.ndarray:
     """[B, N] float32 ~ N(0, 1) for the standalone reduce_axis0 cases."""
     rng = np.random.default_rng(seed)
     return rng.standard_normal((B, N), dtype=np.float32)
+
+
+# The pages' single-head tau-cell, FP32, on the tiny and smoke shapes: x, h0 ~
+# N(0, 1); W_in ~ U(+-1/sqrt(n_in)), W_rec ~ U(+-1/sqrt(n_hid)); b = 0;
+# tau ~ U(0.5, 2.0) per unit; dt = 1.0 (or U(0.5, 1.5) per sample); y ~ N(0, 1).
+TAU_TINY = Workload("tau_tiny_B4_K8_16x32_fp32", B=4, K=8, n_in=16, n_hid=32)
+TAU_SMOKE = Workload("tau_smoke_B32_K64_64x128_fp32", B=32, K=64, n_in=64, n_hid=128)
+
+
+def make_tau_inputs(w: Workload, seed: int | None = None) -> dict:
+    """Draw the inputs of a tau-cell workload (all float32 numpy arrays)."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+    x = rng.standard_normal((B, K, n_in), dtype=np.float64).astype(np.float32)
+    h0 = (rng.standard_normal((B, H), dtype=np.float64) * w.h0_std).astype(np.float32)
+    a_in, a_rec = 1.0 / np.sqrt(n_in), 1.0 / np.sqrt(H)
+    W_in = rng.uniform(-a_in, a_in, size=(H, n_in)).astype(np.float32)
+    W_rec = rng.uniform(-a_rec, a_rec, size=(H, H)).astype(np.float32)
+    tau = rng.uniform(0.5, 2.0, size=(H,)).astype(np.float32)
+    y = rng.standard_normal((B, H), dtype=np.float64).astype(np.float32)
+    if w.dt_per_sample:
+        dt = rng.uniform(0.5, 1.5, size=(B,)).astype(np.float32)
+    else:
+        dt = np.full((1,), 1.0, dtype=np.float32)
+    b = np.zeros((H,), dtype=np.float32)
+    return dict(x=x, h0=h0, W_in=W_in, W_rec=W_rec, b=b, tau=tau, dt=dt, y=y)

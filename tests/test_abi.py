@@ -139,3 +139,30 @@ def test_reduce_multi_argument_validation(lib):
     assert call([P, P], [4, 4], [10, 10], [P, None]) == ERR_NULL
     assert call([P, P + 2], [4, 4], [10, 10], [P, P]) == ERR_ALIGN
     assert call([P, P], [4, 4], [10, 10], [P, P + 1]) == ERR_ALIGN
+
+
+def test_tau_argument_validation(lib):
+    """tau-cell entry points reject bad arguments before launching anything."""
+    B, K, n_in, H = 4, 8, 16, 32
+    ws = lib.cfc_tau_kloop_workspace_bytes(B, K, n_in, H)
+    assert ws >= B * K * H * 4 and ws % 256 == 0
+    assert lib.cfc_tau_per_sample_length(n_in, H) == (n_in + H + 2) * H
+    assert lib.cfc_tau_kloop_workspace_bytes(B, K, 64, 300) == 0         # exceeds one SM's shared memory
+    assert lib.cfc_tau_kloop_workspace_bytes(0, K, n_in, H) == 0
+
+    def fwd(x=P, dt_stride=0, Hh=H, ws_bytes=ws, ws_ptr=P):
+        return lib.cfc_tau_kloop_forward(x, P, P, P, P, P, P, dt_stride, B, K, n_in, Hh, P, ws_ptr, ws_bytes, None)
+    assert fwd(x=None) == ERR_NULL
+    assert fwd(x=P + 4) == ERR_ALIGN
+    assert fwd(dt_stride=2) == ERR_SHAPE
+    assert fwd(Hh=0) == ERR_SHAPE
+    assert fwd(ws_bytes=ws - 1) == ERR_WORKSPACE
+    assert fwd(ws_ptr=None) == ERR_WORKSPACE
+
+    def bwd(y=P, gtau=P, scratch=P, gx=None):
+        return lib.cfc_tau_kloop_backward(P, P, P, P, P, P, P, 0, B, K, n_in, H, P, None, None, y,
+                                          P, P, P, gtau, None, gx, scratch, P, ws, None)
+    assert bwd(y=None) == ERR_NULL                        # no upstream gradient
+    assert bwd(gtau=None) == ERR_NULL
+    assert bwd(scratch=None) == ERR_NULL
+    assert bwd(gx=P + 8) == ERR_ALIGN
