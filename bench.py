@@ -513,7 +513,9 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reduce-only", action="store_true",
-                    help="time only the standalone reduce_axis0 cases (profiling aid)")
+                    help="time only the standalone reduce_axis0 cases and the multi-matrix reducer (profiling aid)")
+    ap.add_argument("--tau-only", action="store_true",
+                    help="time only the tau-cell K loop on the smoke shape (profiling aid)")
     args = ap.parse_args()
     w = wl.SHORT_NAMES[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -571,8 +573,12 @@ def main():
     if args.reduce_only:
         red = [measure_reduce(B, N, args.steps, device, peaks, flush)
                for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
+        multi = measure_reduce_multi(args.steps, device, peaks, flush)
         print(json.dumps(dict(metric="reduce_axis0 GB/s", unit="GB/s", steps=args.steps,
-                              results=red, peak_hbm_gbs=peaks["hbm"])))
+                              results=red, multi=multi, peak_hbm_gbs=peaks["hbm"])))
+        return 0
+    if args.tau_only:
+        print(json.dumps(measure_tau(wl.TAU_SMOKE, args.steps, args.warmup, device, peaks, flush)))
         return 0
 
     props = torch.cuda.get_device_properties(device)
