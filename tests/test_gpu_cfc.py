@@ -147,6 +147,10 @@ EDGE = [
     wl.Workload("edge_tcs_bf16_H200", B=150, K=3, n_in=40, n_hid=200, math=wl.MATH_BF16,
                 dt_per_sample=True),
     wl.Workload("edge_tcs_tf32_H160", B=70, K=4, n_in=24, n_hid=160, math=wl.MATH_TF32),
+    # three and four unit blocks: a second half of two blocks, longer schedules
+    wl.Workload("edge_tcs_bf16_H384", B=70, K=3, n_in=64, n_hid=384, math=wl.MATH_BF16,
+                dt_per_sample=True),
+    wl.Workload("edge_tcs_bf16_H512", B=40, K=2, n_in=64, n_hid=512, math=wl.MATH_BF16),
     # TMA-fed weight gradient (bf16, GEMM path): 64 steps of one sample per
     # chunk with a ragged 3H tile, and whole samples per chunk
     wl.Workload("edge_tma_K128_H64", B=3, K=128, n_in=64, n_hid=64, math=wl.MATH_BF16,
@@ -159,6 +163,9 @@ EDGE = [
                 grad_path=wl.GRAD_GEMM, dt_per_sample=True),
     wl.Workload("edge_tma_tf32_K64_H32", B=3, K=64, n_in=32, n_hid=32, math=wl.MATH_TF32,
                 grad_path=wl.GRAD_GEMM),
+    # two samples per 32-row chunk, three x boxes
+    wl.Workload("edge_tma_tf32_K16_n96", B=20, K=16, n_in=96, n_hid=64, math=wl.MATH_TF32,
+                grad_path=wl.GRAD_GEMM, dt_per_sample=True),
 ]
 
 
