@@ -68,9 +68,23 @@ __global__ void k_tau_fwd(const float* __restrict__ x, const float* __restrict__
     bu = bias[tid];
     du = expf(-dtb / fmaxf(tau[tid], kTauEps));
   }
+  // x of the next step is loaded one step ahead (n_in <= 1024 <= 8 T)
+  constexpr int kXR = 8;
+  float xr[kXR];
+  auto load_x = [&](int kk) {
+#pragma unroll
+    for (int q = 0; q < kXR; ++q) {
+      const int j = tid + q * T;
+      xr[q] = (kk < K && j < n_in) ? x[(bi * K + kk) * n_in + j] : 0.f;
+    }
+  };
+  load_x(0);
   for (int k = 0; k < K; ++k) {
     const long long row = bi * K + k;
-    for (int j = tid; j < n_in; j += T) z[j] = x[row * n_in + j];
+#pragma unroll
+    for (int q = 0; q < kXR; ++q)
+      if (tid + q * T < n_in) z[tid + q * T] = xr[q];
+    load_x(k + 1);
     __syncthreads();
     if (u < H) {
       const float* __restrict__ w = W + u * ld;
@@ -130,25 +144,44 @@ __global__ void k_tau_bwd(const float* __restrict__ x, const float* __restrict__
     live = tau[tid] > kTauEps;
     du = expf(-dtb / tau_eff);
   }
+  // Inputs of step k (s, h_k, the per-step seed, x_k) are loaded one step
+  // ahead (n_in <= 1024 <= 8 T).
+  constexpr int kXR = 8;
+  float xr[kXR], ps = 0.f, php = 0.f, pup = 0.f;
+  auto load_step = [&](int kk) {
+    const long long rr = bi * K + kk;
+    if (kk >= 0 && tid < H) {
+      ps = s_in[rr * H + tid];
+      php = (kk == 0) ? h0[bi * H + tid] : h_seq[(rr - 1) * H + tid];
+      pup = grad_h_seq ? grad_h_seq[rr * H + tid] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kXR; ++q) {
+      const int j = tid + q * T;
+      xr[q] = (kk >= 0 && j < n_in) ? x[rr * n_in + j] : 0.f;
+    }
+  };
+  load_step(K - 1);
   for (int k = K - 1; k >= 0; --k) {
     const long long row = bi * K + k;
+    const float s = ps, hp = php, up = pup;
+#pragma unroll
+    for (int q = 0; q < kXR; ++q)
+      if (tid + q * T < n_in) z[tid + q * T] = xr[q];
+    load_step(k - 1);
     // phase A (one thread per unit): dh, d_pre, gb, gtau, h_k into z
     if (tid < H) {
-      dh = carry;
-      if (grad_h_seq) dh += grad_h_seq[row * H + tid];
+      dh = carry + up;
       if (k == K - 1) {
         if (grad_h_last) dh += grad_h_last[bi * H + tid];
         if (y) dh += h_seq[row * H + tid] - y[bi * H + tid];
       }
-      const float s = s_in[row * H + tid];
-      const float hp = (k == 0) ? h0[bi * H + tid] : h_seq[(row - 1) * H + tid];
       const float dp = dh * (1.f - du) * (1.f - s * s);
       dpre[tid] = dp;
       gb += dp;
       if (live) gtau += dh * (hp - s) * du * dtb / (tau_eff * tau_eff);
       z[n_in + tid] = hp;
     }
-    for (int j = tid; j < n_in; j += T) z[j] = x[row * n_in + j];
     __syncthreads();
     // phase B (Q threads per unit): part p of the gradient row and of the carry
     if (u < H) {
