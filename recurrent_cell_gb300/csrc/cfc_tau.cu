@@ -42,7 +42,7 @@ __device__ __forceinline__ float sum_parts(const float* part, int Q, int H, int 
   return part[u];
 }
 
-__global__ void k_tau_fwd(const float* __restrict__ x, const float* __restrict__ h0,
+__global__ void __launch_bounds__(1024) k_tau_fwd(const float* __restrict__ x, const float* __restrict__ h0,
                           const float* __restrict__ W_in, const float* __restrict__ W_rec,
                           const float* __restrict__ bias, const float* __restrict__ tau,
                           const float* __restrict__ dt, int dt_stride, int K, int n_in, int H,
@@ -111,7 +111,12 @@ __global__ void k_tau_fwd(const float* __restrict__ x, const float* __restrict__
   }
 }
 
-__global__ void k_tau_bwd(const float* __restrict__ x, const float* __restrict__ h0,
+// REG: each thread keeps its kGReg-or-fewer gradient entries of row u in
+// registers (no shared-memory G); used when they fit.
+constexpr int kGReg = 64;
+
+template <bool REG>
+__global__ void __launch_bounds__(REG ? 512 : 1024) k_tau_bwd(const float* __restrict__ x, const float* __restrict__ h0,
                           const float* __restrict__ W_in, const float* __restrict__ W_rec,
                           const float* __restrict__ tau, const float* __restrict__ dt, int dt_stride, int K,
                           int n_in, int H, const float* __restrict__ h_seq, const float* __restrict__ s_in,
@@ -122,8 +127,8 @@ __global__ void k_tau_bwd(const float* __restrict__ x, const float* __restrict__
   const int Zc = n_in + H, ld = Zc | 1;
   const int Q = tau_parts(H), Hr = tau_round32(H);
   float* W = sm;                      // [H][ld]
-  float* G = W + (size_t)H * ld;      // [H][ld]: gradient of [W_in | W_rec]
-  float* z = G + (size_t)H * ld;      // [Zc]: x_k, then h_k
+  float* G = W + (size_t)H * ld;      // [H][ld]: gradient of [W_in | W_rec] (not REG)
+  float* z = G + (REG ? 0 : (size_t)H * ld);   // [Zc]: x_k, then h_k
   float* dpre = z + Zc;               // [H]
   float* part = dpre + H;             // [Q][H] partial carries
   const long long bi = blockIdx.x;
@@ -134,8 +139,11 @@ __global__ void k_tau_bwd(const float* __restrict__ x, const float* __restrict__
   for (int e = tid; e < H * Zc; e += T) {
     const int uu = e / Zc, j = e - uu * Zc;
     W[uu * ld + j] = (j < n_in) ? W_in[(long long)uu * n_in + j] : W_rec[(long long)uu * H + (j - n_in)];
-    G[uu * ld + j] = 0.f;
+    if (!REG) G[uu * ld + j] = 0.f;
   }
+  float greg[REG ? kGReg : 1];
+#pragma unroll
+  for (int i = 0; i < (REG ? kGReg : 1); ++i) greg[i] = 0.f;
   const float dtb = dt[dt_stride ? bi : 0];
   float du = 0.f, tau_eff = 1.f, carry = 0.f, gb = 0.f, gtau = 0.f, dh = 0.f;
   bool live = false;
@@ -186,10 +194,16 @@ __global__ void k_tau_bwd(const float* __restrict__ x, const float* __restrict__
     // phase B (Q threads per unit): part p of the gradient row and of the carry
     if (u < H) {
       const float dp = dpre[u];
-      float* __restrict__ g = G + u * ld;
       const float* __restrict__ zz = z;
+      if constexpr (REG) {
+#pragma unroll
+        for (int i = 0; i < kGReg; ++i)
+          if (j0 + i < j1) greg[i] = fmaf(dp, zz[j0 + i], greg[i]);
+      } else {
+        float* __restrict__ g = G + u * ld;
 #pragma unroll 4
-      for (int j = j0; j < j1; ++j) g[j] = fmaf(dp, zz[j], g[j]);
+        for (int j = j0; j < j1; ++j) g[j] = fmaf(dp, zz[j], g[j]);
+      }
       const float* __restrict__ wc = W + n_in + u;
       const float* __restrict__ dpr = dpre;
       float c0 = 0.f, c1 = 0.f;
@@ -222,10 +236,24 @@ __global__ void k_tau_bwd(const float* __restrict__ x, const float* __restrict__
   if (tid < H && grad_h0) grad_h0[bi * H + tid] = carry;
   // packed row [gW_in (u, j) | gW_rec (u, j) | gb (u) | gtau (u)]
   float* out = per_sample + bi * (long long)(Zc + 2) * H;
-  for (int e = tid; e < H * Zc; e += T) {
-    const int uu = e / Zc, j = e - uu * Zc;
-    const long long off = (j < n_in) ? (long long)uu * n_in + j : (long long)H * n_in + (long long)uu * H + (j - n_in);
-    out[off] = G[uu * ld + j];
+  if constexpr (REG) {
+    if (u < H) {
+#pragma unroll
+      for (int i = 0; i < kGReg; ++i) {
+        const int j = j0 + i;
+        if (j < j1) {
+          const long long off = (j < n_in) ? (long long)u * n_in + j : (long long)H * n_in + (long long)u * H + (j - n_in);
+          out[off] = greg[i];
+        }
+      }
+    }
+  } else {
+    for (int e = tid; e < H * Zc; e += T) {
+      const int uu = e / Zc, j = e - uu * Zc;
+      const long long off =
+          (j < n_in) ? (long long)uu * n_in + j : (long long)H * n_in + (long long)uu * H + (j - n_in);
+      out[off] = G[uu * ld + j];
+    }
   }
   if (tid < H) {
     out[(long long)H * Zc + tid] = gb;
@@ -238,6 +266,15 @@ size_t fwd_smem(int n_in, int H) {
 }
 size_t bwd_smem(int n_in, int H) {
   return ((size_t)2 * H * ((n_in + H) | 1) + (n_in + H) + H + (size_t)tau_parts(H) * H) * sizeof(float);
+}
+// A thread's share of a gradient row fits kGReg registers, with at most 512
+// threads (128 registers each).
+bool bwd_reg(int n_in, int H) {
+  const int Q = tau_parts(H);
+  return tau_threads(H) <= 512 && (n_in + H + Q - 1) / Q <= kGReg;
+}
+size_t bwd_smem_reg(int n_in, int H) {
+  return ((size_t)H * ((n_in + H) | 1) + (n_in + H) + H + (size_t)tau_parts(H) * H) * sizeof(float);
 }
 
 }  // namespace
@@ -264,14 +301,15 @@ cudaError_t launch_tau_backward(const float* x, const float* h0, const float* W_
                                 const float* grad_h_last, const float* y, float* per_sample, float* grad_h0,
                                 float* grad_x, float* grad_W_in, float* grad_W_rec, float* grad_b,
                                 float* grad_tau, cudaStream_t s) {
-  const size_t smem = bwd_smem(n_in, H);
-  cudaError_t e = cudaFuncSetAttribute(k_tau_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool reg = bwd_reg(n_in, H);
+  const size_t smem = reg ? bwd_smem_reg(n_in, H) : bwd_smem(n_in, H);
+  auto kern = reg ? k_tau_bwd<true> : k_tau_bwd<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   {
     TraceScope trace("tau_bwd", s);
-    k_tau_bwd<<<B, tau_threads(H), smem, s>>>(x, h0, W_in, W_rec, tau, dt, dt_stride, K, n_in, H, h_seq,
-                                                     s_ws, grad_h_seq, grad_h_last, y, per_sample, grad_h0,
-                                                     grad_x);
+    kern<<<B, tau_threads(H), smem, s>>>(x, h0, W_in, W_rec, tau, dt, dt_stride, K, n_in, H, h_seq, s_ws,
+                                         grad_h_seq, grad_h_last, y, per_sample, grad_h0, grad_x);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -57,6 +57,10 @@ CASES = [
     wl.Workload("tau_edge_B1_K1", B=1, K=1, n_in=3, n_hid=5),
     wl.Workload("tau_edge_odd_B5_K9", B=5, K=9, n_in=7, n_hid=33, dt_per_sample=True),
     wl.Workload("tau_edge_n_in_wide", B=3, K=4, n_in=200, n_hid=40),
+    # gradient rows in shared memory: a thread's share above 64 floats, or
+    # more than 512 threads
+    wl.Workload("tau_edge_smem_rows", B=3, K=4, n_in=240, n_hid=64),
+    wl.Workload("tau_edge_H160", B=3, K=3, n_in=8, n_hid=160, dt_per_sample=True),
 ]
 
 
