@@ -85,7 +85,7 @@ def kernel_work(name, w, n_split):
     Zc, H3, R = n_in + H, 3 * H, w.B * w.K
     s = 2 if w.math == wl.MATH_BF16 else 4
     N = w.N
-    engine = "tensor" if name.endswith("_tc") else "alu"
+    engine = "tensor" if (name.endswith("_tc") or "tma" in name) else "alu"
     if name.startswith("cfc_fwd"):
         flops = 2.0 * R * H3 * Zc
         byts = R * n_in * s + R * H * s + R * H3 * 4 + B * H * s + H3 * Zc * s
@@ -119,11 +119,10 @@ def kernel_work(name, w, n_split):
 # sources they were taken from: KERNEL_SOURCE_HASH is the hash of
 # recurrent_cell_gb300/csrc/* and include/* at capture time, and any change to
 # those files makes `traffic` null until the captures are repeated.
-KERNEL_SOURCE_HASH = "3cc0cfecf7a1ac10"
+KERNEL_SOURCE_HASH = "0420446ad2ffaaca"
 PROFILED_TRAFFIC = {
     ("smoke", "cfc_fwd_cluster"): 885248,
     ("smoke", "cfc_bwd_cluster"): 3412224,
-    ("smoke", "wgrad_simt"): 4748544,
     ("mid", "cfc_fwd_tc"): 91625216,
     ("mid", "cfc_bwd_cluster_tc"): 159102464,
     ("mid", "wgrad_tma_tf32"): 154297600,
@@ -160,9 +159,13 @@ def roofline_for(name, w, n_split, avg_ms, peaks, sustained=False):
     t = avg_ms * 1e-3
     if engine == "tensor":
         bf16 = peaks["bf16_sust"] if sustained else peaks["bf16"]
-        flop_peak = bf16 * (TF32_OVER_BF16 if w.math == wl.MATH_TF32 else 1.0)
-        flop_src = (f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'}"
-                    + (" x 1.1/2.25 (TF32)" if w.math == wl.MATH_TF32 else ""))
+        if w.math == wl.MATH_FP32:       # 3xTF32: three TF32 products per fp32 product
+            flop_peak = bf16 * TF32_OVER_BF16 / 3.0
+            flop_src = f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'} x 1.1/2.25 (TF32) / 3 (3xTF32)"
+        else:
+            flop_peak = bf16 * (TF32_OVER_BF16 if w.math == wl.MATH_TF32 else 1.0)
+            flop_src = (f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'}"
+                        + (" x 1.1/2.25 (TF32)" if w.math == wl.MATH_TF32 else ""))
         flop_bound = "tensor"
     else:
         flop_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])

@@ -74,15 +74,17 @@ bool make_layout(int B, int K, int n_in, int n_hid, int math, int grad_path, Lay
     L->rows_per_split = K;
   } else if (math == CFC_MATH_FP32) {
     // Fixed split of the B*K rows into row blocks: about four blocks of the
-    // 64 x 64 output tiling per SM.  Depends on the sizes only, so results are
-    // reproducible for a given configuration.
+    // 64 x 64 SIMT output tiling per SM (the 3xTF32 contraction serves the
+    // per-sample path, whose split is the batch).  Depends on the sizes only,
+    // so results are reproducible for a given configuration.
     const long long tiles = (long long)((L->H3 + 63) / 64) * ((L->Zc + 1 + 63) / 64);
     long long split = (4ll * kNumSMs + tiles - 1) / tiles;
     split = std::max(1ll, std::min(split, std::min<long long>(L->R, 256)));
     L->rows_per_split = (L->R + split - 1) / split;
     L->n_split = (int)((L->R + L->rows_per_split - 1) / L->rows_per_split);
   } else if (const int tma_splits = tma_wgrad_splits(B, K, n_in, n_hid, math, grad_path)) {
-    // TMA-fed tensor-core contraction: one block per SM, (3H / 128) x splits.
+    // TMA-fed tensor-core contraction (bf16, TF32): one block per SM,
+    // (3H / 128) x splits.
     L->n_split = tma_splits;
     L->rows_per_split = (L->R + tma_splits - 1) / tma_splits;
   } else {
@@ -235,8 +237,11 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;
   float* part = (grad_path == CFC_GRAD_SCRATCH) ? per_sample_scratch
                                                 : reinterpret_cast<float*>(a.ws + L.off_part);
-  e = (math == CFC_MATH_FP32) ? launch_wgrad_simt(L, a, part, L.n_split, L.rows_per_split, s)
-                              : launch_wgrad_tc(L, a, part, s);
+  // FP32: the tensor-core contraction with 3xTF32 operands where it applies,
+  // else the SIMT tiles.
+  e = launch_wgrad_tc(L, a, part, s);
+  if (e == cudaErrorNotSupported && math == CFC_MATH_FP32)
+    e = launch_wgrad_simt(L, a, part, L.n_split, L.rows_per_split, s);
   if (e != cudaSuccess) return CFC_ERR_LAUNCH;
   ReduceOut out{};
   out.nseg = 3;

@@ -838,13 +838,20 @@ constexpr uint32_t kT32TmemCols = 256;
 struct Tf32WgradPlan {
   int nx = 0, nh = 0;    // 32-column boxes of x and of h
   int Ntot = 0;          // accumulator columns: Zc + 1 rounded up to 16
-  int nMt = 0, S = 0, chunks = 0, raw_stages = 0;
+  int nMt = 0, S = 0, chunks = 0, raw_stages = 0, k_stages = 0;
   int kb = 0, nb = 0;    // chunk = kb steps x nb samples
+  bool split = false;    // FP32 operands as TF32 high + low parts (three MMAs)
   size_t raw_bytes = 0, k_bytes = 0, smem = 0;
 };
 
+// TF32 mode: GEMM path.  FP32 mode ("3xTF32"): every operand a is split into
+// a_hi = tf32(a) and a_lo = tf32(a - a_hi) and the products accumulate
+// a_hi b_hi + a_hi b_lo + a_lo b_hi in fp32 (the dropped a_lo b_lo and the
+// rounding of a_lo are below 2^-21 relative), on the GEMM path or, with one
+// split per sample (K a multiple of 32), on the per-sample scratch path.
 bool plan_tf32_wgrad(int B, int K, int n_in, int H, int math, int grad_path, Tf32WgradPlan* p) {
-  if (math != CFC_MATH_TF32 || grad_path != CFC_GRAD_GEMM) return false;
+  const bool split = (math == CFC_MATH_FP32);
+  if (math == CFC_MATH_TF32 ? grad_path != CFC_GRAD_GEMM : !split) return false;
   if (n_in % 32 || H % 32) return false;
   int kb, nb;
   if (K <= kT32Rows && kT32Rows % K == 0) {
@@ -857,6 +864,7 @@ bool plan_tf32_wgrad(int B, int K, int n_in, int H, int math, int grad_path, Tf3
   } else {
     return false;
   }
+  if (grad_path == CFC_GRAD_SCRATCH && nb != 1) return false;   // a chunk must not span samples
   const int Zc = n_in + H;
   const int Ntot = (Zc + 1 + 15) / 16 * 16;
   if (Ntot > 256) return false;   // one MMA of N <= 256
@@ -867,13 +875,15 @@ bool plan_tf32_wgrad(int B, int K, int n_in, int H, int math, int grad_path, Tf3
   p->chunks = (int)((long long)B * K / kT32Rows);
   p->kb = kb;
   p->nb = nb;
+  p->split = split;
   p->raw_bytes = (size_t)(4 + p->nx + p->nh) * kT32Box;
-  p->k_bytes = 128 * 128 + (size_t)Ntot * 128;
-  const size_t fixed = 1024 + kT32KStages * p->k_bytes;
+  p->k_bytes = (split ? 2 : 1) * (128 * 128 + (size_t)Ntot * 128);
+  p->k_stages = split ? 1 : kT32KStages;
+  const size_t fixed = 1024 + p->k_stages * p->k_bytes;
   if (fixed + 2 * p->raw_bytes > 227 * 1024) return false;
   p->raw_stages = (int)std::min<size_t>(kT32MaxRaw, (227 * 1024 - fixed) / p->raw_bytes);
   p->smem = fixed + (size_t)p->raw_stages * p->raw_bytes;
-  p->S = std::max(1, std::min(p->chunks, kNumSMs / p->nMt));
+  p->S = (grad_path == CFC_GRAD_SCRATCH) ? B : std::max(1, std::min(p->chunks, kNumSMs / p->nMt));
   return true;
 }
 
@@ -890,16 +900,19 @@ __device__ __forceinline__ void chunk_origin_rows(int c, int K, int nb, int rows
 
 __device__ __forceinline__ uint32_t tf32_bits(uint32_t u) { return (u + 0x1000u) & 0xFFFFE000u; }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kT32Threads, 1)
 k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ CUtensorMap map_x,
                  const __grid_constant__ CUtensorMap map_h, const float* __restrict__ h0, int K, int n_in,
-                 int H, int chunks, int S, int raw_stages, int kb, int nb, int Ntot, float* __restrict__ out) {
+                 int H, int chunks, int S, int raw_stages, int k_stages, int kb, int nb, int Ntot,
+                 float* __restrict__ out) {
   const int mt = blockIdx.x, s = blockIdx.y;
   const int c_begin = (int)((long long)chunks * s / S), c_end = (int)((long long)chunks * (s + 1) / S);
   const int nx = n_in / 32, nh = H / 32, nbox = 4 + nx + nh;
   const int H3 = 3 * H, Zc = n_in + H;
   const uint32_t raw_bytes = (uint32_t)nbox * kT32Box;
-  const uint32_t k_bytes = 128u * 128u + (uint32_t)Ntot * 128u;
+  const uint32_t tile_bytes = 128u * 128u + (uint32_t)Ntot * 128u;   // A tile + B tile
+  const uint32_t k_bytes = (SPLIT ? 2u : 1u) * tile_bytes;            // SPLIT: high parts, then low parts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ uint8_t smraw[];
@@ -918,7 +931,7 @@ k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_consta
       tc::mbar_init(&ready[i], 1);
       tc::mbar_init(&rfree[i], kT32Tr);
     }
-    for (int i = 0; i < kT32KStages; ++i) {
+    for (int i = 0; i < k_stages; ++i) {
       tc::mbar_init(&kfull[i], kT32Tr);
       tc::mbar_init(&kempty[i], 1);
     }
@@ -929,12 +942,14 @@ k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_consta
   if (warp == 0) tc::tmem_alloc(&tmem_base, kT32TmemCols);
   // Rows Zc .. Ntot-1 of every K-major B tile never change: row Zc is the ones
   // column of the bias gradient, the rest zero padding.
-  for (int ks = 0; ks < kT32KStages; ++ks) {
-    uint8_t* bt = kst + (size_t)ks * k_bytes + 128 * 128;
-    for (int e = tid; e < (Ntot - Zc) * 8; e += kT32Threads) {
-      const int row = Zc + (e >> 3), q = e & 7;
-      const uint32_t one = (row == Zc) ? 0x3F800000u : 0u;
-      *reinterpret_cast<uint4*>(bt + row * 128 + ((q ^ (row & 7)) << 4)) = make_uint4(one, one, one, one);
+  for (int ks = 0; ks < k_stages; ++ks) {
+    for (int part = 0; part < (SPLIT ? 2 : 1); ++part) {   // the low part of 1.0 is 0
+      uint8_t* bt = kst + (size_t)ks * k_bytes + (size_t)part * tile_bytes + 128 * 128;
+      for (int e = tid; e < (Ntot - Zc) * 8; e += kT32Threads) {
+        const int row = Zc + (e >> 3), q = e & 7;
+        const uint32_t one = (row == Zc && part == 0) ? 0x3F800000u : 0u;
+        *reinterpret_cast<uint4*>(bt + row * 128 + ((q ^ (row & 7)) << 4)) = make_uint4(one, one, one, one);
+      }
     }
   }
   tc::fence_proxy_async_smem();
@@ -1064,8 +1079,19 @@ k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_consta
         for (int j = 0; j < 4; ++j) {
           const int row = row0 + j;
           uint4 v = make_uint4(w[0][j], w[1][j], w[2][j], w[3][j]);
-          if (rnd) v = make_uint4(tf32_bits(v.x), tf32_bits(v.y), tf32_bits(v.z), tf32_bits(v.w));
-          *reinterpret_cast<uint4*>(dst + row * 128 + ((kq ^ (row & 7)) << 4)) = v;
+          const uint32_t off = row * 128 + ((kq ^ (row & 7)) << 4);
+          if constexpr (SPLIT) {
+            const uint4 hi = make_uint4(tf32_bits(v.x), tf32_bits(v.y), tf32_bits(v.z), tf32_bits(v.w));
+            auto lo1 = [](uint32_t a, uint32_t h) {
+              return tf32_bits(__float_as_uint(__uint_as_float(a) - __uint_as_float(h)));
+            };
+            const uint4 lo = make_uint4(lo1(v.x, hi.x), lo1(v.y, hi.y), lo1(v.z, hi.z), lo1(v.w, hi.w));
+            *reinterpret_cast<uint4*>(dst + off) = hi;
+            *reinterpret_cast<uint4*>(dst + tile_bytes + off) = lo;
+          } else {
+            if (rnd) v = make_uint4(tf32_bits(v.x), tf32_bits(v.y), tf32_bits(v.z), tf32_bits(v.w));
+            *reinterpret_cast<uint4*>(dst + off) = v;
+          }
         }
       }
       tc::fence_proxy_async_smem();
@@ -1078,7 +1104,7 @@ k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_consta
         rs = 0;
         ++rwrap;
       }
-      if (++ks == kT32KStages) {
+      if (++ks == k_stages) {
         ks = 0;
         ++kwrap;
       }
@@ -1102,13 +1128,19 @@ k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (c > c_begin || kk > 0) ? 1u : 0u;
-          tc::mma_tf32(tmem, tc::sdesc_advance(a_desc, so + 32 * kk), tc::sdesc_advance(b_desc, so + 32 * kk), id,
-                       acc);
+          const uint64_t ah = tc::sdesc_advance(a_desc, so + 32 * kk), bh = tc::sdesc_advance(b_desc, so + 32 * kk);
+          if constexpr (SPLIT) {   // small terms first: a_hi b_lo, a_lo b_hi, a_hi b_hi
+            tc::mma_tf32(tmem, ah, tc::sdesc_advance(bh, tile_bytes), id, acc);
+            tc::mma_tf32(tmem, tc::sdesc_advance(ah, tile_bytes), bh, id, 1u);
+            tc::mma_tf32(tmem, ah, bh, id, 1u);
+          } else {
+            tc::mma_tf32(tmem, ah, bh, id, acc);
+          }
         }
         tc::mma_commit(&kempty[ks]);
       }
       __syncwarp();
-      if (++ks == kT32KStages) {
+      if (++ks == k_stages) {
         ks = 0;
         ++wrap;
       }
@@ -1178,12 +1210,13 @@ cudaError_t launch_wgrad_tma_tf32(const Layout& L, const Tf32WgradPlan& p, const
       !encode_bkc_f32(&mx, a.x, L.n_in, L.K, L.B, p.kb, p.nb) ||
       !encode_bkc_f32(&mh, a.h_seq, L.H, L.K, L.B, p.kb, p.nb))
     return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_wgrad_tma_tf32, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  auto kern = p.split ? k_wgrad_tma_tf32<true> : k_wgrad_tma_tf32<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  TraceScope trace("wgrad_tma_tf32", s);
-  k_wgrad_tma_tf32<<<dim3((unsigned)p.nMt, (unsigned)p.S, 1), kT32Threads, p.smem, s>>>(
-      mdA, mx, mh, static_cast<const float*>(a.h0), L.K, L.n_in, L.H, p.chunks, p.S, p.raw_stages, p.kb, p.nb,
-      p.Ntot, out);
+  TraceScope trace(p.split ? "wgrad_tma_3xtf32" : "wgrad_tma_tf32", s);
+  kern<<<dim3((unsigned)p.nMt, (unsigned)p.S, 1), kT32Threads, p.smem, s>>>(
+      mdA, mx, mh, static_cast<const float*>(a.h0), L.K, L.n_in, L.H, p.chunks, p.S, p.raw_stages, p.k_stages, p.kb,
+      p.nb, p.Ntot, out);
   return cudaGetLastError();
 }
 
