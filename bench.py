@@ -121,8 +121,9 @@ def kernel_work(name, w, n_split):
 # those files makes `traffic` null until the captures are repeated.
 KERNEL_SOURCE_HASH = "0420446ad2ffaaca"
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): 885248,
+    ("smoke", "cfc_fwd_cluster"): 885504,
     ("smoke", "cfc_bwd_cluster"): 3412224,
+    ("smoke", "wgrad_tma_3xtf32"): 4786944,
     ("mid", "cfc_fwd_tc"): 91625216,
     ("mid", "cfc_bwd_cluster_tc"): 159102464,
     ("mid", "wgrad_tma_tf32"): 154297600,
