@@ -119,7 +119,7 @@ def kernel_work(name, w, n_split):
 # sources they were taken from: KERNEL_SOURCE_HASH is the hash of
 # recurrent_cell_gb300/csrc/* and include/* at capture time, and any change to
 # those files makes `traffic` null until the captures are repeated.
-KERNEL_SOURCE_HASH = "0420446ad2ffaaca"
+KERNEL_SOURCE_HASH = "3b0cb7b61f83aa50"
 PROFILED_TRAFFIC = {
     ("smoke", "cfc_fwd_cluster"): 885504,
     ("smoke", "cfc_bwd_cluster"): 3412224,

@@ -107,6 +107,14 @@ int cfc_kloop_grad_splits(int B, int K, int n_in, int n_hid, int math, int grad_
  * valid), or CFC_ERR_DEVICE if the word cannot be read.  clear != 0 resets it. */
 int cfc_device_error(int clear);
 
+/* Diagnostic of the timeout path: launches one kernel whose bounded mbarrier
+ * wait (the wait helper of the K-loop kernels) runs out after max_polls polls
+ * (1 .. 2^20) because nothing completes the barrier; the kernel then sets the
+ * device error word and returns, so cfc_device_error reports 1 afterwards.  No
+ * other state changes; the context stays usable.  CFC_ERR_SHAPE for max_polls
+ * out of range. */
+int cfc_selftest_timeout(int max_polls, void* stream);
+
 /* Forward K-loop.
  *   x      [B, K, n_in]      (float or bf16 by `math`)
  *   h0     [B, n_hid]        (float or bf16)

@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cfc_kloop_grad_splits.restype = i32
     lib.cfc_device_error.argtypes = [i32]
     lib.cfc_device_error.restype = i32
+    lib.cfc_selftest_timeout.argtypes = [i32, vp]
+    lib.cfc_selftest_timeout.restype = i32
     lib.cfc_trace_enable.argtypes = [i32]
     lib.cfc_trace_enable.restype = i32
     lib.cfc_trace_count.argtypes = []
@@ -99,6 +101,12 @@ def cfc_kloop_grad_splits(B, K, n_in, n_hid, math, grad_path=GRAD_SCRATCH) -> in
 def cfc_device_error(clear: bool = False) -> int:
     """0 unless a kernel reported a device-side error (waits for the device)."""
     return int(load_library().cfc_device_error(1 if clear else 0))
+
+
+def cfc_selftest_timeout(max_polls: int = 1000, stream=None) -> None:
+    """Run one bounded wait that runs out (see include/cfc.h); afterwards
+    cfc_device_error() reports 1 until cleared."""
+    _check("cfc_selftest_timeout", load_library().cfc_selftest_timeout(int(max_polls), _stream(stream)))
 
 
 def _torch():

@@ -154,6 +154,12 @@ int cfc_device_error(int clear) {
   return (a || b || c) ? 1 : 0;
 }
 
+int cfc_selftest_timeout(int max_polls, void* stream) {
+  if (max_polls < 1 || max_polls > (1 << 20)) return CFC_ERR_SHAPE;
+  cudaError_t e = launch_selftest_wait_timeout((uint32_t)max_polls, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
+}
+
 size_t cfc_kloop_workspace_bytes(int B, int K, int n_in, int n_hid, int math, int grad_path) {
   Layout L;
   if (!make_layout(B, K, n_in, n_hid, math, grad_path, &L)) return 0;

@@ -153,6 +153,10 @@ struct ReduceOut {
 
 cudaError_t launch_reduce(const float* in, int n_batch, long long n_tail, long long ld,
                           const ReduceOut& out, cudaStream_t stream);
+// One bounded wait that runs out (max_polls polls) and sets the device error
+// word (cfc_tc.cu); diagnostic for the timeout path.
+cudaError_t launch_selftest_wait_timeout(uint32_t max_polls, cudaStream_t s);
+
 // tau-cell K loop (cfc_tau.cu), FP32.
 bool tau_shape_supported(int n_in, int n_hid);
 cudaError_t launch_tau_forward(const float* x, const float* h0, const float* W_in, const float* W_rec,

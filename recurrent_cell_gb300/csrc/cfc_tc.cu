@@ -1446,6 +1446,26 @@ cudaError_t launch_grad_x(const Layout& L, const GradXPlan& p, const CfcArgs& a,
 
 }  // namespace
 
+namespace {
+// Waits, bounded by max_polls, on an mbarrier that nothing completes -- the
+// wait helper and the error word of the K-loop kernels -- so that a test can
+// see a timeout reported without any real kernel failing.
+__global__ void k_selftest_wait_timeout(uint32_t max_polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0, max_polls)) atomicExch(&g_cfc_device_error, 1);
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait_timeout(uint32_t max_polls, cudaStream_t s) {
+  k_selftest_wait_timeout<<<1, 32, 0, s>>>(max_polls);
+  return cudaGetLastError();
+}
+
 int read_device_error(int clear) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_cfc_device_error, sizeof(int)) != cudaSuccess) return CFC_ERR_DEVICE;

@@ -166,3 +166,8 @@ def test_tau_argument_validation(lib):
     assert bwd(gtau=None) == ERR_NULL
     assert bwd(scratch=None) == ERR_NULL
     assert bwd(gx=P + 8) == ERR_ALIGN
+
+
+def test_selftest_timeout_argument_validation(lib):
+    assert lib.cfc_selftest_timeout(0, None) == ERR_SHAPE
+    assert lib.cfc_selftest_timeout((1 << 20) + 1, None) == ERR_SHAPE
