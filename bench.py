@@ -115,44 +115,54 @@ def kernel_work(name, w, n_split):
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # dominant kernels, from the ncu captures summarised under profiles/ (one
-# launch each, the bench command of that workload).  Valid only for the kernel
-# sources they were taken from: KERNEL_SOURCE_HASH is the hash of
-# recurrent_cell_gb300/csrc/* and include/* at capture time, and any change to
-# those files makes `traffic` null until the captures are repeated.
-KERNEL_SOURCE_HASH = "3b0cb7b61f83aa50"
+# launch each, the bench command of that workload).  Each entry is valid only
+# for the sources it was taken from: the second field is the hash of the
+# kernel's own file, the shared device headers and the host dispatch
+# (KERNEL_FILES, COMMON_FILES) at capture time; any change to one of those
+# files makes that kernel's `traffic` null until its capture is repeated.
+COMMON_FILES = ("cfc_internal.cuh", "tc_common.cuh", "api.cu")
+KERNEL_FILES = {
+    "cfc_fwd_cluster": "cfc_cluster.cu",
+    "cfc_bwd_cluster": "cfc_cluster.cu",
+    "cfc_fwd_tc": "cfc_tc_kloop.cu",
+    "cfc_bwd_cluster_tc": "cfc_tc_kloop.cu",
+    "cfc_fwd_stream_tc": "cfc_tc_stream.cu",
+    "cfc_bwd_tc": "cfc_tc_stream.cu",
+    "wgrad_tma_3xtf32": "cfc_tc.cu",
+    "wgrad_tma_tf32": "cfc_tc.cu",
+    "wgrad_tma_tc": "cfc_tc.cu",
+}
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): 885504,
-    ("smoke", "cfc_bwd_cluster"): 3412224,
-    ("smoke", "wgrad_tma_3xtf32"): 4786944,
-    ("mid", "cfc_fwd_tc"): 91625216,
-    ("mid", "cfc_bwd_cluster_tc"): 159102464,
-    ("mid", "wgrad_tma_tf32"): 154297600,
-    ("large", "cfc_fwd_stream_tc"): 195872256,
-    ("large", "cfc_bwd_tc"): 287868672,
-    ("large", "wgrad_tma_tc"): 154775808,
+    ("smoke", "cfc_fwd_cluster"): (885504, "42271f7a085d7473"),
+    ("smoke", "cfc_bwd_cluster"): (3412224, "42271f7a085d7473"),
+    ("smoke", "wgrad_tma_3xtf32"): (4786944, "f9b62c465d4c7cd6"),
+    ("mid", "cfc_fwd_tc"): (91625216, "bc0d15dbd48d8151"),
+    ("mid", "cfc_bwd_cluster_tc"): (159102464, "bc0d15dbd48d8151"),
+    ("mid", "wgrad_tma_tf32"): (154297600, "f9b62c465d4c7cd6"),
+    ("large", "cfc_fwd_stream_tc"): (192039680, "5e0ae08a97717dbd"),
+    ("large", "cfc_bwd_tc"): (284591360, "5e0ae08a97717dbd"),
+    ("large", "wgrad_tma_tc"): (154775808, "f9b62c465d4c7cd6"),
 }
 
 
-def kernel_source_hash():
-    import glob
+def kernel_source_hash(name):
+    """Hash of the files kernel `name` is built and dispatched from."""
     import hashlib
-    root = os.path.dirname(os.path.abspath(__file__))
-    files = sorted(glob.glob(os.path.join(root, "recurrent_cell_gb300", "csrc", "*.cu")) +
-                   glob.glob(os.path.join(root, "recurrent_cell_gb300", "csrc", "*.cuh")) +
-                   glob.glob(os.path.join(root, "include", "*.h")))
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "recurrent_cell_gb300", "csrc")
     h = hashlib.sha256()
-    for f in files:
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for f in sorted(set(COMMON_FILES + (KERNEL_FILES[name],))):
+        h.update(f.encode())
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(w, name):
     short = {v.name: k for k, v in wl.SHORT_NAMES.items()}.get(w.name)
-    if short is None or kernel_source_hash() != KERNEL_SOURCE_HASH:
+    entry = PROFILED_TRAFFIC.get((short, name))
+    if entry is None or kernel_source_hash(name) != entry[1]:
         return None
-    return PROFILED_TRAFFIC.get((short, name))
+    return entry[0]
 
 
 def roofline_for(name, w, n_split, avg_ms, peaks, sustained=False):

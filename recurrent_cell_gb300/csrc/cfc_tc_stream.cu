@@ -35,6 +35,7 @@
 //
 // Waits are bounded; a timeout records an error in the device error word.
 #include <algorithm>
+#include <climits>
 #include <vector>
 
 #include "cfc_internal.cuh"
@@ -103,52 +104,77 @@ __device__ __forceinline__ uint32_t kmajor_off(int row, int kk, int rows) {
   return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
 }
 
+// Store EPU = 16 / sizeof(ET) consecutive K elements as one 16-byte unit of
+// a swizzled tile row.
+template <typename ET>
+__device__ __forceinline__ void st_unit(uint8_t* p, const float* v) {
+  uint4 w;
+  if constexpr (sizeof(ET) == 4) {
+    w = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+  } else {
+    uint32_t r[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+      r[q] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    w = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+  *reinterpret_cast<uint4*>(p) = w;
+}
+
+// Both tile builders run one thread per 16-byte unit (row i of the tile,
+// unit u of its 128-byte K row): 128 x 8 units per tile, 32-bit indices
+// (the launchers check the unit count).
+
 // W_rec^T tiles: tile (mt, a) holds rows j = 128*mt .. 128*mt+127 (units)
 // and K elements a*EPA .. a*EPA+EPA-1 (EPA = 128 bytes / element), at byte
 // offset tile_offset(a, mt, nM), swizzled exactly as in shared memory.
+// Consecutive threads take consecutive rows j, so each of a thread's EPU
+// loads (one row kk of W_rec each) is coalesced across the warp.
 template <typename ET, int MODE>
 __global__ void k_prep_wt_tiles(const ET* __restrict__ W_rec, int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
-  constexpr int EPA = 128 / sizeof(ET);
+  constexpr int EPU = 16 / sizeof(ET);
   const int H3 = 3 * H;
-  const long long total = (long long)nM * nAk * 128 * EPA;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-       e += (long long)gridDim.x * blockDim.x) {
-    const int kl = (int)(e % EPA);
-    const long long rest = e / EPA;
-    const int i = (int)(rest % 128);
-    const long long t = rest / 128;            // a * nM + mt
-    const int mt = (int)(t % nM), a = (int)(t / nM);
-    const int j = mt * 128 + i, kk = a * EPA + kl;
-    float v = 0.f;
-    if (j < H && kk < H3) v = ld_operand<MODE>(W_rec + (long long)kk * H + j);
-    st_elem<ET>(tiles + tile_offset(a, mt, nM) + tc::sw128_offset(i, kl * sizeof(ET)), v);
+  const int total = nM * nAk * 1024;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    const int i = e & 127, u = (e >> 7) & 7, t = e >> 10;   // t = a * nM + mt
+    const int mt = t % nM, a = t / nM;
+    const int j = mt * 128 + i, k0 = a * (8 * EPU) + u * EPU;
+    float v[EPU];
+#pragma unroll
+    for (int q = 0; q < EPU; ++q)
+      v[q] = (j < H && k0 + q < H3) ? ld_operand<MODE>(W_rec + (size_t)(k0 + q) * H + j) : 0.f;
+    st_unit<ET>(tiles + tile_offset(a, mt, nM) + tc::sw128_offset(i, u * 16), v);
   }
 }
 
 // W_cat tiles of the forward: tile (a, m), m = 3*ub + c, holds the rows of
 // head c for units 128*ub + i (i = 0..127) and K elements a*EPA .. +EPA-1 of z,
 // at byte offset tile_offset(a, m, nM), swizzled as in shared memory.
+// Consecutive threads take consecutive units u of one row, so a warp reads
+// four 128-byte runs of [W_in | W_rec] rows and writes four whole tile rows.
 template <typename ET, int MODE>
 __global__ void k_prep_w_tiles_fwd(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, int n_in,
                                    int H, int nM, int nAk, uint8_t* __restrict__ tiles) {
-  constexpr int EPA = 128 / sizeof(ET);
+  constexpr int EPU = 16 / sizeof(ET);
   const int Zc = n_in + H;
-  const long long total = (long long)nM * nAk * 128 * EPA;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-       e += (long long)gridDim.x * blockDim.x) {
-    const int kl = (int)(e % EPA);
-    const long long rest = e / EPA;
-    const int i = (int)(rest % 128);
-    const long long t = rest / 128;            // a * nM + m
-    const int m = (int)(t % nM), a = (int)(t / nM);
+  const int total = nM * nAk * 1024;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    const int u = e & 7, i = (e >> 3) & 127, t = e >> 10;     // t = a * nM + m
+    const int m = t % nM, a = t / nM;
     const int c = m % 3, ub = m / 3;
-    const int unit = ub * 128 + i, kk = a * EPA + kl;
-    float v = 0.f;
-    if (unit < H && kk < Zc) {
-      const long long row = (long long)c * H + unit;
-      v = (kk < n_in) ? ld_operand<MODE>(W_in + row * n_in + kk) : ld_operand<MODE>(W_rec + row * H + (kk - n_in));
+    const int unit = ub * 128 + i, k0 = a * (8 * EPU) + u * EPU;
+    const size_t row = (size_t)c * H + unit;
+    float v[EPU];
+#pragma unroll
+    for (int q = 0; q < EPU; ++q) {
+      const int kk = k0 + q;
+      v[q] = 0.f;
+      if (unit < H && kk < Zc)
+        v[q] = (kk < n_in) ? ld_operand<MODE>(W_in + row * n_in + kk) : ld_operand<MODE>(W_rec + row * H + (kk - n_in));
     }
-    st_elem<ET>(tiles + tile_offset(a, m, nM) + tc::sw128_offset(i, kl * sizeof(ET)), v);
+    st_unit<ET>(tiles + tile_offset(a, m, nM) + tc::sw128_offset(i, u * 16), v);
   }
 }
 
@@ -892,7 +918,8 @@ template <typename ET, int MODE>
 cudaError_t launch_fwd_stream(const Layout& L, const FwdPlan& p, const CfcArgs& a, cudaStream_t s) {
   uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
   {
-    const long long total = (long long)3 * p.nUB * p.nAk * 128 * (128 / sizeof(ET));
+    const long long total = (long long)3 * p.nUB * p.nAk * 1024;   // 16-byte tile units
+    if (total > INT_MAX) return cudaErrorInvalidValue;
     const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
     TraceScope trace("prep_w", s);
     k_prep_w_tiles_fwd<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_in),
@@ -961,7 +988,8 @@ template <typename ET, int MODE>
 cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cudaStream_t s) {
   uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
   {
-    const long long total = (long long)p.nM * p.nAk * 128 * (128 / sizeof(ET));
+    const long long total = (long long)p.nM * p.nAk * 1024;   // 16-byte tile units
+    if (total > INT_MAX) return cudaErrorInvalidValue;
     const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
     TraceScope trace("prep_wt_tiles", s);
     k_prep_wt_tiles<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_rec), L.H, p.nM, p.nAk, tiles);
