@@ -486,8 +486,125 @@ k_grad_x_simt(const DT* __restrict__ dA, const T* __restrict__ W_in, long long R
   }
 }
 
+// Staged form for float dA and W_in (FP32 / TF32) when a 32-row tile of dA and
+// a 64-column slice of W_in fit in shared memory together: every copy of the
+// block is issued up front with cp.async in four commit groups along m (one
+// memory latency instead of one per m chunk), and the products of chunk c run
+// while chunks c+1.. are still landing.  32 x 64 outputs per block of 128
+// threads, 4 x 4 per thread; every output sums m in ascending order with the
+// same fmaf chain as k_grad_x_simt (identical results).
+constexpr int kGxsRows = 32, kGxsCols = 64, kGxsThreads = 128, kGxsChunks = 4;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+size_t grad_x_staged_smem(int H3) {
+  return sizeof(float) * ((size_t)kGxsRows * (H3 + 4) + (size_t)H3 * kGxsCols);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGxsThreads)
+k_grad_x_staged(const float* __restrict__ dA, const float* __restrict__ W_in, long long R, int H3, int n_in,
+                float* __restrict__ grad_x) {
+  extern __shared__ __align__(16) float gsm[];
+  const int lda = H3 + 4;                        // row stride of the dA tile (16-byte rows)
+  float* As = gsm;                               // [32][lda]
+  float* Bs = As + (size_t)kGxsRows * lda;       // [H3][64]
+  const long long r0 = (long long)blockIdx.x * kGxsRows;
+  const int c0 = blockIdx.y * kGxsCols;
+  const int tid = threadIdx.x;
+  const int nq = H3 / 4;                         // 16-byte units along m (H3 % 4 == 0)
+
+#pragma unroll
+  for (int c = 0; c < kGxsChunks; ++c) {
+    const int q0 = c * nq / kGxsChunks, q1 = (c + 1) * nq / kGxsChunks, w = q1 - q0;
+    for (int e = tid; e < kGxsRows * w; e += kGxsThreads) {
+      const int rr = e / w, q = q0 + (e - rr * w);
+      const long long row = r0 + rr;
+      const bool in = row < R;                   // rows past R are zero-filled
+      cp_async16(smem_addr(As + (size_t)rr * lda + 4 * q), dA + (in ? row : 0) * H3 + 4 * q, in ? 16u : 0u);
+    }
+    for (int e = tid; e < 4 * w * (kGxsCols / 4); e += kGxsThreads) {
+      const int m = 4 * q0 + e / (kGxsCols / 4), cq = e % (kGxsCols / 4);
+      const int col = c0 + 4 * cq;
+      const bool in = col < n_in;                // n_in % 4 == 0: a unit is all in or all out
+      cp_async16(smem_addr(Bs + (size_t)m * kGxsCols + 4 * cq), W_in + (long long)m * n_in + (in ? col : 0),
+                 in ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+
+  const int tr = tid / 16, tc = tid % 16;        // rows 4tr..4tr+3, columns 4tc..4tc+3
+  float acc[4][4] = {};
+  auto products = [&](int c) {
+    const int q0 = c * nq / kGxsChunks, q1 = (c + 1) * nq / kGxsChunks;
+    for (int q = q0; q < q1; ++q) {
+      float a[4][4], b[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(As + (size_t)(4 * tr + i) * lda + 4 * q);
+        a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float4 v = *reinterpret_cast<const float4*>(Bs + (size_t)(4 * q + t) * kGxsCols + 4 * tc);
+        b[t][0] = to_operand<MODE>(v.x); b[t][1] = to_operand<MODE>(v.y);
+        b[t][2] = to_operand<MODE>(v.z); b[t][3] = to_operand<MODE>(v.w);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t)                // m = 4q + t, ascending
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i][t], b[t][j], acc[i][j]);
+    }
+  };
+  static_assert(kGxsChunks == 4, "one wait per commit group");
+  cp_async_wait<3>();
+  __syncthreads();
+  products(0);
+  cp_async_wait<2>();
+  __syncthreads();
+  products(1);
+  cp_async_wait<1>();
+  __syncthreads();
+  products(2);
+  cp_async_wait<0>();
+  __syncthreads();
+  products(3);
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long row = r0 + 4 * tr + i;
+    if (row >= R) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = c0 + 4 * tc + j;
+      if (col < n_in) grad_x[row * n_in + col] = acc[i][j];
+    }
+  }
+}
+
 template <typename T, typename DT, int MODE>
 cudaError_t grad_x_mode(const Layout& L, const CfcArgs& a, cudaStream_t s) {
+  if constexpr (sizeof(T) == 4 && sizeof(DT) == 4) {
+    const float* dA = reinterpret_cast<const float*>(a.ws + L.off_dA);
+    const size_t smem = grad_x_staged_smem(L.H3);
+    const bool aligned = ((reinterpret_cast<uintptr_t>(dA) | reinterpret_cast<uintptr_t>(a.W_in)) & 15) == 0;
+    if (L.H3 % 4 == 0 && L.n_in % 4 == 0 && aligned && smem <= 200 * 1024) {
+      auto kern = k_grad_x_staged<MODE>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      dim3 grid((unsigned)((L.R + kGxsRows - 1) / kGxsRows), (unsigned)((L.n_in + kGxsCols - 1) / kGxsCols));
+      TraceScope trace("grad_x_simt", s);
+      kern<<<grid, kGxsThreads, smem, s>>>(dA, static_cast<const float*>(a.W_in), L.R, L.H3, L.n_in, a.grad_x);
+      return cudaGetLastError();
+    }
+  }
   dim3 grid((unsigned)((L.R + kGxTile - 1) / kGxTile), (unsigned)((L.n_in + kGxTile - 1) / kGxTile));
   TraceScope trace("grad_x_simt", s);
   k_grad_x_simt<T, DT, MODE><<<grid, 256, 0, s>>>(reinterpret_cast<const DT*>(a.ws + L.off_dA),
