@@ -137,6 +137,9 @@ EDGE = [
     wl.Workload("edge_B3000_K2_bf16", B=3000, K=2, n_in=40, n_hid=72, math=wl.MATH_BF16,
                 grad_path=wl.GRAD_GEMM, dt_per_sample=True),
     wl.Workload("edge_wide_H600", B=3, K=2, n_in=100, n_hid=600),            # units loop (>512 threads)
+    # staged grad_x after the cluster backward: 35 rows (a ragged 32-row tile)
+    # and 68 input columns (a second, 4-wide column block)
+    wl.Workload("edge_gx_B7_K5_n68", B=7, K=5, n_in=68, n_hid=44, dt_per_sample=True),
     # tensor-core K loop: cluster of H/32 blocks, ragged batch tiles, K padding
     wl.Workload("edge_tc_tf32_B70_K3", B=70, K=3, n_in=16, n_hid=64, math=wl.MATH_TF32),
     wl.Workload("edge_tc_bf16_B45_K5", B=45, K=5, n_in=40, n_hid=96, math=wl.MATH_BF16,
