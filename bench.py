@@ -406,6 +406,53 @@ def measure_tau(w, steps, warmup, device, peaks, flush):
                               peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"))
 
 
+def measure_grn(w, steps, warmup, device, peaks, flush):
+    """The multi-horizon GRN heads on every K position (FP32): forward over the
+    B*K trunk rows, backward with grad_h_carry, per-sample rows summed by
+    reduce_axis0.  Algorithmic flops per row: forward 2 J M (Hd + M) + 2 J (2 M
+    + Hd); backward rows 2 J M (M + Hd) (W2^T dz2, W1^T dz1); per-sample
+    gradient 2 J M (Hd + M) + 2 J (2 M + Hd) (one FMA per packed element and
+    row).  Roofline of the dominant kernel against the FFMA peak."""
+    import torch
+    import recurrent_cell_gb300 as cfc
+    inp = wl.make_grn_inputs(w)
+    t = {k: torch.from_numpy(v).to(device) for k, v in inp.items()}
+    Hd, M, J, R = w.hidden, w.head_mid, w.n_horizons, w.rows
+    N = cfc.cfc_grn_param_length(Hd, M, J)
+    probs = torch.empty(R, J, device=device)
+    saved = torch.empty(R, cfc.cfc_grn_saved_per_row(M, J), device=device)
+    gh = torch.empty(R, Hd, device=device)
+    scratch = torch.empty(w.B, N, device=device)
+    grad = torch.empty(N, device=device)
+    ws = torch.empty(cfc.cfc_grn_workspace_bytes(w.B, w.K, Hd, M, J), dtype=torch.uint8, device=device)
+
+    def step():
+        cfc.cfc_grn_forward(t["h"], t["params"], probs, saved, M, J)
+        cfc.cfc_grn_backward(t["h"], t["params"], probs, saved, t["grad_probs"], t["lam"], gh, scratch, grad, ws,
+                             w.B, w.K, M, J, grad_h_carry=t["carry"])
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    cfc.cfc_trace_enable(True)
+    ms = timed(torch, step, steps, flush)
+    records = cfc.cfc_trace_records()
+    cfc.cfc_trace_enable(False)
+    kernels = summarize_trace(records, steps)
+    ms_step = sum(ms) / len(ms)
+    flops = {"grn_fwd": (2.0 * J * M * (Hd + M) + 2.0 * J * (2 * M + Hd)) * R,
+             "grn_bwd_rows": 2.0 * J * M * (M + Hd) * R,
+             "grn_wgrad": 2.0 * N * R}
+    top = max((n for n in kernels if n in flops), key=lambda n: kernels[n]["ms_total"])
+    achieved = flops[top] / (kernels[top]["avg_ms"] * 1e-3) / 1e12
+    peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+    return dict(workload=w.name, value=R / (ms_step * 1e-3), unit="rows/s", ms_per_step=ms_step,
+                kernels=kernels,
+                roofline=dict(kernel=top, bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s",
+                              frac=achieved / peak,
+                              peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"))
+
+
 def measure_reduce_multi(steps, device, peaks, flush, B=32, count=17):
     """count reducer calls of one training step (the pages' step makes 17, one
     per scratch buffer) as count single reduce_axis0 launches and as one
@@ -530,6 +577,8 @@ def main():
                     help="time only the standalone reduce_axis0 cases and the multi-matrix reducer (profiling aid)")
     ap.add_argument("--tau-only", action="store_true",
                     help="time only the tau-cell K loop on the smoke shape (profiling aid)")
+    ap.add_argument("--grn-only", action="store_true",
+                    help="time only the multi-horizon GRN heads (forward + backward) on the smoke shape")
     args = ap.parse_args()
     w = wl.SHORT_NAMES[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -594,6 +643,9 @@ def main():
     if args.tau_only:
         print(json.dumps(measure_tau(wl.TAU_SMOKE, args.steps, args.warmup, device, peaks, flush)))
         return 0
+    if args.grn_only:
+        print(json.dumps(measure_grn(wl.GRN_SMOKE, args.steps, args.warmup, device, peaks, flush)))
+        return 0
 
     props = torch.cuda.get_device_properties(device)
     uuid = getattr(props, "uuid", None)
@@ -630,6 +682,7 @@ def main():
         secondary["reduce_axis0"] = red
         secondary["reduce_axis0_multi"] = measure_reduce_multi(20, device, peaks, flush)
         secondary["tau_cell"] = measure_tau(wl.TAU_SMOKE, 30, 3, device, peaks, flush)
+        secondary["grn_heads"] = measure_grn(wl.GRN_SMOKE, 30, 3, device, peaks, flush)
         secondary["cuda_graph"] = {wl.SHORT_NAMES[n].name: measure_graph(wl.SHORT_NAMES[n], 50, device)
                                    for n in ("tiny", "smoke")}
     if rank == 0 and world == 1:

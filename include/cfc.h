@@ -211,6 +211,53 @@ int cfc_tau_kloop_backward(const float* x, const float* h0, const float* W_in, c
                            float* grad_b, float* grad_tau, float* grad_h0, float* grad_x,
                            float* per_sample_scratch, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Multi-horizon GRN heads on every K position of the trunk state, FP32.
+ * Forward per horizon j of a row h (the ml-alpha commit history, commit "wire
+ * TFT GRN heads into PerceptionTrainer (Phase 1.7)"):
+ *   z1 = W1[j] h + b1[j],  a1 = GELU(z1) (exact: z Phi(z)),  z2 = W2[j] a1 + b2[j],
+ *   gate = w_gate[j].z2 + b_gate[j],  main = w_main[j].z2 + b_main[j],
+ *   skip = w_skip[j].h + b_skip[j],   p[j] = sigmoid(skip + sigmoid(gate) main).
+ * Backward ("K-loop Parallelization Implementation Plan", Commit 2 / Task 11):
+ * the chain rule of that forward from dL/dp, with
+ *   grad_h = grad_h_carry + sum_j lambda[j] (W1[j]^T dz1_j + dskip_j w_skip[j])
+ * (lambda scales the trunk gradient only) and every parameter gradient summed
+ * per sample over its K rows (k = K-1 .. 0), then over the batch by
+ * reduce_axis0.
+ * Sizes: hidden (Hd) a multiple of 4 in [4, 256], head_mid (M) a multiple of 4
+ * in [4, 64], n_horizons (J) in [1, 8]; otherwise CFC_ERR_SHAPE.  Rows are
+ * r = b*K + k, so h may be the K loop's h_seq [B, K, Hd] and grad_h its
+ * grad_h_seq.  Parameters (and gradients) are one packed vector of
+ * cfc_grn_param_length floats, the ten tensors in this order, horizon-major:
+ * [W1 (J,M,Hd) | b1 (J,M) | W2 (J,M,M) | b2 (J,M) | w_gate (J,M) | b_gate (J) |
+ *  w_main (J,M) | b_main (J) | w_skip (J,Hd) | b_skip (J)].
+ * Every pointer 16-byte aligned (CFC_ERR_ALIGN). */
+
+/* Packed parameter / per-sample gradient length; 0 if unsupported. */
+long long cfc_grn_param_length(int hidden, int head_mid, int n_horizons);
+
+/* Floats per row of the forward's saved intermediates (z1, a1, z2 [J, M],
+ * gate, main [J]): J (3 M + 2); 0 if unsupported. */
+long long cfc_grn_saved_per_row(int head_mid, int n_horizons);
+
+/* Workspace bytes of cfc_grn_backward for B*K rows; 0 if unsupported. */
+size_t cfc_grn_workspace_bytes(int B, int K, int hidden, int head_mid, int n_horizons);
+
+/* Forward over `rows` rows: probs [rows, J] and saved [rows, saved_per_row]
+ * (both overwrite).  rows = 0 is a no-op. */
+int cfc_grn_forward(const float* h, long long rows, int hidden, int head_mid, int n_horizons,
+                    const float* params, float* probs, float* saved, void* stream);
+
+/* Backward of the forward that wrote probs and saved for h [B*K, Hd]:
+ * grad_probs [B*K, J] = dL/dp, lambda [J], grad_h_carry [B*K, Hd] (optional,
+ * NULL = zero).  Outputs (overwrite): grad_h [B*K, Hd], per_sample_scratch
+ * [B, cfc_grn_param_length] (each sample's gradient), grad_params
+ * [cfc_grn_param_length] (their sum in reduce_axis0's order). */
+int cfc_grn_backward(const float* h, int B, int K, int hidden, int head_mid, int n_horizons, const float* params,
+                     const float* probs, const float* saved, const float* grad_probs, const float* lambda,
+                     const float* grad_h_carry, float* grad_h, float* per_sample_scratch, float* grad_params,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* reduce_axis0 for `count` independent matrices with one launch per kernel
  * configuration (the pages' training step calls the reducer 17 times, once per
  * scratch buffer: "K-loop Parallelization Implementation Plan", Self-Review).

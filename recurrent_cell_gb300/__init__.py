@@ -64,6 +64,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cfc_tau_kloop_forward.restype = i32
     lib.cfc_tau_kloop_backward.argtypes = [vp] * 7 + [i32] * 5 + [vp] * 4 + [vp] * 7 + [vp, sz, vp]
     lib.cfc_tau_kloop_backward.restype = i32
+    lib.cfc_grn_param_length.argtypes = [i32, i32, i32]
+    lib.cfc_grn_param_length.restype = i64
+    lib.cfc_grn_saved_per_row.argtypes = [i32, i32]
+    lib.cfc_grn_saved_per_row.restype = i64
+    lib.cfc_grn_workspace_bytes.argtypes = [i32] * 5
+    lib.cfc_grn_workspace_bytes.restype = sz
+    lib.cfc_grn_forward.argtypes = [vp, i64, i32, i32, i32, vp, vp, vp, vp]
+    lib.cfc_grn_forward.restype = i32
+    lib.cfc_grn_backward.argtypes = [vp] + [i32] * 5 + [vp] * 9 + [vp, sz, vp]
+    lib.cfc_grn_backward.restype = i32
     lib.cfc_kloop_forward_backward_static.argtypes = [vp] * 6 + [i32] * 6 + [vp] * 3 + [vp] * 6 + [vp]
     lib.cfc_kloop_forward_backward_static.restype = i32
     lib.cfc_kloop_grad_splits.argtypes = [i32] * 6
@@ -207,6 +217,52 @@ def reduce_axis0(per_batch, out, stream=None):
         _ptr(per_batch, "per_batch", torch.float32), B, N,
         _ptr(out, "out", torch.float32, (N,)), _stream(stream))
     _check("reduce_axis0", status)
+
+
+def cfc_grn_param_length(hidden: int, head_mid: int, n_horizons: int) -> int:
+    return int(load_library().cfc_grn_param_length(hidden, head_mid, n_horizons))
+
+
+def cfc_grn_saved_per_row(head_mid: int, n_horizons: int) -> int:
+    return int(load_library().cfc_grn_saved_per_row(head_mid, n_horizons))
+
+
+def cfc_grn_workspace_bytes(B: int, K: int, hidden: int, head_mid: int, n_horizons: int) -> int:
+    return int(load_library().cfc_grn_workspace_bytes(B, K, hidden, head_mid, n_horizons))
+
+
+def cfc_grn_forward(h, params, probs, saved, head_mid: int, n_horizons: int, stream=None):
+    """GRN heads forward over the rows of h [R, hidden] (float32): probs
+    [R, n_horizons] and the saved intermediates [R, cfc_grn_saved_per_row]."""
+    torch = _torch()
+    f32 = torch.float32
+    R, Hd = h.shape
+    N = cfc_grn_param_length(Hd, head_mid, n_horizons)
+    S = cfc_grn_saved_per_row(head_mid, n_horizons)
+    status = load_library().cfc_grn_forward(
+        _ptr(h, "h", f32, (R, Hd)), R, Hd, head_mid, n_horizons, _ptr(params, "params", f32, (N,)),
+        _ptr(probs, "probs", f32, (R, n_horizons)), _ptr(saved, "saved", f32, (R, S)), _stream(stream))
+    _check("cfc_grn_forward", status)
+
+
+def cfc_grn_backward(h, params, probs, saved, grad_probs, lam, grad_h, per_sample_scratch, grad_params, workspace,
+                     B: int, K: int, head_mid: int, n_horizons: int, grad_h_carry=None, stream=None):
+    """GRN heads backward for h [B*K, hidden] rows (r = b*K + k): grad_h,
+    the per-sample gradient rows and their batch sum (packed parameter order)."""
+    torch = _torch()
+    f32 = torch.float32
+    R, Hd = h.shape
+    N = cfc_grn_param_length(Hd, head_mid, n_horizons)
+    S = cfc_grn_saved_per_row(head_mid, n_horizons)
+    J = n_horizons
+    status = load_library().cfc_grn_backward(
+        _ptr(h, "h", f32, (R, Hd)), B, K, Hd, head_mid, J, _ptr(params, "params", f32, (N,)),
+        _ptr(probs, "probs", f32, (R, J)), _ptr(saved, "saved", f32, (R, S)),
+        _ptr(grad_probs, "grad_probs", f32, (R, J)), _ptr(lam, "lambda", f32, (J,)),
+        _ptr(grad_h_carry, "grad_h_carry", f32, (R, Hd), optional=True), _ptr(grad_h, "grad_h", f32, (R, Hd)),
+        _ptr(per_sample_scratch, "per_sample_scratch", f32, (B, N)), _ptr(grad_params, "grad_params", f32, (N,)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check("cfc_grn_backward", status)
 
 
 def cfc_tau_per_sample_length(n_in: int, n_hid: int) -> int:

@@ -1,0 +1,503 @@
+// cfc_grn.cu -- multi-horizon GRN heads on every K position of the trunk
+// state, forward and backward, FP32.
+//
+// Per horizon j of a trunk row h (length Hd; the ml-alpha commit history,
+// commit "wire TFT GRN heads into PerceptionTrainer (Phase 1.7)"):
+//   z1 = W1[j] h + b1[j],  a1 = GELU(z1) = z1 Phi(z1),  z2 = W2[j] a1 + b2[j],
+//   gate = w_gate[j].z2 + b_gate[j],  main = w_main[j].z2 + b_main[j],
+//   skip = w_skip[j].h + b_skip[j],  p = sigmoid(skip + sigmoid(gate) main).
+// The backward ("K-loop Parallelization Implementation Plan", Commit 2 /
+// Task 11: inputs probs, grad_probs, the saved z1 / a1 / z2 / gate / main, h,
+// grad_h_carry and a per-horizon lambda on the trunk gradient only; ten
+// parameter gradients accumulated per sample over the K positions; grad_h
+// written whole) is the chain rule of that forward.
+//
+// The pages run one launch per K position.  The heads do not feed the
+// recurrence, so here all B*K rows (r = b*K + k, the K loop's h_seq layout)
+// go through one forward launch and one backward launch:
+//   k_grn_fwd      grid (rows / 32, J): a 32-row tile, one horizon; W1[j],
+//                  W2[j] and the row tile staged in shared memory (rows
+//                  padded by 16 bytes), 2 rows x 4 units per thread.
+//   k_grn_bwd_rows grid (rows / 32): all J horizons of a 32-row tile in turn
+//                  (fixed order, so grad_h sums the horizons in order j = 0..J-1),
+//                  dz2, dz1 = (W2^T dz2) GELU'(z1) and the trunk gradient
+//                  W1^T dz1 + dskip w_skip, scaled by lambda_j, in registers;
+//                  dz1, dz2, dgate, dmain, dskip go to the workspace.
+//   k_grn_wgrad    grid (B, N / 256): one thread per element of a sample's
+//                  packed gradient row, summed over k = K-1 .. 0 (the pages'
+//                  loop order) and written once (no += into scratch).
+// reduce_axis0 then sums the B rows into the packed parameter gradient.
+#include "cfc_internal.cuh"
+
+namespace cfc {
+namespace {
+
+constexpr int kGrnRows = 32;          // rows per block
+constexpr int kGrnThreads = 256;
+constexpr int kGrnLdT = kGrnRows + 4; // row stride of the transposed dz tiles
+
+struct GrnDims {
+  int Hd, M, J;
+  long long oW1, ob1, oW2, ob2, owg, obg, owm, obm, ows, obs, N;
+  long long sv, sw;   // floats per row of the saved intermediates / of the workspace
+};
+
+__host__ __device__ inline GrnDims grn_dims(int Hd, int M, int J) {
+  GrnDims d;
+  d.Hd = Hd; d.M = M; d.J = J;
+  const long long JM = (long long)J * M;
+  d.oW1 = 0;
+  d.ob1 = d.oW1 + JM * Hd;
+  d.oW2 = d.ob1 + JM;
+  d.ob2 = d.oW2 + JM * M;
+  d.owg = d.ob2 + JM;
+  d.obg = d.owg + JM;
+  d.owm = d.obg + J;
+  d.obm = d.owm + JM;
+  d.ows = d.obm + J;
+  d.obs = d.ows + (long long)J * Hd;
+  d.N = d.obs + J;
+  d.sv = 3 * JM + 2 * J;   // [z1 | a1 | z2 | gate | main]
+  d.sw = 2 * JM + 3 * J;   // [dz1 | dz2 | dgate | dmain | dskip]
+  return d;
+}
+
+__device__ __forceinline__ float gelu_f(float z) { return 0.5f * z * (1.f + erff(z * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_grad_f(float z) {
+  return 0.5f * (1.f + erff(z * 0.70710678118654752f)) + z * expf(-0.5f * z * z) * 0.39894228040143268f;
+}
+__device__ __forceinline__ float sigmoid_f(float z) { return 1.f / (1.f + expf(-z)); }
+
+size_t fwd_smem_floats(int Hd, int M) {
+  const int ldh = Hd + 4, ldm = M + 4;
+  return (size_t)M * ldh + (size_t)kGrnRows * ldh + (size_t)M * ldm + 2 * (size_t)kGrnRows * ldm + 4 * (size_t)M +
+         Hd;
+}
+size_t bwd_smem_floats(int Hd, int M) {
+  const int ldh = Hd + 4, ldm = M + 4;
+  return (size_t)M * ldh + (size_t)M * ldm + 2 * (size_t)M * kGrnLdT + 2 * (size_t)M + Hd + 3 * kGrnRows;
+}
+
+__global__ void __launch_bounds__(kGrnThreads)
+k_grn_fwd(const float* __restrict__ h, long long R, int Hd, int M, int J, const float* __restrict__ params,
+          float* __restrict__ probs, float* __restrict__ saved) {
+  extern __shared__ __align__(16) float sm[];
+  const GrnDims d = grn_dims(Hd, M, J);
+  const int j = blockIdx.y;
+  const long long r0 = (long long)blockIdx.x * kGrnRows;
+  const int ldh = Hd + 4, ldm = M + 4, tid = threadIdx.x;
+  float* W1s = sm;                                  // [M][ldh]
+  float* hs = W1s + (size_t)M * ldh;                // [32][ldh]
+  float* W2s = hs + (size_t)kGrnRows * ldh;         // [M][ldm]
+  float* as = W2s + (size_t)M * ldm;                // [32][ldm]  a1
+  float* zs = as + (size_t)kGrnRows * ldm;          // [32][ldm]  z2
+  float* b1s = zs + (size_t)kGrnRows * ldm;         // [M]
+  float* b2s = b1s + M;                             // [M]
+  float* wgs = b2s + M;                             // [M]
+  float* wms = wgs + M;                             // [M]
+  float* wss = wms + M;                             // [Hd]
+
+  const float* W1 = params + d.oW1 + (long long)j * M * Hd;
+  const float* W2 = params + d.oW2 + (long long)j * M * M;
+  const int hq = Hd / 4, mq4 = M / 4;
+  for (int e = tid; e < M * hq; e += kGrnThreads) {
+    const int m = e / hq, q = e - m * hq;
+    *reinterpret_cast<float4*>(W1s + (size_t)m * ldh + 4 * q) = *reinterpret_cast<const float4*>(W1 + (size_t)m * Hd + 4 * q);
+  }
+  for (int e = tid; e < kGrnRows * hq; e += kGrnThreads) {
+    const int rr = e / hq, q = e - rr * hq;
+    const long long row = r0 + rr;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < R) v = *reinterpret_cast<const float4*>(h + row * Hd + 4 * q);
+    *reinterpret_cast<float4*>(hs + (size_t)rr * ldh + 4 * q) = v;
+  }
+  for (int e = tid; e < M * mq4; e += kGrnThreads) {
+    const int m = e / mq4, q = e - m * mq4;
+    *reinterpret_cast<float4*>(W2s + (size_t)m * ldm + 4 * q) = *reinterpret_cast<const float4*>(W2 + (size_t)m * M + 4 * q);
+  }
+  for (int e = tid; e < M; e += kGrnThreads) {
+    b1s[e] = params[d.ob1 + (long long)j * M + e];
+    b2s[e] = params[d.ob2 + (long long)j * M + e];
+    wgs[e] = params[d.owg + (long long)j * M + e];
+    wms[e] = params[d.owm + (long long)j * M + e];
+  }
+  for (int e = tid; e < Hd; e += kGrnThreads) wss[e] = params[d.ows + (long long)j * Hd + e];
+  __syncthreads();
+
+  // thread -> rows 2rp, 2rp+1 and units m = mq + 16 t (t = 0..3)
+  const int rp = tid / 16, mq = tid % 16;
+  {
+    float acc[2][4] = {};
+    for (int i = 0; i < Hd; i += 4) {
+      const float4 x0 = *reinterpret_cast<const float4*>(hs + (size_t)(2 * rp) * ldh + i);
+      const float4 x1 = *reinterpret_cast<const float4*>(hs + (size_t)(2 * rp + 1) * ldh + i);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int m = mq + 16 * t;
+        if (m < M) {
+          const float4 w = *reinterpret_cast<const float4*>(W1s + (size_t)m * ldh + i);
+          acc[0][t] = fmaf(w.x, x0.x, acc[0][t]);
+          acc[0][t] = fmaf(w.y, x0.y, acc[0][t]);
+          acc[0][t] = fmaf(w.z, x0.z, acc[0][t]);
+          acc[0][t] = fmaf(w.w, x0.w, acc[0][t]);
+          acc[1][t] = fmaf(w.x, x1.x, acc[1][t]);
+          acc[1][t] = fmaf(w.y, x1.y, acc[1][t]);
+          acc[1][t] = fmaf(w.z, x1.z, acc[1][t]);
+          acc[1][t] = fmaf(w.w, x1.w, acc[1][t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int lr = 2 * rp + rr;
+      const long long row = r0 + lr;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int m = mq + 16 * t;
+        if (m >= M) continue;
+        const float z = acc[rr][t] + b1s[m];
+        const float a = gelu_f(z);
+        as[(size_t)lr * ldm + m] = a;
+        if (row < R) {
+          saved[row * d.sv + (long long)j * M + m] = z;
+          saved[row * d.sv + (long long)J * M + (long long)j * M + m] = a;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  {
+    float acc[2][4] = {};
+    for (int n = 0; n < M; n += 4) {
+      const float4 x0 = *reinterpret_cast<const float4*>(as + (size_t)(2 * rp) * ldm + n);
+      const float4 x1 = *reinterpret_cast<const float4*>(as + (size_t)(2 * rp + 1) * ldm + n);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int m = mq + 16 * t;
+        if (m < M) {
+          const float4 w = *reinterpret_cast<const float4*>(W2s + (size_t)m * ldm + n);
+          acc[0][t] = fmaf(w.x, x0.x, acc[0][t]);
+          acc[0][t] = fmaf(w.y, x0.y, acc[0][t]);
+          acc[0][t] = fmaf(w.z, x0.z, acc[0][t]);
+          acc[0][t] = fmaf(w.w, x0.w, acc[0][t]);
+          acc[1][t] = fmaf(w.x, x1.x, acc[1][t]);
+          acc[1][t] = fmaf(w.y, x1.y, acc[1][t]);
+          acc[1][t] = fmaf(w.z, x1.z, acc[1][t]);
+          acc[1][t] = fmaf(w.w, x1.w, acc[1][t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int lr = 2 * rp + rr;
+      const long long row = r0 + lr;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int m = mq + 16 * t;
+        if (m >= M) continue;
+        const float z = acc[rr][t] + b2s[m];
+        zs[(size_t)lr * ldm + m] = z;
+        if (row < R) saved[row * d.sv + 2ll * J * M + (long long)j * M + m] = z;
+      }
+    }
+  }
+  __syncthreads();
+  // gate, main, skip and p: one warp per row (lane partial sums, then a
+  // fixed xor tree)
+  const int warp = tid / 32, lane = tid % 32;
+  const float bg = params[d.obg + j], bm = params[d.obm + j], bsk = params[d.obs + j];
+  for (int lr = warp * 4; lr < warp * 4 + 4; ++lr) {
+    const long long row = r0 + lr;
+    float g = 0.f, mn = 0.f, sk = 0.f;
+    for (int m = lane; m < M; m += 32) {
+      const float z = zs[(size_t)lr * ldm + m];
+      g = fmaf(wgs[m], z, g);
+      mn = fmaf(wms[m], z, mn);
+    }
+    for (int i = lane; i < Hd; i += 32) sk = fmaf(wss[i], hs[(size_t)lr * ldh + i], sk);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, off);
+      mn += __shfl_xor_sync(0xffffffffu, mn, off);
+      sk += __shfl_xor_sync(0xffffffffu, sk, off);
+    }
+    if (lane == 0 && row < R) {
+      const float gate = g + bg, main = mn + bm, skip = sk + bsk;
+      const float logit = skip + sigmoid_f(gate) * main;
+      probs[row * J + j] = sigmoid_f(logit);
+      saved[row * d.sv + 3ll * J * M + j] = gate;
+      saved[row * d.sv + 3ll * J * M + J + j] = main;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kGrnThreads)
+k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ params,
+               const float* __restrict__ probs, const float* __restrict__ saved,
+               const float* __restrict__ grad_probs, const float* __restrict__ lambda,
+               const float* __restrict__ grad_h_carry, float* __restrict__ grad_h, float* __restrict__ ws) {
+  extern __shared__ __align__(16) float sm[];
+  const GrnDims d = grn_dims(Hd, M, J);
+  const long long r0 = (long long)blockIdx.x * kGrnRows;
+  const int ldh = Hd + 4, ldm = M + 4, tid = threadIdx.x;
+  float* W1s = sm;                                  // [M][ldh]
+  float* W2s = W1s + (size_t)M * ldh;               // [M][ldm]
+  float* dz2T = W2s + (size_t)M * ldm;              // [M][kGrnLdT]
+  float* dz1T = dz2T + (size_t)M * kGrnLdT;         // [M][kGrnLdT]
+  float* wgs = dz1T + (size_t)M * kGrnLdT;          // [M]
+  float* wms = wgs + M;                             // [M]
+  float* wss = wms + M;                             // [Hd]
+  float* sc = wss + Hd;                             // [32][3]: dgate, dmain, dskip
+  const int hq = Hd / 4, mq4 = M / 4;
+  const long long JM = (long long)J * M;
+  const int rg = tid / 32, lane = tid % 32;         // rows 4rg..4rg+3; columns 4 (lane + 32 c) ..
+  float acc[4][8] = {};                             // lambda-weighted trunk gradient, c = 0, 1
+
+  for (int j = 0; j < J; ++j) {
+    __syncthreads();                                // the previous horizon's readers are done
+    const float* W1 = params + d.oW1 + (long long)j * M * Hd;
+    const float* W2 = params + d.oW2 + (long long)j * M * M;
+    for (int e = tid; e < M * hq; e += kGrnThreads) {
+      const int m = e / hq, q = e - m * hq;
+      *reinterpret_cast<float4*>(W1s + (size_t)m * ldh + 4 * q) =
+          *reinterpret_cast<const float4*>(W1 + (size_t)m * Hd + 4 * q);
+    }
+    for (int e = tid; e < M * mq4; e += kGrnThreads) {
+      const int m = e / mq4, q = e - m * mq4;
+      *reinterpret_cast<float4*>(W2s + (size_t)m * ldm + 4 * q) =
+          *reinterpret_cast<const float4*>(W2 + (size_t)m * M + 4 * q);
+    }
+    for (int e = tid; e < M; e += kGrnThreads) {
+      wgs[e] = params[d.owg + (long long)j * M + e];
+      wms[e] = params[d.owm + (long long)j * M + e];
+    }
+    for (int e = tid; e < Hd; e += kGrnThreads) wss[e] = params[d.ows + (long long)j * Hd + e];
+    if (tid < kGrnRows) {
+      const long long row = r0 + tid;
+      float dgate = 0.f, dmain = 0.f, dskip = 0.f;
+      if (row < R) {
+        const float p = probs[row * J + j], gp = grad_probs[row * J + j];
+        const float gate = saved[row * d.sv + 3 * JM + j], main = saved[row * d.sv + 3 * JM + J + j];
+        const float dl = gp * p * (1.f - p);
+        const float sg = sigmoid_f(gate);
+        dmain = dl * sg;
+        dgate = dl * main * sg * (1.f - sg);
+        dskip = dl;
+        ws[row * d.sw + 2 * JM + j] = dgate;
+        ws[row * d.sw + 2 * JM + J + j] = dmain;
+        ws[row * d.sw + 2 * JM + 2 * J + j] = dskip;
+      }
+      sc[3 * tid] = dgate;
+      sc[3 * tid + 1] = dmain;
+      sc[3 * tid + 2] = dskip;
+    }
+    __syncthreads();
+    // dz2 = dmain w_main + dgate w_gate (rows past R are zero)
+    for (int e = tid; e < kGrnRows * M; e += kGrnThreads) {
+      const int lr = e / M, m = e - lr * M;
+      const long long row = r0 + lr;
+      const float v = fmaf(sc[3 * lr + 1], wms[m], sc[3 * lr] * wgs[m]);
+      dz2T[(size_t)m * kGrnLdT + lr] = v;
+      if (row < R) ws[row * d.sw + JM + (long long)j * M + m] = v;
+    }
+    __syncthreads();
+    // dz1 = (W2^T dz2) GELU'(z1): thread -> rows 4rg.., units n = lane + 32 t
+    {
+      float a2[4][2] = {};
+      for (int m = 0; m < M; ++m) {
+        const float4 dz = *reinterpret_cast<const float4*>(dz2T + (size_t)m * kGrnLdT + 4 * rg);
+        const float w0 = (lane < M) ? W2s[(size_t)m * ldm + lane] : 0.f;
+        const float w1 = (lane + 32 < M) ? W2s[(size_t)m * ldm + lane + 32] : 0.f;
+        a2[0][0] = fmaf(w0, dz.x, a2[0][0]);
+        a2[1][0] = fmaf(w0, dz.y, a2[1][0]);
+        a2[2][0] = fmaf(w0, dz.z, a2[2][0]);
+        a2[3][0] = fmaf(w0, dz.w, a2[3][0]);
+        a2[0][1] = fmaf(w1, dz.x, a2[0][1]);
+        a2[1][1] = fmaf(w1, dz.y, a2[1][1]);
+        a2[2][1] = fmaf(w1, dz.z, a2[2][1]);
+        a2[3][1] = fmaf(w1, dz.w, a2[3][1]);
+      }
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int lr = 4 * rg + rr;
+        const long long row = r0 + lr;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int n = lane + 32 * t;
+          if (n >= M) continue;
+          float v = 0.f;
+          if (row < R) {
+            v = a2[rr][t] * gelu_grad_f(saved[row * d.sv + (long long)j * M + n]);
+            ws[row * d.sw + (long long)j * M + n] = v;
+          }
+          dz1T[(size_t)n * kGrnLdT + lr] = v;
+        }
+      }
+    }
+    __syncthreads();
+    // trunk gradient W1^T dz1 + dskip w_skip, scaled by lambda_j
+    {
+      float t[4][8] = {};
+      for (int m = 0; m < M; ++m) {
+        const float4 dz = *reinterpret_cast<const float4*>(dz1T + (size_t)m * kGrnLdT + 4 * rg);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int cq = lane + 32 * c;
+          if (4 * cq >= Hd) continue;
+          const float4 w = *reinterpret_cast<const float4*>(W1s + (size_t)m * ldh + 4 * cq);
+          const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            t[0][4 * c + e] = fmaf(wv[e], dz.x, t[0][4 * c + e]);
+            t[1][4 * c + e] = fmaf(wv[e], dz.y, t[1][4 * c + e]);
+            t[2][4 * c + e] = fmaf(wv[e], dz.z, t[2][4 * c + e]);
+            t[3][4 * c + e] = fmaf(wv[e], dz.w, t[3][4 * c + e]);
+          }
+        }
+      }
+      const float lam = lambda[j];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const float dskip = sc[3 * (4 * rg + rr) + 2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int cq = lane + 32 * c;
+          if (4 * cq >= Hd) continue;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = fmaf(dskip, wss[4 * cq + e], t[rr][4 * c + e]);
+            acc[rr][4 * c + e] = fmaf(lam, v, acc[rr][4 * c + e]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const long long row = r0 + 4 * rg + rr;
+    if (row >= R) continue;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int cq = lane + 32 * c;
+      if (4 * cq >= Hd) continue;
+      float4 v = make_float4(acc[rr][4 * c], acc[rr][4 * c + 1], acc[rr][4 * c + 2], acc[rr][4 * c + 3]);
+      if (grad_h_carry) {
+        const float4 cr = *reinterpret_cast<const float4*>(grad_h_carry + row * Hd + 4 * cq);
+        v.x += cr.x; v.y += cr.y; v.z += cr.z; v.w += cr.w;
+      }
+      *reinterpret_cast<float4*>(grad_h + row * Hd + 4 * cq) = v;
+    }
+  }
+}
+
+// One thread per element n of sample b's packed gradient row: the sum over
+// k = K-1 .. 0 of (left factor) x (right factor), both read per row r = b*K + k.
+__global__ void __launch_bounds__(256)
+k_grn_wgrad(const float* __restrict__ h, const float* __restrict__ saved, const float* __restrict__ ws, int K,
+            int Hd, int M, int J, float* __restrict__ per_sample) {
+  const GrnDims d = grn_dims(Hd, M, J);
+  const long long n = (long long)blockIdx.y * 256 + threadIdx.x;
+  const long long b = blockIdx.x;
+  if (n >= d.N) return;
+  const long long JM = (long long)J * M;
+  const float* L;                 // left factor of row r at L[r * d.sw]
+  const float* Rt = nullptr;      // right factor at Rt[r * rs] (null: bias, factor 1)
+  long long rs = 0;
+  if (n < d.ob1) {                          // W1[j][m][i] <- dz1[j][m] h[i]
+    const long long jm = n / Hd;
+    L = ws + jm;
+    Rt = h + (n - jm * Hd);
+    rs = Hd;
+  } else if (n < d.oW2) {                   // b1
+    L = ws + (n - d.ob1);
+  } else if (n < d.ob2) {                   // W2[j][m][q] <- dz2[j][m] a1[j][q]
+    const long long e = n - d.oW2, jm = e / M, q = e - jm * M, j = jm / M;
+    L = ws + JM + jm;
+    Rt = saved + JM + j * M + q;
+    rs = d.sv;
+  } else if (n < d.owg) {                   // b2
+    L = ws + JM + (n - d.ob2);
+  } else if (n < d.obg) {                   // w_gate[j][m] <- dgate[j] z2[j][m]
+    const long long e = n - d.owg;
+    L = ws + 2 * JM + e / M;
+    Rt = saved + 2 * JM + e;
+    rs = d.sv;
+  } else if (n < d.owm) {                   // b_gate
+    L = ws + 2 * JM + (n - d.obg);
+  } else if (n < d.obm) {                   // w_main[j][m] <- dmain[j] z2[j][m]
+    const long long e = n - d.owm;
+    L = ws + 2 * JM + J + e / M;
+    Rt = saved + 2 * JM + e;
+    rs = d.sv;
+  } else if (n < d.ows) {                   // b_main
+    L = ws + 2 * JM + J + (n - d.obm);
+  } else if (n < d.obs) {                   // w_skip[j][i] <- dskip[j] h[i]
+    const long long e = n - d.ows, j = e / Hd;
+    L = ws + 2 * JM + 2 * J + j;
+    Rt = h + (e - j * Hd);
+    rs = Hd;
+  } else {                                  // b_skip
+    L = ws + 2 * JM + 2 * J + (n - d.obs);
+  }
+  float acc = 0.f;
+  for (int k = K - 1; k >= 0; --k) {
+    const long long r = b * K + k;
+    const float l = L[r * d.sw];
+    acc = Rt ? fmaf(l, Rt[r * rs], acc) : acc + l;
+  }
+  per_sample[b * d.N + n] = acc;
+}
+
+}  // namespace
+
+bool grn_shape_supported(int Hd, int M, int J) {
+  return Hd >= 4 && Hd <= 256 && Hd % 4 == 0 && M >= 4 && M <= 64 && M % 4 == 0 && J >= 1 && J <= 8;
+}
+
+long long grn_param_length(int Hd, int M, int J) { return grn_dims(Hd, M, J).N; }
+long long grn_saved_per_row(int M, int J) { return grn_dims(4, M, J).sv; }
+long long grn_ws_per_row(int M, int J) { return grn_dims(4, M, J).sw; }
+
+cudaError_t launch_grn_forward(const float* h, long long R, int Hd, int M, int J, const float* params,
+                               float* probs, float* saved, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const size_t smem = fwd_smem_floats(Hd, M) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_grn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((R + kGrnRows - 1) / kGrnRows), (unsigned)J);
+  TraceScope trace("grn_fwd", s);
+  k_grn_fwd<<<grid, kGrnThreads, smem, s>>>(h, R, Hd, M, J, params, probs, saved);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grn_backward(const float* h, int B, int K, int Hd, int M, int J, const float* params,
+                                const float* probs, const float* saved, const float* grad_probs,
+                                const float* lambda, const float* grad_h_carry, float* grad_h, float* ws,
+                                float* per_sample, float* grad_params, cudaStream_t s) {
+  const long long R = (long long)B * K;
+  const GrnDims d = grn_dims(Hd, M, J);
+  {
+    const size_t smem = bwd_smem_floats(Hd, M) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_grn_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    TraceScope trace("grn_bwd_rows", s);
+    k_grn_bwd_rows<<<(unsigned)((R + kGrnRows - 1) / kGrnRows), kGrnThreads, smem, s>>>(
+        R, Hd, M, J, params, probs, saved, grad_probs, lambda, grad_h_carry, grad_h, ws);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    TraceScope trace("grn_wgrad", s);
+    dim3 grid((unsigned)B, (unsigned)((d.N + 255) / 256));
+    k_grn_wgrad<<<grid, 256, 0, s>>>(h, saved, ws, K, Hd, M, J, per_sample);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  ReduceOut o{};
+  o.nseg = 1;
+  o.ptr[0] = grad_params;
+  o.begin[0] = 0;
+  return launch_reduce(per_sample, B, d.N, d.N, o, s);
+}
+
+}  // namespace cfc

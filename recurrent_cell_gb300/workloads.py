@@ -132,3 +132,46 @@ def make_tau_inputs(w: Workload, seed: int | None = None) -> dict:
         dt = np.full((1,), 1.0, dtype=np.float32)
     b = np.zeros((H,), dtype=np.float32)
     return dict(x=x, h0=h0, W_in=W_in, W_rec=W_rec, b=b, tau=tau, dt=dt, y=y)
+
+
+# Multi-horizon GRN heads on the trunk rows, FP32.  The pages' shapes:
+# HIDDEN = 128 (the CfC state), HEAD_MID = 64, 5 horizons, B = 32, K = 64
+# (B*K = 2048 rows).  h ~ U(-1, 1) (a tanh-bounded state); weights
+# Xavier-uniform with scale sqrt(1 / fan_in) as the pages initialise them
+# (W1, w_skip: fan_in HIDDEN; W2, w_gate, w_main: fan_in HEAD_MID); biases
+# ~ U(+-0.1) (the pages do not state theirs); grad_probs ~ N(0, 1) (dL/dp of a sum loss);
+# lambda ~ U(0.5, 1.5) per horizon; grad_h_carry ~ N(0, 0.1).
+@dataclass(frozen=True)
+class GrnWorkload:
+    name: str
+    B: int
+    K: int
+    hidden: int = 128
+    head_mid: int = 64
+    n_horizons: int = 5
+    seed: int = 0
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.K
+
+
+GRN_TINY = GrnWorkload("grn_tiny_B4_K8_32x16x3", B=4, K=8, hidden=32, head_mid=16, n_horizons=3)
+GRN_SMOKE = GrnWorkload("grn_smoke_B32_K64_128x64x5", B=32, K=64)
+
+
+def make_grn_inputs(w: GrnWorkload, seed: int | None = None) -> dict:
+    """Draw the inputs of a GRN-heads workload (float32 numpy arrays); the
+    parameter vector is packed in the documented order [W1 | b1 | W2 | b2 |
+    w_gate | b_gate | w_main | b_main | w_skip | b_skip]."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    Hd, M, J, R = w.hidden, w.head_mid, w.n_horizons, w.rows
+    sh, sm = np.sqrt(1.0 / Hd), np.sqrt(1.0 / M)
+    sizes_scales = [(J * M * Hd, sh), (J * M, 0.1), (J * M * M, sm), (J * M, 0.1), (J * M, sm), (J, 0.1),
+                    (J * M, sm), (J, 0.1), (J * Hd, sh), (J, 0.1)]
+    params = np.concatenate([rng.uniform(-a, a, size=n) for n, a in sizes_scales]).astype(np.float32)
+    h = rng.uniform(-1.0, 1.0, size=(R, Hd)).astype(np.float32)
+    grad_probs = rng.standard_normal((R, J)).astype(np.float32)
+    lam = rng.uniform(0.5, 1.5, size=(J,)).astype(np.float32)
+    carry = (0.1 * rng.standard_normal((R, Hd))).astype(np.float32)
+    return dict(h=h, params=params, grad_probs=grad_probs, lam=lam, carry=carry)

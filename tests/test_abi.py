@@ -171,3 +171,35 @@ def test_tau_argument_validation(lib):
 def test_selftest_timeout_argument_validation(lib):
     assert lib.cfc_selftest_timeout(0, None) == ERR_SHAPE
     assert lib.cfc_selftest_timeout((1 << 20) + 1, None) == ERR_SHAPE
+
+
+def test_grn_argument_validation(lib):
+    """GRN-heads entry points: lengths and argument checks, no launch."""
+    from oracle import grn_oracle as go
+    for Hd, M, J in ((128, 64, 5), (4, 4, 1), (256, 64, 8), (132, 20, 2)):
+        assert lib.cfc_grn_param_length(Hd, M, J) == go.grn_param_length(Hd, M, J)
+        assert lib.cfc_grn_saved_per_row(M, J) == J * (3 * M + 2)
+    assert lib.cfc_grn_param_length(130, 64, 5) == 0
+    assert lib.cfc_grn_param_length(128, 0, 5) == 0
+    assert lib.cfc_grn_param_length(128, 64, 0) == 0
+    B, K, Hd, M, J = 4, 8, 32, 16, 3
+    ws = lib.cfc_grn_workspace_bytes(B, K, Hd, M, J)
+    assert ws >= B * K * J * (2 * M + 3) * 4 and ws % 256 == 0
+    assert lib.cfc_grn_workspace_bytes(0, K, Hd, M, J) == 0
+
+    def fwd(h=P, rows=B * K, Hh=Hd, probs=P):
+        return lib.cfc_grn_forward(h, rows, Hh, M, J, P, probs, P, None)
+    assert fwd(rows=0, h=None) == 0                       # nothing to do
+    assert fwd(rows=-1) == ERR_SHAPE
+    assert fwd(Hh=6) == ERR_SHAPE
+    assert fwd(h=None) == ERR_NULL
+    assert fwd(probs=P + 4) == ERR_ALIGN
+
+    def bwd(gp=P, lam=P, carry=None, ws_bytes=ws, ws_ptr=P, Bb=B):
+        return lib.cfc_grn_backward(P, Bb, K, Hd, M, J, P, P, P, gp, lam, carry, P, P, P, ws_ptr, ws_bytes, None)
+    assert bwd(Bb=0) == ERR_SHAPE
+    assert bwd(gp=None) == ERR_NULL
+    assert bwd(lam=None) == ERR_NULL
+    assert bwd(carry=P + 8) == ERR_ALIGN
+    assert bwd(ws_bytes=ws - 1) == ERR_WORKSPACE
+    assert bwd(ws_ptr=None) == ERR_WORKSPACE
