@@ -48,6 +48,29 @@ def test_gradients_match_central_differences(name):
         assert g["grad_tau"][2] == 0.0
 
 
+def test_clamped_tau_gets_no_gradient_while_its_decay_is_live():
+    """A tau below the 1e-6 clamp enters the forward only as max(tau, 1e-6), so
+    the loss is flat in it and its gradient is exactly 0 ("grad_tau only
+    where tau > eps").  With a step dt of a few 1e-7 the clamped unit's decay
+    exp(-dt / 1e-6) stays near 0.8 instead of underflowing, so a gradient
+    formula that ignored the clamp would give a non-zero value here."""
+    c = _case(tau=[0.7, 1.3, 5e-7, 2.0], dt=[2e-7, 3e-7])
+    g = to.tau_backward(c["x"], c["h0"], c["W_in"], c["W_rec"], c["b"], c["tau"], c["dt"],
+                        grad_h_seq=c["gseq"], y=c["y"])
+    num = np.zeros(4)
+    for i in range(4):
+        # the live units' gradients are ~1e-6 (dt / tau^2 scale): a wide step
+        # keeps the difference quotient above the loss's rounding noise
+        eps = 1e-9 if c["tau"][i] < to.TAU_EPS else 1e-3
+        p, m = c["tau"].copy(), c["tau"].copy()
+        p[i] += eps
+        m[i] -= eps
+        num[i] = (_loss(c, tau=p) - _loss(c, tau=m)) / (2 * eps)
+    assert g["grad_tau"][2] == 0.0 and num[2] == 0.0
+    np.testing.assert_allclose(g["grad_tau"], num, rtol=1e-4, atol=1e-12)
+    assert np.all(np.abs(g["grad_tau"][[0, 1, 3]]) > 1e-9)      # the live units do move
+
+
 def test_zero_weights_closed_form():
     """W_in = W_rec = 0: s = tanh(b) every step, so h_K = s + decay^K (h0 - s)."""
     c = _case(B=3, K=7, n_in=2, H=5, seed=3)
