@@ -249,9 +249,13 @@ def cfc_grn_backward(h, params, probs, saved, grad_probs, lam, grad_h, per_sampl
                      B: int, K: int, head_mid: int, n_horizons: int, grad_h_carry=None, stream=None):
     """GRN heads backward for h [B*K, hidden] rows (r = b*K + k): grad_h,
     the per-sample gradient rows and their batch sum (packed parameter order)."""
+    R, Hd = h.shape
+    if B < 1 or K < 1 or R != B * K:
+        # the library reads B*K rows of every per-row tensor: a mismatch would
+        # read past the tensors, so it is refused here
+        raise ValueError(f"h has {R} rows; cfc_grn_backward needs B*K = {B}*{K} rows")
     torch = _torch()
     f32 = torch.float32
-    R, Hd = h.shape
     N = cfc_grn_param_length(Hd, head_mid, n_horizons)
     S = cfc_grn_saved_per_row(head_mid, n_horizons)
     J = n_horizons

@@ -203,3 +203,15 @@ def test_grn_argument_validation(lib):
     assert bwd(carry=P + 8) == ERR_ALIGN
     assert bwd(ws_bytes=ws - 1) == ERR_WORKSPACE
     assert bwd(ws_ptr=None) == ERR_WORKSPACE
+
+
+def test_grn_binding_refuses_a_row_count_other_than_B_times_K():
+    """The library reads B*K rows of h, probs, saved, grad_probs and grad_h;
+    the Python binding checks the row count before it touches the library or
+    a device (CPU tensors suffice: the check comes first)."""
+    torch = pytest.importorskip("torch")
+    h = torch.zeros(10, 8)
+    with pytest.raises(ValueError, match="B\\*K"):
+        cfc.cfc_grn_backward(h, None, None, None, None, None, None, None, None, None, 4, 3, 4, 1)
+    with pytest.raises(ValueError, match="B\\*K"):
+        cfc.cfc_grn_backward(h, None, None, None, None, None, None, None, None, None, 0, 10, 4, 1)
