@@ -347,54 +347,6 @@ int cfc_tau_kloop_backward(const float* x, const float* h0, const float* W_in, c
   return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
 }
 
-long long cfc_grn_param_length(int hidden, int head_mid, int n_horizons) {
-  return grn_shape_supported(hidden, head_mid, n_horizons) ? grn_param_length(hidden, head_mid, n_horizons) : 0;
-}
-
-long long cfc_grn_saved_per_row(int head_mid, int n_horizons) {
-  return grn_shape_supported(4, head_mid, n_horizons) ? grn_saved_per_row(head_mid, n_horizons) : 0;
-}
-
-size_t cfc_grn_workspace_bytes(int B, int K, int hidden, int head_mid, int n_horizons) {
-  if (B < 1 || K < 1 || !grn_shape_supported(hidden, head_mid, n_horizons)) return 0;
-  return align256((size_t)B * K * grn_ws_per_row(head_mid, n_horizons) * sizeof(float));
-}
-
-int cfc_grn_forward(const float* h, long long rows, int hidden, int head_mid, int n_horizons,
-                    const float* params, float* probs, float* saved, void* stream) {
-  if (rows < 0 || rows > (1ll << 31) || !grn_shape_supported(hidden, head_mid, n_horizons)) return CFC_ERR_SHAPE;
-  if (rows == 0) return CFC_OK;
-  const void* ptrs[] = {h, params, probs, saved};
-  for (const void* p : ptrs)
-    if (!p) return CFC_ERR_NULL;
-  for (const void* p : ptrs)
-    if (!al16(p)) return CFC_ERR_ALIGN;
-  cudaError_t e = launch_grn_forward(h, rows, hidden, head_mid, n_horizons, params, probs, saved,
-                                     static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
-}
-
-int cfc_grn_backward(const float* h, int B, int K, int hidden, int head_mid, int n_horizons, const float* params,
-                     const float* probs, const float* saved, const float* grad_probs, const float* lambda,
-                     const float* grad_h_carry, float* grad_h, float* per_sample_scratch, float* grad_params,
-                     void* workspace, size_t workspace_bytes, void* stream) {
-  if (B < 1 || K < 1 || (long long)B * K > (1ll << 31) || !grn_shape_supported(hidden, head_mid, n_horizons))
-    return CFC_ERR_SHAPE;
-  const void* ptrs[] = {h, params, probs, saved, grad_probs, lambda, grad_h, per_sample_scratch, grad_params};
-  for (const void* p : ptrs)
-    if (!p) return CFC_ERR_NULL;
-  for (const void* p : ptrs)
-    if (!al16(p)) return CFC_ERR_ALIGN;
-  if (grad_h_carry && !al16(grad_h_carry)) return CFC_ERR_ALIGN;
-  if (!workspace || workspace_bytes < cfc_grn_workspace_bytes(B, K, hidden, head_mid, n_horizons))
-    return CFC_ERR_WORKSPACE;
-  if (!al16(workspace)) return CFC_ERR_ALIGN;
-  cudaError_t e = launch_grn_backward(h, B, K, hidden, head_mid, n_horizons, params, probs, saved, grad_probs,
-                                      lambda, grad_h_carry, grad_h, static_cast<float*>(workspace),
-                                      per_sample_scratch, grad_params, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
-}
-
 int reduce_axis0_multi(const float* const* per_batch, const int* n_batch, const long long* n_tail,
                        float* const* out, int count, void* stream) {
   if (count < 0 || count > 4096) return CFC_ERR_SHAPE;

@@ -27,6 +27,9 @@
 //                  packed gradient row, summed over k = K-1 .. 0 (the pages'
 //                  loop order) and written once (no += into scratch).
 // reduce_axis0 then sums the B rows into the packed parameter gradient.
+//
+// The extern "C" entry points of the heads (declared in cfc.h) are at the end
+// of this file; they validate the arguments before anything is launched.
 #include "cfc_internal.cuh"
 
 namespace cfc {
@@ -501,3 +504,66 @@ cudaError_t launch_grn_backward(const float* h, int B, int K, int Hd, int M, int
 }
 
 }  // namespace cfc
+
+// ---------------------------------------------------------------------------
+// C entry points
+// ---------------------------------------------------------------------------
+
+namespace {
+bool grn_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t grn_align256(size_t v) { return (v + 255) & ~size_t(255); }
+}  // namespace
+
+using namespace cfc;
+
+extern "C" {
+
+long long cfc_grn_param_length(int hidden, int head_mid, int n_horizons) {
+  return grn_shape_supported(hidden, head_mid, n_horizons) ? grn_param_length(hidden, head_mid, n_horizons) : 0;
+}
+
+long long cfc_grn_saved_per_row(int head_mid, int n_horizons) {
+  return grn_shape_supported(4, head_mid, n_horizons) ? grn_saved_per_row(head_mid, n_horizons) : 0;
+}
+
+size_t cfc_grn_workspace_bytes(int B, int K, int hidden, int head_mid, int n_horizons) {
+  if (B < 1 || K < 1 || !grn_shape_supported(hidden, head_mid, n_horizons)) return 0;
+  return grn_align256((size_t)B * K * grn_ws_per_row(head_mid, n_horizons) * sizeof(float));
+}
+
+int cfc_grn_forward(const float* h, long long rows, int hidden, int head_mid, int n_horizons,
+                    const float* params, float* probs, float* saved, void* stream) {
+  if (rows < 0 || rows > (1ll << 31) || !grn_shape_supported(hidden, head_mid, n_horizons)) return CFC_ERR_SHAPE;
+  if (rows == 0) return CFC_OK;
+  const void* ptrs[] = {h, params, probs, saved};
+  for (const void* p : ptrs)
+    if (!p) return CFC_ERR_NULL;
+  for (const void* p : ptrs)
+    if (!grn_al16(p)) return CFC_ERR_ALIGN;
+  cudaError_t e = launch_grn_forward(h, rows, hidden, head_mid, n_horizons, params, probs, saved,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
+}
+
+int cfc_grn_backward(const float* h, int B, int K, int hidden, int head_mid, int n_horizons, const float* params,
+                     const float* probs, const float* saved, const float* grad_probs, const float* lambda,
+                     const float* grad_h_carry, float* grad_h, float* per_sample_scratch, float* grad_params,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || K < 1 || (long long)B * K > (1ll << 31) || !grn_shape_supported(hidden, head_mid, n_horizons))
+    return CFC_ERR_SHAPE;
+  const void* ptrs[] = {h, params, probs, saved, grad_probs, lambda, grad_h, per_sample_scratch, grad_params};
+  for (const void* p : ptrs)
+    if (!p) return CFC_ERR_NULL;
+  for (const void* p : ptrs)
+    if (!grn_al16(p)) return CFC_ERR_ALIGN;
+  if (grad_h_carry && !grn_al16(grad_h_carry)) return CFC_ERR_ALIGN;
+  if (!workspace || workspace_bytes < cfc_grn_workspace_bytes(B, K, hidden, head_mid, n_horizons))
+    return CFC_ERR_WORKSPACE;
+  if (!grn_al16(workspace)) return CFC_ERR_ALIGN;
+  cudaError_t e = launch_grn_backward(h, B, K, hidden, head_mid, n_horizons, params, probs, saved, grad_probs,
+                                      lambda, grad_h_carry, grad_h, static_cast<float*>(workspace),
+                                      per_sample_scratch, grad_params, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CFC_OK : CFC_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -169,18 +169,6 @@ cudaError_t launch_tau_backward(const float* x, const float* h0, const float* W_
                                 float* grad_x, float* grad_W_in, float* grad_W_rec, float* grad_b,
                                 float* grad_tau, cudaStream_t s);
 
-// multi-horizon GRN heads (cfc_grn.cu), FP32.
-bool grn_shape_supported(int Hd, int M, int J);
-long long grn_param_length(int Hd, int M, int J);
-long long grn_saved_per_row(int M, int J);
-long long grn_ws_per_row(int M, int J);
-cudaError_t launch_grn_forward(const float* h, long long R, int Hd, int M, int J, const float* params,
-                               float* probs, float* saved, cudaStream_t s);
-cudaError_t launch_grn_backward(const float* h, int B, int K, int Hd, int M, int J, const float* params,
-                                const float* probs, const float* saved, const float* grad_probs,
-                                const float* lambda, const float* grad_h_carry, float* grad_h, float* ws,
-                                float* per_sample, float* grad_params, cudaStream_t s);
-
 // count matrices (host arrays of device pointers and sizes, already checked),
 // one launch per kernel configuration and up to 32 matrices.
 cudaError_t launch_reduce_multi(const float* const* in, const int* n_batch, const long long* n_tail,
