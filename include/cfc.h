@@ -1,15 +1,24 @@
 /*
  * cfc.h -- C ABI of the batched CfC K-loop library for one NVIDIA GB300 (sm_103a).
  *
- * Three operations:
+ * The three operations of the method:
  *
  *   cfc_kloop_forward   the three-head closed-form continuous-time (CfC) cell
  *                       run over K steps for B independent samples;
  *   cfc_kloop_backward  backward through time: parameter gradients summed over
  *                       the batch, grad_h0 and (optionally) grad_x;
  *   reduce_axis0        deterministic, atomic-free column sum [B, N] -> [N];
- *   reduce_axis0_multi  the same for a list of matrices in few launches;
- *   cfc_tau_kloop_*     the pages' single-head tau-cell K loop (FP32).
+ *
+ * and around them:
+ *
+ *   reduce_axis0_multi  reduce_axis0 for a list of matrices in few launches;
+ *   cfc_tau_kloop_*     the pages' single-head tau-cell K loop (FP32);
+ *   cfc_grn_*           the multi-horizon GRN heads on every K position (FP32);
+ *   cfc_kloop_forward_backward_static
+ *                       forward + backward for callers that cannot allocate
+ *                       device memory (fixed workspace inside the library);
+ *   helpers             workspace sizes, status strings, the device error
+ *                       word and its self-test, per-kernel event tracing.
  *
  * Cell (per sample, step k = 0..K-1, heads c = f, g, h~ in that order):
  *   A_c    = b[c] + W_in[c] x_k + W_rec[c] h_k
