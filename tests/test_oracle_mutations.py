@@ -52,6 +52,8 @@ def cfc_checks(m):
         ("tf32 definition", p.test_tf32_rounding_definition),
         ("bf16 rounding points", lambda: p.test_mode_rounding_points_single_step(m.BF16, m.round_bf16)),
         ("tf32 rounding points", lambda: p.test_mode_rounding_points_single_step(m.TF32, m.round_tf32)),
+        ("bf16 operands", lambda: p.test_mode_rounds_every_contraction_operand(m.BF16, m.round_bf16)),
+        ("tf32 operands", lambda: p.test_mode_rounds_every_contraction_operand(m.TF32, m.round_tf32)),
         ("reduce: integer sums", lambda: r.test_integer_valued_sums_are_exact(1031, 3)),
         ("reduce: empty", r.test_empty_batch_gives_zero),
         ("reduce: copy", r.test_single_row_is_a_copy),
@@ -156,6 +158,14 @@ MUTANTS = [
     # precision modes
     ("cfc_oracle.py", "bf16 state not rounded", "return round_bf16(h)", "return np.asarray(h, dtype=np.float64)"),
     ("cfc_oracle.py", "dA not rounded", "dAo = _operand(dA, mode)", "dAo = dA"),
+    ("cfc_oracle.py", "W_in not rounded in the projection",
+     "Wi = _operand(W_in, mode)\n", "Wi = np.asarray(W_in, dtype=np.float64)\n"),
+    ("cfc_oracle.py", "state operand not rounded in the projection",
+     "ho = _operand(h_k, mode)", "ho = np.asarray(h_k, dtype=np.float64)"),
+    ("cfc_oracle.py", "W_in not rounded in grad_x",
+     "Wi = _operand(W_in, mode).reshape(3 * H, n_in)", "Wi = np.asarray(W_in, dtype=np.float64).reshape(3 * H, n_in)"),
+    ("cfc_oracle.py", "x not rounded in the weight gradient",
+     "Z = np.concatenate([_operand(x, mode)", "Z = np.concatenate([np.asarray(x, dtype=np.float64)"),
     ("cfc_oracle.py", "bf16 ties away from zero", "lsb = (u >> 16) & 1", "lsb = 0 * u"),
     ("cfc_oracle.py", "tf32 truncation", "u = (u + 0x1000) & 0xFFFFE000", "u = u & 0xFFFFE000"),
     # reducer order

@@ -281,3 +281,36 @@ def test_mode_rounding_points_single_step(mode, rnd):
     np.testing.assert_array_equal(gb, rnd(gb_ref))
     np.testing.assert_allclose(gWi, np.einsum("bci,bj->bcij", gb, x[:, 0]), rtol=1e-15, atol=0)
     np.testing.assert_allclose(gWr, np.einsum("bci,bj->bcij", gb, h0), rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("mode, rnd", [(BF16, oracle.round_bf16), (TF32, oracle.round_tf32)])
+def test_mode_rounds_every_contraction_operand(mode, rnd):
+    """Unrounded float64 inputs over K = 3 steps.  Forward: each step of a
+    reduced-precision mode is an FP32 step on operands rounded to the mode's
+    type (x_k, h_k, W_in, W_rec), and only BF16 rounds the carried state (h0
+    arrives bf16 in that mode).  Backward: dA is mode-valued, and grad_x,
+    grad_h0 and the weight gradients are its contractions with the rounded
+    W_in, W_rec, x_k and h_k."""
+    B, K, n_in, H = 3, 3, 4, 5
+    x, h0, W_in, W_rec, b, dt = _rand_problem(B, K, n_in, H, seed=61)
+    got = oracle.backward(x, h0, W_in, W_rec, b, dt, mode, y=np.ones((B, H)))
+    h = rnd(h0) if mode == BF16 else h0
+    hs = [h]
+    for k in range(K):
+        h_next = oracle.cell_forward(rnd(x[:, k]), rnd(h), rnd(W_in), rnd(W_rec), b, dt, FP32)[0]
+        if mode == BF16:
+            h_next = rnd(h_next)
+        np.testing.assert_array_equal(got["h_seq"][:, k], h_next)
+        h = h_next
+        hs.append(h)
+    dA = got["dA"].reshape(B, K, 3 * H)
+    np.testing.assert_array_equal(rnd(dA), dA)
+    assert np.any(dA != 0.0)
+    for k in range(K):
+        np.testing.assert_allclose(got["grad_x"][:, k], dA[:, k] @ rnd(W_in).reshape(3 * H, n_in),
+                                   rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(got["grad_h0"], dA[:, 0] @ rnd(W_rec).reshape(3 * H, H), rtol=1e-14, atol=1e-15)
+    gWi = np.einsum("bkc,bkj->cj", dA, rnd(x)).reshape(3, H, n_in)
+    gWr = np.einsum("bkc,bkj->cj", dA, rnd(np.stack(hs[:-1], axis=1))).reshape(3, H, H)
+    np.testing.assert_allclose(got["grad_W_in"], gWi, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(got["grad_W_rec"], gWr, rtol=1e-13, atol=1e-15)
