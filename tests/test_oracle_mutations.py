@@ -78,6 +78,7 @@ def tau_checks(m):
         ("huge tau", p.test_huge_tau_keeps_the_state),
         ("independence", p.test_samples_are_independent_and_rows_sum_to_the_batch_gradient),
         ("clamped tau, live decay", p.test_clamped_tau_gets_no_gradient_while_its_decay_is_live),
+        ("clamp value", p.test_clamp_value_in_the_closed_form),
     ]
     for name in ("W_in", "W_rec", "b", "tau", "h0", "x"):
         checks.append((f"finite differences {name}", lambda n=name: p.test_gradients_match_central_differences(n)))
@@ -168,6 +169,10 @@ MUTANTS = [
      "Z = np.concatenate([_operand(x, mode)", "Z = np.concatenate([np.asarray(x, dtype=np.float64)"),
     ("cfc_oracle.py", "bf16 ties away from zero", "lsb = (u >> 16) & 1", "lsb = 0 * u"),
     ("cfc_oracle.py", "tf32 truncation", "u = (u + 0x1000) & 0xFFFFE000", "u = u & 0xFFFFE000"),
+    ("cfc_oracle.py", "first sample's dt for every sample", "    return dt\n", "    return np.full(B, dt[0])\n"),
+    ("cfc_oracle.py", "last-step seeds added at every step", "        if k == K - 1:\n", "        if True:\n"),
+    ("cfc_oracle.py", "weight gradient's h_k shifted by one step",
+     "h_seq[:, :-1]], axis=1)", "h_seq[:, 1:]], axis=1)"),
     # reducer order
     ("cfc_oracle.py", "leaf rows in descending order",
      "for bi in range(t, B, T):", "for bi in reversed(range(t, B, T)):"),
@@ -184,6 +189,12 @@ MUTANTS = [
     ("tau_oracle.py", "carry through W_rec^T", "carry = d_pre @ Wr + dh * d", "carry = d_pre @ Wr.T + dh * d"),
     ("tau_oracle.py", "grad_tau sign", "dh * (hp - s) * d", "dh * (s - hp) * d"),
     ("tau_oracle.py", "clamp ignored in grad_tau", "np.where(live[None, :], ", "np.where(True, "),
+    ("tau_oracle.py", "clamp at 1e-3", "TAU_EPS = 1e-6", "TAU_EPS = 1e-3"),
+    ("tau_oracle.py", "clamp at 1e-9", "TAU_EPS = 1e-6", "TAU_EPS = 1e-9"),
+    ("tau_oracle.py", "gradient mask at tau >= eps", "live = tau > TAU_EPS", "live = tau >= TAU_EPS"),
+    ("tau_oracle.py", "first sample's dt for every sample",
+     "return np.full(B, dt[0]) if dt.size == 1 else dt", "return np.full(B, dt[0])"),
+    ("tau_oracle.py", "last-step seeds added at every step", "        if k == K - 1:\n", "        if True:\n"),
     # GRN heads
     ("grn_oracle.py", "GELU with the wrong CDF scale",
      "return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))", "return 0.5 * z * (1.0 + erf(z))"),

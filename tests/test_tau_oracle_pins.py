@@ -71,6 +71,27 @@ def test_clamped_tau_gets_no_gradient_while_its_decay_is_live():
     assert np.all(np.abs(g["grad_tau"][[0, 1, 3]]) > 1e-9)      # the live units do move
 
 
+def test_clamp_value_in_the_closed_form():
+    """W = 0 with step sizes of a few 1e-7, so that the decay of units with
+    tau near the clamp is neither 0 nor 1: h_K = s + decay^K (h0 - s) with
+    decay = exp(-dt / max(tau, 1e-6)), the pages' constant written out here.
+    Units below, at, just above and well above 1e-6; those above it get a
+    non-zero tau gradient, the others exactly zero."""
+    tau = np.array([5e-7, 1e-6, 3e-6, 1e-5, 1.0])
+    dt = np.array([2e-7, 3e-7])
+    c = _case(B=2, K=4, n_in=2, H=5, seed=13, tau=tau, dt=dt)
+    c["W_in"][:] = 0.0
+    c["W_rec"][:] = 0.0
+    hs = to.tau_forward(c["x"], c["h0"], c["W_in"], c["W_rec"], c["b"], c["tau"], c["dt"])["h_seq"]
+    s = np.tanh(c["b"])[None, :]
+    d = np.exp(-dt[:, None] / np.maximum(tau, 1e-6)[None, :])
+    for k in range(4):
+        np.testing.assert_allclose(hs[:, k], s + d ** (k + 1) * (c["h0"] - s), rtol=1e-13, atol=1e-14)
+    g = to.tau_backward(c["x"], c["h0"], c["W_in"], c["W_rec"], c["b"], c["tau"], c["dt"], y=c["y"])
+    assert g["grad_tau"][0] == 0.0 and g["grad_tau"][1] == 0.0
+    assert np.all(g["grad_tau"][2:] != 0.0)
+
+
 def test_zero_weights_closed_form():
     """W_in = W_rec = 0: s = tanh(b) every step, so h_K = s + decay^K (h0 - s)."""
     c = _case(B=3, K=7, n_in=2, H=5, seed=3)
