@@ -209,6 +209,12 @@ MUTANTS = [
      'da1 = np.einsum("jmn,rjm->rjn", P["W2"], dz2)', 'da1 = np.einsum("jnm,rjm->rjn", P["W2"], dz2)'),
     ("grn_oracle.py", "skip path dropped from the trunk gradient",
      ' + dskip[:, :, None] * P["w_skip"][None]', ""),
+    ("grn_oracle.py", "b1 dropped", 'P["W1"], h) + P["b1"][None]', 'P["W1"], h)'),
+    ("grn_oracle.py", "sigmoid' dropped from dlogit", "dlogit = gp * p * (1.0 - p)", "dlogit = gp * p"),
+    ("grn_oracle.py", "gate and main weights swapped in dz2",
+     'dmain[:, :, None] * P["w_main"][None] + dgate[:, :, None] * P["w_gate"][None]',
+     'dmain[:, :, None] * P["w_gate"][None] + dgate[:, :, None] * P["w_main"][None]'),
+    ("grn_oracle.py", "skip term halved", 'skip = h @ P["w_skip"].T', 'skip = h @ P["w_skip"].T * 0.5'),
     ("grn_oracle.py", "rows taken step-major",
      "per_row = pack_grn(rows, Hd, M, J).reshape(B, K, -1)",
      "per_row = pack_grn(rows, Hd, M, J).reshape(K, B, -1).transpose(1, 0, 2)"),
