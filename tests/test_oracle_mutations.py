@@ -57,6 +57,7 @@ def cfc_checks(m):
         ("reduce: integer sums", lambda: r.test_integer_valued_sums_are_exact(1031, 3)),
         ("reduce: empty", r.test_empty_batch_gives_zero),
         ("reduce: copy", r.test_single_row_is_a_copy),
+        ("reduce: -0.0 columns", lambda: [r.test_negative_zero_columns_sum_to_positive_zero(b) for b in (2, 256)]),
         ("reduce: bit-reversed tree", r.test_equals_contiguous_tree_over_bit_reversed_leaves),
     ]
     for name, col, expect in r.load_reduce_golden():
@@ -179,6 +180,8 @@ MUTANTS = [
     ("cfc_oracle.py", "tree pairs adjacent leaves",
      "p[:s] = p[:s] + p[s:2 * s]", "p[:s] = p[0:2 * s:2] + p[1:2 * s:2]"),
     ("cfc_oracle.py", "128 leaves", "T = REDUCE_THREADS", "T = REDUCE_THREADS // 2"),
+    ("cfc_oracle.py", "leaf sums start from -0.0",
+     "acc = np.zeros(N, dtype=np.float32)", "acc = np.full(N, -0.0, dtype=np.float32)"),
     # tau cell
     ("tau_oracle.py", "decay sign", "np.exp(-np.asarray(dt_b", "np.exp(np.asarray(dt_b"),
     ("tau_oracle.py", "decay and input weight swapped",

@@ -50,6 +50,16 @@ def test_empty_batch_gives_zero():
     assert np.all(out.view(np.uint32) == 0)
 
 
+@pytest.mark.parametrize("B", [1, 2, 255, 256, 300])
+def test_negative_zero_columns_sum_to_positive_zero(B):
+    """Every leaf starts from +0.0f, and +0.0f + (-0.0f) = +0.0f under round to
+    nearest, so a column of -0.0 sums to +0.0 whatever B is; a sum that
+    started from the first row instead would keep -0.0 once all 256 leaves
+    hold one."""
+    out = oracle.reduce_axis0(np.full((B, 3), -0.0, np.float32))
+    assert np.all(out.view(np.uint32) == 0), B
+
+
 def test_single_row_is_a_copy():
     a = np.random.default_rng(0).standard_normal((1, 100)).astype(np.float32)
     np.testing.assert_array_equal(oracle.reduce_axis0(a), a[0])
