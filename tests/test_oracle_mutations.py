@@ -134,7 +134,12 @@ MUTANTS = [
      "ho @ Wr.reshape(3 * H, H).T", "ho @ Wr.transpose(0, 2, 1).reshape(3 * H, H).T"),
     ("cfc_oracle.py", "bias dropped",
      "A = (np.asarray(b, dtype=np.float64)", "A = (0.0 * np.asarray(b, dtype=np.float64)"),
+    ("cfc_oracle.py", "heads interleaved per unit instead of head-major",
+     ".T).reshape(n, 3, H)", ".T).reshape(n, H, 3).transpose(0, 2, 1)"),
+    ("cfc_oracle.py", "h~ head reads the g pre-activation", "hh = np.tanh(A[:, 2])", "hh = np.tanh(A[:, 1])"),
     # backward
+    ("cfc_oracle.py", "grad_x written at the mirrored step",
+     "grad_x[:, k] = dAo.reshape(B, 3 * H) @ Wi", "grad_x[:, K - 1 - k] = dAo.reshape(B, 3 * H) @ Wi"),
     ("cfc_oracle.py", "dA_g without tanh'",
      "dA[:, 1] = delta * gate * (1.0 - g * g)", "dA[:, 1] = delta * gate"),
     ("cfc_oracle.py", "dA_h with gate for 1 - gate",
