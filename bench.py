@@ -543,6 +543,22 @@ def oracle_sample_batch(w):
     return min(w.B, {wl.MATH_FP32: 64}.get(w.math, 128))
 
 
+def host_cpu():
+    """The host the oracle runs on: architecture, logical CPUs, model name
+    where /proc/cpuinfo gives one."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model", "hardware")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return dict(arch=platform.machine(), logical_cpus=os.cpu_count(), model=model)
+
+
 def time_oracle(w, seconds=10.0, max_reps=None):
     import oracle
     b = oracle_sample_batch(w)
@@ -557,7 +573,7 @@ def time_oracle(w, seconds=10.0, max_reps=None):
         if el >= seconds or (max_reps and reps >= max_reps):
             break
     value = reps * b * w.K / el
-    return dict(value=value, unit=UNIT, cores=1, kind="oracle",
+    return dict(value=value, unit=UNIT, cores=1, kind="oracle", host=host_cpu(),
                 sample=f"{reps} x oracle fwd+bwd on {b} of {w.B} samples, K={w.K} "
                        f"({el:.1f} s, numpy float64, 1 BLAS thread)"), el / reps
 
@@ -603,7 +619,7 @@ def main():
                     data="synthetic",
                     config=dict(workload=w.name, B=w.B, K=w.K, n_in=w.n_in, n_hid=w.n_hid,
                                 math=wl.MATH_NAMES[w.math], sample_batch=b),
-                    cpu_baseline=dict(kind="oracle", cores=1, value=value, unit=UNIT,
+                    cpu_baseline=dict(kind="oracle", cores=1, value=value, unit=UNIT, host=host_cpu(),
                                       sample=f"each step: oracle fwd+bwd on {b} of {w.B} samples"),
                     e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
         print(json.dumps(line))
