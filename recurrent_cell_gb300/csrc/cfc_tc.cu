@@ -347,12 +347,6 @@ cudaError_t launch_mode(const Layout& L, const CfcArgs& a, float* out, cudaStrea
 // k = 0 rows, warp 1 issues the MMAs (N pieces of at most 256 columns; the
 // accumulator D[128 x Ntot] lives in TMEM), and all eight warps write D into
 // the packed partial row of split s at the end.  Waits are bounded.
-//
-// The M tiles of one split form a thread-block cluster (up to 8): every tile
-// needs the same z blocks, so each z block of a chunk is fetched by one CTA
-// and multicast to all; a stage is refilled once the MMAs of every CTA of the
-// cluster have released it (MMA completion multicast to every CTA's `empty`
-// barrier).  This cuts the L2 -> SM traffic of z by the cluster size.
 // ---------------------------------------------------------------------------
 constexpr int kTmaRows = 64;                    // rows (MMA K) per chunk
 constexpr int kTmaBlock = kTmaRows * 128;       // one 64-column block of a chunk
@@ -361,7 +355,6 @@ constexpr int kTmaWarpProducer = 0, kTmaWarpMma = 1, kTmaWarpPatch = 2;
 constexpr uint32_t kTmaTmemCols = 512;
 
 struct TmaWgradPlan {
-  int C = 1;             // cluster size (M tiles sharing z by multicast)
   int nx = 0, nh = 0;    // 64-column blocks of x and of h
   int Ntot = 0;          // accumulator columns: Zc + 1 rounded up to 16
   int nMt = 0, S = 0, chunks = 0, stages = 0;
@@ -371,44 +364,7 @@ struct TmaWgradPlan {
 
 __global__ void k_wgrad_tma(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                             const __grid_constant__ CUtensorMap, const __nv_bfloat16*, int, int, int, int, int,
-                            int, int, int, int, int, float*);
-
-// Clusters of C blocks (kTcThreads threads, smem bytes each) of k_wgrad_tma
-// resident at once on the current device; 0 if it cannot be queried.
-int max_active_clusters(int C, size_t smem) {
-  static std::mutex mu;
-  static int cached_dev = -1, cached_C = 0, cached_n = 0;
-  static size_t cached_smem = 0;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev == cached_dev && C == cached_C && smem == cached_smem) return cached_n;
-  if (cudaFuncSetAttribute(k_wgrad_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)C, 64, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_wgrad_tma, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cached_dev = dev;
-  cached_C = C;
-  cached_smem = smem;
-  cached_n = n;
-  return n;
-}
+                            int, int, int, int, float*);
 
 bool plan_tma_wgrad(int B, int K, int n_in, int H, int math, int grad_path, TmaWgradPlan* p) {
   if (math != CFC_MATH_BF16 || grad_path != CFC_GRAD_GEMM) return false;
@@ -438,19 +394,8 @@ bool plan_tma_wgrad(int B, int K, int n_in, int H, int math, int grad_path, TmaW
   p->stages = (int)std::min<size_t>(kTmaMaxStages, (227 * 1024 - 1024) / p->stage_bytes);
   if (p->stages < 2) return false;
   p->smem = 1024 + (size_t)p->stages * p->stage_bytes;
-  // z multicast across the M tiles of a split (CFC_WGRAD_MULTICAST): measured
-  // slower than one CTA per tile (the cluster advances at its slowest CTA's
-  // pace and fewer clusters fit), so off by default.
-  p->C = (p->nMt <= 8 && getenv("CFC_WGRAD_MULTICAST")) ? p->nMt : 1;
-  // One wave: as many splits as clusters of C CTAs fit at once (clusters live
-  // inside one GPC, so this can be below 152 / C); 152 / nMt without a
-  // device or without clusters.
-  int fit = kNumSMs / p->nMt;
-  if (p->C > 1) {
-    const int q = max_active_clusters(p->C, p->smem);
-    if (q > 0) fit = q;
-  }
-  p->S = std::max(1, std::min(p->chunks, fit));
+  // One wave: every M tile of every split resident at once.
+  p->S = std::max(1, std::min(p->chunks, kNumSMs / p->nMt));
   return true;
 }
 
@@ -461,27 +406,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "[%5];" ::"r"(tc::smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(tc::smem_u32(bar))
       : "memory");
-}
-// The same box delivered to every CTA of the cluster in `mask` (same
-// shared-memory offset, each CTA's own mbarrier at the same offset).
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3, %4}], [%5], %6;" ::"r"(tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(tc::smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   tc::smem_u32(bar)),
-               "h"(mask)
-               : "memory");
-}
-__device__ __forceinline__ uint32_t cta_rank_in_cluster() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
 }
 __device__ __forceinline__ void expect_tx_bytes(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
@@ -523,10 +447,8 @@ __device__ __forceinline__ void chunk_origin(int c, int K, int nb, int* b0, int*
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ CUtensorMap map_x,
             const __grid_constant__ CUtensorMap map_h, const __nv_bfloat16* __restrict__ h0, int K, int n_in,
-            int H, int chunks, int S, int stages, int kb, int nb, int Ntot, int C, float* __restrict__ out) {
+            int H, int chunks, int S, int stages, int kb, int nb, int Ntot, float* __restrict__ out) {
   const int mt = blockIdx.x, s = blockIdx.y;
-  const uint32_t rank = (C > 1) ? cta_rank_in_cluster() : 0u;
-  const uint16_t cmask = (uint16_t)((1u << C) - 1u);
   const int c_begin = (int)((long long)chunks * s / S), c_end = (int)((long long)chunks * (s + 1) / S);
   const int nx = n_in / 64, nh = H / 64;
   const int H3 = 3 * H, Zc = n_in + H;
@@ -545,7 +467,7 @@ k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ 
     for (int i = 0; i < stages; ++i) {
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&ready[i], 1);
-      tc::mbar_init(&empty[i], C);   // MMA completion of every CTA of the cluster
+      tc::mbar_init(&empty[i], 1);
     }
     tc::mbar_init(&done, 1);
     tc::mbar_init_fence();
@@ -566,10 +488,6 @@ k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ 
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
-  if (C > 1) {   // every CTA's barriers are initialised before any multicast lands
-    cluster_arrive_release();
-    cluster_wait_acquire();
-  }
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
 
@@ -589,15 +507,12 @@ k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ 
         expect_tx_bytes(&full[st], tx_bytes);
         tma_load_3d(base, &map_dA, mt * 128, k0, b0, &full[st]);
         tma_load_3d(base + kTmaBlock, &map_dA, mt * 128 + 64, k0, b0, &full[st]);
-        // z blocks: block j by CTA j % C, multicast to the cluster
         for (int j = 0; j < nx + nh; ++j) {
-          if (C > 1 && (uint32_t)(j % C) != rank) continue;
           uint8_t* dst = base + (size_t)(2 + j) * kTmaBlock;
           const CUtensorMap* map = (j < nx) ? &map_x : &map_h;
           const int col = (j < nx) ? 64 * j : 64 * (j - nx);
           const int kc = (j < nx) ? k0 : k0 - 1;
-          if (C > 1) tma_load_3d_mc(dst, map, col, kc, b0, &full[st], cmask);
-          else tma_load_3d(dst, map, col, kc, b0, &full[st]);
+          tma_load_3d(dst, map, col, kc, b0, &full[st]);
         }
       }
       __syncwarp();
@@ -689,8 +604,7 @@ k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ 
           tc::mma_bf16(tmem, ad, bd, id1, acc);
           if (n2 > 0) tc::mma_bf16(tmem + 256, ad, tc::sdesc_advance(bd, 4 * kTmaBlock), id2, acc);
         }
-        if (C > 1) mma_commit_multicast(&empty[st], cmask);
-        else tc::mma_commit(&empty[st]);
+        tc::mma_commit(&empty[st]);
       }
       __syncwarp();
       if (++st == stages) {
@@ -737,10 +651,6 @@ k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ 
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (C > 1) {   // no CTA leaves while a peer may still signal its barriers
-    cluster_arrive_release();
-    cluster_wait_acquire();
-  }
   if (*errp) atomicExch(&g_cfc_device_error, 1);
   if (warp == 0) tc::tmem_dealloc(tmem, kTmaTmemCols);
 }
@@ -785,22 +695,11 @@ cudaError_t launch_wgrad_tma(const Layout& L, const TmaWgradPlan& p, const CfcAr
     return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k_wgrad_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  const int C = p.C;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.nMt, (unsigned)p.S, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = p.smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   TraceScope trace("wgrad_tma_tc", s);
-  return cudaLaunchKernelEx(&cfg, k_wgrad_tma, mdA, mx, mh, static_cast<const __nv_bfloat16*>(a.h0), L.K, L.n_in,
-                            L.H, p.chunks, p.S, p.stages, p.kb, p.nb, p.Ntot, C, out);
+  k_wgrad_tma<<<dim3((unsigned)p.nMt, (unsigned)p.S, 1), kTcThreads, p.smem, s>>>(
+      mdA, mx, mh, static_cast<const __nv_bfloat16*>(a.h0), L.K, L.n_in, L.H, p.chunks, p.S, p.stages, p.kb, p.nb,
+      p.Ntot, out);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

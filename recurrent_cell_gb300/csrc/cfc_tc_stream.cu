@@ -69,29 +69,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 
-// Multicast forms: one copy lands at the same shared-memory offset of every
-// CTA in `mask` and completes the transaction bytes on each one's mbarrier;
-// one MMA completion arrives on the mbarrier of every CTA in `mask`.
-__device__ __forceinline__ void bulk_g2s_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                            uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(tc::smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   tc::smem_u32(bar)),
-               "h"(mask)
-               : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
 template <typename ET>
 __device__ __forceinline__ void st_elem(uint8_t* p, float v) {
   if constexpr (sizeof(ET) == 4) *reinterpret_cast<float*>(p) = v;
@@ -229,13 +206,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restrict__ wtiles,
               const ET* __restrict__ x, const ET* __restrict__ h0, const float* __restrict__ bias,
               const float* __restrict__ dt, int dt_stride, int B, int K, int n_in, int H, int Bt, int nUB,
-              int nAk, int nst, uint32_t tmem_cols, int C, ET* __restrict__ h_seq, float* __restrict__ act) {
+              int nAk, int nst, uint32_t tmem_cols, ET* __restrict__ h_seq, float* __restrict__ act) {
   constexpr int EPU = 16 / (int)sizeof(ET);
   constexpr int EPA = 128 / (int)sizeof(ET);
   const int Zc = n_in + H, H3 = 3 * H;
   const int nM = 3 * nUB;
-  const uint32_t rank = (C > 1) ? cluster_rank() : 0u;
-  const uint16_t cmask = (uint16_t)((1u << C) - 1u);
   const int Kpad = nAk * EPA;
   const int b0 = blockIdx.x * Bt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
@@ -258,7 +233,7 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
   if (tid == 0) {
     for (int i = 0; i < nst; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], C);   // one MMA completion of every CTA of the cluster
+      tc::mbar_init(&empty[i], 1);
     }
     tc::mbar_init(&acc0, 1);
     tc::mbar_init(&acc1, 1);
@@ -269,10 +244,6 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
   if (warp == 0) tc::tmem_alloc(&tmem_base, tmem_cols);
   tc::fence_before_sync();
   __syncthreads();
-  if (C > 1) {   // every CTA's barriers are initialised before any remote arrival
-    cluster_arrive_release();
-    cluster_wait_acquire();
-  }
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
   volatile int* err_flag = &err;
@@ -316,10 +287,9 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
 
   if (warp == kFwdProducerWarp) {
     // ---- producer warp: the W_cat stages of every step, in schedule order,
-    // through the ring.  In a cluster of C CTAs stage g is fetched once, by
-    // CTA g % C, and multicast to all; a slot is refilled once every CTA's
-    // MMAs released it.
-    int st = 0, t = 0, issuer = 0;
+    // through the ring; a slot is refilled once the MMAs that read it have
+    // committed to its `empty` barrier.
+    int st = 0, t = 0;
     uint32_t wrap = 0;
     for (long long g = 0; g < total_tiles; ++g) {
       if (__shfl_sync(0xffffffffu, *err_flag, 0)) break;
@@ -330,12 +300,10 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
       if (lane == 0) {
         expect_tx(&full[st], kStage);
         const uint8_t* src = wtiles + ((size_t)sched.pa[t] * nM + sched.m[t]) * kStage;
-        if (C == 1) bulk_g2s(stage + (size_t)st * kStage, src, kStage, &full[st]);
-        else if ((uint32_t)issuer == rank) bulk_g2s_mc(stage + (size_t)st * kStage, src, kStage, &full[st], cmask);
+        bulk_g2s(stage + (size_t)st * kStage, src, kStage, &full[st]);
       }
       __syncwarp();
       if (++t == T) t = 0;
-      if (++issuer == C) issuer = 0;
       if (++st == nst) {
         st = 0;
         ++wrap;
@@ -382,8 +350,7 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
               }
             }
           }
-          if (C == 1) tc::mma_commit(&empty[cst]);
-          else mma_commit_mc(&empty[cst], cmask);
+          tc::mma_commit(&empty[cst]);
           if (t == sched.nacc0 - 1) tc::mma_commit(&acc0);
           if (t == T - 1) tc::mma_commit(&acc1);
         }
@@ -505,16 +472,12 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (C > 1) {   // no CTA leaves while a peer may still signal its barriers
-    cluster_arrive_release();
-    cluster_wait_acquire();
-  }
   if (err) atomicExch(&g_tc_bwd_error, 1);
   if (warp == 0) tc::tmem_dealloc(tmem, tmem_cols);
 }
 
 struct FwdPlan {
-  int Bt = 0, nUB = 0, nAk = 0, nst = 0, C = 1;
+  int Bt = 0, nUB = 0, nAk = 0, nst = 0;
   uint32_t tmem_cols = 0;
   size_t smem = 0;
   TileSchedule sched;
@@ -593,10 +556,6 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
   while (cols < (uint32_t)(nM * Bt)) cols <<= 1;
   p->tmem_cols = cols;
   p->smem = fixed_for(Bt) + (size_t)nst * kStage;
-  // Tile multicast across a cluster (CFC_TC_CLUSTER = cluster size) measured
-  // no faster than one CTA per sample tile; off by default.
-  p->C = 1;
-  if (const char* v = getenv("CFC_TC_CLUSTER")) p->C = std::max(1, std::min(8, atoi(v)));
   return true;
 }
 
@@ -932,23 +891,12 @@ cudaError_t launch_fwd_stream(const Layout& L, const FwdPlan& p, const CfcArgs& 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
   const int blocks = (L.B + p.Bt - 1) / p.Bt;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((blocks + p.C - 1) / p.C * p.C), 1, 1);   // whole clusters
-  cfg.blockDim = dim3(kFwdThreads, 1, 1);
-  cfg.dynamicSmemBytes = p.smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   TraceScope trace("cfc_fwd_stream_tc", s);
-  return cudaLaunchKernelEx(&cfg, kern, p.sched, static_cast<const uint8_t*>(tiles), static_cast<const ET*>(a.x),
-                            static_cast<const ET*>(a.h0), a.b, a.dt, a.dt_stride, L.B, L.K, L.n_in, L.H, p.Bt,
-                            p.nUB, p.nAk, p.nst, p.tmem_cols, p.C, static_cast<ET*>(a.h_seq),
-                            reinterpret_cast<float*>(a.ws + L.off_act));
+  kern<<<blocks, kFwdThreads, p.smem, s>>>(p.sched, static_cast<const uint8_t*>(tiles), static_cast<const ET*>(a.x),
+                                           static_cast<const ET*>(a.h0), a.b, a.dt, a.dt_stride, L.B, L.K, L.n_in,
+                                           L.H, p.Bt, p.nUB, p.nAk, p.nst, p.tmem_cols,
+                                           static_cast<ET*>(a.h_seq), reinterpret_cast<float*>(a.ws + L.off_act));
+  return cudaGetLastError();
 }
 
 
