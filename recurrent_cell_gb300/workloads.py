@@ -13,8 +13,13 @@ Input recipe (fixed draw order, one ``numpy.random.default_rng(seed)``):
 4. ``W_rec`` [3, n_hid, n_hid] ~ U(-1/sqrt(n_hid), +1/sqrt(n_hid))
 5. ``y``     [B, n_hid]    ~ N(0, 1)          target of the loss 0.5*||h_K - y||^2
 6. ``dt``    [B]           ~ U(0.5, 1.5) when ``dt_per_sample``; else the scalar 1.0
+7. ``b``     [3, n_hid]    ~ U(-bias_scale, +bias_scale), drawn only when
+   ``bias_scale > 0``; otherwise all zeros (the benchmark workloads)
 
-``b`` is all zeros.  When the workload stores activations and weights in
+Drawing ``b`` last keeps every other input of a seed the same whether or not
+a bias is drawn.  The parity tests draw a nonzero bias (independent values
+per head and unit) so that the kernels' bias loads and head offsets are
+exercised; the benchmark workloads keep ``b = 0``.  When the workload stores activations and weights in
 bf16, x, h0, W_in and W_rec are quantised to bf16 (round to nearest even)
 after drawing; the arrays stay float32 but every value is bf16-exact.
 """
@@ -81,8 +86,9 @@ def bf16_quantise(a: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32)
 
 
-def make_inputs(w: Workload, seed: int | None = None) -> dict:
-    """Draw the inputs of workload ``w`` (all float32 numpy arrays)."""
+def make_inputs(w: Workload, seed: int | None = None, bias_scale: float = 0.0) -> dict:
+    """Draw the inputs of workload ``w`` (all float32 numpy arrays); ``b`` is
+    U(+-bias_scale) per head and unit when ``bias_scale > 0``, else zero."""
     rng = np.random.default_rng(w.seed if seed is None else seed)
     B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
     x = rng.standard_normal((B, K, n_in), dtype=np.float64).astype(np.float32)
@@ -96,7 +102,10 @@ def make_inputs(w: Workload, seed: int | None = None) -> dict:
         dt = rng.uniform(0.5, 1.5, size=(B,)).astype(np.float32)
     else:
         dt = np.full((1,), 1.0, dtype=np.float32)
-    b = np.zeros((3, H), dtype=np.float32)
+    if bias_scale > 0:
+        b = rng.uniform(-bias_scale, bias_scale, size=(3, H)).astype(np.float32)
+    else:
+        b = np.zeros((3, H), dtype=np.float32)
     if w.math == MATH_BF16:
         x, h0, W_in, W_rec = (bf16_quantise(a) for a in (x, h0, W_in, W_rec))
     return dict(x=x, h0=h0, W_in=W_in, W_rec=W_rec, b=b, dt=dt, y=y)
@@ -109,13 +118,14 @@ def make_reduce_input(B: int, N: int, seed: int = 0) -> np.ndarray:
 
 
 # The pages' single-head tau-cell, FP32, on the tiny and smoke shapes: x, h0 ~
-# N(0, 1); W_in ~ U(+-1/sqrt(n_in)), W_rec ~ U(+-1/sqrt(n_hid)); b = 0;
-# tau ~ U(0.5, 2.0) per unit; dt = 1.0 (or U(0.5, 1.5) per sample); y ~ N(0, 1).
+# N(0, 1); W_in ~ U(+-1/sqrt(n_in)), W_rec ~ U(+-1/sqrt(n_hid)); b = 0 (or
+# U(+-bias_scale), drawn last); tau ~ U(0.5, 2.0) per unit; dt = 1.0 (or
+# U(0.5, 1.5) per sample); y ~ N(0, 1).
 TAU_TINY = Workload("tau_tiny_B4_K8_16x32_fp32", B=4, K=8, n_in=16, n_hid=32)
 TAU_SMOKE = Workload("tau_smoke_B32_K64_64x128_fp32", B=32, K=64, n_in=64, n_hid=128)
 
 
-def make_tau_inputs(w: Workload, seed: int | None = None) -> dict:
+def make_tau_inputs(w: Workload, seed: int | None = None, bias_scale: float = 0.0) -> dict:
     """Draw the inputs of a tau-cell workload (all float32 numpy arrays)."""
     rng = np.random.default_rng(w.seed if seed is None else seed)
     B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
@@ -130,7 +140,10 @@ def make_tau_inputs(w: Workload, seed: int | None = None) -> dict:
         dt = rng.uniform(0.5, 1.5, size=(B,)).astype(np.float32)
     else:
         dt = np.full((1,), 1.0, dtype=np.float32)
-    b = np.zeros((H,), dtype=np.float32)
+    if bias_scale > 0:
+        b = rng.uniform(-bias_scale, bias_scale, size=(H,)).astype(np.float32)
+    else:
+        b = np.zeros((H,), dtype=np.float32)
     return dict(x=x, h0=h0, W_in=W_in, W_rec=W_rec, b=b, tau=tau, dt=dt, y=y)
 
 

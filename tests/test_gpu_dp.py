@@ -13,7 +13,7 @@ import recurrent_cell_gb300 as cfc
 from recurrent_cell_gb300 import dp
 from recurrent_cell_gb300 import workloads as wl
 
-from gpu_common import assert_close, dev, host, require_gpu, torch_mod
+from gpu_common import PARITY_BIAS, assert_close, dev, host, require_gpu, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +58,7 @@ def _sharded_step(w, inp, G):
 @pytest.mark.parametrize("w, G", CASES, ids=[f"{w.name}_G{G}" for w, G in CASES])
 def test_sharded_gradient_matches_full_batch(w, G):
     require_gpu()
-    inp = wl.make_inputs(w)
+    inp = wl.make_inputs(w, bias_scale=PARITY_BIAS)
     gathered, out = _sharded_step(w, inp, G)
     # the device reduction of the gathered rows is the canonical order, bit for bit
     rows = gathered.cpu().numpy()

@@ -9,7 +9,7 @@ import oracle
 import recurrent_cell_gb300 as cfc
 from recurrent_cell_gb300 import workloads as wl
 
-from gpu_common import CfcRun, assert_close, require_gpu, torch_mod
+from gpu_common import PARITY_BIAS, CfcRun, assert_close, require_gpu, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def test_timed_out_wait_is_reported_and_the_context_survives():
     assert cfc.cfc_device_error() == 0
     # the same context still runs a step correctly
     w = wl.TINY
-    inp = wl.make_inputs(w)
+    inp = wl.make_inputs(w, bias_scale=PARITY_BIAS)
     r = CfcRun(w, inp)
     r.forward()
     r.backward()

@@ -10,7 +10,7 @@ import oracle
 import recurrent_cell_gb300 as cfc
 from recurrent_cell_gb300 import workloads as wl
 
-from gpu_common import CfcRun, assert_close, dev, host, require_gpu, torch_mod
+from gpu_common import PARITY_BIAS, CfcRun, assert_close, dev, host, require_gpu, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -40,14 +40,14 @@ def _graph_of(fn):
 def test_captured_step_replays_bit_exact(w):
     require_gpu()
     torch = torch_mod()
-    r = CfcRun(w, wl.make_inputs(w, seed=1))
+    r = CfcRun(w, wl.make_inputs(w, seed=1, bias_scale=PARITY_BIAS))
 
     def step():
         r.forward()
         r.backward()
 
     g = _graph_of(step)
-    inp = wl.make_inputs(w, seed=2)
+    inp = wl.make_inputs(w, seed=2, bias_scale=PARITY_BIAS)
     r.set_inputs(inp)
     g.replay()
     torch.cuda.synchronize()
@@ -72,7 +72,7 @@ def test_captured_static_entry_point():
     require_gpu()
     torch = torch_mod()
     w = wl.SMOKE.with_(grad_path=wl.GRAD_GEMM)
-    inp = wl.make_inputs(w, seed=3)
+    inp = wl.make_inputs(w, seed=3, bias_scale=PARITY_BIAS)
     t = {k: dev(inp[k]) for k in ("x", "h0", "W_in", "W_rec", "b", "dt", "y")}
     H, n_in = w.n_hid, w.n_in
     h_seq = torch.empty(w.B, w.K, H, device="cuda")
@@ -85,7 +85,7 @@ def test_captured_static_entry_point():
                                               h_seq, gWi, gWr, gb, y=t["y"], math=w.math)
 
     g = _graph_of(step)
-    inp2 = wl.make_inputs(w, seed=4)
+    inp2 = wl.make_inputs(w, seed=4, bias_scale=PARITY_BIAS)
     for k in t:
         t[k].copy_(dev(inp2[k]))
     g.replay()

@@ -13,7 +13,7 @@ from oracle import cfc_oracle as co
 from oracle import grn_oracle as go
 from recurrent_cell_gb300 import workloads as wl
 
-from gpu_common import CfcRun, assert_close, dev, host, require_gpu, torch_mod
+from gpu_common import PARITY_BIAS, CfcRun, assert_close, dev, host, require_gpu, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -111,7 +111,7 @@ def test_grn_heads_chained_with_the_kloop():
     require_gpu()
     cw = wl.TINY
     gw = wl.GrnWorkload("grn_on_tiny", B=cw.B, K=cw.K, hidden=cw.n_hid, head_mid=16, n_horizons=3, seed=4)
-    cin = wl.make_inputs(cw)
+    cin = wl.make_inputs(cw, bias_scale=PARITY_BIAS)
     gin = wl.make_grn_inputs(gw)
     run = CfcRun(cw, cin)
     run.forward()

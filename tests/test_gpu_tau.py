@@ -8,7 +8,7 @@ import recurrent_cell_gb300 as cfc
 from oracle import tau_oracle as to
 from recurrent_cell_gb300 import workloads as wl
 
-from gpu_common import assert_close, dev, host, require_gpu, torch_mod
+from gpu_common import PARITY_BIAS, assert_close, dev, host, require_gpu, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,7 @@ CASES = [
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_tau_cell_matches_oracle(w):
     require_gpu()
-    inp = wl.make_tau_inputs(w)
+    inp = wl.make_tau_inputs(w, bias_scale=PARITY_BIAS)
     got = TauRun(w, inp).step()
     ref = to.tau_backward(inp["x"], inp["h0"], inp["W_in"], inp["W_rec"], inp["b"], inp["tau"], inp["dt"],
                           y=inp["y"])
@@ -79,7 +79,7 @@ def test_tau_cell_upstream_seeds_and_clamped_taus():
     exactly zero gradient."""
     require_gpu()
     w = wl.TAU_TINY
-    inp = wl.make_tau_inputs(w, seed=3)
+    inp = wl.make_tau_inputs(w, seed=3, bias_scale=PARITY_BIAS)
     inp["tau"][[1, 5]] = np.float32(1e-7)
     rng = np.random.default_rng(4)
     gseq = rng.standard_normal((w.B, w.K, w.n_hid)).astype(np.float32)
@@ -94,7 +94,7 @@ def test_tau_cell_upstream_seeds_and_clamped_taus():
 def test_tau_cell_run_to_run_bit_identical():
     require_gpu()
     w = wl.TAU_SMOKE
-    r = TauRun(w, wl.make_tau_inputs(w))
+    r = TauRun(w, wl.make_tau_inputs(w, bias_scale=PARITY_BIAS))
     first = r.step()
     for _ in range(3):
         cur = r.step()
