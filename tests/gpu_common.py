@@ -11,21 +11,40 @@ from recurrent_cell_gb300 import workloads as wl
 # fp32 path: |gpu - ref| <= 1e-5 + 1e-4 |ref| elementwise.
 # TF32 / bf16 tensor-core modes: the stated relative tolerance 2e-3 is taken
 # per tensor, normwise: ||gpu - ref||_2 <= 2e-3 ||ref||_2, together with an
-# elementwise guard |gpu - ref| <= 2e-3 |ref| + 1e-2 max|ref| that catches
-# isolated wrong elements.  Elementwise 2e-3 alone cannot hold in bf16 mode:
-# the carried state is rounded to bf16 every step, and where the GPU's fp32
-# value and the oracle's float64 value fall on opposite sides of a rounding
-# boundary (about 1 in 10^5 elements) the two states differ by one bf16 ulp
-# (2^-8 relative), which moves that sample's downstream values by ~0.2% of
-# their scale.  A bf16-stored state may itself differ by one ulp (2^-7 |ref|).
-# grad_h0 is the one output carried back through all K rounding stages of the
-# backward recurrence: a float32 re-computation with exactly the kernels'
-# rounding points already differs from the float64 oracle by 2.09e-3 (mid,
-# TF32, K=64) and 2.03e-3 (large, bf16, K=8) normwise, so 2e-3 is below the
-# modes' own noise floor there; it gets 5e-3.
+# elementwise guard |gpu - ref| <= 2e-3 |ref| + 2e-3 max|ref| that catches
+# isolated wrong elements.  Elementwise 2e-3 alone cannot hold: the operands
+# are rounded to TF32 / bf16 (and the bf16 state every step), and where the
+# GPU's fp32 value and the oracle's float64 value fall on opposite sides of a
+# rounding boundary the two roundings differ by one unit, which moves that
+# sample's downstream values.  A bf16-stored state may itself differ by one
+# ulp (2^-7 |ref|).
+#
+# These figures are set from a measurement, tests/test_tolerance_floor.py:
+# a float32 rendition of the K loop with exactly the kernels' rounding points
+# (tests/fp32_rendition.py) is a correct float32 implementation, so its
+# distance from the float64 oracle is the least any such implementation
+# must be allowed.  Every tolerance is at least twice that floor.  On the
+# mid (TF32, K = 64) and large (bf16, K = 8) workloads the floor is below
+# 2.5e-4 normwise and 9.3e-4 max|ref| elementwise for every output except
+# grad_h0, the one output carried back through all K rounding stages of the
+# backward recurrence: 2.25e-3 .. 2.35e-3 normwise at mid (above the stated
+# 2e-3) and 4.6e-3 max|ref| elementwise at large.  grad_h0 therefore gets
+# 5e-3 normwise and a 1e-2 max|ref| guard.
 FP32_REL, FP32_ABS = 1e-4, 1e-5
-LP_REL, LP_GUARD_FRAC = 2e-3, 1e-2
-LP_REL_GRAD_H0 = 5e-3
+# Scale of the nonzero bias the parity tests draw (b ~ U(+-0.5) per head and
+# unit), so every kernel's bias load and head offsets are compared with the
+# oracle; the benchmark workloads themselves keep b = 0.
+PARITY_BIAS = 0.5
+LP_REL, LP_GUARD_FRAC = 2e-3, 2e-3
+LP_REL_GRAD_H0, LP_GUARD_FRAC_GRAD_H0 = 5e-3, 1e-2
+
+
+def lp_tolerance(name: str):
+    """(normwise rel, elementwise guard fraction) of a TF32 / bf16 output,
+    by the output's name (the part after the last ':')."""
+    if name.rsplit(":", 1)[-1] == "grad_h0":
+        return LP_REL_GRAD_H0, LP_GUARD_FRAC_GRAD_H0
+    return LP_REL, LP_GUARD_FRAC
 
 
 def torch_mod():
@@ -52,7 +71,7 @@ def host(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def assert_close(got, ref, math, name, state_bf16=False, lp_rel=LP_REL):
+def assert_close(got, ref, math, name, state_bf16=False):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
@@ -60,11 +79,12 @@ def assert_close(got, ref, math, name, state_bf16=False, lp_rel=LP_REL):
     if math == wl.MATH_FP32:
         tol = FP32_ABS + FP32_REL * np.abs(ref)
     else:
+        lp_rel, lp_guard = lp_tolerance(name)
         nrm = np.linalg.norm(ref)
         err = np.linalg.norm(got - ref)
         assert err <= lp_rel * nrm + 1e-30, \
             f"{name}: normwise relative error {err / max(nrm, 1e-30):.3g} > {lp_rel}"
-        tol = LP_REL * np.abs(ref) + LP_GUARD_FRAC * (np.abs(ref).max() if ref.size else 0.0)
+        tol = LP_REL * np.abs(ref) + lp_guard * (np.abs(ref).max() if ref.size else 0.0)
         if state_bf16:
             tol = tol + 2.0 ** -7 * np.abs(ref)
     excess = np.abs(got - ref) - tol

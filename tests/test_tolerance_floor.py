@@ -1,0 +1,83 @@
+"""The reduced-precision tolerances of the GPU parity tests (gpu_common) are
+checked against a measurement, not chosen after the fact.
+
+A float32 rendition of the K loop with exactly the kernels' rounding points
+(fp32_rendition.kloop) is a correct float32 implementation of the TF32 and
+bf16 modes; its distance from the float64 oracle on the same inputs is
+therefore the noise floor that any such implementation, the GPU's included,
+must be allowed.  These tests measure that floor on the mid (TF32, K = 64,
+n_in 64, n_hid 128) and large (bf16, K = 8, n_in 128, n_hid 256) shapes at
+full K and widths with fewer samples (the figures are per-sample statistics;
+at the full batches they were 2.25e-3 .. 2.35e-3 normwise for grad_h0 at mid
+and 4.6e-3 max|ref| elementwise for grad_h0 at large, the worst cases), and
+require every tolerance to be at least MARGIN times the floor.
+
+CPU only: nothing here touches a GPU.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import fp32_rendition as fr
+from gpu_common import (LP_GUARD_FRAC, LP_GUARD_FRAC_GRAD_H0, LP_REL, LP_REL_GRAD_H0, PARITY_BIAS,
+                        lp_tolerance)
+from recurrent_cell_gb300 import workloads as wl
+
+MARGIN = 2.0
+OUTPUTS = ("h_seq", "grad_W_in", "grad_W_rec", "grad_b", "grad_h0", "grad_x")
+CASES = [wl.MID.with_(B=256), wl.LARGE.with_(B=1024)]
+
+_cache = {}
+
+
+def floor(w):
+    if w not in _cache:
+        inp = wl.make_inputs(w, seed=0, bias_scale=PARITY_BIAS)
+        ref = oracle.backward(inp["x"], inp["h0"], inp["W_in"], inp["W_rec"], inp["b"], inp["dt"],
+                              mode=w.math, per_sample=False, y=inp["y"])
+        got = fr.kloop(inp, w.math)
+        _cache[w] = fr.deviation(got, {k: ref[k] for k in OUTPUTS}, LP_REL, w.math == wl.MATH_BF16)
+    return _cache[w]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name.split("_")[0])
+@pytest.mark.parametrize("out", OUTPUTS)
+def test_tolerance_is_at_least_twice_the_fp32_floor(w, out):
+    dv = floor(w)[out]
+    rel, guard = lp_tolerance(f"{w.name}:{out}")
+    assert MARGIN * dv["norm"] <= rel, (out, dv)
+    assert MARGIN * dv["guard"] <= guard, (out, dv)
+
+
+def test_grad_h0_floor_exceeds_the_stated_tolerance():
+    """The wider grad_h0 tolerance is needed: at mid (K = 64) even the
+    correct float32 rendition is further than 2e-3 from the oracle."""
+    assert floor(CASES[0])["grad_h0"]["norm"] > LP_REL
+    assert max(floor(w)["grad_h0"]["guard"] for w in CASES) > LP_GUARD_FRAC
+
+
+def test_tolerances_stay_near_the_floor():
+    """No tolerance is loosened beyond need: the general ones are the stated
+    2e-3 (normwise and elementwise, the benchmark spec's figure), the grad_h0 ones
+    at most 2.5 times the larger of the two floors."""
+    assert LP_REL == 2e-3 and LP_GUARD_FRAC == 2e-3
+    worst_norm = max(floor(w)["grad_h0"]["norm"] for w in CASES)
+    worst_guard = max(floor(w)["grad_h0"]["guard"] for w in CASES)
+    assert LP_REL_GRAD_H0 <= 2.5 * worst_norm
+    assert LP_GUARD_FRAC_GRAD_H0 <= 2.5 * worst_guard
+
+
+def test_rendition_is_not_the_oracle():
+    """The instrument is a genuine float32 computation (a nonzero distance
+    from the oracle on every output) and an accurate one: at FP32, with no
+    rounding points, it is within the fp32 tolerance of the oracle."""
+    w = wl.TINY
+    inp = wl.make_inputs(w, seed=3, bias_scale=PARITY_BIAS)
+    ref = oracle.backward(inp["x"], inp["h0"], inp["W_in"], inp["W_rec"], inp["b"], inp["dt"],
+                          per_sample=False, y=inp["y"])
+    got = fr.kloop(inp, fr.FP32)
+    for k in OUTPUTS:
+        d = np.abs(np.asarray(got[k], np.float64) - ref[k])
+        assert d.max() > 0, k
+        assert np.all(d <= 1e-5 + 1e-4 * np.abs(ref[k])), k
