@@ -283,19 +283,26 @@ int reduce_axis0_multi(const float* const* per_batch, const int* n_batch, const 
  * in the pages; it exists for callers that cannot allocate device memory
  * when they run the K loop (code running under an allocator it does not own,
  * plugins barred from cudaMalloc, real-time loops where an allocation would
- * stall).  It computes exactly what cfc_kloop_forward followed by
- * cfc_kloop_backward with CFC_GRAD_GEMM computes, with the same kernels, but
- * keeps the whole workspace in a fixed device array inside the library.
+ * stall).  It computes what cfc_kloop_forward followed by cfc_kloop_backward
+ * with CFC_GRAD_GEMM computes, but keeps the whole workspace in a fixed device
+ * array inside the library and always runs the CUDA-core (SIMT) kernels: the
+ * SIMT forward and backward K loops, the SIMT weight-gradient tiles and
+ * reduce_axis0, in every precision mode.  The regular entry points choose
+ * cluster or tensor-core kernels, which sum in other orders, so the two
+ * agree within the parity tolerances (fp32: 1e-4 relative; TF32 / bf16:
+ * 2e-3 normwise), not bit for bit; each is run-to-run bit-identical.
  *   - The array holds CFC_STATIC_WORKSPACE_BYTES bytes on every device that
- *     loads the library, until the process exits.  Sizes whose workspace
- *     (cfc_kloop_workspace_bytes(..., CFC_GRAD_GEMM)) is larger are rejected
- *     with CFC_ERR_TOO_LARGE before anything is launched.
+ *     loads the library, until the process exits.  Sizes whose SIMT workspace
+ *     (the W_cat^T copy, the [B,K,3H] activations and dA, and the weight
+ *     gradient's split partials) is larger are rejected with
+ *     CFC_ERR_TOO_LARGE before anything is launched.
  *   - The caller passes all inputs and outputs (same meaning, layout and
  *     overwrite rules as the two calls it replaces); nothing is allocated or
  *     freed by the call.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process: a
+ *     device reset after that first call is not supported.
  *   - All calls share the one array, which keeps the last call's contents.
  *     Nothing in it has to start at zero (every part that is read is written
  *     earlier in the same call), but calls whose work overlaps on the GPU

@@ -347,9 +347,11 @@ def reduce_axis0_multi(per_batch, out, stream=None):
 def cfc_kloop_forward_backward_static(x, h0, W_in, W_rec, b, dt, h_seq, grad_W_in, grad_W_rec,
                                       grad_b, grad_h_seq=None, grad_h_last=None, y=None,
                                       grad_h0=None, grad_x=None, math=MATH_FP32, stream=None):
-    """Forward + backward with the library's fixed internal workspace: for
-    callers that cannot allocate device memory.  Same results as
-    cfc_kloop_forward + cfc_kloop_backward(grad_path=GRAD_GEMM)."""
+    """Forward + backward with the library's fixed internal workspace, for
+    callers that cannot allocate device memory.  Computes what
+    cfc_kloop_forward + cfc_kloop_backward(grad_path=GRAD_GEMM) compute, always
+    on the CUDA-core (SIMT) kernels, so the results agree with those calls
+    within the parity tolerances, not bit for bit."""
     torch = _torch()
     B, K, n_in = x.shape
     H = h0.shape[1]

@@ -14,7 +14,16 @@
 // The array's name in host code is only a host-side stand-in for the device
 // symbol.  Its device address is looked up with cudaGetSymbolAddress once per
 // device, on the first call made with that device current, and that address
-// is what the kernels receive.
+// is what the kernels receive.  The address is kept for the life of the
+// process, so a device reset (cudaDeviceReset) after the first call on that
+// device is not supported.
+//
+// It always runs the CUDA-core (SIMT) kernels: the forward and backward K
+// loops, the SIMT weight-gradient tiles and reduce_axis0.  Those need the
+// smallest workspace (no tensor-core weight tiles), so the fixed array
+// serves the widest range of sizes.  The regular entry points pick the
+// cluster or tensor-core kernels instead, which sum in other orders, so the
+// results of the two agree within the parity tolerances, not bit for bit.
 #include <mutex>
 
 #include "cfc_internal.cuh"
@@ -43,6 +52,28 @@ void* static_workspace_for_current_device() {
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace of the SIMT kernels in the fixed array: the W_cat^T copy, the
+// saved activations, dA and the weight gradient's split partials, with the
+// rows split by the FP32 rule (about four 64 x 64 output tiles per SM, at
+// most 256 row blocks) in every precision mode.
+bool static_layout(int B, int K, int n_in, int n_hid, int math, Layout* L) {
+  if (!make_layout(B, K, n_in, n_hid, math, CFC_GRAD_GEMM, L)) return false;
+  const long long tiles = (long long)((L->H3 + 63) / 64) * ((L->Zc + 1 + 63) / 64);
+  long long split = (4ll * kNumSMs + tiles - 1) / tiles;
+  split = std::max(1ll, std::min(split, std::min<long long>(L->R, 256)));
+  L->rows_per_split = (L->R + split - 1) / split;
+  L->n_split = (int)((L->R + L->rows_per_split - 1) / L->rows_per_split);
+  size_t off = 0;
+  L->off_wt = off;   off = align256(off + (size_t)L->Zc * L->H3 * L->elem);
+  L->off_act = off;  off = align256(off + (size_t)L->R * L->H3 * sizeof(float));
+  L->off_dA = off;   off = align256(off + (size_t)L->R * L->H3 * L->dA_elem);
+  L->off_part = off; off = align256(off + (size_t)L->n_split * L->N * sizeof(float));
+  L->off_wtt = off;
+  L->total = off;
+  return true;
+}
 
 }  // namespace
 }  // namespace cfc
@@ -58,7 +89,7 @@ extern "C" int cfc_kloop_forward_backward_static(
     float* grad_h0, float* grad_x, void* stream) {
   if (math < CFC_MATH_FP32 || math > CFC_MATH_BF16) return CFC_ERR_MODE;
   Layout L;
-  if (!make_layout(B, K, n_in, n_hid, math, CFC_GRAD_GEMM, &L)) return CFC_ERR_SHAPE;
+  if (!static_layout(B, K, n_in, n_hid, math, &L)) return CFC_ERR_SHAPE;
   if (L.total > (size_t)CFC_STATIC_WORKSPACE_BYTES) return CFC_ERR_TOO_LARGE;
   if (!x || !h0 || !W_in || !W_rec || !b || !dt || !h_seq) return CFC_ERR_NULL;
   if (!grad_W_in || !grad_W_rec || !grad_b) return CFC_ERR_NULL;

@@ -42,7 +42,7 @@ LP_REL_GRAD_H0, LP_GUARD_FRAC_GRAD_H0 = 5e-3, 1e-2
 def lp_tolerance(name: str):
     """(normwise rel, elementwise guard fraction) of a TF32 / bf16 output,
     by the output's name (the part after the last ':')."""
-    if name.rsplit(":", 1)[-1] == "grad_h0":
+    if name.rsplit(":", 1)[-1].strip() == "grad_h0":
         return LP_REL_GRAD_H0, LP_GUARD_FRAC_GRAD_H0
     return LP_REL, LP_GUARD_FRAC
 

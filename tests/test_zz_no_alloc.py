@@ -3,16 +3,19 @@ allocate device memory while they run the K loop (for example code that runs
 under an allocator it does not own, or a plugin that may not call cudaMalloc).
 It keeps its workspace in a fixed array inside the library.
 
-Checked through the C ABI against the regular entry points (forward, then
-backward with the GEMM gradient path and a caller-allocated workspace), with
-the tolerances of the other parity tests, on two calls in a row with
-different inputs, so that anything a call left behind in the shared array
-would show up in the second call.  This file is collected last on purpose.
+It always runs the CUDA-core (SIMT) kernels, so it is checked through the C
+ABI against both the oracle and the regular entry points (forward, then
+backward with the GEMM gradient path and a caller-allocated workspace, which
+run the cluster or tensor-core kernels), with the tolerances of the other
+parity tests, in every precision mode, on two calls in a row with different
+inputs, so that anything a call left behind in the shared array would show
+up in the second call.  This file is collected last on purpose.
 """
 
 import numpy as np
 import pytest
 
+import oracle
 import recurrent_cell_gb300 as cfc
 from recurrent_cell_gb300 import workloads as wl
 from gpu_common import PARITY_BIAS, CfcRun, assert_close, host, require_gpu, torch_mod
@@ -21,9 +24,12 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     wl.SMOKE,
+    wl.Workload("static_tf32_B37_K5_odd", B=37, K=5, n_in=23, n_hid=40, math=wl.MATH_TF32,
+                dt_per_sample=True),
     wl.Workload("static_bf16_B37_K5", B=37, K=5, n_in=24, n_hid=40, math=wl.MATH_BF16,
                 dt_per_sample=True),
 ]
+OUTPUTS = ("h_seq", "grad_W_in", "grad_W_rec", "grad_b", "grad_h0", "grad_x")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,14 +63,17 @@ def run_regular(w, inp):
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_static_workspace_matches_regular_entry_points_twice(w):
+def test_static_workspace_matches_oracle_and_regular_entry_points_twice(w):
     for seed in (101, 202):                      # two calls in a row, different inputs
         inp = wl.make_inputs(w, seed=seed, bias_scale=PARITY_BIAS)
         got = run_static(w, inp)
         want = run_regular(w, inp)
-        for k in ("h_seq", "grad_W_in", "grad_W_rec", "grad_b", "grad_h0", "grad_x"):
-            assert_close(got[k], want[k], w.math, f"{w.name} seed {seed}: {k}",
-                         state_bf16=(k == "h_seq" and w.math == wl.MATH_BF16))
+        ref = oracle.backward(inp["x"], inp["h0"], inp["W_in"], inp["W_rec"], inp["b"], inp["dt"],
+                              mode=w.math, per_sample=False, y=inp["y"])
+        for k in OUTPUTS:
+            bf = (k == "h_seq" and w.math == wl.MATH_BF16)
+            assert_close(got[k], ref[k], w.math, f"{w.name} seed {seed} vs oracle: {k}", state_bf16=bf)
+            assert_close(got[k], want[k], w.math, f"{w.name} seed {seed} vs regular: {k}", state_bf16=bf)
 
 
 def test_sizes_beyond_the_static_workspace_are_rejected():
