@@ -15,8 +15,16 @@ runs an independent replica of the workload on its own GPU (there is no
 exchange step on this path in a single-GPU deployment), timing is the max
 over ranks and the value is the total over ranks.
 
---impl reference times the CPU oracle (numpy, single BLAS thread) on a
-bounded sample of the same workload.
+--impl reference times the CPU oracle (numpy float64) on bounded samples of
+the same workload on all of the host's cores: a process pool (spawn start)
+of one single-threaded worker per logical CPU, each worker running the oracle
+on its own slice of samples.  The GPU line's cpu_baseline reports that
+all-cores figure and the single-core one.
+
+The line ends with a compact `gates` object (the throughput workloads mid and
+large, and reduce_axis0 at B = 1024): per case the measured time and the
+fraction of its roofline, t_roof / t_measured with t_roof = max(flops / tensor
+peak, bytes / HBM peak) over the algorithmic work of the whole step.
 """
 
 import os
@@ -46,7 +54,7 @@ UNIT = "samples·steps/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-SM_COUNT = 152
+SM_COUNT_NOMINAL = 152          # used only when no device can be queried
 FP32_LANES_PER_SM = 128
 L2_FLUSH_BYTES = 512 << 20
 
@@ -63,9 +71,14 @@ def load_peaks():
                     sm_max_mhz=2070.0, source="fallback")
 
 
-def fp32_alu_peak_tflops(sm_mhz):
-    """FFMA peak: SMs x 128 fp32 lanes x 2 flop x SM clock."""
-    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+def fp32_alu_peak_tflops(peaks):
+    """FFMA peak: SMs (the device's own count) x 128 fp32 lanes x 2 flop x
+    maximum SM clock."""
+    return peaks["sm_count"] * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+
+
+def fp32_alu_peak_source(peaks):
+    return f"{peaks['sm_count']} SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"
 
 
 # ----------------------------------------------------------------------------
@@ -78,8 +91,14 @@ TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor throughput
 def kernel_work(name, w, n_split):
     """(flops, bytes, flop engine) of one launch of kernel `name` on workload w.
 
-    Bytes are algorithmic: every operand read once and every result written
-    once (saved activations and dA included, they are this path's own data).
+    Algorithmic work: the method's operands read once and its results written
+    once.  Per sample-step the path reads x (forward and weight gradient) and
+    writes then reads the state history h_seq; the weights, h0, y and the
+    outputs are per call.  The saved activations, dA, the weight gradient's
+    split partials and the per-sample scratch are this implementation's
+    intermediates and are not counted (an implementation may recompute them
+    or keep them on chip).  The reducer's own launch counts its [S, N] input,
+    which is its operand.
     """
     B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
     Zc, H3, R = n_in + H, 3 * H, w.B * w.K
@@ -88,29 +107,50 @@ def kernel_work(name, w, n_split):
     engine = "tensor" if (name.endswith("_tc") or "tma" in name) else "alu"
     if name.startswith("cfc_fwd"):
         flops = 2.0 * R * H3 * Zc
-        byts = R * n_in * s + R * H * s + R * H3 * 4 + B * H * s + H3 * Zc * s
+        byts = R * n_in * s + B * H * s + H3 * Zc * s + H3 * 4 + R * H * s
         return flops, byts, engine
     if name.startswith("cfc_bwd"):
-        if name != "cfc_bwd_simt":
-            # the cluster and tensor-core K loops carry W_rec^T dA only; grad_x
-            # (when requested) is its own GEMM
-            flops = 2.0 * R * H3 * H
-            byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * H * s
-        else:
-            flops = 2.0 * R * H3 * Zc
-            byts = R * H3 * 4 + R * H3 * s + B * H * 4 + H3 * Zc * s
+        # the carry W_rec^T dA per step; the SIMT kernel also forms grad_x
+        kc = Zc if name == "cfc_bwd_simt" else H
+        flops = 2.0 * R * H3 * kc
+        byts = H3 * kc * s + B * H * s + 2 * B * H * 4
         return flops, byts, engine
     if name.startswith("grad_x"):
-        return 2.0 * R * H3 * n_in, R * H3 * s + R * n_in * 4 + H3 * n_in * s, engine
+        return 2.0 * R * H3 * n_in, R * n_in * 4 + H3 * n_in * s, engine
     if name.startswith("wgrad"):
         flops = 2.0 * R * H3 * (Zc + 1)
-        byts = R * H3 * s + R * Zc * s + n_split * N * 4
+        byts = R * Zc * s + (Zc + 1) * H3 * 4
         return flops, byts, engine
     if name == "reduce_axis0":
         return 0.0, 4.0 * (n_split * N + N), "alu"
     if name.startswith("prep_w"):
         return 0.0, 2.0 * H3 * Zc * s, "alu"
     return 0.0, 0.0, "alu"
+
+
+def step_work(w):
+    """(flops, bytes) of one whole step (forward, backward without grad_x,
+    weight gradient): per sample-step 2*3H*(Zc) + 2*3H*H + 2*3H*(Zc + 1)
+    flop and (n_in + H) * s bytes read and written twice (x in the forward
+    and the weight gradient, h_seq written and read back), plus the weights
+    and the per-sample h0, y and gradient outputs."""
+    B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
+    Zc, H3, R = n_in + H, 3 * H, B * K
+    s = 2 if w.math == wl.MATH_BF16 else 4
+    flops = 2.0 * R * H3 * (Zc + H + Zc + 1)
+    byts = 2.0 * R * Zc * s + 2 * H3 * Zc * s + B * H * (s + 4) + (Zc + 1) * H3 * 4
+    return flops, byts
+
+
+def tensor_peak(w, peaks, sustained=False):
+    """(peak TFLOP/s, source) of the tensor pipe for the workload's mode."""
+    bf16 = peaks["bf16_sust"] if sustained else peaks["bf16"]
+    kind = "sustained" if sustained else "burst"
+    if w.math == wl.MATH_FP32:       # 3xTF32: three TF32 products per fp32 product
+        return bf16 * TF32_OVER_BF16 / 3.0, f"{peaks['source']} bf16 {kind} x 1.1/2.25 (TF32) / 3 (3xTF32)"
+    if w.math == wl.MATH_TF32:
+        return bf16 * TF32_OVER_BF16, f"{peaks['source']} bf16 {kind} x 1.1/2.25 (TF32)"
+    return bf16, f"{peaks['source']} bf16 {kind}"
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
@@ -169,30 +209,34 @@ def roofline_for(name, w, n_split, avg_ms, peaks, sustained=False):
     flops, byts, engine = kernel_work(name, w, n_split)
     t = avg_ms * 1e-3
     if engine == "tensor":
-        bf16 = peaks["bf16_sust"] if sustained else peaks["bf16"]
-        if w.math == wl.MATH_FP32:       # 3xTF32: three TF32 products per fp32 product
-            flop_peak = bf16 * TF32_OVER_BF16 / 3.0
-            flop_src = f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'} x 1.1/2.25 (TF32) / 3 (3xTF32)"
-        else:
-            flop_peak = bf16 * (TF32_OVER_BF16 if w.math == wl.MATH_TF32 else 1.0)
-            flop_src = (f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'}"
-                        + (" x 1.1/2.25 (TF32)" if w.math == wl.MATH_TF32 else ""))
+        flop_peak, flop_src = tensor_peak(w, peaks, sustained)
         flop_bound = "tensor"
     else:
-        flop_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
-        flop_src = f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"
+        flop_peak = fp32_alu_peak_tflops(peaks)
+        flop_src = fp32_alu_peak_source(peaks)
         flop_bound = "alu"
     t_flop = flops / (flop_peak * 1e12) if flops else 0.0
     t_byte = byts / (peaks["hbm"] * 1e9) if byts else 0.0
+    traffic = profiled_traffic(w, name)
+    extra = dict(traffic=traffic, traffic_over_algorithmic=(traffic / byts if traffic and byts else None),
+                 algorithmic_flops_per_launch=flops, algorithmic_bytes_per_launch=byts)
     if t_flop >= t_byte and flops:
         achieved = flops / t / 1e12
         return dict(kernel=name, bound=flop_bound, achieved=achieved, peak=flop_peak, unit="TFLOP/s",
-                    frac=achieved / flop_peak, traffic=profiled_traffic(w, name), algorithmic_flops_per_launch=flops,
-                    algorithmic_bytes_per_launch=byts, peak_source=flop_src)
+                    frac=achieved / flop_peak, **extra, peak_source=flop_src)
     achieved = byts / t / 1e9
     return dict(kernel=name, bound="hbm", achieved=achieved, peak=peaks["hbm"], unit="GB/s",
-                frac=achieved / peaks["hbm"], traffic=profiled_traffic(w, name), algorithmic_flops_per_launch=flops,
-                algorithmic_bytes_per_launch=byts, peak_source=f"{peaks['source']} hbm_gbs")
+                frac=achieved / peaks["hbm"], **extra, peak_source=f"{peaks['source']} hbm_gbs")
+
+
+def step_roofline(w, ms_step, peaks):
+    """Fraction of the whole step's roofline: t_roof / t_measured with
+    t_roof = max(step flops / the mode's tensor peak, step bytes / HBM)."""
+    flops, byts = step_work(w)
+    peak, _ = tensor_peak(w, peaks) if w.math != wl.MATH_FP32 else (fp32_alu_peak_tflops(peaks), "")
+    t_roof = max(flops / (peak * 1e12), byts / (peaks["hbm"] * 1e9))
+    return dict(flops=flops, bytes=byts, t_roof_us=t_roof * 1e6, frac=t_roof / (ms_step * 1e-3),
+                bound="tensor" if flops / (peak * 1e12) >= byts / (peaks["hbm"] * 1e9) else "hbm")
 
 
 # ----------------------------------------------------------------------------
@@ -316,6 +360,12 @@ def timed(torch, fn, steps, flush=None):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+def compact_kernels(kernels):
+    """Per kernel: average device time per launch (us) and launches per step."""
+    return {n: dict(avg_us=round(v["avg_ms"] * 1e3, 2), per_step=v["launches_per_step"])
+            for n, v in kernels.items()}
+
+
 def summarize_trace(records, steps):
     per = {}
     for name, ms in records:
@@ -398,12 +448,11 @@ def measure_tau(w, steps, warmup, device, peaks, flush):
     flops = {"tau_fwd": 2.0 * H * Zc * B * K, "tau_bwd": (2.0 * H * Zc + 2.0 * H * H) * B * K}
     top = max((n for n in kernels if n in flops), key=lambda n: kernels[n]["ms_total"])
     achieved = flops[top] / (kernels[top]["avg_ms"] * 1e-3) / 1e12
-    peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+    peak = fp32_alu_peak_tflops(peaks)
     return dict(workload=w.name, value=B * K / (ms_step * 1e-3), unit=UNIT, ms_per_step=ms_step,
-                kernels=kernels,
+                kernels=compact_kernels(kernels),
                 roofline=dict(kernel=top, bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s",
-                              frac=achieved / peak,
-                              peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"))
+                              frac=achieved / peak, peak_source=fp32_alu_peak_source(peaks)))
 
 
 def measure_grn(w, steps, warmup, device, peaks, flush):
@@ -445,12 +494,11 @@ def measure_grn(w, steps, warmup, device, peaks, flush):
              "grn_wgrad": 2.0 * N * R}
     top = max((n for n in kernels if n in flops), key=lambda n: kernels[n]["ms_total"])
     achieved = flops[top] / (kernels[top]["avg_ms"] * 1e-3) / 1e12
-    peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+    peak = fp32_alu_peak_tflops(peaks)
     return dict(workload=w.name, value=R / (ms_step * 1e-3), unit="rows/s", ms_per_step=ms_step,
-                kernels=kernels,
+                kernels=compact_kernels(kernels),
                 roofline=dict(kernel=top, bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s",
-                              frac=achieved / peak,
-                              peak_source=f"152 SMs x 128 FFMA lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"))
+                              frac=achieved / peak, peak_source=fp32_alu_peak_source(peaks)))
 
 
 def measure_reduce_multi(steps, device, peaks, flush, B=32, count=17):
@@ -559,15 +607,33 @@ def host_cpu():
     return dict(arch=platform.machine(), logical_cpus=os.cpu_count(), model=model)
 
 
-def time_oracle(w, seconds=10.0, max_reps=None):
+_ORACLE_INPUTS = {}
+
+
+def _oracle_slice(name, b, offset):
+    """One oracle fwd + bwd on samples offset .. offset+b-1 of workload
+    `name` (wrapping around the batch); runs in the calling process or in a
+    pool worker.  Returns its wall time in seconds."""
     import oracle
+    w = wl.WORKLOADS[name]
+    inp = _ORACLE_INPUTS.get(name)
+    if inp is None:
+        inp = _ORACLE_INPUTS[name] = wl.make_inputs(w)
+    idx = (offset + np.arange(b)) % w.B
+    sl = {k: (v[idx] if k in ("x", "h0", "y") or (k == "dt" and v.size > 1) else v) for k, v in inp.items()}
+    t0 = time.perf_counter()
+    oracle.backward(sl["x"], sl["h0"], sl["W_in"], sl["W_rec"], sl["b"], sl["dt"], mode=w.math,
+                    y=sl["y"], per_sample=(w.grad_path == wl.GRAD_SCRATCH))
+    return time.perf_counter() - t0
+
+
+def time_oracle(w, seconds=10.0, max_reps=None):
+    """The oracle on one core (one BLAS thread), repeated for ~seconds."""
     b = oracle_sample_batch(w)
-    inp = wl.make_inputs(w)
-    sl = {k: (v[:b] if k in ("x", "h0", "y") or (k == "dt" and v.size > 1) else v) for k, v in inp.items()}
+    _oracle_slice(w.name, b, 0)                  # inputs drawn outside the timing
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.backward(sl["x"], sl["h0"], sl["W_in"], sl["W_rec"], sl["b"], sl["dt"], mode=w.math,
-                        y=sl["y"], per_sample=(w.grad_path == wl.GRAD_SCRATCH))
+        _oracle_slice(w.name, b, 0)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or (max_reps and reps >= max_reps):
@@ -576,6 +642,47 @@ def time_oracle(w, seconds=10.0, max_reps=None):
     return dict(value=value, unit=UNIT, cores=1, kind="oracle", host=host_cpu(),
                 sample=f"{reps} x oracle fwd+bwd on {b} of {w.B} samples, K={w.K} "
                        f"({el:.1f} s, numpy float64, 1 BLAS thread)"), el / reps
+
+
+class OraclePool:
+    """One single-threaded oracle worker per logical CPU (spawn start, so it
+    is safe after the GPU has been used).  A round gives every worker its own
+    slice of b samples (slices at offsets i*b, wrapping around the batch) and
+    waits for all of them."""
+
+    def __init__(self, cores=None):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        self.cores = cores or os.cpu_count() or 1
+        self.ex = cf.ProcessPoolExecutor(max_workers=self.cores, mp_context=mp.get_context("spawn"))
+
+    def round(self, w, b):
+        t0 = time.perf_counter()
+        list(self.ex.map(_oracle_slice, [w.name] * self.cores, [b] * self.cores,
+                         [i * b for i in range(self.cores)]))
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.ex.shutdown()
+
+
+def time_oracle_all_cores(w, seconds=10.0):
+    """Throughput of the oracle on all host cores for ~seconds (after one
+    untimed round that starts the workers and draws their inputs)."""
+    b = oracle_sample_batch(w)
+    pool = OraclePool()
+    try:
+        pool.round(w, b)
+        rounds, el = 0, 0.0
+        while el < seconds:
+            el += pool.round(w, b)
+            rounds += 1
+    finally:
+        pool.close()
+    value = rounds * pool.cores * b * w.K / el
+    return dict(value=value, unit=UNIT, cores=pool.cores, kind="oracle", host=host_cpu(),
+                sample=f"{rounds} rounds x {pool.cores} workers x oracle fwd+bwd on {b} of {w.B} "
+                       f"samples, K={w.K} ({el:.1f} s, numpy float64, 1 BLAS thread per worker)")
 
 
 # ----------------------------------------------------------------------------
@@ -604,14 +711,16 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        per_step = []
-        for _ in range(args.warmup):
-            time_oracle(w, seconds=0.0, max_reps=1)
-        for _ in range(args.steps):
-            _, t = time_oracle(w, seconds=0.0, max_reps=1)
-            per_step.append(t)
         b = oracle_sample_batch(w)
-        value = b * w.K / (sum(per_step) / len(per_step))
+        pool = OraclePool()
+        try:
+            for _ in range(args.warmup):
+                pool.round(w, b)
+            per_step = [pool.round(w, b) for _ in range(args.steps)]
+        finally:
+            pool.close()
+        units = pool.cores * b * w.K
+        value = units / (sum(per_step) / len(per_step))
         line = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus,
                     steps=args.steps, warmup=args.warmup,
                     ms_per_step=1e3 * sum(per_step) / len(per_step), higher_is_better=True,
@@ -619,8 +728,10 @@ def main():
                     data="synthetic",
                     config=dict(workload=w.name, B=w.B, K=w.K, n_in=w.n_in, n_hid=w.n_hid,
                                 math=wl.MATH_NAMES[w.math], sample_batch=b),
-                    cpu_baseline=dict(kind="oracle", cores=1, value=value, unit=UNIT, host=host_cpu(),
-                                      sample=f"each step: oracle fwd+bwd on {b} of {w.B} samples"),
+                    cpu_baseline=dict(kind="oracle", cores=pool.cores, value=value, unit=UNIT, host=host_cpu(),
+                                      sample=f"each step: {pool.cores} workers (one per logical CPU, "
+                                             f"1 BLAS thread each), each the oracle fwd+bwd on {b} of "
+                                             f"{w.B} samples"),
                     e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
         print(json.dumps(line))
         return 0
@@ -639,6 +750,7 @@ def main():
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     peaks = load_peaks()
+    peaks["sm_count"] = torch.cuda.get_device_properties(device).multi_processor_count
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     flush_sink = torch.empty(1, dtype=torch.float32, device=device)
 
@@ -682,27 +794,45 @@ def main():
     value = units / (ms * 1e-3)
 
     secondary = {}
+    gates = {}
     cpu = None
     if rank == 0 and not args.no_secondary and world == 1:
         for name in ("mid", "large"):
-            if name == args.workload:
-                continue
             ow = wl.SHORT_NAMES[name]
-            r = measure_workload(ow, max(5, min(args.steps, 30)), 3, device, peaks, flush, None,
-                                 with_e2e=False)
+            if name == args.workload:
+                r = main_res
+            else:
+                r = measure_workload(ow, max(5, min(args.steps, 30)), 3, device, peaks, flush, None,
+                                     with_e2e=False)
+            sr = step_roofline(ow, r["ms_per_step"], peaks)
             secondary[ow.name] = dict(value=ow.B * ow.K / (r["ms_per_step"] * 1e-3), unit=UNIT,
-                                      ms_per_step=r["ms_per_step"], roofline=r["roofline"],
-                                      kernels=r["kernels"])
+                                      ms_per_step=r["ms_per_step"], step_roofline=sr,
+                                      roofline={k: r["roofline"][k] for k in
+                                                ("kernel", "bound", "frac", "traffic", "traffic_over_algorithmic")},
+                                      kernels=compact_kernels(r["kernels"]))
+            gates[name] = dict(value=round(ow.B * ow.K / (r["ms_per_step"] * 1e-3)), unit=UNIT,
+                               ms=round(r["ms_per_step"], 4), gflop=round(sr["flops"] / 1e9, 2),
+                               mb=round(sr["bytes"] / 1e6, 1), t_roof_us=round(sr["t_roof_us"], 1),
+                               bound=sr["bound"], frac=round(sr["frac"], 4), gate=0.60,
+                               met=bool(sr["frac"] >= 0.60))
         red = [measure_reduce(B, N, 20, device, peaks, flush)
                for B in wl.REDUCE_BATCHES for N in wl.REDUCE_TAILS]
         secondary["reduce_axis0"] = red
+        for rr in red:
+            if rr["B"] == 1024:
+                gates[f"reduce_B1024_N{rr['N']}"] = dict(
+                    value=round(rr["GBps"], 1), unit="GB/s", ms=round(rr["ms"], 4),
+                    mb=round(4.0 * (rr["B"] * rr["N"] + rr["N"]) / 1e6, 1), bound="hbm",
+                    frac=round(rr["frac_of_hbm"], 4), gate=0.75, met=bool(rr["frac_of_hbm"] >= 0.75))
         secondary["reduce_axis0_multi"] = measure_reduce_multi(20, device, peaks, flush)
         secondary["tau_cell"] = measure_tau(wl.TAU_SMOKE, 30, 3, device, peaks, flush)
         secondary["grn_heads"] = measure_grn(wl.GRN_SMOKE, 30, 3, device, peaks, flush)
         secondary["cuda_graph"] = {wl.SHORT_NAMES[n].name: measure_graph(wl.SHORT_NAMES[n], 50, device)
                                    for n in ("tiny", "smoke")}
     if rank == 0 and world == 1:
-        cpu, _ = time_oracle(w, seconds=args.cpu_seconds)
+        one, _ = time_oracle(w, seconds=args.cpu_seconds)
+        cpu = time_oracle_all_cores(w, seconds=args.cpu_seconds)
+        cpu["single_core"] = dict(value=one["value"], cores=1, sample=one["sample"])
     if rank != 0:
         return 0
     line = dict(
@@ -720,12 +850,15 @@ def main():
                  h2d_bytes_per_step=main_res["h2d"], d2h_bytes_per_step=main_res["d2h"]),
         gpu_launches=main_res["gpu_launches"],
         clocks=clocks,
-        kernels=main_res["kernels"],
+        step_roofline=step_roofline(w, ms, peaks),
+        kernels=compact_kernels(main_res["kernels"]),
     )
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if secondary:
         line["secondary"] = secondary
+    if gates:
+        line["gates"] = gates          # last, so that a tail of the line keeps it
     print(json.dumps(line))
     if dist_ctx:
         dist_ctx.destroy_process_group()
