@@ -235,8 +235,9 @@ def step_roofline(w, ms_step, peaks):
     flops, byts = step_work(w)
     peak, _ = tensor_peak(w, peaks) if w.math != wl.MATH_FP32 else (fp32_alu_peak_tflops(peaks), "")
     t_roof = max(flops / (peak * 1e12), byts / (peaks["hbm"] * 1e9))
+    compute = "tensor" if w.math != wl.MATH_FP32 else "alu"
     return dict(flops=flops, bytes=byts, t_roof_us=t_roof * 1e6, frac=t_roof / (ms_step * 1e-3),
-                bound="tensor" if flops / (peak * 1e12) >= byts / (peaks["hbm"] * 1e9) else "hbm")
+                bound=compute if flops / (peak * 1e12) >= byts / (peaks["hbm"] * 1e9) else "hbm")
 
 
 # ----------------------------------------------------------------------------

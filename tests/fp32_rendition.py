@@ -40,8 +40,10 @@ def bf16(a: np.ndarray) -> np.ndarray:
     return ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32).view(np.float32)
 
 
-def kloop(inp: dict, mode: int) -> dict:
-    """Forward + backward (loss 0.5*||h_K - y||^2) in float32."""
+def kloop(inp: dict, mode: int, per_sample: bool = False) -> dict:
+    """Forward + backward (loss 0.5*||h_K - y||^2) in float32; with
+    per_sample, also the packed per-sample gradient rows
+    [gW_in (c, i, j) | gW_rec (c, i, j) | gb (c, i)] of each sample's K rows."""
     f32 = np.float32
     opnd = {TF32: tf32, BF16: bf16}.get(mode, lambda a: np.asarray(a, dtype=f32))
     state = bf16 if mode == BF16 else (lambda a: np.asarray(a, dtype=f32))
@@ -83,11 +85,16 @@ def kloop(inp: dict, mode: int) -> dict:
         dA[:, k] = d
         grad_x[:, k] = d @ Wi
         carry = d @ Wr
-    Z = np.concatenate([xo, opnd(hs[:, :K]), np.ones((B, K, 1), dtype=f32)], axis=2).reshape(B * K, -1)
-    G = dA.reshape(B * K, 3 * H).T @ Z
-    return dict(h_seq=hs[:, 1:], grad_W_in=G[:, :n_in].reshape(3, H, n_in),
-                grad_W_rec=G[:, n_in:n_in + H].reshape(3, H, H), grad_b=G[:, n_in + H].reshape(3, H),
-                grad_h0=carry, grad_x=grad_x)
+    Zb = np.concatenate([xo, opnd(hs[:, :K]), np.ones((B, K, 1), dtype=f32)], axis=2)
+    G = dA.reshape(B * K, 3 * H).T @ Zb.reshape(B * K, -1)
+    out = dict(h_seq=hs[:, 1:], grad_W_in=G[:, :n_in].reshape(3, H, n_in),
+               grad_W_rec=G[:, n_in:n_in + H].reshape(3, H, H), grad_b=G[:, n_in + H].reshape(3, H),
+               grad_h0=carry, grad_x=grad_x)
+    if per_sample:
+        Gs = np.matmul(dA.transpose(0, 2, 1), Zb)                        # [B, 3H, n_in + H + 1]
+        out["per_sample"] = np.concatenate([Gs[:, :, :n_in].reshape(B, -1), Gs[:, :, n_in:n_in + H].reshape(B, -1),
+                                            Gs[:, :, n_in + H].reshape(B, -1)], axis=1)
+    return out
 
 
 def deviation(got: dict, ref: dict, rel: float, state_bf16: bool) -> dict:

@@ -29,7 +29,13 @@ from recurrent_cell_gb300 import workloads as wl
 # grad_h0, the one output carried back through all K rounding stages of the
 # backward recurrence: 2.25e-3 .. 2.35e-3 normwise at mid (above the stated
 # 2e-3) and 4.6e-3 max|ref| elementwise at large.  grad_h0 therefore gets
-# 5e-3 normwise and a 1e-2 max|ref| guard.
+# 5e-3 normwise and a 1e-2 max|ref| guard.  The per-sample gradient rows of
+# the scratch path are not averaged over the batch, so a rounding flip in one
+# sample shows in its row at full size: their elementwise floor reaches
+# 2.0e-3 max|ref| (large shape) and they get a 5e-3 guard (normwise they stay
+# below 6e-4).  These figures hold for the tested configurations; bf16 with
+# K = 64 steps, for one, carries grad_h0 1.4e-2 from the oracle and is not a
+# parity configuration.
 FP32_REL, FP32_ABS = 1e-4, 1e-5
 # Scale of the nonzero bias the parity tests draw (b ~ U(+-0.5) per head and
 # unit), so every kernel's bias load and head offsets are compared with the
@@ -37,13 +43,17 @@ FP32_REL, FP32_ABS = 1e-4, 1e-5
 PARITY_BIAS = 0.5
 LP_REL, LP_GUARD_FRAC = 2e-3, 2e-3
 LP_REL_GRAD_H0, LP_GUARD_FRAC_GRAD_H0 = 5e-3, 1e-2
+LP_GUARD_FRAC_PER_SAMPLE = 5e-3
 
 
 def lp_tolerance(name: str):
     """(normwise rel, elementwise guard fraction) of a TF32 / bf16 output,
     by the output's name (the part after the last ':')."""
-    if name.rsplit(":", 1)[-1].strip() == "grad_h0":
+    out = name.rsplit(":", 1)[-1].strip()
+    if out == "grad_h0":
         return LP_REL_GRAD_H0, LP_GUARD_FRAC_GRAD_H0
+    if out == "per_sample":
+        return LP_REL, LP_GUARD_FRAC_PER_SAMPLE
     return LP_REL, LP_GUARD_FRAC
 
 
