@@ -579,7 +579,12 @@ def measure_reduce(B, N, steps, device, peaks, flush):
     ms = timed(torch, lambda: cfc.reduce_axis0(a, out), steps, flush)
     avg = sum(ms) / len(ms)
     gbs = 4.0 * (B * N + N) / (avg * 1e-3) / 1e9
-    return dict(B=B, N=N, ms=avg, GBps=gbs, frac_of_hbm=gbs / peaks["hbm"])
+    # context: torch's own column sum of the same matrix, timed the same way
+    # (a reference point for a read-bound reduction of this size, not a parity check)
+    ref = torch.empty(N, device=device)
+    tms = timed(torch, lambda: torch.sum(a, dim=0, out=ref), steps, flush)
+    return dict(B=B, N=N, ms=avg, GBps=gbs, frac_of_hbm=gbs / peaks["hbm"],
+                torch_sum_dim0_ms=sum(tms) / len(tms))
 
 
 # ----------------------------------------------------------------------------

@@ -51,7 +51,8 @@ def test_standalone_configs_bit_exact(B, N):
 
 @pytest.mark.parametrize("B, N", [(1, 5), (2, 3), (7, 1), (31, 129), (33, 38), (64, 33), (100, 515),
                                   (128, 1027), (129, 5), (255, 130), (257, 131),
-                                  (300, 4), (513, 1000), (1000, 4096), (2049, 77), (4100, 256)])
+                                  (300, 4), (513, 1000), (1000, 4096), (2049, 77), (4100, 256),
+                                  (136, 12), (264, 2048), (512, 1000), (8192, 64)])
 def test_edge_shapes_bit_exact(B, N):
     a = wl.make_reduce_input(B, N, seed=7 * B + N)
     np.testing.assert_array_equal(bits(gpu_reduce(a)), bits(oracle.reduce_axis0(a)))
