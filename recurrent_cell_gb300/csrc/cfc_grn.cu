@@ -18,18 +18,23 @@
 //   k_grn_fwd      grid (rows / 32, J): a 32-row tile, one horizon; W1[j],
 //                  W2[j] and the row tile staged in shared memory (rows
 //                  padded by 16 bytes), 2 rows x 4 units per thread.
-//   k_grn_bwd_rows grid (rows / 32): all J horizons of a 32-row tile in turn
+//   k_grn_bwd_rows grid (rows / 16): all J horizons of a 16-row tile in turn
 //                  (fixed order, so grad_h sums the horizons in order j = 0..J-1),
 //                  dz2, dz1 = (W2^T dz2) GELU'(z1) and the trunk gradient
 //                  W1^T dz1 + dskip w_skip, scaled by lambda_j, in registers;
 //                  dz1, dz2, dgate, dmain, dskip go to the workspace.
-//   k_grn_wgrad    grid (B, N / 256): one thread per element of a sample's
-//                  packed gradient row, summed over k = K-1 .. 0 (the pages'
-//                  loop order) and written once (no += into scratch).
+//   k_grn_wgrad    grid (tiles, B): each packed gradient block is a product
+//                  (left factors)^T x (right factors) over a sample's K rows;
+//                  a block computes one tile of <= 64 x 64 outputs from the
+//                  sample's rows staged in shared memory, every output summed
+//                  over k = K-1 .. 0 (the pages' loop order) and written once
+//                  (no += into scratch).
 // reduce_axis0 then sums the B rows into the packed parameter gradient.
 //
 // The extern "C" entry points of the heads (declared in cfc.h) are at the end
 // of this file; they validate the arguments before anything is launched.
+#include <algorithm>
+
 #include "cfc_internal.cuh"
 
 namespace cfc {
@@ -37,7 +42,9 @@ namespace {
 
 constexpr int kGrnRows = 32;          // rows per block
 constexpr int kGrnThreads = 256;
-constexpr int kGrnLdT = kGrnRows + 4; // row stride of the transposed dz tiles
+constexpr int kGrnBwdRows = 16;       // rows per block of the backward (4 warps x 4 rows)
+constexpr int kGrnBwdThreads = 128;
+constexpr int kGrnBwdLdT = kGrnBwdRows + 4;   // row stride of the transposed dz tiles
 
 struct GrnDims {
   int Hd, M, J;
@@ -65,6 +72,24 @@ __host__ __device__ inline GrnDims grn_dims(int Hd, int M, int J) {
   return d;
 }
 
+// Asynchronous global -> shared copies (no register round trip, so a thread's
+// copies are all in flight at once); src_bytes 0 writes zeros instead.
+__device__ __forceinline__ void cpa16(float* dst, const float* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(valid ? 16u : 0u)
+               : "memory");
+}
+__device__ __forceinline__ void cpa4(float* dst, const float* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(valid ? 4u : 0u)
+               : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cpa_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ float gelu_f(float z) { return 0.5f * z * (1.f + erff(z * 0.70710678118654752f)); }
 __device__ __forceinline__ float gelu_grad_f(float z) {
   return 0.5f * (1.f + erff(z * 0.70710678118654752f)) + z * expf(-0.5f * z * z) * 0.39894228040143268f;
@@ -78,7 +103,8 @@ size_t fwd_smem_floats(int Hd, int M) {
 }
 size_t bwd_smem_floats(int Hd, int M) {
   const int ldh = Hd + 4, ldm = M + 4;
-  return (size_t)M * ldh + (size_t)M * ldm + 2 * (size_t)M * kGrnLdT + 2 * (size_t)M + Hd + 3 * kGrnRows;
+  return 2 * ((size_t)M * ldh + (size_t)M * ldm + 2 * (size_t)M + Hd) + 2 * (size_t)M * kGrnBwdLdT +
+         3 * kGrnBwdRows;
 }
 
 __global__ void __launch_bounds__(kGrnThreads)
@@ -105,26 +131,26 @@ k_grn_fwd(const float* __restrict__ h, long long R, int Hd, int M, int J, const 
   const int hq = Hd / 4, mq4 = M / 4;
   for (int e = tid; e < M * hq; e += kGrnThreads) {
     const int m = e / hq, q = e - m * hq;
-    *reinterpret_cast<float4*>(W1s + (size_t)m * ldh + 4 * q) = *reinterpret_cast<const float4*>(W1 + (size_t)m * Hd + 4 * q);
+    cpa16(W1s + (size_t)m * ldh + 4 * q, W1 + (size_t)m * Hd + 4 * q, true);
   }
   for (int e = tid; e < kGrnRows * hq; e += kGrnThreads) {
     const int rr = e / hq, q = e - rr * hq;
     const long long row = r0 + rr;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < R) v = *reinterpret_cast<const float4*>(h + row * Hd + 4 * q);
-    *reinterpret_cast<float4*>(hs + (size_t)rr * ldh + 4 * q) = v;
+    cpa16(hs + (size_t)rr * ldh + 4 * q, row < R ? h + row * Hd + 4 * q : h, row < R);   // rows past R: zeros
   }
   for (int e = tid; e < M * mq4; e += kGrnThreads) {
     const int m = e / mq4, q = e - m * mq4;
-    *reinterpret_cast<float4*>(W2s + (size_t)m * ldm + 4 * q) = *reinterpret_cast<const float4*>(W2 + (size_t)m * M + 4 * q);
+    cpa16(W2s + (size_t)m * ldm + 4 * q, W2 + (size_t)m * M + 4 * q, true);
   }
   for (int e = tid; e < M; e += kGrnThreads) {
-    b1s[e] = params[d.ob1 + (long long)j * M + e];
-    b2s[e] = params[d.ob2 + (long long)j * M + e];
-    wgs[e] = params[d.owg + (long long)j * M + e];
-    wms[e] = params[d.owm + (long long)j * M + e];
+    cpa4(b1s + e, params + d.ob1 + (long long)j * M + e, true);
+    cpa4(b2s + e, params + d.ob2 + (long long)j * M + e, true);
+    cpa4(wgs + e, params + d.owg + (long long)j * M + e, true);
+    cpa4(wms + e, params + d.owm + (long long)j * M + e, true);
   }
-  for (int e = tid; e < Hd; e += kGrnThreads) wss[e] = params[d.ows + (long long)j * Hd + e];
+  for (int e = tid; e < Hd; e += kGrnThreads) cpa4(wss + e, params + d.ows + (long long)j * Hd + e, true);
+  cpa_commit();
+  cpa_wait<0>();
   __syncthreads();
 
   // thread -> rows 2rp, 2rp+1 and units m = mq + 16 t (t = 0..3)
@@ -234,48 +260,59 @@ k_grn_fwd(const float* __restrict__ h, long long R, int Hd, int M, int J, const 
   }
 }
 
-__global__ void __launch_bounds__(kGrnThreads)
+__global__ void __launch_bounds__(kGrnBwdThreads)
 k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ params,
                const float* __restrict__ probs, const float* __restrict__ saved,
                const float* __restrict__ grad_probs, const float* __restrict__ lambda,
                const float* __restrict__ grad_h_carry, float* __restrict__ grad_h, float* __restrict__ ws) {
   extern __shared__ __align__(16) float sm[];
   const GrnDims d = grn_dims(Hd, M, J);
-  const long long r0 = (long long)blockIdx.x * kGrnRows;
+  const long long r0 = (long long)blockIdx.x * kGrnBwdRows;
   const int ldh = Hd + 4, ldm = M + 4, tid = threadIdx.x;
-  float* W1s = sm;                                  // [M][ldh]
-  float* W2s = W1s + (size_t)M * ldh;               // [M][ldm]
-  float* dz2T = W2s + (size_t)M * ldm;              // [M][kGrnLdT]
-  float* dz1T = dz2T + (size_t)M * kGrnLdT;         // [M][kGrnLdT]
-  float* wgs = dz1T + (size_t)M * kGrnLdT;          // [M]
-  float* wms = wgs + M;                             // [M]
-  float* wss = wms + M;                             // [Hd]
-  float* sc = wss + Hd;                             // [32][3]: dgate, dmain, dskip
+  // two buffers of one horizon's weights {W1 [M][ldh], W2 [M][ldm], w_gate,
+  // w_main [M], w_skip [Hd]}: horizon j + 1 is copied in while j computes
+  const size_t bufsz = (size_t)M * ldh + (size_t)M * ldm + 2 * (size_t)M + Hd;
+  float* dz2T = sm + 2 * bufsz;                     // [M][kGrnBwdLdT]
+  float* dz1T = dz2T + (size_t)M * kGrnBwdLdT;      // [M][kGrnBwdLdT]
+  float* sc = dz1T + (size_t)M * kGrnBwdLdT;        // [16][3]: dgate, dmain, dskip
   const int hq = Hd / 4, mq4 = M / 4;
   const long long JM = (long long)J * M;
   const int rg = tid / 32, lane = tid % 32;         // rows 4rg..4rg+3; columns 4 (lane + 32 c) ..
   float acc[4][8] = {};                             // lambda-weighted trunk gradient, c = 0, 1
 
+  auto stage = [&](int jj) {
+    float* W1b = sm + (size_t)(jj & 1) * bufsz;
+    float* W2b = W1b + (size_t)M * ldh;
+    float* wgb = W2b + (size_t)M * ldm;
+    const float* W1 = params + d.oW1 + (long long)jj * M * Hd;
+    const float* W2 = params + d.oW2 + (long long)jj * M * M;
+    for (int e = tid; e < M * hq; e += kGrnBwdThreads) {
+      const int m = e / hq, q = e - m * hq;
+      cpa16(W1b + (size_t)m * ldh + 4 * q, W1 + (size_t)m * Hd + 4 * q, true);
+    }
+    for (int e = tid; e < M * mq4; e += kGrnBwdThreads) {
+      const int m = e / mq4, q = e - m * mq4;
+      cpa16(W2b + (size_t)m * ldm + 4 * q, W2 + (size_t)m * M + 4 * q, true);
+    }
+    for (int e = tid; e < M; e += kGrnBwdThreads) {
+      cpa4(wgb + e, params + d.owg + (long long)jj * M + e, true);
+      cpa4(wgb + M + e, params + d.owm + (long long)jj * M + e, true);
+    }
+    for (int e = tid; e < Hd; e += kGrnBwdThreads) cpa4(wgb + 2 * M + e, params + d.ows + (long long)jj * Hd + e, true);
+  };
+  stage(0);
+  cpa_commit();
   for (int j = 0; j < J; ++j) {
     __syncthreads();                                // the previous horizon's readers are done
-    const float* W1 = params + d.oW1 + (long long)j * M * Hd;
-    const float* W2 = params + d.oW2 + (long long)j * M * M;
-    for (int e = tid; e < M * hq; e += kGrnThreads) {
-      const int m = e / hq, q = e - m * hq;
-      *reinterpret_cast<float4*>(W1s + (size_t)m * ldh + 4 * q) =
-          *reinterpret_cast<const float4*>(W1 + (size_t)m * Hd + 4 * q);
-    }
-    for (int e = tid; e < M * mq4; e += kGrnThreads) {
-      const int m = e / mq4, q = e - m * mq4;
-      *reinterpret_cast<float4*>(W2s + (size_t)m * ldm + 4 * q) =
-          *reinterpret_cast<const float4*>(W2 + (size_t)m * M + 4 * q);
-    }
-    for (int e = tid; e < M; e += kGrnThreads) {
-      wgs[e] = params[d.owg + (long long)j * M + e];
-      wms[e] = params[d.owm + (long long)j * M + e];
-    }
-    for (int e = tid; e < Hd; e += kGrnThreads) wss[e] = params[d.ows + (long long)j * Hd + e];
-    if (tid < kGrnRows) {
+    if (j + 1 < J) stage(j + 1);                    // into the buffer horizon j - 1 used
+    cpa_commit();
+    cpa_wait<1>();                                  // this thread's copies of horizon j have landed
+    const float* W1s = sm + (size_t)(j & 1) * bufsz;
+    const float* W2s = W1s + (size_t)M * ldh;
+    const float* wgs = W2s + (size_t)M * ldm;
+    const float* wms = wgs + M;
+    const float* wss = wms + M;
+    if (tid < kGrnBwdRows) {
       const long long row = r0 + tid;
       float dgate = 0.f, dmain = 0.f, dskip = 0.f;
       if (row < R) {
@@ -296,11 +333,11 @@ k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ para
     }
     __syncthreads();
     // dz2 = dmain w_main + dgate w_gate (rows past R are zero)
-    for (int e = tid; e < kGrnRows * M; e += kGrnThreads) {
+    for (int e = tid; e < kGrnBwdRows * M; e += kGrnBwdThreads) {
       const int lr = e / M, m = e - lr * M;
       const long long row = r0 + lr;
       const float v = fmaf(sc[3 * lr + 1], wms[m], sc[3 * lr] * wgs[m]);
-      dz2T[(size_t)m * kGrnLdT + lr] = v;
+      dz2T[(size_t)m * kGrnBwdLdT + lr] = v;
       if (row < R) ws[row * d.sw + JM + (long long)j * M + m] = v;
     }
     __syncthreads();
@@ -308,7 +345,7 @@ k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ para
     {
       float a2[4][2] = {};
       for (int m = 0; m < M; ++m) {
-        const float4 dz = *reinterpret_cast<const float4*>(dz2T + (size_t)m * kGrnLdT + 4 * rg);
+        const float4 dz = *reinterpret_cast<const float4*>(dz2T + (size_t)m * kGrnBwdLdT + 4 * rg);
         const float w0 = (lane < M) ? W2s[(size_t)m * ldm + lane] : 0.f;
         const float w1 = (lane + 32 < M) ? W2s[(size_t)m * ldm + lane + 32] : 0.f;
         a2[0][0] = fmaf(w0, dz.x, a2[0][0]);
@@ -333,7 +370,7 @@ k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ para
             v = a2[rr][t] * gelu_grad_f(saved[row * d.sv + (long long)j * M + n]);
             ws[row * d.sw + (long long)j * M + n] = v;
           }
-          dz1T[(size_t)n * kGrnLdT + lr] = v;
+          dz1T[(size_t)n * kGrnBwdLdT + lr] = v;
         }
       }
     }
@@ -342,7 +379,7 @@ k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ para
     {
       float t[4][8] = {};
       for (int m = 0; m < M; ++m) {
-        const float4 dz = *reinterpret_cast<const float4*>(dz1T + (size_t)m * kGrnLdT + 4 * rg);
+        const float4 dz = *reinterpret_cast<const float4*>(dz1T + (size_t)m * kGrnBwdLdT + 4 * rg);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int cq = lane + 32 * c;
@@ -393,62 +430,121 @@ k_grn_bwd_rows(long long R, int Hd, int M, int J, const float* __restrict__ para
   }
 }
 
-// One thread per element n of sample b's packed gradient row: the sum over
-// k = K-1 .. 0 of (left factor) x (right factor), both read per row r = b*K + k.
+// Per-sample parameter gradients as small contractions over the sample's K
+// rows.  Every packed block is a product (left factors)^T x (right factors):
+//   W1[j][m][i]   = sum_k dz1[j][m] h[i]        w_skip[j][i] = sum_k dskip[j] h[i]
+//   W2[j][m][q]   = sum_k dz2[j][m] a1[j][q]
+//   w_gate[j][m]  = sum_k dgate[j] z2[j][m]     w_main[j][m] = sum_k dmain[j] z2[j][m]
+//   b1, b2, b_gate, b_main, b_skip = sum_k of the left factor (right factor 1)
+// A task is one tile of at most 64 left x 64 right columns of one such
+// product; block (task, b) stages the sample's rows of both factors in shared
+// memory, 64 rows at a time, and each thread accumulates 4 x 4 outputs.  Each
+// output is one fmaf chain over k = K-1 .. 0 (the pages' loop order), so the
+// result is exactly the per-element sum.
+constexpr int kWgTile = 64;
+constexpr int kWgLd = kWgTile + 4;          // padded row of the staged tiles
+constexpr int kWgMaxTasks = 96;
+
+struct GrnWgTask {
+  int Lbase, Lcs, nL;       // left column c of row r: ws[r * sw + Lbase + c * Lcs]
+  int Rsel, Rbase, nR;      // right column i of row r: 0 -> 1.0; 1 -> h[r * Hd + Rbase + i];
+                            // 2 -> saved[r * sv + Rbase + i]
+  long long Obase;          // output (c, i) -> per_sample[b * N + Obase + c * Ocs + i]
+  int Ocs;
+};
+struct GrnWgTable {
+  int count;
+  GrnWgTask t[kWgMaxTasks];
+};
+
 __global__ void __launch_bounds__(256)
-k_grn_wgrad(const float* __restrict__ h, const float* __restrict__ saved, const float* __restrict__ ws, int K,
-            int Hd, int M, int J, float* __restrict__ per_sample) {
+k_grn_wgrad(const __grid_constant__ GrnWgTable tab, const float* __restrict__ h, const float* __restrict__ saved,
+            const float* __restrict__ ws, int K, int Hd, int M, int J, float* __restrict__ per_sample) {
+  __shared__ __align__(16) float Ls[kWgTile][kWgLd];
+  __shared__ __align__(16) float Rs[kWgTile][kWgLd];
   const GrnDims d = grn_dims(Hd, M, J);
-  const long long n = (long long)blockIdx.y * 256 + threadIdx.x;
-  const long long b = blockIdx.x;
-  if (n >= d.N) return;
-  const long long JM = (long long)J * M;
-  const float* L;                 // left factor of row r at L[r * d.sw]
-  const float* Rt = nullptr;      // right factor at Rt[r * rs] (null: bias, factor 1)
-  long long rs = 0;
-  if (n < d.ob1) {                          // W1[j][m][i] <- dz1[j][m] h[i]
-    const long long jm = n / Hd;
-    L = ws + jm;
-    Rt = h + (n - jm * Hd);
-    rs = Hd;
-  } else if (n < d.oW2) {                   // b1
-    L = ws + (n - d.ob1);
-  } else if (n < d.ob2) {                   // W2[j][m][q] <- dz2[j][m] a1[j][q]
-    const long long e = n - d.oW2, jm = e / M, q = e - jm * M, j = jm / M;
-    L = ws + JM + jm;
-    Rt = saved + JM + j * M + q;
-    rs = d.sv;
-  } else if (n < d.owg) {                   // b2
-    L = ws + JM + (n - d.ob2);
-  } else if (n < d.obg) {                   // w_gate[j][m] <- dgate[j] z2[j][m]
-    const long long e = n - d.owg;
-    L = ws + 2 * JM + e / M;
-    Rt = saved + 2 * JM + e;
-    rs = d.sv;
-  } else if (n < d.owm) {                   // b_gate
-    L = ws + 2 * JM + (n - d.obg);
-  } else if (n < d.obm) {                   // w_main[j][m] <- dmain[j] z2[j][m]
-    const long long e = n - d.owm;
-    L = ws + 2 * JM + J + e / M;
-    Rt = saved + 2 * JM + e;
-    rs = d.sv;
-  } else if (n < d.ows) {                   // b_main
-    L = ws + 2 * JM + J + (n - d.obm);
-  } else if (n < d.obs) {                   // w_skip[j][i] <- dskip[j] h[i]
-    const long long e = n - d.ows, j = e / Hd;
-    L = ws + 2 * JM + 2 * J + j;
-    Rt = h + (e - j * Hd);
-    rs = Hd;
-  } else {                                  // b_skip
-    L = ws + 2 * JM + 2 * J + (n - d.obs);
+  const GrnWgTask T = tab.t[blockIdx.x];
+  const long long b = blockIdx.y;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const float* Rsrc = T.Rsel == 1 ? h : saved;
+  const long long rrs = T.Rsel == 1 ? Hd : d.sv;
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+  // row chunks from the last one down, rows in a chunk from the last one down
+  for (int k1 = K; k1 > 0; k1 -= kWgTile) {
+    const int k0 = k1 > kWgTile ? k1 - kWgTile : 0, nk = k1 - k0;
+    __syncthreads();
+    for (int e = tid; e < kWgTile * kWgTile; e += 256) {
+      const int kk = e >> 6, c = e & 63;
+      const long long r = b * K + k0 + kk;
+      const bool lv = kk < nk && c < T.nL, rv = kk < nk && c < T.nR;
+      cpa4(&Ls[kk][c], lv ? ws + r * d.sw + T.Lbase + (long long)c * T.Lcs : ws, lv);   // zeros outside
+      if (T.Rsel == 0) Rs[kk][c] = rv ? 1.f : 0.f;
+      else cpa4(&Rs[kk][c], rv ? Rsrc + r * rrs + T.Rbase + c : Rsrc, rv);
+    }
+    cpa_commit();
+    cpa_wait<0>();
+    __syncthreads();
+    for (int kk = nk - 1; kk >= 0; --kk) {
+      const float4 l4 = *reinterpret_cast<const float4*>(&Ls[kk][4 * ty]);
+      const float4 r4 = *reinterpret_cast<const float4*>(&Rs[kk][4 * tx]);
+      const float lf[4] = {l4.x, l4.y, l4.z, l4.w}, rf[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(lf[a], rf[c], acc[a][c]);
+    }
   }
-  float acc = 0.f;
-  for (int k = K - 1; k >= 0; --k) {
-    const long long r = b * K + k;
-    const float l = L[r * d.sw];
-    acc = Rt ? fmaf(l, Rt[r * rs], acc) : acc + l;
+  float* out = per_sample + b * d.N + T.Obase;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int c = 4 * ty + a;
+    if (c >= T.nL) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 4 * tx + q;
+      if (i < T.nR) out[(long long)c * T.Ocs + i] = acc[a][q];
+    }
   }
-  per_sample[b * d.N + n] = acc;
+}
+
+// The task table of the packed gradient (at most kWgMaxTasks tiles for the
+// supported shapes: J <= 8, M <= 64, Hd <= 256).
+bool build_wgrad_tasks(const GrnDims& d, GrnWgTable* tab) {
+  const int Hd = d.Hd, M = d.M, J = d.J, JM = J * M;
+  tab->count = 0;
+  auto add = [&](int Lbase, int Lcs, int nL, int Rsel, int Rbase, int nR, long long Obase, int Ocs) {
+    for (int c0 = 0; c0 < nL; c0 += kWgTile)
+      for (int i0 = 0; i0 < nR; i0 += kWgTile) {
+        if (tab->count == kWgMaxTasks) return false;
+        GrnWgTask& t = tab->t[tab->count++];
+        t.Lbase = Lbase + c0 * Lcs;
+        t.Lcs = Lcs;
+        t.nL = std::min(kWgTile, nL - c0);
+        t.Rsel = Rsel;
+        t.Rbase = Rbase + i0;
+        t.nR = std::min(kWgTile, nR - i0);
+        t.Obase = Obase + (long long)c0 * Ocs + i0;
+        t.Ocs = Ocs;
+      }
+    return true;
+  };
+  bool ok = true;
+  ok = ok && add(0, 1, JM, 1, 0, Hd, d.oW1, Hd);                                  // W1
+  ok = ok && add(2 * JM + 2 * J, 1, J, 1, 0, Hd, d.ows, Hd);                      // w_skip
+  for (int j = 0; j < J && ok; ++j)
+    ok = add(JM + j * M, 1, M, 2, JM + j * M, M, d.oW2 + (long long)j * M * M, M);   // W2[j]
+  for (int j = 0; j < J && ok; ++j)                                               // w_gate[j], w_main[j]
+    ok = add(2 * JM + j, J, 2, 2, 2 * JM + j * M, M, d.owg + (long long)j * M, (int)(d.owm - d.owg));
+  ok = ok && add(0, 1, JM, 0, 0, 1, d.ob1, 1);                                    // b1
+  ok = ok && add(JM, 1, JM, 0, 0, 1, d.ob2, 1);                                   // b2
+  ok = ok && add(2 * JM, 1, J, 0, 0, 1, d.obg, 1);                                // b_gate
+  ok = ok && add(2 * JM + J, 1, J, 0, 0, 1, d.obm, 1);                            // b_main
+  ok = ok && add(2 * JM + 2 * J, 1, J, 0, 0, 1, d.obs, 1);                        // b_skip
+  return ok;
 }
 
 }  // namespace
@@ -484,15 +580,17 @@ cudaError_t launch_grn_backward(const float* h, int B, int K, int Hd, int M, int
     cudaError_t e = cudaFuncSetAttribute(k_grn_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     TraceScope trace("grn_bwd_rows", s);
-    k_grn_bwd_rows<<<(unsigned)((R + kGrnRows - 1) / kGrnRows), kGrnThreads, smem, s>>>(
+    k_grn_bwd_rows<<<(unsigned)((R + kGrnBwdRows - 1) / kGrnBwdRows), kGrnBwdThreads, smem, s>>>(
         R, Hd, M, J, params, probs, saved, grad_probs, lambda, grad_h_carry, grad_h, ws);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
+    GrnWgTable tab;
+    if (!build_wgrad_tasks(d, &tab)) return cudaErrorInvalidValue;
     TraceScope trace("grn_wgrad", s);
-    dim3 grid((unsigned)B, (unsigned)((d.N + 255) / 256));
-    k_grn_wgrad<<<grid, 256, 0, s>>>(h, saved, ws, K, Hd, M, J, per_sample);
+    dim3 grid((unsigned)tab.count, (unsigned)B);
+    k_grn_wgrad<<<grid, 256, 0, s>>>(tab, h, saved, ws, K, Hd, M, J, per_sample);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
