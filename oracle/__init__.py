@@ -6,6 +6,6 @@ it never imports the CUDA library.  See ``cfc_oracle`` for the definitions
 it follows and the rounding points it mirrors.
 """
 from .cfc_oracle import (  # noqa: F401
-    FP32, TF32, BF16, round_bf16, round_tf32, round_fp16, cell_forward, forward, backward,
+    FP32, TF32, BF16, round_bf16, round_tf32, cell_forward, forward, backward,
     per_sample_length, unpack_per_sample, reduce_axis0,
 )

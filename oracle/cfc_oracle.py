@@ -33,13 +33,8 @@ Precision modes (the rounding points the CUDA path applies, mirrored here):
   round to nearest, ties away from zero); state and activations are not.
 * BF16: x, h0, W_in, W_rec arrive bf16-valued; the new state h_{k+1} is
   rounded to bf16 (round to nearest even, through float32) and that rounded
-  value is both stored and fed to the next step; the activations gate, g, h~
-  that the forward saves for the backward are stored in 16 bits, as IEEE
-  half precision (round to nearest even, through float32: every saved value
-  lies in [-1, 1], where half keeps 11 significand bits against bf16's 8),
-  so the backward forms dA from their half values; dA is rounded to bf16
-  before the gradient contractions.  Within the forward step the activations
-  are used unrounded.
+  value is both stored and fed to the next step; dA is rounded to bf16
+  before the gradient contractions.  Activations stay unrounded.
 """
 
 from __future__ import annotations
@@ -73,14 +68,6 @@ def round_tf32(a) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def round_fp16(a) -> np.ndarray:
-    """Round to IEEE half precision (11-bit significand, subnormals kept), ties
-    to even; input first taken to float32.  Returned as float64 holding the
-    half value."""
-    f = np.asarray(a, dtype=np.float64).astype(np.float32)
-    return f.astype(np.float16).astype(np.float64)
-
-
 def _operand(a, mode: int) -> np.ndarray:
     """A value as it enters a projection / gradient contraction."""
     if mode == TF32:
@@ -95,14 +82,6 @@ def _stored_state(h, mode: int) -> np.ndarray:
     if mode == BF16:
         return round_bf16(h)
     return np.asarray(h, dtype=np.float64)
-
-
-def _saved_activation(act, mode: int) -> np.ndarray:
-    """An activation (gate, g or h~) as the forward saves it and the backward
-    reads it."""
-    if mode == BF16:
-        return round_fp16(act)
-    return np.asarray(act, dtype=np.float64)
 
 
 def _dt_vector(dt, B: int) -> np.ndarray:
@@ -221,7 +200,7 @@ def backward(x, h0, W_in, W_rec, b, dt, mode: int = FP32,
                 delta += np.asarray(grad_h_last, dtype=np.float64)
             if y is not None:
                 delta += h_seq[:, K - 1] - np.asarray(y, dtype=np.float64)
-        gate, g, hh = (_saved_activation(fw[n][:, k], mode) for n in ("gate", "g", "hh"))
+        gate, g, hh = fw["gate"][:, k], fw["g"][:, k], fw["hh"][:, k]
         dA = np.empty((B, 3, H))
         dA[:, 1] = delta * gate * (1.0 - g * g)
         dA[:, 2] = delta * (1.0 - gate) * (1.0 - hh * hh)

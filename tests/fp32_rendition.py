@@ -18,9 +18,8 @@ Rounding points (the kernels' own, per precision mode):
   binary32 pattern cleared, nearest, ties away from zero).  State,
   activations and accumulators stay float32.
 * BF16: x, h0 and the weights arrive bf16-valued; the new state is rounded
-  to bf16 (nearest even) and that value is stored and carried; the saved
-  activations gate, g, h~ that the backward reads are IEEE half (nearest
-  even); dA is rounded to bf16 before every contraction it enters.
+  to bf16 (nearest even) and that value is stored and carried; dA is rounded
+  to bf16 before every contraction it enters.
 * FP32: no rounding.
 """
 
@@ -77,8 +76,7 @@ def kloop(inp: dict, mode: int, per_sample: bool = False) -> dict:
     grad_x = np.empty((B, K, n_in), dtype=f32)
     for k in range(K - 1, -1, -1):
         delta = carry + (hs[:, K] - y if k == K - 1 else f32(0))
-        saved = (lambda a: a.astype(np.float16).astype(f32)) if mode == BF16 else (lambda a: a)
-        gt, gg, hk = (saved(a[:, k]) for a in (gate, g, hh))
+        gt, gg, hk = gate[:, k], g[:, k], hh[:, k]
         d = np.empty((B, 3 * H), dtype=f32)
         d[:, H:2 * H] = delta * gt * (f32(1) - gg * gg)
         d[:, 2 * H:] = delta * (f32(1) - gt) * (f32(1) - hk * hk)

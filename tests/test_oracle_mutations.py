@@ -165,9 +165,6 @@ MUTANTS = [
     # precision modes
     ("cfc_oracle.py", "bf16 state not rounded", "return round_bf16(h)", "return np.asarray(h, dtype=np.float64)"),
     ("cfc_oracle.py", "dA not rounded", "dAo = _operand(dA, mode)", "dAo = dA"),
-    ("cfc_oracle.py", "saved activations not rounded", "return round_fp16(act)",
-     "return np.asarray(act, dtype=np.float64)"),
-    ("cfc_oracle.py", "saved activations rounded to bf16", "return round_fp16(act)", "return round_bf16(act)"),
     ("cfc_oracle.py", "W_in not rounded in the projection",
      "Wi = _operand(W_in, mode)\n", "Wi = np.asarray(W_in, dtype=np.float64)\n"),
     ("cfc_oracle.py", "state operand not rounded in the projection",
