@@ -701,15 +701,21 @@ def main():
     ap.add_argument("--workload", default="smoke", choices=sorted(wl.SHORT_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="seconds of oracle timing per CPU leg; 0 skips the CPU legs (profiling runs)")
     ap.add_argument("--reduce-only", action="store_true",
                     help="time only the standalone reduce_axis0 cases and the multi-matrix reducer (profiling aid)")
     ap.add_argument("--tau-only", action="store_true",
                     help="time only the tau-cell K loop on the smoke shape (profiling aid)")
     ap.add_argument("--grn-only", action="store_true",
                     help="time only the multi-horizon GRN heads (forward + backward) on the smoke shape")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: run the workload with this many samples instead of its own B "
+                         "(the line's config then names the reduced batch)")
     args = ap.parse_args()
     w = wl.SHORT_NAMES[args.workload]
+    if args.batch > 0:
+        w = w.with_(B=args.batch, name=f"{w.name}_profiled_at_B{args.batch}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -835,7 +841,7 @@ def main():
         secondary["grn_heads"] = measure_grn(wl.GRN_SMOKE, 30, 3, device, peaks, flush)
         secondary["cuda_graph"] = {wl.SHORT_NAMES[n].name: measure_graph(wl.SHORT_NAMES[n], 50, device)
                                    for n in ("tiny", "smoke")}
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0 and args.batch == 0:
         one, _ = time_oracle(w, seconds=args.cpu_seconds)
         cpu = time_oracle_all_cores(w, seconds=args.cpu_seconds)
         cpu["single_core"] = dict(value=one["value"], cores=1, sample=one["sample"])
