@@ -51,6 +51,7 @@ int kernel_choice() {
   if (strcmp(v, "simt") == 0) return kSimt;
   if (strcmp(v, "tc") == 0) return kTc;
   if (strcmp(v, "tcs") == 0) return kTcStream;
+  if (strcmp(v, "solo") == 0) return kSolo;
   return kAuto;
 }
 
@@ -150,8 +151,9 @@ int cfc_device_error(int clear) {
   const int a = read_device_error(clear);
   const int b = read_tc_kloop_error(clear);
   const int c = read_tc_bwd_error(clear);
-  if (a < 0 || b < 0 || c < 0) return CFC_ERR_DEVICE;
-  return (a || b || c) ? 1 : 0;
+  const int d = read_tc_solo_error(clear);
+  if (a < 0 || b < 0 || c < 0 || d < 0) return CFC_ERR_DEVICE;
+  return (a || b || c || d) ? 1 : 0;
 }
 
 int cfc_selftest_timeout(int max_polls, void* stream) {
@@ -190,10 +192,13 @@ int cfc_kloop_forward(const void* x, const void* h0, const void* W_in, const voi
   a.x = x; a.h0 = h0; a.W_in = W_in; a.W_rec = W_rec; a.b = b; a.dt = dt; a.dt_stride = dt_stride;
   a.h_seq = h_seq; a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Tensor-core cluster kernel (weights resident) while its grid fits one
-  // wave, else the tensor-core kernel with streamed weights, else the SIMT
-  // cluster kernel (FP32), else the plain SIMT kernel.
-  cudaError_t e = launch_forward_tc(L, a, s);
+  // Input projection + single-block tensor-core kernel (n_hid <= 128, W_rec
+  // resident in one block) while its grid fits one wave, else the tensor-core
+  // cluster kernel (weights resident) while its grid fits one wave, else the
+  // tensor-core kernel with streamed weights, else the SIMT cluster kernel
+  // (FP32), else the plain SIMT kernel.
+  cudaError_t e = launch_forward_solo_tc(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_forward_tc(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_forward_tc_stream(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_forward_cluster(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_forward_simt(L, a, s);
@@ -232,11 +237,13 @@ int cfc_kloop_backward(const void* x, const void* h0, const void* W_in, const vo
   a.ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // TF32 / bf16: the tensor-core cluster kernel while its grid fits one wave;
-  // then the CUDA-core cluster kernel while its grid stays within ~2 waves
-  // (many steps, fewer samples), else the tensor-core kernel with streamed
-  // weights, else SIMT.
-  cudaError_t e = launch_backward_cluster_tc(L, a, s);
+  // TF32 / bf16: the single-block tensor-core kernel (n_hid <= 128, W_rec^T
+  // resident in one block) while its grid fits one wave; then the tensor-core
+  // cluster kernel while its grid fits one wave; then the CUDA-core cluster
+  // kernel while its grid stays within ~2 waves (many steps, fewer samples),
+  // else the tensor-core kernel with streamed weights, else SIMT.
+  cudaError_t e = launch_backward_solo_tc(L, a, s);
+  if (e == cudaErrorNotSupported) e = launch_backward_cluster_tc(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_backward_cluster(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_backward_tc(L, a, s);
   if (e == cudaErrorNotSupported) e = launch_backward_simt(L, a, s);

@@ -188,7 +188,7 @@ cudaError_t launch_forward_simt(const Layout& L, const CfcArgs& a, cudaStream_t 
 // K-loop kernel family: CFC_KLOOP_KERNELS=tc | cluster | simt forces one
 // family where it supports the sizes (read on every call); anything else
 // selects automatically.
-enum KernelChoice { kAuto = 0, kCluster = 1, kSimt = 2, kTc = 3, kTcStream = 4 };
+enum KernelChoice { kAuto = 0, kCluster = 1, kSimt = 2, kTc = 3, kTcStream = 4, kSolo = 5 };
 int kernel_choice();
 
 // Tensor-core forward (TF32 / bf16 modes); cudaErrorNotSupported, launching
@@ -203,6 +203,11 @@ bool grad_x_gemm_applies(const Layout& L);
 cudaError_t launch_grad_x_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core backward, cluster split by units (TF32 / bf16 modes).
 cudaError_t launch_backward_cluster_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
+// Tensor-core forward and backward in one block per sample tile (TF32 / bf16,
+// n_hid <= 128); the forward first runs the input projection over all rows.
+cudaError_t launch_forward_solo_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
+cudaError_t launch_backward_solo_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
+int read_tc_solo_error(int clear);
 // Tensor-core forward with streamed W_cat tiles (TF32 / bf16 modes).
 cudaError_t launch_forward_tc_stream(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core backward (TF32 / bf16 modes), streamed W_cat^T tiles.

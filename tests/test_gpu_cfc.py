@@ -58,7 +58,7 @@ def test_smoke_fp32_scratch_path():
     assert_close(got["per_sample"], ref["per_sample"], w.math, "smoke:per_sample")
 
 
-@pytest.mark.parametrize("kernels", ["tc", "tcs", "cluster", "simt"])
+@pytest.mark.parametrize("kernels", ["tc", "tcs", "cluster", "simt", "solo"])
 @pytest.mark.parametrize("w", [wl.TINY, wl.SMOKE, wl.MID.with_(B=128, K=16),
                                wl.LARGE.with_(B=96, K=4)], ids=lambda w: w.name)
 def test_kernel_families_on_benchmark_shapes(w, kernels, monkeypatch):
@@ -136,6 +136,11 @@ EDGE = [
     wl.Workload("edge_tcs_bf16_H384", B=70, K=3, n_in=64, n_hid=384, math=wl.MATH_BF16,
                 dt_per_sample=True),
     wl.Workload("edge_tcs_bf16_H512", B=40, K=2, n_in=64, n_hid=512, math=wl.MATH_BF16),
+    # single-block tensor-core backward: ragged last tile (B = 37), n_hid not a
+    # multiple of 32 (idle TMEM lanes) and n_hid = 128 exactly in TF32
+    wl.Workload("edge_solo_tf32_B37_H100", B=37, K=4, n_in=20, n_hid=100, math=wl.MATH_TF32,
+                dt_per_sample=True),
+    wl.Workload("edge_solo_bf16_B20_H128", B=20, K=6, n_in=64, n_hid=128, math=wl.MATH_BF16),
     # TMA-fed weight gradient (bf16, GEMM path): 64 steps of one sample per
     # chunk with a ragged 3H tile, and whole samples per chunk
     wl.Workload("edge_tma_K128_H64", B=3, K=128, n_in=64, n_hid=64, math=wl.MATH_BF16,
@@ -154,7 +159,7 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt"])
+@pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt", "solo"])
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("path", [wl.GRAD_SCRATCH, wl.GRAD_GEMM])
 def test_edge_shapes(w, path, kernels, monkeypatch):
