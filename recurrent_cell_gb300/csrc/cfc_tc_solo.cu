@@ -42,7 +42,8 @@ __device__ int g_tc_solo_error = 0;
 
 namespace {
 
-constexpr int kSoloThreads = 256;          // 8 warps: lane quadrant (warp & 3), sample half (warp >> 2)
+constexpr int kSoloThreads = 256;          // 8 cell warps: lane quadrant (warp & 3), sample half (warp >> 2)
+constexpr int kSoloBlock = kSoloThreads + 32;   // + warp 8, which only issues the MMAs
 constexpr int kSoloBt = 16;                // samples per block (the MMA's N)
 constexpr int kSoloHalf = kSoloBt / 2;     // samples per thread
 constexpr uint32_t kSoloPolls = 1u << 24;
@@ -54,8 +55,8 @@ constexpr uint32_t kSoloTmemCols = 512;
 constexpr uint32_t kSoloColA = 128;
 constexpr size_t kSoloSmemOne = 116 * 1024;
 
-// Eight A-operand values of one TMEM lane as 32-bit columns: tf32 one value a
-// column, bf16 two (lower K index in the low half).
+// Two bf16 operand values as one 32-bit word (lower K index in the low half);
+// a tf32 value as its bits.
 template <typename ET>
 __device__ __forceinline__ uint32_t pack_col(float lo, float hi) {
   if constexpr (sizeof(ET) == 4) {
@@ -79,14 +80,102 @@ __device__ __forceinline__ uint32_t kmaj(int row, int kk, int rows) {
   return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
 }
 
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}" : "=r"(pred));
+  return pred != 0;
+}
+
+// Barrier among the cell warps only (named barrier 1): the issuing warp
+// does not take part.
+__device__ __forceinline__ void cell_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoloThreads) : "memory"); }
+
+// Four (or three) 32x32b.x8 TMEM loads of this warp's lanes at columns
+// taddr + stride * j under one wait.
+__device__ __forceinline__ void tmem_ld8x4(uint32_t taddr, uint32_t stride, float (&v)[4][kSoloHalf]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride), "r"(taddr + 3 * stride)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < kSoloHalf; ++i) v[j][i] = __uint_as_float(r[8 * j + i]);
+}
+__device__ __forceinline__ void tmem_ld8x3(uint32_t taddr, uint32_t stride, float (&v)[3][kSoloHalf]) {
+  uint32_t r[24];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%24];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%25];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%26];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+      : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int i = 0; i < kSoloHalf; ++i) v[j][i] = __uint_as_float(r[8 * j + i]);
+}
+
 // The carry of this thread's lane and samples: the sum of the four partial
 // chains (TMEM columns 16 j + n).
 __device__ __forceinline__ void ld_carry(uint32_t taddr, float (&cz)[kSoloHalf]) {
   float p[4][kSoloHalf];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) tc::tmem_ld8(taddr + (uint32_t)(j * kSoloBt), p[j]);
+  tmem_ld8x4(taddr, (uint32_t)kSoloBt, p);
 #pragma unroll
   for (int i = 0; i < kSoloHalf; ++i) cz[i] = (p[0][i] + p[1][i]) + (p[2][i] + p[3][i]);
+}
+
+// Stage rows [0, 128) x K [0, Kpad) of a row-major matrix (row r at
+// src + r * ld; rows >= rows_valid and K >= k_valid are zero) as a K-major
+// operand of Kpad / (128 B) atoms at dst, rounded to the operand.  All
+// nthreads threads of the block take part: lanes run along K (coalesced
+// loads, conflict-free stores), each thread has eight loads in flight, and
+// the row order is rotated by `rot` so that blocks reading the same matrix
+// at the same time spread their requests over the L2.
+template <typename ET, int MODE>
+__device__ __forceinline__ void stage_kmajor(uint8_t* dst, const ET* __restrict__ src, int ld, int rows_valid,
+                                             int k_valid, int Kpad, int rot, int tid, int nthreads) {
+  const int tot = 128 * Kpad;
+  for (int e0 = tid; e0 < tot; e0 += 8 * nthreads) {
+    float v[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int e = e0 + t * nthreads, i0 = e / Kpad, kk = e - i0 * Kpad, i = (i0 + rot) & 127;
+      v[t] = (e < tot && i < rows_valid && kk < k_valid) ? ldf(src + (long long)i * ld + kk) : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int e = e0 + t * nthreads, i0 = e / Kpad, kk = e - i0 * Kpad, i = (i0 + rot) & 127;
+      if (e < tot) st_el<ET>(dst + kmaj<ET>(i, kk, 128), to_operand<MODE>(v[t]));
+    }
+  }
+}
+
+// Copy the K-major operand staged at src (nA atoms of 128 rows) into TMEM
+// columns from tcol (8 columns per K step), issued by the calling warp.
+__device__ __forceinline__ void copy_operand_to_tmem(uint32_t tcol, const uint8_t* src, int nA) {
+  const uint64_t d0 = tc::sdesc_k_sw128(tc::smem_u32(src));
+  for (int a = 0; a < nA; ++a) {
+    const uint64_t d = tc::sdesc_advance(d0, (uint32_t)a * 128u * 128u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (elect_one()) tc::tmem_cp_128x256b(tcol + (uint32_t)(a * 4 + j) * 8u, d + 2 * j);
+      __syncwarp();
+    }
+  }
 }
 
 template <typename ET, int MODE>
@@ -104,53 +193,81 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
 
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  uint8_t* dAs = sm;                               // nAk x [kSoloBt rows (n)][128 B]
-  __shared__ uint64_t bar;
+  uint8_t* Wt = sm;                                // nAk x [128 rows (j)][128 B]
+  uint8_t* dAs = sm + (size_t)nAk * 128 * 128;     // nAk x [kSoloBt rows (n)][128 B]
+  __shared__ uint64_t bar, bar_cp;
   __shared__ uint32_t tmem_base;
   __shared__ float dts[kSoloBt];
   __shared__ int err;
 
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bar_cp, 1);
     tc::mbar_init_fence();
     err = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kSoloTmemCols);
   for (int e = tid; e < kSoloBt * Kpad; e += kSoloThreads) st_el<ET>(dAs + kmaj<ET>(e / Kpad, e % Kpad, kSoloBt), 0.f);
   if (tid < kSoloBt) dts[tid] = (b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  // A operand in TMEM: lane j (output unit), K index kap = c*H + i ->
-  // W_rec[c][i][j]; lanes j >= H and K beyond 3H are zero.  The two warps of
-  // a lane quadrant fill one half of the nAk*32 columns each, 8 at a time
-  // (for a fixed K index the 32 lanes read 32 consecutive floats).
+  // A operand in shared memory: row j (output unit), K index kap = c*H + i
+  // -> W_rec[c][i][j]; rows j >= H and K beyond 3H are zero.  One task = one
+  // 16-byte chunk (row j, kap0 .. kap0 + 16 B): lanes take consecutive rows,
+  // so each of its loads reads consecutive values, and the swizzle spreads
+  // the 32 chunk stores over all banks.  A group of tasks has all its loads
+  // in flight before the first store.
+  // Every block reads the same weights at the same time: each starts at a
+  // different chunk column (rot) so that the blocks' requests spread over
+  // the L2 instead of queueing on the same lines.
   {
-    const int ncols = nAk * 32, half = ncols / 2;
-    const int j = u;
-    for (int col0 = (warp >> 2) * half; col0 < (warp >> 2) * half + half; col0 += 8) {
-      uint32_t r[8];
+    constexpr int EPQ = 16 / (int)sizeof(ET);          // elements per chunk
+    constexpr int TG = (sizeof(ET) == 4) ? 8 : 4;      // tasks per group
+    const int Q = Kpad / EPQ, ntask = 128 * Q;
+    const int rot = (int)((blockIdx.x * 37u) % (unsigned)Q);
+    for (int t0 = tid; t0 < ntask; t0 += TG * kSoloThreads) {
+      float v[TG][EPQ];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int k0 = (sizeof(ET) == 4) ? col0 + t : 2 * (col0 + t);
-        const float lo = (j < H && k0 < H3) ? ld_operand<MODE>(W_rec + (long long)k0 * H + j) : 0.f;
-        float hi = 0.f;
-        if constexpr (sizeof(ET) == 2) hi = (j < H && k0 + 1 < H3) ? ld_operand<MODE>(W_rec + (long long)(k0 + 1) * H + j) : 0.f;
-        r[t] = pack_col<ET>(lo, hi);
+      for (int g = 0; g < TG; ++g) {
+        const int task = t0 + g * kSoloThreads, j = task & 127;
+        const int q = (task >> 7) + rot, kap0 = (q < Q ? q : q - Q) * EPQ;
+#pragma unroll
+        for (int e = 0; e < EPQ; ++e)
+          v[g][e] = (task < ntask && j < H && kap0 + e < H3) ? ldf(W_rec + (long long)(kap0 + e) * H + j) : 0.f;
       }
-      tc::tmem_st8(tmem + lane_off + kSoloColA + (uint32_t)col0, r);
+#pragma unroll
+      for (int g = 0; g < TG; ++g) {
+        const int task = t0 + g * kSoloThreads, j = task & 127;
+        const int q = (task >> 7) + rot, kap0 = (q < Q ? q : q - Q) * EPQ;
+        if (task < ntask) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            w[q] = (sizeof(ET) == 4) ? __float_as_uint(to_operand<MODE>(v[g][q]))
+                                     : pack_col<ET>(to_operand<MODE>(v[g][2 * q]), to_operand<MODE>(v[g][(2 * q + 1) % EPQ]));
+          *reinterpret_cast<uint4*>(Wt + kmaj<ET>(j, kap0, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
     }
-    tc::tmem_st_wait();
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const bool mine = u < H;
   const uint32_t taddr = tmem + lane_off + (uint32_t)n0;
   const uint32_t id = tc::idesc(128, (uint32_t)kSoloBt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
-  const bool mine = u < H;
+  // The staged A operand into TMEM (columns kSoloColA + 8 s for K step s),
+  // where the MMAs read it; the copies complete before the first MMA.
+  if (warp == 0) {
+    copy_operand_to_tmem(tmem + kSoloColA, Wt, nAk);
+    tc::mma_commit_w(&bar_cp);
+    if (!tc::mbar_wait(&bar_cp, 0, kSoloPolls) && lane == 0) err = 1;
+    __syncwarp();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
   // Saved activations and per-step seeds of step k for this thread's samples,
   // loaded one step ahead of their use.
@@ -210,7 +327,7 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    // ---- 2. carry_k^T = W_rec^T dA_k^T (one thread issues; the next step's
+    // ---- 2. carry_k^T = W_rec^T dA_k^T (warp 0 issues; the next step's
     // activations load meanwhile)
     if (warp == 0 && !err) {
       // K step (a, j) accumulates into partial carry j: four independent
@@ -236,7 +353,7 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
     tc::fence_after_sync();
   }
   // grad_h0 = the carry after step 0
-  if (grad_h0) {
+  {
     float cz[kSoloHalf];
     if (!err) {
       ld_carry(taddr, cz);
@@ -244,7 +361,7 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
 #pragma unroll
       for (int i = 0; i < kSoloHalf; ++i) cz[i] = 0.f;
     }
-    if (mine) {
+    if (mine && grad_h0) {
 #pragma unroll
       for (int i = 0; i < kSoloHalf; ++i) {
         const int bb = b0 + n0 + i;
@@ -268,10 +385,8 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
 // MMAs, so that its stalls on a full MMA queue (the look-ahead input part)
 // delay no cell work.
 // ---------------------------------------------------------------------------
-constexpr int kFwdThreads = kSoloThreads + 32;
-
 template <typename ET, int MODE>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(kSoloBlock, 1)
 k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __restrict__ W_in,
                const ET* __restrict__ W_rec, const float* __restrict__ bias, const float* __restrict__ dt,
                int dt_stride, int B, int K, int n_in, int H, int nAx, int nAh, float* __restrict__ act,
@@ -293,83 +408,101 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
   uint8_t* Wi = sm;                                           // head c: c * nAx * 16 KB
   uint8_t* Xs = Wi + (size_t)3 * nAx * 128 * 128;             // buffer s: s * nAx * 2 KB
   uint8_t* Zh = Xs + (size_t)2 * nAx * kSoloBt * 128;         // nAh x 2 KB
-  __shared__ uint64_t bar;
+  uint8_t* Wst = Zh + (size_t)nAh * kSoloBt * 128;            // W_rec[c] staging: nAh x 16 KB
+  __shared__ uint64_t bar, bar_cp;
   __shared__ uint32_t tmem_base;
   __shared__ float dts[kSoloBt];
   __shared__ int err;
 
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bar_cp, 1);
     tc::mbar_init_fence();
     err = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kSoloTmemCols);
 
-  auto load_x = [&](int k, float (&r)[kMaxQ]) {
+  // x rows are kept as stored (raw) in registers until they are staged, so
+  // that the loads of step k+2 stay in flight through step k.
+  auto load_x = [&](int k, ET (&r)[kMaxQ]) {
     const int bb = b0 + xn;
     const ET* src = x + ((long long)bb * K + k) * n_in;
 #pragma unroll
     for (int q = 0; q < kMaxQ; ++q) {
       const int kk = xk0 + 16 * q;
-      r[q] = (q < nq && k < K && bb < B && kk < n_in) ? ld_operand<MODE>(src + kk) : 0.f;
+      r[q] = (q < nq && k < K && bb < B && kk < n_in) ? src[kk] : ET(0.f);
     }
   };
-  auto store_x = [&](int s, const float (&r)[kMaxQ]) {
+  auto store_x = [&](int s, const ET (&r)[kMaxQ]) {
     uint8_t* dst = Xs + (size_t)s * nAx * kSoloBt * 128;
 #pragma unroll
     for (int q = 0; q < kMaxQ; ++q)
-      if (q < nq) st_el<ET>(dst + kmaj<ET>(xn, xk0 + 16 * q, kSoloBt), r[q]);
+      if (q < nq) st_el<ET>(dst + kmaj<ET>(xn, xk0 + 16 * q, kSoloBt), to_operand<MODE>((float)r[q]));
   };
 
-  // W_in[c] (A, rows = units, K = input features), x_0 and x_1, h_0
-  for (int e = tid; e < 3 * 128 * KpadX; e += kFwdThreads) {
-    const int c = e / (128 * KpadX), rem = e - c * 128 * KpadX, i = rem / KpadX, kk = rem - i * KpadX;
-    const float v = (i < H && kk < n_in) ? ld_operand<MODE>(W_in + ((long long)c * H + i) * n_in + kk) : 0.f;
-    st_el<ET>(Wi + (size_t)c * nAx * 128 * 128 + kmaj<ET>(i, kk, 128), v);
-  }
-  if (tid < kSoloThreads) {
-    float r[kMaxQ];
-    load_x(0, r);
-    store_x(0, r);
-    load_x(1, r);
-    store_x(1, r);
-  }
-  for (int e = tid; e < kSoloBt * KpadH; e += kFwdThreads) {
-    const int n = e / KpadH, kk = e - n * KpadH, bb = b0 + n;
-    const float v = (bb < B && kk < H) ? ld_operand<MODE>(h0 + (long long)bb * H + kk) : 0.f;
-    st_el<ET>(Zh + kmaj<ET>(n, kk, kSoloBt), v);
-  }
-  if (tid < kSoloBt) dts[tid] = (b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
+  // W_rec[c] (rows = units, K = state) goes to TMEM head by head through
+  // one staging buffer (copy of head c overlaps the staging of what
+  // follows); W_in[c] (rows = units, K = input features) stays in shared
+  // memory; then x_0, x_1 and h_0.
+  const int rot = (int)((blockIdx.x * 37u) & 127u);
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();                                   // TMEM address visible
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  // W_rec[c] into TMEM: lane i (unit), column c * nAh * 32 + kk (tf32) or
-  // kk / 2 (bf16) -> W_rec[c][i][kk]; lanes i >= H and kk >= H are zero.  The
-  // two warps of a lane quadrant take alternate 8-column chunks.
+  const bool issuer = warp == kSoloThreads / 32;
+  for (int c = 0; c < 3; ++c) {
+    if (c > 0) {                                     // staging buffer free again
+      if (tid == 0 && !tc::mbar_wait(&bar_cp, (uint32_t)((c - 1) & 1), kSoloPolls)) err = 1;
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+    }
+    stage_kmajor<ET, MODE>(Wst, W_rec + (long long)c * H * H, H, H, H, KpadH, rot, tid, kSoloBlock);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (issuer) {
+      copy_operand_to_tmem(tmem + kSoloColA + (uint32_t)(c * nAh * 32), Wst, nAh);
+      tc::mma_commit_w(&bar_cp);
+    }
+    if (c == 0)
+      for (int cc = 0; cc < 3; ++cc)
+        stage_kmajor<ET, MODE>(Wi + (size_t)cc * nAx * 128 * 128, W_in + (long long)cc * H * n_in, n_in, H, n_in, KpadX,
+                               rot, tid, kSoloBlock);
+  }
   if (tid < kSoloThreads) {
-    const int ccols = nAh * 32;
-    for (int chunk = warp >> 2; chunk < 3 * ccols / 8; chunk += 2) {
-      const int col0 = chunk * 8, c = col0 / ccols, cc = col0 - c * ccols;
-      const ET* row = W_rec + ((long long)c * H + u) * H;
-      uint32_t r[8];
+    ET r0[kMaxQ], r1[kMaxQ];
+    load_x(0, r0);
+    load_x(1, r1);
+    store_x(0, r0);
+    store_x(1, r1);
+  }
+  {
+    const int tot = kSoloBt * KpadH;
+    for (int e0 = tid; e0 < tot; e0 += 8 * kSoloBlock) {
+      float v[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const int k0 = (sizeof(ET) == 4) ? cc + t : 2 * (cc + t);
-        const float lo = (mine && k0 < H) ? ld_operand<MODE>(row + k0) : 0.f;
-        float hi = 0.f;
-        if constexpr (sizeof(ET) == 2) hi = (mine && k0 + 1 < H) ? ld_operand<MODE>(row + k0 + 1) : 0.f;
-        r[t] = pack_col<ET>(lo, hi);
+        const int e = e0 + t * kSoloBlock;
+        const int n = e / KpadH, kk = e - n * KpadH, bb = b0 + n;
+        v[t] = (e < tot && bb < B && kk < H) ? ldf(h0 + (long long)bb * H + kk) : 0.f;
       }
-      tc::tmem_st8(tmem + lane_off + kSoloColA + (uint32_t)col0, r);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int e = e0 + t * kSoloBlock;
+        const int n = e / KpadH, kk = e - n * KpadH;
+        if (e < tot) st_el<ET>(Zh + kmaj<ET>(n, kk, kSoloBt), to_operand<MODE>(v[t]));
+      }
     }
-    tc::tmem_st_wait();
   }
+  if (tid < kSoloBt) dts[tid] = (b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
+  if (tid == 0 && !tc::mbar_wait(&bar_cp, 0u, kSoloPolls)) err = 1;   // the copy of head 2
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t id = tc::idesc(128, (uint32_t)kSoloBt, sizeof(ET) == 4 ? tc::kFmtTF32 : tc::kFmtBF16);
   const uint64_t wd0 = tc::sdesc_k_sw128(tc::smem_u32(Wi));
   const uint64_t xd0 = tc::sdesc_k_sw128(tc::smem_u32(Xs));
@@ -390,7 +523,6 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
         }
     }
   };
-  const bool issuer = warp == kSoloThreads / 32;
   if (issuer) issue_x(0);
 
   float bc[3];
@@ -418,32 +550,27 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       if (k + 1 < K) issue_x(k + 1);
     }
     if (warp < kSoloThreads / 32) {
-    float xr[kMaxQ];
+    ET xr[kMaxQ];
     load_x(k + 2, xr);
-    // every cell thread waits for the recurrent part of step k itself
-    bool ok = !err;
-    if (ok && !tc::mbar_wait(&bar, (uint32_t)(k & 1), kSoloPolls)) {
-      ok = false;
-      err = 1;
-    }
-    ok = __all_sync(0xffffffffu, ok);
+    // one cell thread waits for the recurrent part of step k and releases
+    // the other cell warps (the issuing warp is not held)
+    if (tid == 0 && !err && !tc::mbar_wait(&bar, (uint32_t)(k & 1), kSoloPolls)) err = 1;
+    cell_sync();
     tc::fence_after_sync();
+    const bool ok = !err;
     // ---- cell of this thread's unit for its samples
-    float df[kSoloHalf], dg[kSoloHalf], dh[kSoloHalf];
+    float dd[3][kSoloHalf];
     if (ok) {
-      const uint32_t t0 = tmem + lane_off + (uint32_t)((k & 1) * 3 * kSoloBt + n0);
-      tc::tmem_ld8(t0, df);
-      tc::tmem_ld8(t0 + (uint32_t)kSoloBt, dg);
-      tc::tmem_ld8(t0 + 2u * (uint32_t)kSoloBt, dh);
+      tmem_ld8x3(tmem + lane_off + (uint32_t)((k & 1) * 3 * kSoloBt + n0), (uint32_t)kSoloBt, dd);
     } else {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) df[i] = dg[i] = dh[i] = 0.f;
+      for (int i = 0; i < kSoloHalf; ++i) dd[0][i] = dd[1][i] = dd[2][i] = 0.f;
     }
     if (mine) {
 #pragma unroll
       for (int i = 0; i < kSoloHalf; ++i) {
         const int n = n0 + i, bb = b0 + n;
-        const CellAct ca = cell_act(df[i] + bc[0], dg[i] + bc[1], dh[i] + bc[2], dts[n]);
+        const CellAct ca = cell_act(dd[0][i] + bc[0], dd[1][i] + bc[1], dd[2][i] + bc[2], dts[n]);
         const float h = fmaf(ca.gate, ca.g - ca.hh, ca.hh);
         float hop = 0.f;
         if (bb < B) {
@@ -481,8 +608,8 @@ bool plan_bwd_solo(const Layout& L, SoloPlan* p) {
   if (L.math == CFC_MATH_FP32 || L.H > 128) return false;
   const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
   p->nAk = (L.H3 * es + 127) / 128;
-  p->smem = std::max(kSoloSmemOne, 1024 + (size_t)p->nAk * kSoloBt * 128);
-  return kSoloColA + (uint32_t)p->nAk * 32u <= kSoloTmemCols;
+  p->smem = std::max(kSoloSmemOne, 1024 + (size_t)p->nAk * 128 * 128 + (size_t)p->nAk * kSoloBt * 128);
+  return p->smem <= kSoloSmemMax && kSoloColA + (uint32_t)p->nAk * 32u <= kSoloTmemCols;
 }
 
 template <typename ET, int MODE>
@@ -516,7 +643,7 @@ bool plan_fwd_solo(const Layout& L, SoloFwdPlan* p) {
   // x staging: 16 samples x nAx atoms over 256 threads, at most 16 a thread
   if (p->nAx * (128 / es) / 16 > 16) return false;
   p->smem = std::max(kSoloSmemOne, 1024 + (size_t)3 * p->nAx * 128 * 128 + (size_t)2 * p->nAx * kSoloBt * 128 +
-                                       (size_t)p->nAh * kSoloBt * 128);
+                                       (size_t)p->nAh * kSoloBt * 128 + (size_t)p->nAh * 128 * 128);
   return p->smem <= kSoloSmemMax && kSoloColA + 3u * (uint32_t)p->nAh * 32u <= kSoloTmemCols;
 }
 
@@ -527,7 +654,7 @@ cudaError_t launch_fwd_solo(const Layout& L, const SoloFwdPlan& p, const CfcArgs
   if (e != cudaSuccess) return e;
   const int grid = (L.B + kSoloBt - 1) / kSoloBt;
   TraceScope trace("cfc_fwd_solo_tc", s);
-  kern<<<grid, kFwdThreads, p.smem, s>>>(static_cast<const ET*>(a.x), static_cast<const ET*>(a.h0),
+  kern<<<grid, kSoloBlock, p.smem, s>>>(static_cast<const ET*>(a.x), static_cast<const ET*>(a.h0),
                                           static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.b, a.dt,
                                           a.dt_stride, L.B, L.K, L.n_in, L.H, p.nAx, p.nAh,
                                           reinterpret_cast<float*>(a.ws + L.off_act), static_cast<ET*>(a.h_seq));

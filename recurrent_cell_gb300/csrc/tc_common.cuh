@@ -222,15 +222,14 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Registers -> TMEM: 32 lanes x 32 bit, 8 consecutive columns; thread t of the
-// warp writes lane (base lane + t).  Not waited: tmem_st_wait() before the
-// values are read by an MMA.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
+// Shared memory -> TMEM, asynchronous (tensor-core copy path): the 128 x 256
+// bit matrix of the descriptor (rows = lanes 0..127, 32 bytes of each row)
+// into 8 consecutive columns from taddr.  With the K-major 128B-swizzled
+// descriptor of an MMA K step this places the slice as the A operand of a
+// tensor-memory MMA expects it.  Completion: tcgen05.commit, like an MMA.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Three 32x32b.x16 loads (three column groups of the same lanes) under one wait.
 __device__ __forceinline__ void tmem_ld16x3(uint32_t t0, uint32_t t1, uint32_t t2, float (&v0)[16],
