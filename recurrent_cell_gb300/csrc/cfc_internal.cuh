@@ -203,6 +203,11 @@ bool grad_x_gemm_applies(const Layout& L);
 cudaError_t launch_grad_x_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
 // Tensor-core backward, cluster split by units (TF32 / bf16 modes).
 cudaError_t launch_backward_cluster_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);
+// W_rec^T as pre-swizzled shared-memory tiles (tile of K atom a, M tile m at
+// ((a / 2) * nM + m) * 32 KB + (a % 2) * 16 KB; for nM = 1 the atoms follow
+// one another), rounded to the operand: the backward kernels copy them.
+cudaError_t launch_prep_wt_tiles(const Layout& L, int nM, int nAk, uint8_t* tiles, const void* W_rec, cudaStream_t s);
+
 // Tensor-core forward and backward in one block per sample tile (TF32 / bf16,
 // n_hid <= 128); the forward first runs the input projection over all rows.
 cudaError_t launch_forward_solo_tc(const Layout& L, const CfcArgs& a, cudaStream_t s);

@@ -55,17 +55,6 @@ constexpr uint32_t kSoloTmemCols = 512;
 constexpr uint32_t kSoloColA = 128;
 constexpr size_t kSoloSmemOne = 116 * 1024;
 
-// Two bf16 operand values as one 32-bit word (lower K index in the low half);
-// a tf32 value as its bits.
-template <typename ET>
-__device__ __forceinline__ uint32_t pack_col(float lo, float hi) {
-  if constexpr (sizeof(ET) == 4) {
-    return __float_as_uint(lo);
-  } else {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-  }
-}
 
 template <typename ET>
 __device__ __forceinline__ void st_el(uint8_t* p, float v) {
@@ -142,25 +131,60 @@ __device__ __forceinline__ void ld_carry(uint32_t taddr, float (&cz)[kSoloHalf])
 // src + r * ld; rows >= rows_valid and K >= k_valid are zero) as a K-major
 // operand of Kpad / (128 B) atoms at dst, rounded to the operand.  All
 // nthreads threads of the block take part: lanes run along K (coalesced
-// loads, conflict-free stores), each thread has eight loads in flight, and
-// the row order is rotated by `rot` so that blocks reading the same matrix
-// at the same time spread their requests over the L2.
+// loads, conflict-free stores) and each thread has eight loads in flight.
+// Element-wise: the path for rows that are not 16-byte aligned.
 template <typename ET, int MODE>
 __device__ __forceinline__ void stage_kmajor(uint8_t* dst, const ET* __restrict__ src, int ld, int rows_valid,
-                                             int k_valid, int Kpad, int rot, int tid, int nthreads) {
+                                             int k_valid, int Kpad, int tid, int nthreads) {
   const int tot = 128 * Kpad;
   for (int e0 = tid; e0 < tot; e0 += 8 * nthreads) {
     float v[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int e = e0 + t * nthreads, i0 = e / Kpad, kk = e - i0 * Kpad, i = (i0 + rot) & 127;
+      const int e = e0 + t * nthreads, i = e / Kpad, kk = e - i * Kpad;
       v[t] = (e < tot && i < rows_valid && kk < k_valid) ? ldf(src + (long long)i * ld + kk) : 0.f;
     }
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int e = e0 + t * nthreads, i0 = e / Kpad, kk = e - i0 * Kpad, i = (i0 + rot) & 127;
+      const int e = e0 + t * nthreads, i = e / Kpad, kk = e - i * Kpad;
       if (e < tot) st_el<ET>(dst + kmaj<ET>(i, kk, 128), to_operand<MODE>(v[t]));
     }
+  }
+}
+
+// The same staging with 16-byte asynchronous copies, for rows whose byte
+// length ld * sizeof(ET) is a multiple of 16 (16-byte aligned rows): one
+// copy per 16-byte chunk straight into its swizzled place, zero-filled
+// where the chunk is partly or wholly outside the valid rows and K.  The
+// caller waits (cp_async_wait_all) and, for TF32, rounds the staged values
+// (round_staged_tf32) before the tensor cores read them.
+template <typename ET>
+__device__ __forceinline__ void stage_kmajor_async(uint8_t* dst, const ET* __restrict__ src, int ld, int rows_valid,
+                                                   int k_valid, int nA, int tid, int nthreads) {
+  constexpr int EPC = 16 / (int)sizeof(ET), EPA = 128 / (int)sizeof(ET);
+  const uint32_t d0 = tc::smem_u32(dst);
+  for (int q = tid; q < nA * 1024; q += nthreads) {
+    const int a = q >> 10, i = (q >> 3) & 127, ch = q & 7, kk = a * EPA + ch * EPC;
+    const int nvalid = (i < rows_valid && kk < k_valid) ? min(EPC, k_valid - kk) : 0;
+    const ET* g = nvalid ? src + (long long)i * ld + kk : src;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d0 + (uint32_t)a * 16384u +
+                                                                         tc::sw128_offset((uint32_t)i, (uint32_t)ch * 16u)),
+                 "l"(g), "r"(nvalid * (int)sizeof(ET))
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+// Round nbytes (a multiple of 16) of staged fp32 values to TF32 in place.
+__device__ __forceinline__ void round_staged_tf32(uint8_t* p, int nbytes, int tid, int nthreads) {
+  for (int q = tid; q < nbytes / 16; q += nthreads) {
+    float4 v = reinterpret_cast<float4*>(p)[q];
+    v.x = round_tf32(v.x);
+    v.y = round_tf32(v.y);
+    v.z = round_tf32(v.z);
+    v.w = round_tf32(v.w);
+    reinterpret_cast<float4*>(p)[q] = v;
   }
 }
 
@@ -180,7 +204,7 @@ __device__ __forceinline__ void copy_operand_to_tmem(uint32_t tcol, const uint8_
 
 template <typename ET, int MODE>
 __global__ void __launch_bounds__(kSoloThreads, 1)
-k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int dt_stride, int B, int K, int H,
+k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, int dt_stride, int B, int K, int H,
                int nAk, const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
                const float* __restrict__ grad_h_last, const float* __restrict__ y, const float* __restrict__ act,
                ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
@@ -195,7 +219,7 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t* Wt = sm;                                // nAk x [128 rows (j)][128 B]
   uint8_t* dAs = sm + (size_t)nAk * 128 * 128;     // nAk x [kSoloBt rows (n)][128 B]
-  __shared__ uint64_t bar, bar_cp;
+  __shared__ uint64_t bar, bar_cp, bar_ld;
   __shared__ uint32_t tmem_base;
   __shared__ float dts[kSoloBt];
   __shared__ int err;
@@ -203,51 +227,24 @@ k_cfc_bwd_solo(const ET* __restrict__ W_rec, const float* __restrict__ dt, int d
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
     tc::mbar_init(&bar_cp, 1);
+    tc::mbar_init(&bar_ld, 1);
     tc::mbar_init_fence();
     err = 0;
+    // A operand: the W_rec^T image (row j = output unit, K index kap =
+    // c*H + i, swizzled and rounded as in shared memory), 16 KB per atom
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(&bar_ld)),
+                 "r"((uint32_t)nAk * 16384u)
+                 : "memory");
+    for (int a = 0; a < nAk; ++a)
+      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 16384, [%2];" ::"r"(
+                       tc::smem_u32(Wt) + (uint32_t)a * 16384u),
+                   "l"(wimg + (size_t)a * 16384), "r"(tc::smem_u32(&bar_ld))
+                   : "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kSoloTmemCols);
   for (int e = tid; e < kSoloBt * Kpad; e += kSoloThreads) st_el<ET>(dAs + kmaj<ET>(e / Kpad, e % Kpad, kSoloBt), 0.f);
   if (tid < kSoloBt) dts[tid] = (b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
-  // A operand in shared memory: row j (output unit), K index kap = c*H + i
-  // -> W_rec[c][i][j]; rows j >= H and K beyond 3H are zero.  One task = one
-  // 16-byte chunk (row j, kap0 .. kap0 + 16 B): lanes take consecutive rows,
-  // so each of its loads reads consecutive values, and the swizzle spreads
-  // the 32 chunk stores over all banks.  A group of tasks has all its loads
-  // in flight before the first store.
-  // Every block reads the same weights at the same time: each starts at a
-  // different chunk column (rot) so that the blocks' requests spread over
-  // the L2 instead of queueing on the same lines.
-  {
-    constexpr int EPQ = 16 / (int)sizeof(ET);          // elements per chunk
-    constexpr int TG = (sizeof(ET) == 4) ? 8 : 4;      // tasks per group
-    const int Q = Kpad / EPQ, ntask = 128 * Q;
-    const int rot = (int)((blockIdx.x * 37u) % (unsigned)Q);
-    for (int t0 = tid; t0 < ntask; t0 += TG * kSoloThreads) {
-      float v[TG][EPQ];
-#pragma unroll
-      for (int g = 0; g < TG; ++g) {
-        const int task = t0 + g * kSoloThreads, j = task & 127;
-        const int q = (task >> 7) + rot, kap0 = (q < Q ? q : q - Q) * EPQ;
-#pragma unroll
-        for (int e = 0; e < EPQ; ++e)
-          v[g][e] = (task < ntask && j < H && kap0 + e < H3) ? ldf(W_rec + (long long)(kap0 + e) * H + j) : 0.f;
-      }
-#pragma unroll
-      for (int g = 0; g < TG; ++g) {
-        const int task = t0 + g * kSoloThreads, j = task & 127;
-        const int q = (task >> 7) + rot, kap0 = (q < Q ? q : q - Q) * EPQ;
-        if (task < ntask) {
-          uint32_t w[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            w[q] = (sizeof(ET) == 4) ? __float_as_uint(to_operand<MODE>(v[g][q]))
-                                     : pack_col<ET>(to_operand<MODE>(v[g][2 * q]), to_operand<MODE>(v[g][(2 * q + 1) % EPQ]));
-          *reinterpret_cast<uint4*>(Wt + kmaj<ET>(j, kap0, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-    }
-  }
+  if (tid == 0 && !tc::mbar_wait(&bar_ld, 0, kSoloPolls)) err = 1;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
   __syncthreads();
@@ -444,7 +441,9 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
   // one staging buffer (copy of head c overlaps the staging of what
   // follows); W_in[c] (rows = units, K = input features) stays in shared
   // memory; then x_0, x_1 and h_0.
-  const int rot = (int)((blockIdx.x * 37u) & 127u);
+  // 16-byte-aligned rows take the asynchronous 16-byte path
+  const bool vrec = (H * (int)sizeof(ET)) % 16 == 0, vin = (n_in * (int)sizeof(ET)) % 16 == 0;
+  constexpr bool kTf32 = MODE == CFC_MATH_TF32;
   tc::fence_before_sync();
   __syncthreads();                                   // TMEM address visible
   tc::fence_after_sync();
@@ -457,7 +456,22 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       __syncthreads();
       tc::fence_after_sync();
     }
-    stage_kmajor<ET, MODE>(Wst, W_rec + (long long)c * H * H, H, H, H, KpadH, rot, tid, kSoloBlock);
+    const ET* wr = W_rec + (long long)c * H * H;
+    if (vrec) stage_kmajor_async<ET>(Wst, wr, H, H, H, nAh, tid, kSoloBlock);
+    else stage_kmajor<ET, MODE>(Wst, wr, H, H, H, KpadH, tid, kSoloBlock);
+    if (c == 0)
+      for (int cc = 0; cc < 3; ++cc) {
+        uint8_t* wi = Wi + (size_t)cc * nAx * 128 * 128;
+        const ET* gi = W_in + (long long)cc * H * n_in;
+        if (vin) stage_kmajor_async<ET>(wi, gi, n_in, H, n_in, nAx, tid, kSoloBlock);
+        else stage_kmajor<ET, MODE>(wi, gi, n_in, H, n_in, KpadX, tid, kSoloBlock);
+      }
+    cp_async_wait_all();
+    if (kTf32 && (vrec || (c == 0 && vin))) {
+      __syncthreads();
+      if (vrec) round_staged_tf32(Wst, nAh * 16384, tid, kSoloBlock);
+      if (c == 0 && vin) round_staged_tf32(Wi, 3 * nAx * 16384, tid, kSoloBlock);
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::fence_before_sync();
     __syncthreads();
@@ -466,10 +480,6 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       copy_operand_to_tmem(tmem + kSoloColA + (uint32_t)(c * nAh * 32), Wst, nAh);
       tc::mma_commit_w(&bar_cp);
     }
-    if (c == 0)
-      for (int cc = 0; cc < 3; ++cc)
-        stage_kmajor<ET, MODE>(Wi + (size_t)cc * nAx * 128 * 128, W_in + (long long)cc * H * n_in, n_in, H, n_in, KpadX,
-                               rot, tid, kSoloBlock);
   }
   if (tid < kSoloThreads) {
     ET r0[kMaxQ], r1[kMaxQ];
@@ -614,13 +624,17 @@ bool plan_bwd_solo(const Layout& L, SoloPlan* p) {
 
 template <typename ET, int MODE>
 cudaError_t launch_bwd_solo(const Layout& L, const SoloPlan& p, const CfcArgs& a, cudaStream_t s) {
+  // W_rec^T image (one M tile: nAk consecutive 16 KB atoms)
+  uint8_t* wimg = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
+  cudaError_t e = launch_prep_wt_tiles(L, 1, p.nAk, wimg, a.W_rec, s);
+  if (e != cudaSuccess) return e;
   auto kern = k_cfc_bwd_solo<ET, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
   const int grid = (L.B + kSoloBt - 1) / kSoloBt;
   {
     TraceScope trace("cfc_bwd_solo_tc", s);
-    kern<<<grid, kSoloThreads, p.smem, s>>>(static_cast<const ET*>(a.W_rec), a.dt, a.dt_stride, L.B, L.K, L.H,
+    kern<<<grid, kSoloThreads, p.smem, s>>>(wimg, a.dt, a.dt_stride, L.B, L.K, L.H,
                                             p.nAk, static_cast<const ET*>(a.h_seq), a.grad_h_seq,
                                             a.grad_h_last, a.y, reinterpret_cast<const float*>(a.ws + L.off_act),
                                             reinterpret_cast<ET*>(a.ws + L.off_dA), a.grad_h0);

@@ -935,17 +935,10 @@ bool plan_bwd(const Layout& L, BwdPlan* p) {
 template <typename ET, int MODE>
 cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cudaStream_t s) {
   uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
-  {
-    const long long total = (long long)p.nM * p.nAk * 1024;   // 16-byte tile units
-    if (total > INT_MAX) return cudaErrorInvalidValue;
-    const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
-    TraceScope trace("prep_wt_tiles", s);
-    k_prep_wt_tiles<ET, MODE><<<blocks, 256, 0, s>>>(static_cast<const ET*>(a.W_rec), L.H, p.nM, p.nAk, tiles);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = launch_prep_wt_tiles(L, p.nM, p.nAk, tiles, a.W_rec, s);
+  if (e != cudaSuccess) return e;
   auto kern = k_cfc_bwd_tcb<ET, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
   const int grid = (L.B + p.Bt - 1) / p.Bt;
   {
@@ -961,6 +954,19 @@ cudaError_t launch_bwd(const Layout& L, const BwdPlan& p, const CfcArgs& a, cuda
 }
 
 }  // namespace
+
+cudaError_t launch_prep_wt_tiles(const Layout& L, int nM, int nAk, uint8_t* tiles, const void* W_rec, cudaStream_t s) {
+  const long long total = (long long)nM * nAk * 1024;   // 16-byte tile units
+  if (total > INT_MAX) return cudaErrorInvalidValue;
+  const int blocks = (int)std::min<long long>((total + 255) / 256, 4 * kNumSMs);
+  TraceScope trace("prep_wt_tiles", s);
+  if (L.math == CFC_MATH_TF32)
+    k_prep_wt_tiles<float, CFC_MATH_TF32><<<blocks, 256, 0, s>>>(static_cast<const float*>(W_rec), L.H, nM, nAk, tiles);
+  else
+    k_prep_wt_tiles<__nv_bfloat16, CFC_MATH_BF16>
+        <<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W_rec), L.H, nM, nAk, tiles);
+  return cudaGetLastError();
+}
 
 size_t tc_bwd_tiles_bytes(int n_in, int n_hid, int math) {
   if (math == CFC_MATH_FP32) return 0;

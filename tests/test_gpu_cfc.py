@@ -136,11 +136,15 @@ EDGE = [
     wl.Workload("edge_tcs_bf16_H384", B=70, K=3, n_in=64, n_hid=384, math=wl.MATH_BF16,
                 dt_per_sample=True),
     wl.Workload("edge_tcs_bf16_H512", B=40, K=2, n_in=64, n_hid=512, math=wl.MATH_BF16),
-    # single-block tensor-core backward: ragged last tile (B = 37), n_hid not a
-    # multiple of 32 (idle TMEM lanes) and n_hid = 128 exactly in TF32
+    # single-block tensor-core kernels: ragged last tile (B = 37), n_hid not a
+    # multiple of 32 (idle TMEM lanes) and n_hid = 128 exactly in bf16
     wl.Workload("edge_solo_tf32_B37_H100", B=37, K=4, n_in=20, n_hid=100, math=wl.MATH_TF32,
                 dt_per_sample=True),
     wl.Workload("edge_solo_bf16_B20_H128", B=20, K=6, n_in=64, n_hid=128, math=wl.MATH_BF16),
+    # rows that are not 16-byte aligned (n_hid % 4, n_in odd): the single-block
+    # kernels' element-wise weight staging
+    wl.Workload("edge_solo_tf32_H66_odd_n_in", B=19, K=5, n_in=13, n_hid=66, math=wl.MATH_TF32,
+                dt_per_sample=True),
     # TMA-fed weight gradient (bf16, GEMM path): 64 steps of one sample per
     # chunk with a ragged 3H tile, and whole samples per chunk
     wl.Workload("edge_tma_K128_H64", B=3, K=128, n_in=64, n_hid=64, math=wl.MATH_BF16,
