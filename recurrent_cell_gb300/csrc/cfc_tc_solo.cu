@@ -32,6 +32,8 @@
 // The MMA waits are bounded; a timeout sets the device error word and the
 // block keeps its barrier schedule without issuing more work.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 #include "cfc_internal.cuh"
 #include "tc_common.cuh"
@@ -44,8 +46,9 @@ namespace {
 
 constexpr int kSoloThreads = 256;          // 8 cell warps: lane quadrant (warp & 3), sample half (warp >> 2)
 constexpr int kSoloBlock = kSoloThreads + 32;   // + warp 8, which only issues the MMAs
-constexpr int kSoloBt = 16;                // samples per block (the MMA's N)
-constexpr int kSoloHalf = kSoloBt / 2;     // samples per thread
+constexpr int kSoloBt = 16;                // MMA N: rows of the B tiles, TMEM columns per accumulator
+// A block carries 2 * HALF samples (HALF = 4 or 8 per thread; the B tile rows
+// beyond them stay zero), so that a small batch still spreads over the SMs.
 constexpr uint32_t kSoloPolls = 1u << 24;
 constexpr size_t kSoloSmemMax = 227 * 1024;
 // TMEM: all 512 columns per block; accumulators from column 0, the A operand
@@ -79,52 +82,89 @@ __device__ __forceinline__ bool elect_one() {
 // does not take part.
 __device__ __forceinline__ void cell_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoloThreads) : "memory"); }
 
-// Four (or three) 32x32b.x8 TMEM loads of this warp's lanes at columns
-// taddr + stride * j under one wait.
-__device__ __forceinline__ void tmem_ld8x4(uint32_t taddr, uint32_t stride, float (&v)[4][kSoloHalf]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride), "r"(taddr + 3 * stride)
-      : "memory");
+// Four (or three) 32x32b TMEM loads of N = 4 or 8 columns of this warp's
+// lanes at columns taddr + stride * j, under one wait.
+template <int N> struct TmemShape;
+template <> struct TmemShape<4> {
+  static __device__ __forceinline__ void ld4(uint32_t t, uint32_t st, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%16];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4,%5,%6,%7}, [%17];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8,%9,%10,%11}, [%18];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%12,%13,%14,%15}, [%19];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(t), "r"(t + st), "r"(t + 2 * st), "r"(t + 3 * st)
+        : "memory");
+  }
+  static __device__ __forceinline__ void ld3(uint32_t t, uint32_t st, uint32_t (&r)[12]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%12];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4,%5,%6,%7}, [%13];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8,%9,%10,%11}, [%14];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11])
+        : "r"(t), "r"(t + st), "r"(t + 2 * st)
+        : "memory");
+  }
+};
+template <> struct TmemShape<8> {
+  static __device__ __forceinline__ void ld4(uint32_t t, uint32_t st, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(t), "r"(t + st), "r"(t + 2 * st), "r"(t + 3 * st)
+        : "memory");
+  }
+  static __device__ __forceinline__ void ld3(uint32_t t, uint32_t st, uint32_t (&r)[24]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%24];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%25];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%26];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+        : "r"(t), "r"(t + st), "r"(t + 2 * st)
+        : "memory");
+  }
+};
+template <int N>
+__device__ __forceinline__ void tmem_ldx4(uint32_t taddr, uint32_t stride, float (&v)[4][N]) {
+  uint32_t r[4 * N];
+  TmemShape<N>::ld4(taddr, stride, r);
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int i = 0; i < kSoloHalf; ++i) v[j][i] = __uint_as_float(r[8 * j + i]);
+    for (int i = 0; i < N; ++i) v[j][i] = __uint_as_float(r[N * j + i]);
 }
-__device__ __forceinline__ void tmem_ld8x3(uint32_t taddr, uint32_t stride, float (&v)[3][kSoloHalf]) {
-  uint32_t r[24];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%24];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%25];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%26];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
-      : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride)
-      : "memory");
+template <int N>
+__device__ __forceinline__ void tmem_ldx3(uint32_t taddr, uint32_t stride, float (&v)[3][N]) {
+  uint32_t r[3 * N];
+  TmemShape<N>::ld3(taddr, stride, r);
 #pragma unroll
   for (int j = 0; j < 3; ++j)
 #pragma unroll
-    for (int i = 0; i < kSoloHalf; ++i) v[j][i] = __uint_as_float(r[8 * j + i]);
+    for (int i = 0; i < N; ++i) v[j][i] = __uint_as_float(r[N * j + i]);
 }
 
 // The carry of this thread's lane and samples: the sum of the four partial
 // chains (TMEM columns 16 j + n).
-__device__ __forceinline__ void ld_carry(uint32_t taddr, float (&cz)[kSoloHalf]) {
-  float p[4][kSoloHalf];
-  tmem_ld8x4(taddr, (uint32_t)kSoloBt, p);
+template <int HALF>
+__device__ __forceinline__ void ld_carry(uint32_t taddr, float (&cz)[HALF]) {
+  float p[4][HALF];
+  tmem_ldx4<HALF>(taddr, (uint32_t)kSoloBt, p);
 #pragma unroll
-  for (int i = 0; i < kSoloHalf; ++i) cz[i] = (p[0][i] + p[1][i]) + (p[2][i] + p[3][i]);
+  for (int i = 0; i < HALF; ++i) cz[i] = (p[0][i] + p[1][i]) + (p[2][i] + p[3][i]);
 }
 
 // Stage rows [0, 128) x K [0, Kpad) of a row-major matrix (row r at
@@ -202,17 +242,18 @@ __device__ __forceinline__ void copy_operand_to_tmem(uint32_t tcol, const uint8_
   }
 }
 
-template <typename ET, int MODE>
+template <typename ET, int MODE, int HALF>
 __global__ void __launch_bounds__(kSoloThreads, 1)
 k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, int dt_stride, int B, int K, int H,
                int nAk, const ET* __restrict__ h_seq, const float* __restrict__ grad_h_seq,
                const float* __restrict__ grad_h_last, const float* __restrict__ y, const float* __restrict__ act,
                ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
   const int H3 = 3 * H;
-  const int b0 = blockIdx.x * kSoloBt;
+  constexpr int SPB = 2 * HALF;                    // samples of the block
+  const int b0 = blockIdx.x * SPB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = (warp & 3) * 32 + lane;            // unit = TMEM lane of this thread
-  const int n0 = (warp >> 2) * kSoloHalf;          // first sample of this thread's half
+  const int n0 = (warp >> 2) * HALF;               // first sample of this thread's half
   const int Kpad = nAk * (128 / (int)sizeof(ET));
 
   extern __shared__ uint8_t smraw[];
@@ -243,7 +284,7 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kSoloTmemCols);
   for (int e = tid; e < kSoloBt * Kpad; e += kSoloThreads) st_el<ET>(dAs + kmaj<ET>(e / Kpad, e % Kpad, kSoloBt), 0.f);
-  if (tid < kSoloBt) dts[tid] = (b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
+  if (tid < kSoloBt) dts[tid] = (tid < SPB && b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
   if (tid == 0 && !tc::mbar_wait(&bar_ld, 0, kSoloPolls)) err = 1;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
@@ -268,10 +309,10 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
 
   // Saved activations and per-step seeds of step k for this thread's samples,
   // loaded one step ahead of their use.
-  float pg[kSoloHalf], pgg[kSoloHalf], phh[kSoloHalf], pu[kSoloHalf];
+  float pg[HALF], pgg[HALF], phh[HALF], pu[HALF];
   auto load_step = [&](int k) {
 #pragma unroll
-    for (int i = 0; i < kSoloHalf; ++i) {
+    for (int i = 0; i < HALF; ++i) {
       pg[i] = pgg[i] = phh[i] = pu[i] = 0.f;
       const int bb = b0 + n0 + i;
       if (mine && k >= 0 && bb < B) {
@@ -288,16 +329,16 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
   for (int step = 0; step < K; ++step) {
     const int k = K - 1 - step;
     // ---- 1. dA_k of this thread's unit and samples
-    float cz[kSoloHalf];
+    float cz[HALF];
     if (step > 0 && !err) {
-      ld_carry(taddr, cz);
+      ld_carry<HALF>(taddr, cz);
     } else {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) cz[i] = 0.f;
+      for (int i = 0; i < HALF; ++i) cz[i] = 0.f;
     }
     if (mine) {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) {
+      for (int i = 0; i < HALF; ++i) {
         const int n = n0 + i, bb = b0 + n;
         float d0 = 0.f, d1 = 0.f, d2 = 0.f;
         if (bb < B) {
@@ -351,16 +392,16 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
   }
   // grad_h0 = the carry after step 0
   {
-    float cz[kSoloHalf];
+    float cz[HALF];
     if (!err) {
-      ld_carry(taddr, cz);
+      ld_carry<HALF>(taddr, cz);
     } else {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) cz[i] = 0.f;
+      for (int i = 0; i < HALF; ++i) cz[i] = 0.f;
     }
     if (mine && grad_h0) {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) {
+      for (int i = 0; i < HALF; ++i) {
         const int bb = b0 + n0 + i;
         if (bb < B) grad_h0[(long long)bb * H + u] = cz[i];
       }
@@ -382,17 +423,18 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
 // MMAs, so that its stalls on a full MMA queue (the look-ahead input part)
 // delay no cell work.
 // ---------------------------------------------------------------------------
-template <typename ET, int MODE>
+template <typename ET, int MODE, int HALF>
 __global__ void __launch_bounds__(kSoloBlock, 1)
 k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __restrict__ W_in,
                const ET* __restrict__ W_rec, const float* __restrict__ bias, const float* __restrict__ dt,
                int dt_stride, int B, int K, int n_in, int H, int nAx, int nAh, float* __restrict__ act,
                ET* __restrict__ h_seq) {
   const int H3 = 3 * H;
-  const int b0 = blockIdx.x * kSoloBt;
+  constexpr int SPB = 2 * HALF;                    // samples of the block
+  const int b0 = blockIdx.x * SPB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = (warp & 3) * 32 + lane;            // unit = TMEM lane of this thread
-  const int n0 = (warp >> 2) * kSoloHalf;
+  const int n0 = (warp >> 2) * HALF;
   constexpr int kEl = 128 / (int)sizeof(ET);       // K elements per atom
   const int KpadX = nAx * kEl, KpadH = nAh * kEl;
   const bool mine = u < H;
@@ -427,7 +469,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
 #pragma unroll
     for (int q = 0; q < kMaxQ; ++q) {
       const int kk = xk0 + 16 * q;
-      r[q] = (q < nq && k < K && bb < B && kk < n_in) ? src[kk] : ET(0.f);
+      r[q] = (q < nq && k < K && xn < SPB && bb < B && kk < n_in) ? src[kk] : ET(0.f);
     }
   };
   auto store_x = [&](int s, const ET (&r)[kMaxQ]) {
@@ -496,7 +538,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       for (int t = 0; t < 8; ++t) {
         const int e = e0 + t * kSoloBlock;
         const int n = e / KpadH, kk = e - n * KpadH, bb = b0 + n;
-        v[t] = (e < tot && bb < B && kk < H) ? ldf(h0 + (long long)bb * H + kk) : 0.f;
+        v[t] = (e < tot && n < SPB && bb < B && kk < H) ? ldf(h0 + (long long)bb * H + kk) : 0.f;
       }
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
@@ -506,7 +548,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       }
     }
   }
-  if (tid < kSoloBt) dts[tid] = (b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
+  if (tid < kSoloBt) dts[tid] = (tid < SPB && b0 + tid < B) ? dt[dt_stride ? b0 + tid : 0] : 0.f;
   if (tid == 0 && !tc::mbar_wait(&bar_cp, 0u, kSoloPolls)) err = 1;   // the copy of head 2
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
@@ -569,16 +611,16 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
     tc::fence_after_sync();
     const bool ok = !err;
     // ---- cell of this thread's unit for its samples
-    float dd[3][kSoloHalf];
+    float dd[3][HALF];
     if (ok) {
-      tmem_ld8x3(tmem + lane_off + (uint32_t)((k & 1) * 3 * kSoloBt + n0), (uint32_t)kSoloBt, dd);
+      tmem_ldx3<HALF>(tmem + lane_off + (uint32_t)((k & 1) * 3 * kSoloBt + n0), (uint32_t)kSoloBt, dd);
     } else {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) dd[0][i] = dd[1][i] = dd[2][i] = 0.f;
+      for (int i = 0; i < HALF; ++i) dd[0][i] = dd[1][i] = dd[2][i] = 0.f;
     }
     if (mine) {
 #pragma unroll
-      for (int i = 0; i < kSoloHalf; ++i) {
+      for (int i = 0; i < HALF; ++i) {
         const int n = n0 + i, bb = b0 + n;
         const CellAct ca = cell_act(dd[0][i] + bc[0], dd[1][i] + bc[1], dd[2][i] + bc[2], dts[n]);
         const float h = fmaf(ca.gate, ca.g - ca.hh, ca.hh);
@@ -614,6 +656,16 @@ struct SoloPlan {
   size_t smem = 0;
 };
 
+// Samples per thread: 4 (8 samples a block) while that grid fits one wave,
+// else 8.  CFC_SOLO_TILE=8 or 16 (samples a block) overrides the choice.
+int solo_half(int B) {
+  if (const char* v = getenv("CFC_SOLO_TILE")) {
+    if (strcmp(v, "8") == 0) return 4;
+    if (strcmp(v, "16") == 0) return 8;
+  }
+  return (B + 7) / 8 <= kNumSMs ? 4 : 8;
+}
+
 bool plan_bwd_solo(const Layout& L, SoloPlan* p) {
   if (L.math == CFC_MATH_FP32 || L.H > 128) return false;
   const int es = (L.math == CFC_MATH_TF32) ? 4 : 2;
@@ -622,16 +674,16 @@ bool plan_bwd_solo(const Layout& L, SoloPlan* p) {
   return p->smem <= kSoloSmemMax && kSoloColA + (uint32_t)p->nAk * 32u <= kSoloTmemCols;
 }
 
-template <typename ET, int MODE>
+template <typename ET, int MODE, int HALF>
 cudaError_t launch_bwd_solo(const Layout& L, const SoloPlan& p, const CfcArgs& a, cudaStream_t s) {
   // W_rec^T image (one M tile: nAk consecutive 16 KB atoms)
   uint8_t* wimg = reinterpret_cast<uint8_t*>(a.ws + L.off_wtt);
   cudaError_t e = launch_prep_wt_tiles(L, 1, p.nAk, wimg, a.W_rec, s);
   if (e != cudaSuccess) return e;
-  auto kern = k_cfc_bwd_solo<ET, MODE>;
+  auto kern = k_cfc_bwd_solo<ET, MODE, HALF>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  const int grid = (L.B + kSoloBt - 1) / kSoloBt;
+  const int grid = (L.B + 2 * HALF - 1) / (2 * HALF);
   {
     TraceScope trace("cfc_bwd_solo_tc", s);
     kern<<<grid, kSoloThreads, p.smem, s>>>(wimg, a.dt, a.dt_stride, L.B, L.K, L.H,
@@ -661,12 +713,12 @@ bool plan_fwd_solo(const Layout& L, SoloFwdPlan* p) {
   return p->smem <= kSoloSmemMax && kSoloColA + 3u * (uint32_t)p->nAh * 32u <= kSoloTmemCols;
 }
 
-template <typename ET, int MODE>
+template <typename ET, int MODE, int HALF>
 cudaError_t launch_fwd_solo(const Layout& L, const SoloFwdPlan& p, const CfcArgs& a, cudaStream_t s) {
-  auto kern = k_cfc_fwd_solo<ET, MODE>;
+  auto kern = k_cfc_fwd_solo<ET, MODE, HALF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  const int grid = (L.B + kSoloBt - 1) / kSoloBt;
+  const int grid = (L.B + 2 * HALF - 1) / (2 * HALF);
   TraceScope trace("cfc_fwd_solo_tc", s);
   kern<<<grid, kSoloBlock, p.smem, s>>>(static_cast<const ET*>(a.x), static_cast<const ET*>(a.h0),
                                           static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.b, a.dt,
@@ -684,9 +736,13 @@ cudaError_t launch_forward_solo_tc(const Layout& L, const CfcArgs& a, cudaStream
   if (choice != kAuto && choice != kSolo) return cudaErrorNotSupported;
   SoloFwdPlan p;
   if (!plan_fwd_solo(L, &p)) return cudaErrorNotSupported;
-  if (choice == kAuto && (long long)(L.B + kSoloBt - 1) / kSoloBt > kNumSMs) return cudaErrorNotSupported;
-  if (L.math == CFC_MATH_TF32) return launch_fwd_solo<float, CFC_MATH_TF32>(L, p, a, s);
-  return launch_fwd_solo<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+  const int half = solo_half(L.B);
+  if (choice == kAuto && (long long)(L.B + 2 * half - 1) / (2 * half) > kNumSMs) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32)
+    return half == 4 ? launch_fwd_solo<float, CFC_MATH_TF32, 4>(L, p, a, s)
+                     : launch_fwd_solo<float, CFC_MATH_TF32, 8>(L, p, a, s);
+  return half == 4 ? launch_fwd_solo<__nv_bfloat16, CFC_MATH_BF16, 4>(L, p, a, s)
+                   : launch_fwd_solo<__nv_bfloat16, CFC_MATH_BF16, 8>(L, p, a, s);
 }
 
 // Single-block tensor-core backward (TF32 / bf16, n_hid <= 128); with the
@@ -697,9 +753,13 @@ cudaError_t launch_backward_solo_tc(const Layout& L, const CfcArgs& a, cudaStrea
   SoloPlan p;
   if (!plan_bwd_solo(L, &p)) return cudaErrorNotSupported;
   if (a.grad_x && !grad_x_gemm_applies(L)) return cudaErrorNotSupported;
-  if (choice == kAuto && (long long)(L.B + kSoloBt - 1) / kSoloBt > kNumSMs) return cudaErrorNotSupported;
-  if (L.math == CFC_MATH_TF32) return launch_bwd_solo<float, CFC_MATH_TF32>(L, p, a, s);
-  return launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16>(L, p, a, s);
+  const int half = solo_half(L.B);
+  if (choice == kAuto && (long long)(L.B + 2 * half - 1) / (2 * half) > kNumSMs) return cudaErrorNotSupported;
+  if (L.math == CFC_MATH_TF32)
+    return half == 4 ? launch_bwd_solo<float, CFC_MATH_TF32, 4>(L, p, a, s)
+                     : launch_bwd_solo<float, CFC_MATH_TF32, 8>(L, p, a, s);
+  return half == 4 ? launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16, 4>(L, p, a, s)
+                   : launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16, 8>(L, p, a, s);
 }
 
 int read_tc_solo_error(int clear) {

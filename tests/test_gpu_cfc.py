@@ -58,11 +58,22 @@ def test_smoke_fp32_scratch_path():
     assert_close(got["per_sample"], ref["per_sample"], w.math, "smoke:per_sample")
 
 
-@pytest.mark.parametrize("kernels", ["tc", "tcs", "cluster", "simt", "solo"])
+def set_kernels(monkeypatch, kernels):
+    """Kernel family for the K loops; "solo16" is the single-block family
+    with 16-sample blocks (8 a thread) instead of the automatic tile."""
+    if kernels == "solo16":
+        monkeypatch.setenv("CFC_KLOOP_KERNELS", "solo")
+        monkeypatch.setenv("CFC_SOLO_TILE", "16")
+    else:
+        monkeypatch.setenv("CFC_KLOOP_KERNELS", kernels)
+        monkeypatch.delenv("CFC_SOLO_TILE", raising=False)
+
+
+@pytest.mark.parametrize("kernels", ["tc", "tcs", "cluster", "simt", "solo", "solo16"])
 @pytest.mark.parametrize("w", [wl.TINY, wl.SMOKE, wl.MID.with_(B=128, K=16),
                                wl.LARGE.with_(B=96, K=4)], ids=lambda w: w.name)
 def test_kernel_families_on_benchmark_shapes(w, kernels, monkeypatch):
-    monkeypatch.setenv("CFC_KLOOP_KERNELS", kernels)
+    set_kernels(monkeypatch, kernels)
     inp = wl.make_inputs(w, seed=9, bias_scale=PARITY_BIAS)
     r, got = run(w, inp)
     ref = oracle_ref(w, inp, per_sample=False, y=inp["y"])
@@ -163,13 +174,13 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt", "solo"])
+@pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt", "solo", "solo16"])
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("path", [wl.GRAD_SCRATCH, wl.GRAD_GEMM])
 def test_edge_shapes(w, path, kernels, monkeypatch):
     """Both K-loop kernel families (cluster-resident weights, streaming
     weights) and the automatic choice, on ragged shapes."""
-    monkeypatch.setenv("CFC_KLOOP_KERNELS", kernels)
+    set_kernels(monkeypatch, kernels)
     inp = wl.make_inputs(w, seed=5, bias_scale=PARITY_BIAS)
     r, got = run(w, inp, grad_path=path)
     ref = oracle_ref(w, inp, per_sample=(path == wl.GRAD_SCRATCH), y=inp["y"])
