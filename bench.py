@@ -154,8 +154,10 @@ def tensor_peak(w, peaks, sustained=False):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant kernels, from the ncu captures summarised under profiles/ (one
-# launch each, the bench command of that workload).  Each entry is valid only
+# dominant kernels, from the ncu captures summarised under profiles/ (smoke at
+# its full size; mid and large captured at a quarter of their batch and
+# scaled by 4, the units processed -- at that size the kernels' stores stay
+# in L2, so these two count the DRAM reads).  Each entry is valid only
 # for the sources it was taken from: the second field is the hash of the
 # kernel's own file, the shared device headers and the host dispatch
 # (KERNEL_FILES, COMMON_FILES) at capture time; any change to one of those
@@ -168,20 +170,22 @@ KERNEL_FILES = {
     "cfc_bwd_cluster_tc": "cfc_tc_kloop.cu",
     "cfc_fwd_stream_tc": "cfc_tc_stream.cu",
     "cfc_bwd_tc": "cfc_tc_stream.cu",
+    "cfc_fwd_solo_tc": "cfc_tc_solo.cu",
+    "cfc_bwd_solo_tc": "cfc_tc_solo.cu",
     "wgrad_tma_3xtf32": "cfc_tc.cu",
     "wgrad_tma_tf32": "cfc_tc.cu",
     "wgrad_tma_tc": "cfc_tc.cu",
 }
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): (885504, "42271f7a085d7473"),
-    ("smoke", "cfc_bwd_cluster"): (3412224, "42271f7a085d7473"),
-    ("smoke", "wgrad_tma_3xtf32"): (4786944, "f9b62c465d4c7cd6"),
-    ("mid", "cfc_fwd_tc"): (91625216, "bc0d15dbd48d8151"),
-    ("mid", "cfc_bwd_cluster_tc"): (159102464, "bc0d15dbd48d8151"),
-    ("mid", "wgrad_tma_tf32"): (154297600, "f9b62c465d4c7cd6"),
-    ("large", "cfc_fwd_stream_tc"): (192039680, "5e0ae08a97717dbd"),
-    ("large", "cfc_bwd_tc"): (284591360, "5e0ae08a97717dbd"),
-    ("large", "wgrad_tma_tc"): (154775808, "f9b62c465d4c7cd6"),
+    ("smoke", "cfc_fwd_cluster"): (888356, "bc2ec9c7fb8e4466"),
+    ("smoke", "cfc_bwd_cluster"): (3411675, "bc2ec9c7fb8e4466"),
+    ("smoke", "wgrad_tma_3xtf32"): (4787200, "9cfeda62cb6bba26"),
+    ("mid", "cfc_fwd_solo_tc"): (18842624, "a6b4465d43450a6b"),
+    ("mid", "cfc_bwd_solo_tc"): (102753936, "a6b4465d43450a6b"),
+    ("mid", "wgrad_tma_tf32"): (151279248, "9cfeda62cb6bba26"),
+    ("large", "cfc_fwd_stream_tc"): (26538276, "191b996d9af0b1d2"),
+    ("large", "cfc_bwd_tc"): (217265588, "191b996d9af0b1d2"),
+    ("large", "wgrad_tma_tc"): (151892552, "9cfeda62cb6bba26"),
 }
 
 
