@@ -250,15 +250,18 @@ k_wgrad_tc(const ET* __restrict__ dA, const ET* __restrict__ x, const ET* __rest
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) {  // warp-uniform issue, one elected lane
+    if (warp == 0) {  // operands from the converged warp, one elected lane issues
       const uint64_t ad = tc::sdesc_k_sw128(tc::smem_u32(As + st * kATile));
       const uint64_t bd = tc::sdesc_k_sw128(tc::smem_u32(Bs + st * kBTile));
+      if (tc::elect_one()) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if constexpr (sizeof(ET) == 4) tc::mma_tf32_w(tmem, ad + 2 * k, bd + 2 * k, id, (c | k) != 0);
-        else tc::mma_bf16_w(tmem, ad + 2 * k, bd + 2 * k, id, (c | k) != 0);
+        for (int k = 0; k < 4; ++k) {
+          if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad + 2 * k, bd + 2 * k, id, (c | k) != 0);
+          else tc::mma_bf16(tmem, ad + 2 * k, bd + 2 * k, id, (c | k) != 0);
+        }
+        tc::mma_commit(&bars[st]);
       }
-      tc::mma_commit_w(&bars[st]);
+      __syncwarp();
     }
   }
   // Wait for the last committed chunk (MMAs complete in issue order).
@@ -594,17 +597,19 @@ k_wgrad_tma(const __grid_constant__ CUtensorMap map_dA, const __grid_constant__ 
         break;
       }
       tc::fence_after_sync();
-      {  // the whole warp runs the issue (uniform operands), one lane issues
+      {  // operands from the converged warp, one elected lane issues
         const uint32_t so = (uint32_t)st * stage_bytes;
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < kTmaRows / 16; ++ks) {
-          const uint32_t acc = (c > c_begin || ks > 0) ? 1u : 0u;
-          const uint64_t ad = tc::sdesc_advance(a_desc, so + ks * 2048);
-          const uint64_t bd = tc::sdesc_advance(b_desc, so + ks * 2048);
-          tc::mma_bf16_w(tmem, ad, bd, id1, acc);
-          if (n2 > 0) tc::mma_bf16_w(tmem + 256, ad, tc::sdesc_advance(bd, 4 * kTmaBlock), id2, acc);
+          for (int ks = 0; ks < kTmaRows / 16; ++ks) {
+            const uint32_t acc = (c > c_begin || ks > 0) ? 1u : 0u;
+            const uint64_t ad = tc::sdesc_advance(a_desc, so + ks * 2048);
+            const uint64_t bd = tc::sdesc_advance(b_desc, so + ks * 2048);
+            tc::mma_bf16(tmem, ad, bd, id1, acc);
+            if (n2 > 0) tc::mma_bf16(tmem + 256, ad, tc::sdesc_advance(bd, 4 * kTmaBlock), id2, acc);
+          }
+          tc::mma_commit(&empty[st]);
         }
-        tc::mma_commit_w(&empty[st]);
       }
       __syncwarp();
       if (++st == stages) {
@@ -1022,21 +1027,23 @@ k_wgrad_tma_tf32(const __grid_constant__ CUtensorMap map_dA, const __grid_consta
         break;
       }
       tc::fence_after_sync();
-      {  // the whole warp runs the issue (uniform operands), one lane issues
+      {  // operands from the converged warp, one elected lane issues
         const uint32_t so = (uint32_t)ks * k_bytes;
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (c > c_begin || kk > 0) ? 1u : 0u;
-          const uint64_t ah = tc::sdesc_advance(a_desc, so + 32 * kk), bh = tc::sdesc_advance(b_desc, so + 32 * kk);
-          if constexpr (SPLIT) {   // small terms first: a_hi b_lo, a_lo b_hi, a_hi b_hi
-            tc::mma_tf32_w(tmem, ah, tc::sdesc_advance(bh, tile_bytes), id, acc);
-            tc::mma_tf32_w(tmem, tc::sdesc_advance(ah, tile_bytes), bh, id, 1u);
-            tc::mma_tf32_w(tmem, ah, bh, id, 1u);
-          } else {
-            tc::mma_tf32_w(tmem, ah, bh, id, acc);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (c > c_begin || kk > 0) ? 1u : 0u;
+            const uint64_t ah = tc::sdesc_advance(a_desc, so + 32 * kk), bh = tc::sdesc_advance(b_desc, so + 32 * kk);
+            if constexpr (SPLIT) {   // small terms first: a_hi b_lo, a_lo b_hi, a_hi b_hi
+              tc::mma_tf32(tmem, ah, tc::sdesc_advance(bh, tile_bytes), id, acc);
+              tc::mma_tf32(tmem, tc::sdesc_advance(ah, tile_bytes), bh, id, 1u);
+              tc::mma_tf32(tmem, ah, bh, id, 1u);
+            } else {
+              tc::mma_tf32(tmem, ah, bh, id, acc);
+            }
           }
+          tc::mma_commit(&kempty[ks]);
         }
-        tc::mma_commit_w(&kempty[ks]);
       }
       __syncwarp();
       if (++ks == k_stages) {
@@ -1262,16 +1269,18 @@ k_grad_x_tc(const __grid_constant__ CUtensorMap map_dA, const ET* __restrict__ W
           break;
         }
         tc::fence_after_sync();
-        {  // the whole warp runs the issue (uniform operands), one lane issues
+        {  // operands from the converged warp, one elected lane issues
           const uint64_t ad = tc::sdesc_advance(a0, (uint32_t)st * 128 * 128);
           const uint64_t bd = tc::sdesc_advance(b0, (uint32_t)a * NW * 128);
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if constexpr (sizeof(ET) == 4)
-              tc::mma_tf32_w(tmem + (uint32_t)(buf * NW), ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
-            else tc::mma_bf16_w(tmem + (uint32_t)(buf * NW), ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+            for (int q = 0; q < 4; ++q) {
+              if constexpr (sizeof(ET) == 4)
+                tc::mma_tf32(tmem + (uint32_t)(buf * NW), ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+              else tc::mma_bf16(tmem + (uint32_t)(buf * NW), ad + 2 * q, bd + 2 * q, id, (a | q) != 0);
+            }
+            tc::mma_commit(&empty[st]);
           }
-          tc::mma_commit_w(&empty[st]);
         }
         __syncwarp();
         if (++st == nst) {

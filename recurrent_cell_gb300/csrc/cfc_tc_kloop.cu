@@ -235,19 +235,22 @@ k_cfc_fwd_tc(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __re
         xr[q] = (e < nx && k + 1 < K && bb < B) ? ldf(x + ((long long)bb * K + k + 1) * n_in + kk) : 0.f;
       }
     }
-    if (warp == 0) {  // warp-uniform issue, one elected lane
+    if (warp == 0) {  // operands from the converged warp, one elected lane issues
       uint64_t ad = tc::sdesc_k_sw128(tc::smem_u32(Ws)), bd = tc::sdesc_k_sw128(tc::smem_u32(zc));
       const uint32_t b_step = (uint32_t)Bt * 128;
-      for (int a = 0; a < nA; ++a) {
+      if (tc::elect_one()) {
+        for (int a = 0; a < nA; ++a) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if constexpr (sizeof(ET) == 4) tc::mma_tf32_w(tmem, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
-          else tc::mma_bf16_w(tmem, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+          for (int j = 0; j < 4; ++j) {
+            if constexpr (sizeof(ET) == 4) tc::mma_tf32(tmem, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+            else tc::mma_bf16(tmem, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+          }
+          ad = tc::sdesc_advance(ad, 128 * 128);
+          bd = tc::sdesc_advance(bd, b_step);
         }
-        ad = tc::sdesc_advance(ad, 128 * 128);
-        bd = tc::sdesc_advance(bd, b_step);
+        tc::mma_commit(&bar);
       }
-      tc::mma_commit_w(&bar);
+      __syncwarp();
     }
     if (k > 0) store_results(k - 1);
     // One thread waits for the MMAs; the others meet it at the block barrier.
@@ -571,21 +574,24 @@ k_cfc_bwd_tc(const ET* __restrict__ W_in, const ET* __restrict__ W_rec, const fl
       __syncthreads();
       tc::fence_after_sync();
       // ---- 2. partial dz (thread 0 issues; the next step's activations load meanwhile)
-      if (warp == 0) {  // warp-uniform issue, one elected lane
+      if (warp == 0) {  // operands from the converged warp, one elected lane issues
         const uint64_t a0 = tc::sdesc_k_sw128(tc::smem_u32(Wt)), b0d = tc::sdesc_k_sw128(tc::smem_u32(dAs));
-        for (int mt = 0; mt < nMt; ++mt) {
-          for (int a = 0; a < nAk; ++a) {
-            const uint64_t ad = tc::sdesc_advance(a0, (uint32_t)(a * Mrows + mt * 128) * 128u);
-            const uint64_t bd = tc::sdesc_advance(b0d, (uint32_t)(a * Bt) * 128u);
+        if (tc::elect_one()) {
+          for (int mt = 0; mt < nMt; ++mt) {
+            for (int a = 0; a < nAk; ++a) {
+              const uint64_t ad = tc::sdesc_advance(a0, (uint32_t)(a * Mrows + mt * 128) * 128u);
+              const uint64_t bd = tc::sdesc_advance(b0d, (uint32_t)(a * Bt) * 128u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if constexpr (sizeof(ET) == 4)
-                tc::mma_tf32_w(tmem + (uint32_t)(mt * Bt), ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
-              else tc::mma_bf16_w(tmem + (uint32_t)(mt * Bt), ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+              for (int j = 0; j < 4; ++j) {
+                if constexpr (sizeof(ET) == 4)
+                  tc::mma_tf32(tmem + (uint32_t)(mt * Bt), ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+                else tc::mma_bf16(tmem + (uint32_t)(mt * Bt), ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+              }
             }
           }
+          tc::mma_commit(&bar);
         }
-        tc::mma_commit_w(&bar);
+        __syncwarp();
       }
       load_step(k - 1);
       if (tid == 0 && !tc::mbar_wait(&bar, (uint32_t)(step & 1), kMaxPolls)) err = 1;

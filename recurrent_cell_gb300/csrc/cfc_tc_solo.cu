@@ -72,12 +72,6 @@ __device__ __forceinline__ uint32_t kmaj(int row, int kk, int rows) {
   return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
 }
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}" : "=r"(pred));
-  return pred != 0;
-}
-
 // Barrier among the cell warps only (named barrier 1): the issuing warp
 // does not take part.
 __device__ __forceinline__ void cell_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoloThreads) : "memory"); }
@@ -236,7 +230,7 @@ __device__ __forceinline__ void copy_operand_to_tmem(uint32_t tcol, const uint8_
     const uint64_t d = tc::sdesc_advance(d0, (uint32_t)a * 128u * 128u);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      if (elect_one()) tc::tmem_cp_128x256b(tcol + (uint32_t)(a * 4 + j) * 8u, d + 2 * j);
+      if (tc::elect_one()) tc::tmem_cp_128x256b(tcol + (uint32_t)(a * 4 + j) * 8u, d + 2 * j);
       __syncwarp();
     }
   }
@@ -369,19 +363,23 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
     // activations load meanwhile)
     if (warp == 0 && !err) {
       // K step (a, j) accumulates into partial carry j: four independent
-      // chains, summed by the elementwise step
+      // chains, summed by the elementwise step.  One elected lane issues the
+      // step's MMAs back to back.
       const uint64_t bd0 = tc::sdesc_k_sw128(tc::smem_u32(dAs));
-      for (int a = 0; a < nAk; ++a) {
-        const uint64_t bd = tc::sdesc_advance(bd0, (uint32_t)a * (uint32_t)kSoloBt * 128u);
+      if (tc::elect_one()) {
+        for (int a = 0; a < nAk; ++a) {
+          const uint64_t bd = tc::sdesc_advance(bd0, (uint32_t)a * (uint32_t)kSoloBt * 128u);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t at = tmem + kSoloColA + (uint32_t)(a * 4 + j) * 8u;
-          const uint32_t d = tmem + (uint32_t)(j * kSoloBt);
-          if constexpr (sizeof(ET) == 4) tc::mma_tf32_ts_w(d, at, bd + 2 * j, id, a != 0);
-          else tc::mma_bf16_ts_w(d, at, bd + 2 * j, id, a != 0);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t at = tmem + kSoloColA + (uint32_t)(a * 4 + j) * 8u;
+            const uint32_t d = tmem + (uint32_t)(j * kSoloBt);
+            if constexpr (sizeof(ET) == 4) tc::mma_tf32_ts(d, at, bd + 2 * j, id, a != 0);
+            else tc::mma_bf16_ts(d, at, bd + 2 * j, id, a != 0);
+          }
         }
+        tc::mma_commit(&bar);
       }
-      tc::mma_commit_w(&bar);
+      __syncwarp();
     }
     load_step(k - 1);
     // ---- 3. wait for the carry
@@ -559,7 +557,8 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
   const uint64_t wd0 = tc::sdesc_k_sw128(tc::smem_u32(Wi));
   const uint64_t xd0 = tc::sdesc_k_sw128(tc::smem_u32(Xs));
   const uint64_t hd0 = tc::sdesc_k_sw128(tc::smem_u32(Zh));
-  // input part of step k into accumulator set k & 1 (fresh)
+  // input part of step k into accumulator set k & 1 (fresh); called by the
+  // elected lane of the issuing warp
   auto issue_x = [&](int k) {
     const uint32_t d = tmem + (uint32_t)((k & 1) * 3 * kSoloBt);
     const uint64_t xd = tc::sdesc_advance(xd0, (uint32_t)((k & 1) * nAx * kSoloBt * 128));
@@ -570,12 +569,15 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
           const uint64_t ad = tc::sdesc_advance(wd0, (uint32_t)((c * nAx + a) * 128 * 128));
-          if constexpr (sizeof(ET) == 4) tc::mma_tf32_w(d + c * kSoloBt, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
-          else tc::mma_bf16_w(d + c * kSoloBt, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+          if constexpr (sizeof(ET) == 4) tc::mma_tf32(d + c * kSoloBt, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
+          else tc::mma_bf16(d + c * kSoloBt, ad + 2 * j, bd + 2 * j, id, (a | j) != 0);
         }
     }
   };
-  if (issuer) issue_x(0);
+  if (issuer) {
+    if (tc::elect_one()) issue_x(0);
+    __syncwarp();
+  }
 
   float bc[3];
 #pragma unroll
@@ -585,21 +587,25 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
     // ---- recurrent part of step k onto its input part; then the input part
     // of step k+1 into the other accumulator set
     if (issuer && !err) {
-      // the three heads' chains interleaved: consecutive MMAs are independent
+      // the three heads' chains interleaved: consecutive MMAs are independent;
+      // one elected lane issues the step's MMAs back to back
       const uint32_t d = tmem + (uint32_t)((k & 1) * 3 * kSoloBt);
-      for (int a = 0; a < nAh; ++a) {
-        const uint64_t bd = tc::sdesc_advance(hd0, (uint32_t)(a * kSoloBt * 128));
+      if (tc::elect_one()) {
+        for (int a = 0; a < nAh; ++a) {
+          const uint64_t bd = tc::sdesc_advance(hd0, (uint32_t)(a * kSoloBt * 128));
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            const uint32_t at = tmem + kSoloColA + (uint32_t)(c * nAh * 32 + (a * 4 + j) * 8);
-            if constexpr (sizeof(ET) == 4) tc::mma_tf32_ts_w(d + c * kSoloBt, at, bd + 2 * j, id, 1u);
-            else tc::mma_bf16_ts_w(d + c * kSoloBt, at, bd + 2 * j, id, 1u);
-          }
+            for (int c = 0; c < 3; ++c) {
+              const uint32_t at = tmem + kSoloColA + (uint32_t)(c * nAh * 32 + (a * 4 + j) * 8);
+              if constexpr (sizeof(ET) == 4) tc::mma_tf32_ts(d + c * kSoloBt, at, bd + 2 * j, id, 1u);
+              else tc::mma_bf16_ts(d + c * kSoloBt, at, bd + 2 * j, id, 1u);
+            }
+        }
+        tc::mma_commit(&bar);
+        if (k + 1 < K) issue_x(k + 1);
       }
-      tc::mma_commit_w(&bar);
-      if (k + 1 < K) issue_x(k + 1);
+      __syncwarp();
     }
     if (warp < kSoloThreads / 32) {
     ET xr[kMaxQ];

@@ -332,27 +332,29 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
           break;
         }
         tc::fence_after_sync();
-        {  // the whole warp runs the issue (uniform operands), one lane issues
+        {  // operands from the converged warp, one elected lane issues
           const int pa = sched.pa[t];
           const uint32_t d = tmem + (uint32_t)sched.m[t] * (uint32_t)Bt;
           const bool first = sched.first[t] != 0;
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const int a = 2 * pa + sub;
-            if (a < nAk) {
-              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
-              const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+            for (int sub = 0; sub < 2; ++sub) {
+              const int a = 2 * pa + sub;
+              if (a < nAk) {
+                const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
+                const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t accum = (first && sub == 0 && q == 0) ? 0u : 1u;
-                if constexpr (sizeof(ET) == 4) tc::mma_tf32_w(d, ad + 2 * q, bd + 2 * q, id, accum);
-                else tc::mma_bf16_w(d, ad + 2 * q, bd + 2 * q, id, accum);
+                for (int q = 0; q < 4; ++q) {
+                  const uint32_t accum = (first && sub == 0 && q == 0) ? 0u : 1u;
+                  if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, accum);
+                  else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, accum);
+                }
               }
             }
+            tc::mma_commit(&empty[cst]);
+            if (t == sched.nacc0 - 1) tc::mma_commit(&acc0);
+            if (t == T - 1) tc::mma_commit(&acc1);
           }
-          tc::mma_commit_w(&empty[cst]);
-          if (t == sched.nacc0 - 1) tc::mma_commit_w(&acc0);
-          if (t == T - 1) tc::mma_commit_w(&acc1);
         }
         __syncwarp();
         if (++cst == nst) {
@@ -677,27 +679,29 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
           break;
         }
         tc::fence_after_sync();
-        {  // the whole warp runs the issue (uniform operands), one lane issues
+        {  // operands from the converged warp, one elected lane issues
           const int pa = sched.pa[t];
           const uint32_t d = tmem + (uint32_t)sched.m[t] * (uint32_t)Bt;
           const bool first = sched.first[t] != 0;
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const int a = 2 * pa + sub;
-            if (a < nAk) {
-              const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
-              const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
+            for (int sub = 0; sub < 2; ++sub) {
+              const int a = 2 * pa + sub;
+              if (a < nAk) {
+                const uint64_t ad = tc::sdesc_advance(a_desc0, (uint32_t)cst * kStage + (uint32_t)sub * kTile);
+                const uint64_t bd = tc::sdesc_advance(b_desc0, (uint32_t)(a * Bt * 128));
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t accum = (first && sub == 0 && q == 0) ? 0u : 1u;
-                if constexpr (sizeof(ET) == 4) tc::mma_tf32_w(d, ad + 2 * q, bd + 2 * q, id, accum);
-                else tc::mma_bf16_w(d, ad + 2 * q, bd + 2 * q, id, accum);
+                for (int q = 0; q < 4; ++q) {
+                  const uint32_t accum = (first && sub == 0 && q == 0) ? 0u : 1u;
+                  if constexpr (sizeof(ET) == 4) tc::mma_tf32(d, ad + 2 * q, bd + 2 * q, id, accum);
+                  else tc::mma_bf16(d, ad + 2 * q, bd + 2 * q, id, accum);
+                }
               }
             }
+            tc::mma_commit(&empty[cst]);
+            if (t == sched.nacc0 - 1) tc::mma_commit(&acc0);
+            if (t == T - 1) tc::mma_commit(&acc1);
           }
-          tc::mma_commit_w(&empty[cst]);
-          if (t == sched.nacc0 - 1) tc::mma_commit_w(&acc0);
-          if (t == T - 1) tc::mma_commit_w(&acc1);
         }
         __syncwarp();
         if (++cst == nst) {

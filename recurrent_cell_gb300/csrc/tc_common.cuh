@@ -141,42 +141,18 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
       : "memory");
 }
-// Warp-collective forms: the whole warp executes the call with warp-uniform
-// operands and one elected lane issues the instruction.  Keeping the issue
-// loop convergent lets the operands stay warp-uniform; a loop run by a single
-// thread of a divergent branch issues markedly slower.
-__device__ __forceinline__ void mma_tf32_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}" : "=r"(pred));
+  return pred != 0;
 }
-__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
-}
+
+// MMA issue: the operands are computed by the converged warp and one lane,
+// chosen by `if (elect_one())` once per burst, issues the burst back to back
+// with the plain forms above (the fastest shape measured; a loop run by
+// `if (tid == 0)`, operands included, issued markedly slower).
+// Warp-collective commit: one elected lane commits.
 __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
