@@ -44,11 +44,17 @@ __device__ int g_tc_solo_error = 0;
 
 namespace {
 
-constexpr int kSoloThreads = 256;          // 8 cell warps: lane quadrant (warp & 3), sample half (warp >> 2)
-constexpr int kSoloBlock = kSoloThreads + 32;   // + warp 8, which only issues the MMAs
+// Cell warps: lane quadrant (warp & 3) = TMEM lanes of the thread's unit,
+// sample group (warp >> 2) of HALF samples.  Backward: 16 warps, warp 0 also
+// issues the MMAs.  Forward: 8 cell warps and warp 8, which only issues them
+// (more cell warps there slowed the issue, which shares warp 0's scheduler).
+constexpr int kSoloThreads = 512;                 // backward block
+constexpr int kFwdCell = 256;                     // forward cell threads
+constexpr int kSoloFwdBlock = kFwdCell + 32;
 constexpr int kSoloBt = 16;                // MMA N: rows of the B tiles, TMEM columns per accumulator
-// A block carries 2 * HALF samples (HALF = 4 or 8 per thread; the B tile rows
-// beyond them stay zero), so that a small batch still spreads over the SMs.
+// A block carries 8 or 16 samples (the B tile rows beyond them stay zero),
+// so that a small batch still spreads over the SMs: HALF = samples a thread
+// = samples a block / (cell warps / 4).
 constexpr uint32_t kSoloPolls = 1u << 24;
 constexpr size_t kSoloSmemMax = 227 * 1024;
 // TMEM: all 512 columns per block; accumulators from column 0, the A operand
@@ -72,13 +78,33 @@ __device__ __forceinline__ uint32_t kmaj(int row, int kk, int rows) {
   return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
 }
 
-// Barrier among the cell warps only (named barrier 1): the issuing warp
-// does not take part.
-__device__ __forceinline__ void cell_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoloThreads) : "memory"); }
 
-// Four (or three) 32x32b TMEM loads of N = 4 or 8 columns of this warp's
+// Four (or three) 32x32b TMEM loads of N = 2, 4 or 8 columns of this warp's
 // lanes at columns taddr + stride * j, under one wait.
 template <int N> struct TmemShape;
+template <> struct TmemShape<2> {
+  static __device__ __forceinline__ void ld4(uint32_t t, uint32_t st, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%8];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%2,%3}, [%9];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%4,%5}, [%10];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%6,%7}, [%11];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(t), "r"(t + st), "r"(t + 2 * st), "r"(t + 3 * st)
+        : "memory");
+  }
+  static __device__ __forceinline__ void ld3(uint32_t t, uint32_t st, uint32_t (&r)[6]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%6];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%2,%3}, [%7];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%4,%5}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5])
+        : "r"(t), "r"(t + st), "r"(t + 2 * st)
+        : "memory");
+  }
+};
 template <> struct TmemShape<4> {
   static __device__ __forceinline__ void ld4(uint32_t t, uint32_t st, uint32_t (&r)[16]) {
     asm volatile(
@@ -243,11 +269,11 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
                const float* __restrict__ grad_h_last, const float* __restrict__ y, const float* __restrict__ act,
                ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
   const int H3 = 3 * H;
-  constexpr int SPB = 2 * HALF;                    // samples of the block
+  constexpr int SPB = 4 * HALF;                    // samples of the block
   const int b0 = blockIdx.x * SPB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = (warp & 3) * 32 + lane;            // unit = TMEM lane of this thread
-  const int n0 = (warp >> 2) * HALF;               // first sample of this thread's half
+  const int n0 = (warp >> 2) * HALF;               // first sample of this thread's group
   const int Kpad = nAk * (128 / (int)sizeof(ET));
 
   extern __shared__ uint8_t smraw[];
@@ -416,13 +442,13 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
 // comment).  TMEM columns: accumulator set s (s = k & 1) of head c at
 // 48 s + 16 c (N = kSoloBt columns), W_rec[c] from kSoloColA + c * nAh * 32.
 // Shared memory: W_in of the three heads (A, K-major, nAx atoms each), two
-// x tiles (B, rows = samples), the h tile (B).  Warps 0-7 compute the cell
-// (lane quadrant warp & 3, sample half warp >> 2); warp 8 only issues the
-// MMAs, so that its stalls on a full MMA queue (the look-ahead input part)
-// delay no cell work.
+// x tiles (B, rows = samples), the h tile (B).  All 16 warps compute the
+// cell (lane quadrant warp & 3, sample group warp >> 2); warp 0 first issues
+// the step's recurrent part and the next step's input part, which it
+// finishes before the recurrent part completes.
 // ---------------------------------------------------------------------------
 template <typename ET, int MODE, int HALF>
-__global__ void __launch_bounds__(kSoloBlock, 1)
+__global__ void __launch_bounds__(kSoloFwdBlock, 1)
 k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __restrict__ W_in,
                const ET* __restrict__ W_rec, const float* __restrict__ bias, const float* __restrict__ dt,
                int dt_stride, int B, int K, int n_in, int H, int nAx, int nAh, float* __restrict__ act,
@@ -435,8 +461,10 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
   const int n0 = (warp >> 2) * HALF;
   constexpr int kEl = 128 / (int)sizeof(ET);       // K elements per atom
   const int KpadX = nAx * kEl, KpadH = nAh * kEl;
-  const bool mine = u < H;
-  // x staging: thread -> sample xn, K indices xk0 + 16 q (q < nq)
+  const bool cell = warp < kFwdCell / 32;
+  const bool mine = cell && u < H;
+  // x staging: thread -> sample row xn (rows < kSoloBt; samples < SPB are
+  // loaded, the other rows stay zero), K indices xk0 + 16 q (q < nq)
   const int xn = tid >> 4, xk0 = tid & 15, nq = KpadX / 16;
   constexpr int kMaxQ = 16;
 
@@ -471,6 +499,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
     }
   };
   auto store_x = [&](int s, const ET (&r)[kMaxQ]) {
+    if (xn >= kSoloBt) return;                     // the tile has kSoloBt rows
     uint8_t* dst = Xs + (size_t)s * nAx * kSoloBt * 128;
 #pragma unroll
     for (int q = 0; q < kMaxQ; ++q)
@@ -488,7 +517,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
   __syncthreads();                                   // TMEM address visible
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const bool issuer = warp == kSoloThreads / 32;
+  const bool issuer = warp == kFwdCell / 32;
   for (int c = 0; c < 3; ++c) {
     if (c > 0) {                                     // staging buffer free again
       if (tid == 0 && !tc::mbar_wait(&bar_cp, (uint32_t)((c - 1) & 1), kSoloPolls)) err = 1;
@@ -497,20 +526,20 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       tc::fence_after_sync();
     }
     const ET* wr = W_rec + (long long)c * H * H;
-    if (vrec) stage_kmajor_async<ET>(Wst, wr, H, H, H, nAh, tid, kSoloBlock);
-    else stage_kmajor<ET, MODE>(Wst, wr, H, H, H, KpadH, tid, kSoloBlock);
+    if (vrec) stage_kmajor_async<ET>(Wst, wr, H, H, H, nAh, tid, kSoloFwdBlock);
+    else stage_kmajor<ET, MODE>(Wst, wr, H, H, H, KpadH, tid, kSoloFwdBlock);
     if (c == 0)
       for (int cc = 0; cc < 3; ++cc) {
         uint8_t* wi = Wi + (size_t)cc * nAx * 128 * 128;
         const ET* gi = W_in + (long long)cc * H * n_in;
-        if (vin) stage_kmajor_async<ET>(wi, gi, n_in, H, n_in, nAx, tid, kSoloBlock);
-        else stage_kmajor<ET, MODE>(wi, gi, n_in, H, n_in, KpadX, tid, kSoloBlock);
+        if (vin) stage_kmajor_async<ET>(wi, gi, n_in, H, n_in, nAx, tid, kSoloFwdBlock);
+        else stage_kmajor<ET, MODE>(wi, gi, n_in, H, n_in, KpadX, tid, kSoloFwdBlock);
       }
     cp_async_wait_all();
     if (kTf32 && (vrec || (c == 0 && vin))) {
       __syncthreads();
-      if (vrec) round_staged_tf32(Wst, nAh * 16384, tid, kSoloBlock);
-      if (c == 0 && vin) round_staged_tf32(Wi, 3 * nAx * 16384, tid, kSoloBlock);
+      if (vrec) round_staged_tf32(Wst, nAh * 16384, tid, kSoloFwdBlock);
+      if (c == 0 && vin) round_staged_tf32(Wi, 3 * nAx * 16384, tid, kSoloFwdBlock);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::fence_before_sync();
@@ -521,7 +550,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       tc::mma_commit_w(&bar_cp);
     }
   }
-  if (tid < kSoloThreads) {
+  if (cell) {
     ET r0[kMaxQ], r1[kMaxQ];
     load_x(0, r0);
     load_x(1, r1);
@@ -530,17 +559,17 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
   }
   {
     const int tot = kSoloBt * KpadH;
-    for (int e0 = tid; e0 < tot; e0 += 8 * kSoloBlock) {
+    for (int e0 = tid; e0 < tot; e0 += 8 * kSoloFwdBlock) {
       float v[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const int e = e0 + t * kSoloBlock;
+        const int e = e0 + t * kSoloFwdBlock;
         const int n = e / KpadH, kk = e - n * KpadH, bb = b0 + n;
         v[t] = (e < tot && n < SPB && bb < B && kk < H) ? ldf(h0 + (long long)bb * H + kk) : 0.f;
       }
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const int e = e0 + t * kSoloBlock;
+        const int e = e0 + t * kSoloFwdBlock;
         const int n = e / KpadH, kk = e - n * KpadH;
         if (e < tot) st_el<ET>(Zh + kmaj<ET>(n, kk, kSoloBt), to_operand<MODE>(v[t]));
       }
@@ -581,7 +610,7 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
 
   float bc[3];
 #pragma unroll
-  for (int c = 0; c < 3; ++c) bc[c] = (mine && tid < kSoloThreads) ? bias[c * H + u] : 0.f;
+  for (int c = 0; c < 3; ++c) bc[c] = mine ? bias[c * H + u] : 0.f;
 
   for (int k = 0; k < K; ++k) {
     // ---- recurrent part of step k onto its input part; then the input part
@@ -607,13 +636,15 @@ k_cfc_fwd_solo(const ET* __restrict__ x, const ET* __restrict__ h0, const ET* __
       }
       __syncwarp();
     }
-    if (warp < kSoloThreads / 32) {
+    if (cell) {
     ET xr[kMaxQ];
     load_x(k + 2, xr);
     // one cell thread waits for the recurrent part of step k and releases
-    // the other cell warps (the issuing warp is not held)
+    // the cell warps at a barrier of their own (the issuing warp, still
+    // issuing the next input part, is not held)
     if (tid == 0 && !err && !tc::mbar_wait(&bar, (uint32_t)(k & 1), kSoloPolls)) err = 1;
-    cell_sync();
+    tc::fence_before_sync();
+    asm volatile("bar.sync 1, %0;" ::"n"(kFwdCell) : "memory");
     tc::fence_after_sync();
     const bool ok = !err;
     // ---- cell of this thread's unit for its samples
@@ -662,14 +693,14 @@ struct SoloPlan {
   size_t smem = 0;
 };
 
-// Samples per thread: 4 (8 samples a block) while that grid fits one wave,
-// else 8.  CFC_SOLO_TILE=8 or 16 (samples a block) overrides the choice.
-int solo_half(int B) {
+// Samples a block: 8 while that grid fits one wave, else 16.
+// CFC_SOLO_TILE=8 or 16 overrides the choice.
+int solo_tile(int B) {
   if (const char* v = getenv("CFC_SOLO_TILE")) {
-    if (strcmp(v, "8") == 0) return 4;
-    if (strcmp(v, "16") == 0) return 8;
+    if (strcmp(v, "8") == 0) return 8;
+    if (strcmp(v, "16") == 0) return 16;
   }
-  return (B + 7) / 8 <= kNumSMs ? 4 : 8;
+  return (B + 7) / 8 <= kNumSMs ? 8 : 16;
 }
 
 bool plan_bwd_solo(const Layout& L, SoloPlan* p) {
@@ -689,7 +720,7 @@ cudaError_t launch_bwd_solo(const Layout& L, const SoloPlan& p, const CfcArgs& a
   auto kern = k_cfc_bwd_solo<ET, MODE, HALF>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  const int grid = (L.B + 2 * HALF - 1) / (2 * HALF);
+  const int grid = (L.B + 4 * HALF - 1) / (4 * HALF);
   {
     TraceScope trace("cfc_bwd_solo_tc", s);
     kern<<<grid, kSoloThreads, p.smem, s>>>(wimg, a.dt, a.dt_stride, L.B, L.K, L.H,
@@ -726,7 +757,7 @@ cudaError_t launch_fwd_solo(const Layout& L, const SoloFwdPlan& p, const CfcArgs
   if (e != cudaSuccess) return e;
   const int grid = (L.B + 2 * HALF - 1) / (2 * HALF);
   TraceScope trace("cfc_fwd_solo_tc", s);
-  kern<<<grid, kSoloBlock, p.smem, s>>>(static_cast<const ET*>(a.x), static_cast<const ET*>(a.h0),
+  kern<<<grid, kSoloFwdBlock, p.smem, s>>>(static_cast<const ET*>(a.x), static_cast<const ET*>(a.h0),
                                           static_cast<const ET*>(a.W_in), static_cast<const ET*>(a.W_rec), a.b, a.dt,
                                           a.dt_stride, L.B, L.K, L.n_in, L.H, p.nAx, p.nAh,
                                           reinterpret_cast<float*>(a.ws + L.off_act), static_cast<ET*>(a.h_seq));
@@ -742,12 +773,12 @@ cudaError_t launch_forward_solo_tc(const Layout& L, const CfcArgs& a, cudaStream
   if (choice != kAuto && choice != kSolo) return cudaErrorNotSupported;
   SoloFwdPlan p;
   if (!plan_fwd_solo(L, &p)) return cudaErrorNotSupported;
-  const int half = solo_half(L.B);
-  if (choice == kAuto && (long long)(L.B + 2 * half - 1) / (2 * half) > kNumSMs) return cudaErrorNotSupported;
+  const int tile = solo_tile(L.B);
+  if (choice == kAuto && (long long)(L.B + tile - 1) / tile > kNumSMs) return cudaErrorNotSupported;
   if (L.math == CFC_MATH_TF32)
-    return half == 4 ? launch_fwd_solo<float, CFC_MATH_TF32, 4>(L, p, a, s)
+    return tile == 8 ? launch_fwd_solo<float, CFC_MATH_TF32, 4>(L, p, a, s)
                      : launch_fwd_solo<float, CFC_MATH_TF32, 8>(L, p, a, s);
-  return half == 4 ? launch_fwd_solo<__nv_bfloat16, CFC_MATH_BF16, 4>(L, p, a, s)
+  return tile == 8 ? launch_fwd_solo<__nv_bfloat16, CFC_MATH_BF16, 4>(L, p, a, s)
                    : launch_fwd_solo<__nv_bfloat16, CFC_MATH_BF16, 8>(L, p, a, s);
 }
 
@@ -759,13 +790,13 @@ cudaError_t launch_backward_solo_tc(const Layout& L, const CfcArgs& a, cudaStrea
   SoloPlan p;
   if (!plan_bwd_solo(L, &p)) return cudaErrorNotSupported;
   if (a.grad_x && !grad_x_gemm_applies(L)) return cudaErrorNotSupported;
-  const int half = solo_half(L.B);
-  if (choice == kAuto && (long long)(L.B + 2 * half - 1) / (2 * half) > kNumSMs) return cudaErrorNotSupported;
+  const int tile = solo_tile(L.B);
+  if (choice == kAuto && (long long)(L.B + tile - 1) / tile > kNumSMs) return cudaErrorNotSupported;
   if (L.math == CFC_MATH_TF32)
-    return half == 4 ? launch_bwd_solo<float, CFC_MATH_TF32, 4>(L, p, a, s)
-                     : launch_bwd_solo<float, CFC_MATH_TF32, 8>(L, p, a, s);
-  return half == 4 ? launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16, 4>(L, p, a, s)
-                   : launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16, 8>(L, p, a, s);
+    return tile == 8 ? launch_bwd_solo<float, CFC_MATH_TF32, 2>(L, p, a, s)
+                     : launch_bwd_solo<float, CFC_MATH_TF32, 4>(L, p, a, s);
+  return tile == 8 ? launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16, 2>(L, p, a, s)
+                   : launch_bwd_solo<__nv_bfloat16, CFC_MATH_BF16, 4>(L, p, a, s);
 }
 
 int read_tc_solo_error(int clear) {
