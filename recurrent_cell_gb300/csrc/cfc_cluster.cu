@@ -5,8 +5,10 @@
 //
 // Forward: block r of the cluster owns hidden units [r*Hc, (r+1)*Hc)
 // (Hc = H / C) and keeps the rows of W_cat = [W_in | W_rec] of those units
-// (all three heads) in shared memory, transposed to [Zc][3][Hc] so that the
-// threads of a warp read consecutive units.  Each step it computes the three
+// (all three heads) in shared memory, [3][Hc][ldw]: a unit's row is
+// contiguous (16-byte reads of four columns) and the row stride
+// ldw = 4 (mod 8) floats puts eight consecutive units' 16-byte reads on
+// distinct bank groups.  Each step it computes the three
 // pre-activations of its units (the Zc-long dot products split over S thread
 // groups, summed in a fixed order), applies the cell, and writes its slice of
 // h_{k+1} into the next operand buffer of EVERY block of the cluster
@@ -42,6 +44,8 @@ constexpr int kXPerThread = 8;     // forward: x elements per thread prefetched 
 // (sample, unit) items per thread kept in registers, by samples per cluster.
 __host__ __device__ constexpr int items_per_thread(int bt) { return bt <= 4 ? 2 : (bt <= 8 ? 4 : 8); }
 constexpr int kMaxSplit = 8;       // thread groups a dot product is split over
+// Row stride (floats) of the forward's weight rows: Zc rounded up to 8, + 4.
+__host__ __device__ constexpr int fwd_ldw(int Zc) { return (Zc + 7) / 8 * 8 + 4; }
 
 struct ClusterPlan {
   int C = 0, BT = 0, S = 0, threads = 0;
@@ -65,18 +69,19 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
   const int b0 = (int)(blockIdx.x / C) * BT;
   const int tid = threadIdx.x, nthr = blockDim.x;
 
+  const int ldw = fwd_ldw(Zc);
   extern __shared__ float sm[];
-  float* Ws = sm;                              // [Zc][3][Hc] operand values
-  float* zb = Ws + (size_t)Zc * 3 * Hc;        // [2][BT][Zc]
+  float* Ws = sm;                              // [3][Hc][ldw] operand values
+  float* zb = Ws + (size_t)3 * Hc * ldw;       // [2][BT][Zc]
   float* part = zb + 2 * BT * Zc;              // [S][BT][3][Hc]
   float* bs = part + (size_t)S * BT * 3 * Hc;  // [3][Hc] bias of the owned units
   float* dts = bs + 3 * Hc;                    // [BT] dt of the tile's samples
 
-  for (int e = tid; e < Zc * 3 * Hc; e += nthr) {
-    const int j = e / (3 * Hc), rem = e - j * 3 * Hc, c = rem / Hc, u = rem - c * Hc;
+  for (int e = tid; e < 3 * Hc * Zc; e += nthr) {
+    const int cu = e / Zc, j = e - cu * Zc, c = cu / Hc, u = cu - c * Hc;
     const long long row = (long long)c * H + r * Hc + u;
-    Ws[e] = (j < n_in) ? ld_operand<MODE>(W_in + row * n_in + j)
-                       : ld_operand<MODE>(W_rec + row * H + (j - n_in));
+    Ws[(size_t)cu * ldw + j] = (j < n_in) ? ld_operand<MODE>(W_in + row * n_in + j)
+                                          : ld_operand<MODE>(W_rec + row * H + (j - n_in));
   }
   for (int e = tid; e < BT * Zc; e += nthr) {
     const int n = e / Zc, j = e - n * Zc, bb = b0 + n;
@@ -109,10 +114,17 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
 #pragma unroll
   for (int p = 0; p < 8; ++p) peer_zb[p] = (p < C) ? dsmem_map(smem_addr(zb), (uint32_t)p) : 0u;
 
-  // thread -> (unit u, column group s) of the dot products
+  // thread -> (unit u, column group s) of the dot products; with Zc a
+  // multiple of 4 the groups are whole 4-column quads (16-byte reads)
   const int u = tid % Hc, s = tid / Hc;
   const bool dot = s < S;
-  const int j0 = (int)((long long)s * Zc / S), j1 = (int)((long long)(s + 1) * Zc / S);
+  const bool quads = (Zc & 3) == 0;
+  const int nq = Zc / 4;
+  const int j0 = quads ? 4 * (int)((long long)s * nq / S) : (int)((long long)s * Zc / S);
+  const int j1 = quads ? 4 * (int)((long long)(s + 1) * nq / S) : (int)((long long)(s + 1) * Zc / S);
+  const float* wrow0 = Ws + (size_t)u * ldw;             // head f, unit u
+  const float* wrow1 = wrow0 + (size_t)Hc * ldw;          // head g
+  const float* wrow2 = wrow1 + (size_t)Hc * ldw;          // head h~
 
   for (int k = 0; k < K; ++k) {
     const float* zs = zb + (k & 1) * BT * Zc;
@@ -121,16 +133,35 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
       float a0[BT], a1[BT], a2[BT];
 #pragma unroll
       for (int n = 0; n < BT; ++n) { a0[n] = 0.f; a1[n] = 0.f; a2[n] = 0.f; }
-#pragma unroll 4
-      for (int j = j0; j < j1; ++j) {
-        const float* w = Ws + (size_t)j * 3 * Hc + u;
-        const float wf = w[0], wg = w[Hc], wh = w[2 * Hc];
+      if (quads) {
+        // four columns a read, added in ascending column order
+#pragma unroll 2
+        for (int j = j0; j < j1; j += 4) {
+          const float4 wf = *reinterpret_cast<const float4*>(wrow0 + j);
+          const float4 wg = *reinterpret_cast<const float4*>(wrow1 + j);
+          const float4 wh = *reinterpret_cast<const float4*>(wrow2 + j);
 #pragma unroll
-        for (int n = 0; n < BT; ++n) {
-          const float z = zs[n * Zc + j];
-          a0[n] = fmaf(wf, z, a0[n]);
-          a1[n] = fmaf(wg, z, a1[n]);
-          a2[n] = fmaf(wh, z, a2[n]);
+          for (int n = 0; n < BT; ++n) {
+            const float4 z = *reinterpret_cast<const float4*>(zs + n * Zc + j);
+            a0[n] = fmaf(wf.x, z.x, a0[n]); a0[n] = fmaf(wf.y, z.y, a0[n]);
+            a0[n] = fmaf(wf.z, z.z, a0[n]); a0[n] = fmaf(wf.w, z.w, a0[n]);
+            a1[n] = fmaf(wg.x, z.x, a1[n]); a1[n] = fmaf(wg.y, z.y, a1[n]);
+            a1[n] = fmaf(wg.z, z.z, a1[n]); a1[n] = fmaf(wg.w, z.w, a1[n]);
+            a2[n] = fmaf(wh.x, z.x, a2[n]); a2[n] = fmaf(wh.y, z.y, a2[n]);
+            a2[n] = fmaf(wh.z, z.z, a2[n]); a2[n] = fmaf(wh.w, z.w, a2[n]);
+          }
+        }
+      } else {
+#pragma unroll 4
+        for (int j = j0; j < j1; ++j) {
+          const float wf = wrow0[j], wg = wrow1[j], wh = wrow2[j];
+#pragma unroll
+          for (int n = 0; n < BT; ++n) {
+            const float z = zs[n * Zc + j];
+            a0[n] = fmaf(wf, z, a0[n]);
+            a1[n] = fmaf(wg, z, a1[n]);
+            a2[n] = fmaf(wh, z, a2[n]);
+          }
         }
       }
 #pragma unroll
@@ -377,7 +408,7 @@ constexpr size_t kSmemLimit = 200 * 1024;
 
 size_t fwd_smem(const Layout& L, int C, int BT, int S) {
   const int Hc = L.H / C;
-  return sizeof(float) * ((size_t)L.Zc * 3 * Hc + 2 * (size_t)BT * L.Zc + (size_t)S * BT * 3 * Hc +
+  return sizeof(float) * ((size_t)3 * Hc * fwd_ldw(L.Zc) + 2 * (size_t)BT * L.Zc + (size_t)S * BT * 3 * Hc +
                           3 * (size_t)Hc + BT);
 }
 
