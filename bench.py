@@ -177,15 +177,15 @@ KERNEL_FILES = {
     "wgrad_tma_tc": "cfc_tc.cu",
 }
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): (888356, "bc2ec9c7fb8e4466"),
-    ("smoke", "cfc_bwd_cluster"): (3411675, "bc2ec9c7fb8e4466"),
-    ("smoke", "wgrad_tma_3xtf32"): (4787200, "9cfeda62cb6bba26"),
-    ("mid", "cfc_fwd_solo_tc"): (18842624, "a6b4465d43450a6b"),
-    ("mid", "cfc_bwd_solo_tc"): (102753936, "a6b4465d43450a6b"),
-    ("mid", "wgrad_tma_tf32"): (151279248, "9cfeda62cb6bba26"),
-    ("large", "cfc_fwd_stream_tc"): (26538276, "191b996d9af0b1d2"),
-    ("large", "cfc_bwd_tc"): (217265588, "191b996d9af0b1d2"),
-    ("large", "wgrad_tma_tc"): (151892552, "9cfeda62cb6bba26"),
+    ("smoke", "cfc_fwd_cluster"): (892105, "c24a7efb34768559"),
+    ("smoke", "cfc_bwd_cluster"): (3410213, "c24a7efb34768559"),
+    ("smoke", "wgrad_tma_3xtf32"): (4786926, "5fc1947b6465fb79"),
+    ("mid", "cfc_fwd_solo_tc"): (18811904, "b00d873dc931d298"),
+    ("mid", "cfc_bwd_solo_tc"): (102676773, "b00d873dc931d298"),
+    ("mid", "wgrad_tma_tf32"): (151279250, "5fc1947b6465fb79"),
+    ("large", "cfc_fwd_stream_tc"): (26556050, "7bdc4aaeb8a8d8f5"),
+    ("large", "cfc_bwd_tc"): (217286363, "7bdc4aaeb8a8d8f5"),
+    ("large", "wgrad_tma_tc"): (151967159, "5fc1947b6465fb79"),
 }
 
 

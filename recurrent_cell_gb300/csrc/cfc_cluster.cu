@@ -178,7 +178,6 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
         const int e = tid + q * nthr;
         if (e < BT * n_in) zn[(e / n_in) * Zc + (e % n_in)] = xr[q];
       }
-      load_x(k + 2);
     }
     __syncthreads();
     // Cell of (sample n, unit u) pairs; partial sums added in the fixed order
@@ -219,6 +218,9 @@ k_cfc_fwd_cluster(const T* __restrict__ x, const T* __restrict__ h0, const T* __
         if (q < C) dsmem_st(peer_zb[q] + off, hop);
     }
     cluster_arrive_release();
+    // x of step k+2, issued after the arrive: a release waits for the
+    // thread's outstanding loads too
+    if (k + 1 < K) load_x(k + 2);
 #pragma unroll
     for (int it = 0; it < kItemsPerThread; ++it) {
       const int e = tid + it * nthr;
@@ -322,7 +324,6 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
     float cg_[kItemsPerThread], cgg[kItemsPerThread], chh[kItemsPerThread], cup[kItemsPerThread];
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) { cg_[q] = pg[q]; cgg[q] = pgg[q]; chh[q] = phh[q]; cup[q] = pup[q]; }
-    load_act(k - 1);
     float rd0[kItemsPerThread], rd1[kItemsPerThread], rd2[kItemsPerThread];
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) {
@@ -355,6 +356,9 @@ k_cfc_bwd_cluster(const T* __restrict__ W_in, const T* __restrict__ W_rec,
       }
     }
     cluster_arrive_release();
+    // activations of step k-1, issued after the arrive: a release waits for
+    // the thread's outstanding loads too
+    load_act(k - 1);
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) {
       const int e = tid + q * nthr;
