@@ -177,9 +177,9 @@ KERNEL_FILES = {
     "wgrad_tma_tc": "cfc_tc.cu",
 }
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): (892105, "c24a7efb34768559"),
-    ("smoke", "cfc_bwd_cluster"): (3410213, "c24a7efb34768559"),
-    ("smoke", "wgrad_tma_3xtf32"): (4786926, "5fc1947b6465fb79"),
+    ("smoke", "cfc_fwd_cluster"): (897152, "d8a6db2f1ceb97ee"),
+    ("smoke", "cfc_bwd_cluster"): (3409865, "d8a6db2f1ceb97ee"),
+    ("smoke", "wgrad_tma_3xtf32"): (4787017, "5fc1947b6465fb79"),
     ("mid", "cfc_fwd_solo_tc"): (18811904, "b00d873dc931d298"),
     ("mid", "cfc_bwd_solo_tc"): (102676773, "b00d873dc931d298"),
     ("mid", "wgrad_tma_tf32"): (151279250, "5fc1947b6465fb79"),
