@@ -6,18 +6,20 @@
 // (TF32, H = 128: 3 x 128 columns of 128 lanes), so a block can carry its own
 // samples through all K steps with no exchange between blocks: no cluster,
 // no distributed shared memory, no cluster barrier.  The weights are the A
-// operand of every per-step product and are read from TMEM by the MMA, not
-// from shared memory: with only 16 samples per block each MMA is small, and
-// a 4 KB A tile re-read from shared memory per MMA is what bounds it.
+// operand of every per-step product and are read from TMEM by the MMA (with
+// 8 or 16 samples per block each MMA is small and its cost is the 4 KB of A
+// it reads; from TMEM that measured faster than from shared memory).  They
+// reach TMEM through shared memory and tcgen05.cp.
 //
 // Backward, per step k (reverse):
-//   1. elementwise: thread (unit u = TMEM lane, half of the samples) reads
+//   1. elementwise: thread (unit u = TMEM lane, a group of the samples) reads
 //      the carry of step k+1 from TMEM (zero at k = K-1), adds the upstream
 //      seeds, forms dA_k of its unit from the saved activations (loaded one
 //      step ahead), writes dA to global memory (for the weight gradient) and
 //      into the K-major B tile (rows = samples, K index c*H + u);
-//   2. one thread issues the MMAs of carry_k^T = W_rec^T dA_k^T (A = W_rec^T,
-//      K = 3H, in TMEM) into TMEM (N = the tile's samples);
+//   2. one elected lane of warp 0 issues the MMAs of carry_k^T =
+//      W_rec^T dA_k^T (A = W_rec^T, K = 3H, in TMEM) into TMEM (N = 16 columns,
+//      the tile's samples and zero rows) as one burst;
 //   3. the block waits for them; after step 0 the carry is grad_h0.
 // grad_x = dA W_in does not feed the recurrence: one GEMM after the loop.
 //
@@ -51,7 +53,7 @@ namespace {
 constexpr int kSoloThreads = 512;                 // backward block
 constexpr int kFwdCell = 256;                     // forward cell threads
 constexpr int kSoloFwdBlock = kFwdCell + 32;
-constexpr int kSoloBt = 16;                // MMA N: rows of the B tiles, TMEM columns per accumulator
+constexpr int kSoloBt = 16;                       // MMA N: rows of the B tiles, TMEM columns per accumulator
 // A block carries 8 or 16 samples (the B tile rows beyond them stay zero),
 // so that a small batch still spreads over the SMs: HALF = samples a thread
 // = samples a block / (cell warps / 4).
@@ -63,7 +65,6 @@ constexpr size_t kSoloSmemMax = 227 * 1024;
 constexpr uint32_t kSoloTmemCols = 512;
 constexpr uint32_t kSoloColA = 128;
 constexpr size_t kSoloSmemOne = 116 * 1024;
-
 
 template <typename ET>
 __device__ __forceinline__ void st_el(uint8_t* p, float v) {
@@ -77,7 +78,6 @@ __device__ __forceinline__ uint32_t kmaj(int row, int kk, int rows) {
   const uint32_t kb = (uint32_t)kk * sizeof(ET);
   return (kb >> 7) * (uint32_t)rows * 128u + tc::sw128_offset(row, kb & 127u);
 }
-
 
 // Four (or three) 32x32b TMEM loads of N = 2, 4 or 8 columns of this warp's
 // lanes at columns taddr + stride * j, under one wait.
@@ -438,14 +438,15 @@ k_cfc_bwd_solo(const uint8_t* __restrict__ wimg, const float* __restrict__ dt, i
 }
 
 // ---------------------------------------------------------------------------
-// Forward K loop in one block per tile of kSoloBt samples (see the file
+// Forward K loop in one block per tile of 8 or 16 samples (see the file
 // comment).  TMEM columns: accumulator set s (s = k & 1) of head c at
 // 48 s + 16 c (N = kSoloBt columns), W_rec[c] from kSoloColA + c * nAh * 32.
 // Shared memory: W_in of the three heads (A, K-major, nAx atoms each), two
-// x tiles (B, rows = samples), the h tile (B).  All 16 warps compute the
-// cell (lane quadrant warp & 3, sample group warp >> 2); warp 0 first issues
-// the step's recurrent part and the next step's input part, which it
-// finishes before the recurrent part completes.
+// x tiles (B, rows = samples), the h tile (B), the W_rec staging buffer.
+// Warps 0-7 compute the cell (lane quadrant warp & 3, sample half
+// warp >> 2); warp 8 only issues the MMAs (one elected lane), so that its
+// stalls on the input part's MMAs (A from shared memory, slower to issue)
+// delay no cell work.
 // ---------------------------------------------------------------------------
 template <typename ET, int MODE, int HALF>
 __global__ void __launch_bounds__(kSoloFwdBlock, 1)
