@@ -156,6 +156,7 @@ EDGE = [
     # kernels' element-wise weight staging
     wl.Workload("edge_solo_tf32_H66_odd_n_in", B=19, K=5, n_in=13, n_hid=66, math=wl.MATH_TF32,
                 dt_per_sample=True),
+
     # TMA-fed weight gradient (bf16, GEMM path): 64 steps of one sample per
     # chunk with a ragged 3H tile, and whole samples per chunk
     wl.Workload("edge_tma_K128_H64", B=3, K=128, n_in=64, n_hid=64, math=wl.MATH_BF16,
@@ -172,6 +173,28 @@ EDGE = [
     wl.Workload("edge_tma_tf32_K16_n96", B=20, K=16, n_in=96, n_hid=64, math=wl.MATH_TF32,
                 grad_path=wl.GRAD_GEMM, dt_per_sample=True),
 ]
+
+
+# One and two steps through the single-block kernels (the automatic choice
+# takes them for these shapes): the look-ahead input part and the x staging
+# stop early, the backward's first step is also its last.
+EDGE_SHORT = [
+    wl.Workload("edge_solo_tf32_K1", B=21, K=1, n_in=64, n_hid=128, math=wl.MATH_TF32),
+    wl.Workload("edge_solo_bf16_K2", B=9, K=2, n_in=32, n_hid=64, math=wl.MATH_BF16, dt_per_sample=True),
+]
+
+
+@pytest.mark.parametrize("kernels", ["auto", "solo", "solo16"])
+@pytest.mark.parametrize("w", EDGE_SHORT, ids=lambda w: w.name)
+@pytest.mark.parametrize("path", [wl.GRAD_SCRATCH, wl.GRAD_GEMM])
+def test_short_loops_single_block(w, path, kernels, monkeypatch):
+    set_kernels(monkeypatch, kernels)
+    inp = wl.make_inputs(w, seed=5, bias_scale=PARITY_BIAS)
+    r, got = run(w, inp, grad_path=path)
+    ref = oracle_ref(w, inp, per_sample=(path == wl.GRAD_SCRATCH), y=inp["y"])
+    check_all(w, got, ref)
+    if path == wl.GRAD_SCRATCH:
+        assert_close(got["per_sample"], ref["per_sample"], w.math, f"{w.name}:per_sample")
 
 
 @pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt", "solo", "solo16"])
