@@ -156,9 +156,10 @@ __global__ void k_prep_w_tiles_fwd(const ET* __restrict__ W_in, const ET* __rest
 }
 
 constexpr int kXUnits = 4;                 // prefetched 16-byte x units per epilogue thread
-constexpr int kFwdConsumers = 256;         // cell epilogue: warps 0..7
-constexpr int kFwdProducerWarp = 8;        // W_cat tile stream
-constexpr int kFwdMmaWarp = 9;             // MMA issue
+constexpr int kFwdConsumers = 512;         // cell epilogue: warps 0..15 (4 sample groups)
+constexpr int kFwdGroups = kFwdConsumers / 128;
+constexpr int kFwdProducerWarp = 16;       // W_cat tile stream
+constexpr int kFwdMmaWarp = 17;            // MMA issue
 constexpr int kFwdThreads = kFwdConsumers + 64;
 constexpr int kFwdMaxStages = 12;
 constexpr int kMaxSched = 256;             // streamed stages per step
@@ -213,7 +214,7 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
   const int nM = 3 * nUB;
   const int Kpad = nAk * EPA;
   const int b0 = blockIdx.x * Bt;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, grp = warp >> 2;
   const int T = sched.T;
   const long long total_tiles = (long long)K * T;
   const bool vec = (n_in % EPU == 0) && (H % EPU == 0);
@@ -367,26 +368,27 @@ k_cfc_fwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
     // ---- epilogue warps
     const int xupr = vec ? n_in / EPU : 0;
     const long long sample_stride_act = (long long)K * H3, sample_stride_h = (long long)K * H;
-    const int nchunk = Bt / 16;
+    constexpr int kP = 8;                        // samples per pass
+    const int nchunk = Bt / kP;
     bool ok = true;
-    // thread <-> unit 128*ub + 32*quad + lane, 16 samples per pass; (ub, sample
-    // chunk) pairs of units [ub_lo, ub_hi) alternate between the two warp halves.
+    // thread <-> unit 128*ub + 32*quad + lane, 8 samples per pass; (ub, sample
+    // chunk) pairs of units [ub_lo, ub_hi) go round the sample groups of warps.
     auto cell_pass = [&](int k, int ub_lo, int ub_hi) {
-      for (int pidx = ub_lo * nchunk + half; pidx < ub_hi * nchunk; pidx += 2) {
-        const int ub = pidx / nchunk, n0 = (pidx - ub * nchunk) * 16;
+      for (int pidx = ub_lo * nchunk + grp; pidx < ub_hi * nchunk; pidx += kFwdGroups) {
+        const int ub = pidx / nchunk, n0 = (pidx - ub * nchunk) * kP;
         const int u = ub * 128 + quad * 32 + lane;
-        float af[16], ag[16], ah[16];
+        float af[kP], ag[kP], ah[kP];
         const uint32_t t0 = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(3 * ub * Bt + n0);
-        tc::tmem_ld16x3(t0, t0 + (uint32_t)Bt, t0 + 2u * (uint32_t)Bt, af, ag, ah);
+        tc::tmem_ld8x3(t0, t0 + (uint32_t)Bt, t0 + 2u * (uint32_t)Bt, af, ag, ah);
         if (u < H) {
           const float bf = bs[u], bg = bs[H + u], bh = bs[2 * H + u];
-          const int nvalid = min(16, B - (b0 + n0));
+          const int nvalid = min(kP, B - (b0 + n0));
           float* ap = act + ((long long)(b0 + n0) * K + k) * H3 + u;
           ET* hp = h_seq + ((long long)(b0 + n0) * K + k) * H + u;
           uint8_t* zp = Zs + (size_t)((n_in + u) * (int)sizeof(ET) >> 7) * Bt * 128;
           const uint32_t kb = (uint32_t)(((n_in + u) * (int)sizeof(ET)) & 127);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < kP; ++i) {
             const int n = n0 + i;
             const CellAct c = cell_act(af[i] + bf, ag[i] + bg, ah[i] + bh, dts[n]);
             const float gate = c.gate, g = c.g, hh = c.hh;
