@@ -582,9 +582,10 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
 // So U1's elementwise work overlaps the first U0 MMAs of the step, and U0's
 // elementwise work of the next step overlaps the last U1 MMAs.
 // ---------------------------------------------------------------------------
-constexpr int kBwdElem = 256;              // elementwise warps 0..7
-constexpr int kBwdProducerWarp = 8;
-constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdElem = 512;              // elementwise warps 0..15 (4 sample groups)
+constexpr int kBwdGroups = kBwdElem / 128;
+constexpr int kBwdProducerWarp = 16;
+constexpr int kBwdMmaWarp = 17;
 constexpr int kBwdThreads = kBwdElem + 64;
 
 template <typename ET, int MODE>
@@ -596,7 +597,7 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
               const float* __restrict__ act, ET* __restrict__ dA_out, float* __restrict__ grad_h0) {
   const int H3 = 3 * H;
   const int b0 = blockIdx.x * Bt;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = (warp >> 2) & 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, grp = warp >> 2;
   const int T = sched.T;
   const long long total_tiles = (long long)K * T;
   const int nM0 = sched.nU0;
@@ -713,10 +714,10 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
       }
     }
   } else {
-    // ---- elementwise warps: thread <-> unit 128*mt + 32*quad + lane, 8
-    // samples per pass; (M tile, sample chunk) pairs alternate between the
-    // two warp halves.
-    constexpr int kP = 8;                        // samples per pass
+    // ---- elementwise warps: thread <-> unit 128*mt + 32*quad + lane, 4
+    // samples per pass; (M tile, sample chunk) pairs go round the four
+    // sample groups of warps (warp >> 2).
+    constexpr int kP = 4;                        // samples per pass
     const int nchunk = Bt / kP;
     bool ok = true;
     auto wait_acc = [&](uint64_t* bar, uint32_t parity) {
@@ -756,7 +757,7 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
       const int u = mt * 128 + quad * 32 + lane;
       float dz[kP];
       if (s > 0) {
-        tc::tmem_ld8(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * Bt + n0), dz);
+        tc::tmem_ld4(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * Bt + n0), dz);
       } else {
 #pragma unroll
         for (int i = 0; i < kP; ++i) dz[i] = 0.f;
@@ -809,18 +810,19 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
       }
     };
     // This thread's passes of M tiles [mt_lo, mt_hi): pidx = mt_lo*nchunk +
-    // half, +2, ...; two input buffers, the next pass always in flight.
+    // grp, + kBwdGroups, ...; two input buffers, the next pass always in
+    // flight.
     auto elem = [&](int s, int mt_lo, int mt_hi) {
       const int k = K - 1 - s;
       const int end = mt_hi * nchunk;
       float ga0[kP], gg0[kP], gh0[kP], ga1[kP], gg1[kP], gh1[kP];
-      int p = mt_lo * nchunk + half;
+      int p = mt_lo * nchunk + grp;
       if (p < end) load_pass(k, p, ga0, gg0, gh0);
-      for (; p < end; p += 4) {
-        if (p + 2 < end) load_pass(k, p + 2, ga1, gg1, gh1);
+      for (; p < end; p += 2 * kBwdGroups) {
+        if (p + kBwdGroups < end) load_pass(k, p + kBwdGroups, ga1, gg1, gh1);
         run_pass(s, p, ga0, gg0, gh0);
-        if (p + 4 < end) load_pass(k, p + 4, ga0, gg0, gh0);
-        if (p + 2 < end) run_pass(s, p + 2, ga1, gg1, gh1);
+        if (p + 2 * kBwdGroups < end) load_pass(k, p + 2 * kBwdGroups, ga0, gg0, gh0);
+        if (p + kBwdGroups < end) run_pass(s, p + kBwdGroups, ga1, gg1, gh1);
       }
     };
     for (int s = 0; s <= K; ++s) {
