@@ -733,7 +733,7 @@ cudaError_t launch_wgrad_tma(const Layout& L, const TmaWgradPlan& p, const CfcAr
 // ---------------------------------------------------------------------------
 constexpr int kT32Rows = 32;                     // rows (MMA K) per chunk
 constexpr int kT32Box = kT32Rows * 128;          // one 32-column box of a chunk
-constexpr int kT32Threads = 320;
+constexpr int kT32Threads = 480;
 constexpr int kT32WarpProducer = 0, kT32WarpMma = 1, kT32WarpPatch = 2, kT32FirstTr = 3;
 constexpr int kT32Tr = kT32Threads / 32 - kT32FirstTr;   // transposer warps
 constexpr int kT32MaxRaw = 4, kT32KStages = 2;
