@@ -177,15 +177,15 @@ KERNEL_FILES = {
     "wgrad_tma_tc": "cfc_tc.cu",
 }
 PROFILED_TRAFFIC = {
-    ("smoke", "cfc_fwd_cluster"): (897152, "d8a6db2f1ceb97ee"),
-    ("smoke", "cfc_bwd_cluster"): (3409865, "d8a6db2f1ceb97ee"),
-    ("smoke", "wgrad_tma_3xtf32"): (4787017, "5fc1947b6465fb79"),
-    ("mid", "cfc_fwd_solo_tc"): (18811904, "b00d873dc931d298"),
-    ("mid", "cfc_bwd_solo_tc"): (102676773, "b00d873dc931d298"),
-    ("mid", "wgrad_tma_tf32"): (151279250, "5fc1947b6465fb79"),
-    ("large", "cfc_fwd_stream_tc"): (26556050, "7bdc4aaeb8a8d8f5"),
-    ("large", "cfc_bwd_tc"): (217286363, "7bdc4aaeb8a8d8f5"),
-    ("large", "wgrad_tma_tc"): (151967159, "5fc1947b6465fb79"),
+    ("smoke", "cfc_fwd_cluster"): (892745, "685fdff94c64622b"),
+    ("smoke", "cfc_bwd_cluster"): (3411456, "685fdff94c64622b"),
+    ("smoke", "wgrad_tma_3xtf32"): (4786999, "93311003416cba95"),
+    ("mid", "cfc_fwd_solo_tc"): (18798738, "bccb9b48ccf1cc45"),
+    ("mid", "cfc_bwd_solo_tc"): (102686574, "bccb9b48ccf1cc45"),
+    ("mid", "wgrad_tma_tf32"): (151268645, "93311003416cba95"),
+    ("large", "cfc_fwd_stream_tc"): (26736713, "3f1a4df535aef1c8"),
+    ("large", "cfc_bwd_tc"): (217183232, "3f1a4df535aef1c8"),
+    ("large", "wgrad_tma_tc"): (151907694, "93311003416cba95"),
 }
 
 
