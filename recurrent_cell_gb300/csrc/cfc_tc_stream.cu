@@ -571,8 +571,8 @@ bool plan_fwd_stream(const Layout& L, FwdPlan* p) {
 // compute carry_k^T = W_rec^T dA_k^T (M tiles of 128 units, N = Bt, K = 3H)
 // from the streamed tiles.
 //
-// Warp-specialised like the forward: warp 8 streams tiles, warp 9 issues the
-// MMAs, warps 0..7 do the elementwise work, the units split into halves U0
+// Warp-specialised like the forward: warp 16 streams tiles, warp 17 issues
+// the MMAs, warps 0..15 do the elementwise work, the units split into halves U0
 // (M tiles < nU0) and U1 with their own accumulators:
 //   elementwise(s): [acc0 of s-1] U0: carry -> dA_k(U0)  --dlo-->
 //                   [acc1 of s-1] U1: carry -> dA_k(U1)  --dhi-->
@@ -732,26 +732,32 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar);
     };
-    // Saved activations of one pass, loaded one pass ahead of their use.
+    // Saved activations and upstream gradients of one pass, loaded one pass
+    // ahead of their use (the first pass of a half before its accumulator
+    // wait): none of them depends on the MMAs.
     using VP = float[kP];
     const long long sample_stride = (long long)K * H3;   // act / dA rows of one sample
-    auto load_pass = [&](int k, int pidx, VP& ga, VP& gg, VP& gh) {
+    const long long up_stride = (long long)K * H;        // grad_h_seq rows of one sample
+    auto load_pass = [&](int k, int pidx, VP& ga, VP& gg, VP& gh, VP& gu) {
       const int mt = pidx / nchunk, n0 = (pidx - mt * nchunk) * kP;
       const int u = mt * 128 + quad * 32 + lane;
       const float* ap = act + ((long long)(b0 + n0) * K + k) * H3 + u;
+      const float* up = grad_h_seq ? grad_h_seq + ((long long)(b0 + n0) * K + k) * H + u : nullptr;
       const int nvalid = (u < H && k >= 0) ? min(kP, B - (b0 + n0)) : 0;
 #pragma unroll
       for (int i = 0; i < kP; ++i) {
-        ga[i] = gg[i] = gh[i] = 0.f;
+        ga[i] = gg[i] = gh[i] = gu[i] = 0.f;
         if (i < nvalid) {
           ga[i] = ap[0];
           gg[i] = ap[H];
           gh[i] = ap[2 * H];
+          if (up) gu[i] = up[0];
         }
         ap += sample_stride;
+        if (up) up += up_stride;
       }
     };
-    auto run_pass = [&](int s, int pidx, const VP& ga, const VP& gg, const VP& gh) {
+    auto run_pass = [&](int s, int pidx, const VP& ga, const VP& gg, const VP& gh, const VP& gu) {
       const int k = K - 1 - s;                   // k < 0: grad_h0 read-out
       const int mt = pidx / nchunk, n0 = (pidx - mt * nchunk) * kP;
       const int u = mt * 128 + quad * 32 + lane;
@@ -779,7 +785,7 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
           const int bb = b0 + n0 + i;
           if (i < nvalid) {
             const long long row = (long long)bb * K + k;
-            float up = grad_h_seq ? grad_h_seq[row * H + u] : 0.f;
+            float up = gu[i];
             if (k == K - 1) {
               if (grad_h_last) up += grad_h_last[(long long)bb * H + u];
               if (y) up += ldf(h_seq + row * H + u) - y[(long long)bb * H + u];
@@ -811,24 +817,28 @@ k_cfc_bwd_tcb(const __grid_constant__ TileSchedule sched, const uint8_t* __restr
     };
     // This thread's passes of M tiles [mt_lo, mt_hi): pidx = mt_lo*nchunk +
     // grp, + kBwdGroups, ...; two input buffers, the next pass always in
-    // flight.
+    // flight.  Buffer 0 arrives holding the first pass (prefetch()).
+    float ga0[kP], gg0[kP], gh0[kP], gu0[kP], ga1[kP], gg1[kP], gh1[kP], gu1[kP];
+    auto prefetch = [&](int s, int mt_lo, int mt_hi) {
+      const int p = mt_lo * nchunk + grp;
+      if (p < mt_hi * nchunk) load_pass(K - 1 - s, p, ga0, gg0, gh0, gu0);
+    };
     auto elem = [&](int s, int mt_lo, int mt_hi) {
       const int k = K - 1 - s;
       const int end = mt_hi * nchunk;
-      float ga0[kP], gg0[kP], gh0[kP], ga1[kP], gg1[kP], gh1[kP];
-      int p = mt_lo * nchunk + grp;
-      if (p < end) load_pass(k, p, ga0, gg0, gh0);
-      for (; p < end; p += 2 * kBwdGroups) {
-        if (p + kBwdGroups < end) load_pass(k, p + kBwdGroups, ga1, gg1, gh1);
-        run_pass(s, p, ga0, gg0, gh0);
-        if (p + 2 * kBwdGroups < end) load_pass(k, p + 2 * kBwdGroups, ga0, gg0, gh0);
-        if (p + kBwdGroups < end) run_pass(s, p + kBwdGroups, ga1, gg1, gh1);
+      for (int p = mt_lo * nchunk + grp; p < end; p += 2 * kBwdGroups) {
+        if (p + kBwdGroups < end) load_pass(k, p + kBwdGroups, ga1, gg1, gh1, gu1);
+        run_pass(s, p, ga0, gg0, gh0, gu0);
+        if (p + 2 * kBwdGroups < end) load_pass(k, p + 2 * kBwdGroups, ga0, gg0, gh0, gu0);
+        if (p + kBwdGroups < end) run_pass(s, p + kBwdGroups, ga1, gg1, gh1, gu1);
       }
     };
     for (int s = 0; s <= K; ++s) {
+      prefetch(s, 0, nM0);
       if (s > 0) wait_acc(&acc0, (uint32_t)((s - 1) & 1));
       if (ok) elem(s, 0, nM0);
       if (s < K) signal(&dsig[0]);
+      prefetch(s, nM0, nM);
       if (s > 0) wait_acc(&acc1, (uint32_t)((s - 1) & 1));
       if (ok) elem(s, nM0, nM);
       if (s < K) signal(&dsig[1]);
