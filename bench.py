@@ -183,9 +183,9 @@ PROFILED_TRAFFIC = {
     ("mid", "cfc_fwd_solo_tc"): (18798738, "bccb9b48ccf1cc45"),
     ("mid", "cfc_bwd_solo_tc"): (102686574, "bccb9b48ccf1cc45"),
     ("mid", "wgrad_tma_tf32"): (151268645, "93311003416cba95"),
-    ("large", "cfc_fwd_stream_tc"): (26736713, "3f1a4df535aef1c8"),
-    ("large", "cfc_bwd_tc"): (217183232, "3f1a4df535aef1c8"),
-    ("large", "wgrad_tma_tc"): (151907694, "93311003416cba95"),
+    ("large", "cfc_fwd_stream_tc"): (26883291, "2012e14234dc0310"),
+    ("large", "cfc_bwd_tc"): (216595602, "2012e14234dc0310"),
+    ("large", "wgrad_tma_tc"): (151995977, "93311003416cba95"),
 }
 
 
