@@ -49,6 +49,30 @@ def test_tiny_fp32_all_upstream_seeds():
     assert_close(got["per_sample"], ref["per_sample"], w.math, "tiny:per_sample")
 
 
+SEEDS = [
+    wl.Workload("seeds_tf32_B70_K4_H160", B=70, K=4, n_in=24, n_hid=160, math=wl.MATH_TF32),
+    wl.Workload("seeds_bf16_B37_K5_H40", B=37, K=5, n_in=24, n_hid=40, math=wl.MATH_BF16,
+                dt_per_sample=True),
+]
+
+
+@pytest.mark.parametrize("kernels", ["auto", "tc", "tcs", "cluster", "simt", "solo", "solo16"])
+@pytest.mark.parametrize("w", SEEDS, ids=lambda w: w.name)
+def test_upstream_seeds_every_family(w, kernels, monkeypatch):
+    """Per-step seeds grad_h_seq, the last state's grad_h_last and the y
+    loss together, through every K-loop family of the reduced-precision
+    modes (each loads the per-step seeds in its own way)."""
+    set_kernels(monkeypatch, kernels)
+    inp = wl.make_inputs(w, seed=17, bias_scale=PARITY_BIAS)
+    rng = np.random.default_rng(2)
+    gseq = rng.standard_normal((w.B, w.K, w.n_hid)).astype(np.float32)
+    glast = rng.standard_normal((w.B, w.n_hid)).astype(np.float32)
+    r, got = run(w, inp, y=True, grad_h_seq=dev(gseq), grad_h_last=dev(glast))
+    ref = oracle_ref(w, inp, y=inp["y"], grad_h_seq=gseq, grad_h_last=glast)
+    check_all(w, got, ref)
+    assert_close(got["per_sample"], ref["per_sample"], w.math, f"{w.name}:per_sample")
+
+
 def test_smoke_fp32_scratch_path():
     w = wl.SMOKE
     inp = wl.make_inputs(w, bias_scale=PARITY_BIAS)
