@@ -307,6 +307,34 @@ class ClockSampler:
 # our arm
 # ----------------------------------------------------------------------------
 
+class Packed:
+    def __init__(self, buf, views):
+        self.buf, self.views = buf, views
+
+
+def packed_block(torch, specs, device, pin=False):
+    """One uint8 block holding tensors (name, dtype, shape) as views, each at a
+    256-byte offset (the C ABI wants 16-byte aligned pointers)."""
+    offs, off = {}, 0
+    for name, dt, shape in specs:
+        offs[name] = off
+        n = 1
+        for d in shape:
+            n *= d
+        off += (n * torch.empty((), dtype=dt).element_size() + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = {}
+    for name, dt, shape in specs:
+        n = 1
+        for d in shape:
+            n *= d
+        nb = n * torch.empty((), dtype=dt).element_size()
+        views[name] = buf[offs[name]:offs[name] + nb].view(dt).view(shape)
+    return Packed(buf, views)
+
+
 class Path:
     """Device-resident buffers for one workload and the step = fwd + bwd."""
 
@@ -319,19 +347,29 @@ class Path:
         self.st = st
         B, K, n_in, H = w.B, w.K, w.n_in, w.n_hid
         f32 = torch.float32
-        self.host = {k: torch.from_numpy(v).to(dtype=(st if k in ("x", "h0", "W_in", "W_rec") else f32))
-                     .pin_memory() for k, v in inp.items()}
-        self.t = {k: v.to(device) for k, v in self.host.items()}
+        src = {k: torch.from_numpy(v).to(dtype=(st if k in ("x", "h0", "W_in", "W_rec") else f32))
+               for k, v in inp.items()}
+        # The inputs live in one pinned host block and one device block, the
+        # three gradients in one device block and one pinned host block, each
+        # tensor a view at a 256-byte offset: the end-to-end step moves them
+        # with one host-to-device and one device-to-host copy.
+        in_specs = [(k, v.dtype, tuple(v.shape)) for k, v in src.items()]
+        self.in_host = packed_block(torch, in_specs, device="cpu", pin=True)
+        for k, v in src.items():
+            self.in_host.views[k].copy_(v)
+        self.in_dev = packed_block(torch, in_specs, device=device)
+        self.in_dev.buf.copy_(self.in_host.buf)
+        self.host, self.t = self.in_host.views, self.in_dev.views
         self.ws = torch.empty(cfc.cfc_kloop_workspace_bytes(B, K, n_in, H, w.math, w.grad_path),
                               dtype=torch.uint8, device=device)
         self.h_seq = torch.empty(B, K, H, dtype=st, device=device)
-        self.gWi = torch.empty(3, H, n_in, device=device)
-        self.gWr = torch.empty(3, H, H, device=device)
-        self.gb = torch.empty(3, H, device=device)
+        g_specs = [("gWi", f32, (3, H, n_in)), ("gWr", f32, (3, H, H)), ("gb", f32, (3, H))]
+        self.g_dev = packed_block(torch, g_specs, device=device)
+        self.g_host = packed_block(torch, g_specs, device="cpu", pin=True)
+        self.gWi, self.gWr, self.gb = (self.g_dev.views[k] for k in ("gWi", "gWr", "gb"))
         self.scratch = (torch.empty(B, w.N, device=device) if w.grad_path == wl.GRAD_SCRATCH else None)
-        self.out_host = [torch.empty(t.shape, dtype=f32).pin_memory() for t in (self.gWi, self.gWr, self.gb)]
-        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
-        self.d2h_bytes = sum(v.numel() * v.element_size() for v in self.out_host)
+        self.h2d_bytes = self.in_host.buf.numel()
+        self.d2h_bytes = self.g_host.buf.numel()
         # rows of the gradient partials that reduce_axis0 sums (from the library)
         self.n_split = cfc.cfc_kloop_grad_splits(B, K, n_in, H, w.math, w.grad_path)
 
@@ -344,11 +382,9 @@ class Path:
                                per_sample_scratch=self.scratch, grad_path=w.grad_path, math=w.math)
 
     def step_e2e(self):
-        for k, v in self.host.items():
-            self.t[k].copy_(v, non_blocking=True)
+        self.in_dev.buf.copy_(self.in_host.buf, non_blocking=True)
         self.step()
-        for dst, src in zip(self.out_host, (self.gWi, self.gWr, self.gb)):
-            dst.copy_(src, non_blocking=True)
+        self.g_host.buf.copy_(self.g_dev.buf, non_blocking=True)
 
 
 def timed(torch, fn, steps, flush=None):
